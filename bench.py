@@ -1,0 +1,434 @@
+#!/usr/bin/env python
+"""Benchmark of the routed ReLU^2 MoE layer on GB300: MoE-layer tokens/s and the
+fraction of the HBM roofline reached.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload nano_decode] [--tokens 64]
+
+A step is one full layer forward (router, dispatch, experts up, experts down,
+combine, shared expert; latent projections for latent shapes) over one batch
+of T synthetic tokens.  Weights come in several seeded replicas that the steps
+rotate through, so no step finds the previous step's weights in L2.  Prints
+one JSON line (rank 0).  Multi-GPU (torchrun): every rank runs its own layer
+replica on its own tokens (no collective on the data path; weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="nano_decode")
+    ap.add_argument("--tokens", type=int, default=64)
+    ap.add_argument("--replicas", type=int, default=0, help="weight replicas (0 = enough to defeat L2)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="also time every token count of the workload")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.dev), "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.flush()
+        rows = [l.strip().split(",") for l in open(self.f.name) if l.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+def layer_bytes(shape, n_active: int, T: int) -> dict:
+    """Algorithmic HBM bytes of one layer step: weights of the experts that
+    received routes, shared expert, router, latent pair, and the activations in
+    and out."""
+    ab = 4 if shape.act_dtype == 0 else 2
+    de, I, d, S, E = shape.d_e, shape.d_expert, shape.d_model, shape.d_shared, shape.n_experts
+    if shape.expert_dtype == 2:
+        expert = 2 * (I * de // 2 + I * de // 16) + 8
+    else:
+        expert = 2 * I * de * (4 if shape.expert_dtype == 0 else 2)
+    b = {"experts": n_active * expert, "shared": 2 * d * S * ab, "router": E * d * 4 + E * 4,
+         "latent": 2 * d * shape.d_latent * ab, "activations": 2 * T * d * ab}
+    b["total"] = sum(b.values())
+    return b
+
+
+def layer_flops(shape, T: int) -> int:
+    de, I, d, S, E, K = shape.d_e, shape.d_expert, shape.d_model, shape.d_shared, shape.n_experts, shape.top_k
+    per_tok = 2 * E * d + K * 4 * de * I + 4 * d * S + 4 * d * shape.d_latent
+    return per_tok * T
+
+
+def run_ours(args, rank, world, dev):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import routed_relu_expert_gb300 as M
+    from synth import WORKLOADS, make_weights, make_x
+
+    shape = WORKLOADS[args.workload]
+    T = args.tokens
+    cfg = M.config_from(shape)
+    one = layer_bytes(shape, shape.n_experts, T)["total"]     # one replica's full weight set
+    per_step = layer_bytes(shape, min(T * shape.top_k, shape.n_experts), T)["total"]
+    n_rep = args.replicas or max(2, min(8, -(-4 * L2_BYTES // per_step) + 1))
+    reps = [make_weights(shape, dev, replica=r) for r in range(n_rep)]
+    layers = [M.MoELayer(cfg, w) for w in reps]
+    x = make_x(shape, T, dev)
+    y = torch.empty_like(x)
+    ws = M.new_workspace(cfg, T, dev)
+    for L in layers:
+        L._ws = ws
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        layers[i % n_rep].forward(x, y)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    err = M.moe_get_device_error(ws)
+
+    def timed(fn, K):
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(K):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+            torch.distributed.barrier()
+        return ms
+
+    clocks = ClockSampler(torch.cuda.current_device() if not os.environ.get("CUDA_VISIBLE_DEVICES") else 0)
+    clocks.start()
+    n0 = M.load().moe_launch_count()
+    ms = timed(step, args.steps)
+    n1 = M.load().moe_launch_count()
+    clk = clocks.stop()
+    ms_step = ms / args.steps
+    value = world * T / (ms_step / 1e3)
+
+    # experts that received routes (same routing for every replica: router and bias are shared)
+    ids = torch.empty((T, shape.top_k), dtype=torch.int32, device=dev)
+    layers[0].forward(x, y, ids_out=ids)
+    n_active = int(torch.unique(ids).numel())
+    lb = layer_bytes(shape, n_active, T)
+    pk = peaks()
+
+    # dominant kernel, timed alone on the same stream: the grouped expert up projection
+    K_ = shape.top_k
+    R = T * K_
+    topw = torch.empty((T, K_), dtype=torch.float32, device=dev)
+    x_e = x
+    if shape.d_latent:
+        x_e = torch.empty((T, shape.d_latent), dtype=x.dtype, device=dev)
+        M.moe_latent_down(cfg, x, layers[0].weights, x_e, ws)
+    M.moe_router(cfg, x, reps[0]["w_router"], reps[0]["bias"], ids, topw, ws)
+    counts = torch.empty(shape.n_experts, dtype=torch.int32, device=dev)
+    offsets = torch.empty(shape.n_experts + 1, dtype=torch.int32, device=dev)
+    rt = torch.empty(R, dtype=torch.int32, device=dev)
+    rs = torch.empty(R, dtype=torch.int32, device=dev)
+    tsr = torch.empty((T, K_), dtype=torch.int32, device=dev)
+    M.moe_dispatch(cfg, ids, counts, offsets, rt, rs, tsr, ws)
+    h = torch.empty((R, shape.d_expert), dtype=x.dtype, device=dev)
+
+    def up(i):
+        M.moe_experts_up(cfg, T, rt, offsets, layers[i % n_rep].weights, h, ws, x_e=x_e)
+
+    for i in range(3):
+        up(i)
+    k_up = max(20, args.steps)
+    c0 = M.load().moe_launch_count()
+    ms_up = timed(up, k_up) / k_up
+    assert M.load().moe_launch_count() - c0 == k_up, "expert up is expected to be one launch"
+    ab = 2
+    up_bytes = n_active * shape.d_expert * shape.d_e * ab + R * shape.d_e * ab + R * shape.d_expert * ab
+    achieved = up_bytes / (ms_up / 1e3) / 1e9
+
+    # end to end through the C ABI with host buffers (copies inside the timed region)
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    x_dev = torch.empty_like(x)
+    for i in range(3):
+        M.moe_layer_forward_host(cfg, xh, x_dev, layers[i % n_rep].weights, y, yh, ws)
+    k_e2e = max(10, args.steps // 4)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for i in range(k_e2e):
+        M.moe_layer_forward_host(cfg, xh, x_dev, layers[i % n_rep].weights, y, yh, ws)
+    e2e_s = (time.perf_counter() - t0) / k_e2e
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    sweep = {}
+    if args.sweep:
+        for Ts in shape.tokens:
+            xs = make_x(shape, Ts, dev)
+            ys = torch.empty_like(xs)
+            wss = M.new_workspace(cfg, Ts, dev)
+            for L in layers:
+                L._ws = wss
+            f = lambda i: layers[i % n_rep].forward(xs, ys)
+            for i in range(5):
+                f(i)
+            kk = max(50, args.steps // 2)
+            mss = timed(f, kk) / kk
+            idss = torch.empty((Ts, shape.top_k), dtype=torch.int32, device=dev)
+            layers[0].forward(xs, ys, ids_out=idss)
+            na = int(torch.unique(idss).numel())
+            bb = layer_bytes(shape, na, Ts)["total"]
+            sweep[str(Ts)] = {"ms_per_step": round(mss, 5), "tokens_per_s": round(Ts / (mss / 1e3), 1),
+                              "experts_active": na, "hbm_gb_per_s": round(bb / (mss / 1e3) / 1e9, 1),
+                              "hbm_frac": round(bb / (mss / 1e3) / 1e9 / pk["hbm_gbs"], 3)}
+
+    return {
+        "value": value, "ms_per_step": ms_step, "n_active": n_active, "bytes": lb, "clocks": clk,
+        "launches": int(n1 - n0), "err": err, "ms_up": ms_up, "up_bytes": up_bytes, "achieved_up": achieved,
+        "peaks": pk, "e2e_s": e2e_s, "n_rep": n_rep, "sweep": sweep, "shape": shape, "T": T,
+        "rep_bytes": one,
+    }
+
+
+# ---------------------------------------------------------------------------
+class _Rows:
+    """weights[name][e] as float64 numpy (CPU tensors are converted on access)."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __getitem__(self, e):
+        import numpy as np
+        v = self.t[e]
+        return v.numpy() if v.dtype == __import__("torch").uint8 else v.float().numpy().astype(np.float64)
+
+
+def oracle_inputs(w):
+    import numpy as np
+    out = {}
+    for k, v in w.items():
+        v = v.cpu()
+        if k in ("w_up", "w_down", "w_up_q", "w_down_q", "w_up_sf", "w_down_sf"):
+            out[k] = _Rows(v)
+        elif k in ("w_router", "bias"):
+            out[k] = v.numpy()
+        else:
+            out[k] = v.float().numpy().astype(np.float64)
+    return out
+
+
+def time_oracle(shape, w, x, budget_s: float, min_tokens: int = 1):
+    """Tokens/s of the oracle on the first rows of x, growing the sample until
+    it takes at least budget_s (bounded)."""
+    import numpy as np
+    from oracle import moe_oracle as O
+    ow = oracle_inputs(w)
+    xn = x.float().cpu().numpy().astype(np.float64)
+    n = min_tokens
+    done_t, done_s = 0, 0.0
+    while True:
+        rows = xn[done_t % xn.shape[0]:][:n]
+        t0 = time.perf_counter()
+        O.full_layer(rows, ow, shape.n_experts, shape.top_k, shape.n_group, shape.topk_group,
+                     shape.norm_topk_prob, shape.routed_scaling_factor, bf16_points=shape.act_dtype == 1)
+        done_s += time.perf_counter() - t0
+        done_t += rows.shape[0]
+        if done_s >= budget_s or done_t >= xn.shape[0]:
+            break
+        n = min(2 * n, xn.shape[0] - done_t)
+    return done_t / done_s, done_t, done_s
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores, as the reference arm."""
+    if rank != 0:
+        return None
+    import torch
+    from synth import WORKLOADS, make_weights, make_x
+    shape = WORKLOADS[args.workload]
+    T = args.tokens
+    w = make_weights(shape, "cpu")
+    x = make_x(shape, T, "cpu")
+    budget = 150.0
+    per_step = []
+    t_start = time.perf_counter()
+    steps_done = 0
+    for i in range(args.warmup + args.steps):
+        tps, nt, secs = time_oracle(shape, w, x[i % T:][:1], 0.0)
+        if i >= args.warmup:
+            per_step.append(secs / nt)
+            steps_done += 1
+        if time.perf_counter() - t_start > budget and steps_done >= 1:
+            break
+    s_per_tok = sum(per_step) / len(per_step)
+    value = 1.0 / s_per_tok
+    line = {
+        "impl": "reference", "metric": "MoE-layer tokens/s", "value": round(value, 3), "unit": "tokens/s",
+        "n_gpus": 0, "steps": steps_done, "warmup": args.warmup, "ms_per_step": round(s_per_tok * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{shape.name} T={T}", "sample": "one token of the batch per step"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{steps_done} steps of 1 token ({shape.name}, T={T} batch rows)"},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local)
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    r = run_ours(args, rank, world, dev)
+    shape = r["shape"]
+    T = r["T"]
+    pk = r["peaks"]
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from synth import make_weights, make_x
+        # same workload on the host: weights drawn on the CPU (same recipe), oracle timed on a bounded sample
+        wc = make_weights(shape, "cpu")
+        xc = make_x(shape, T, "cpu")
+        tps, nt, secs = time_oracle(shape, wc, xc, 12.0)
+        cpu = {"value": round(tps, 3), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{nt} of the {T} tokens of one {shape.name} batch, {secs:.1f} s"}
+    lb = r["bytes"]
+    ab = 2 if shape.act_dtype != 0 else 4
+    if rank == 0:
+        frac_up = r["achieved_up"] / pk["hbm_gbs"]
+        layer_gbs = lb["total"] / (r["ms_per_step"] / 1e3) / 1e9
+        line = {
+            "metric": "MoE-layer tokens/s", "value": round(r["value"], 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(r["ms_per_step"], 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if shape.act_dtype else "f32", "data": "synthetic",
+            "config": {"workload": f"{shape.name} T={T}", "tokens_per_step_per_gpu": T,
+                       "d_model": shape.d_model, "experts": shape.n_experts, "top_k": shape.top_k,
+                       "d_expert": shape.d_expert, "d_shared": shape.d_shared, "d_latent": shape.d_latent,
+                       "parallelism": f"replicas x{world}",
+                       "l2": f"weights rotate over {r['n_rep']} seeded replicas "
+                             f"({r['rep_bytes'] / 1e9:.2f} GB each); no step reads the previous step's weights",
+                       "experts_active": r["n_active"]},
+            "roofline": {"bound": "hbm", "kernel": "grouped expert up projection (moe_experts_up)",
+                         "achieved": round(r["achieved_up"], 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(frac_up, 4), "traffic": None,
+                         "algorithmic_bytes_per_launch": int(r["up_bytes"]),
+                         "avg_launch_ms": round(r["ms_up"], 5), "peak_source": pk["source"] + " (burst copy)"},
+            "layer_roofline": {"bound": "hbm", "bytes_per_step": int(lb["total"]),
+                               "achieved": round(layer_gbs, 1), "unit": "GB/s",
+                               "frac": round(layer_gbs / pk["hbm_gbs"], 4), "bytes_breakdown": lb},
+            "clocks": r["clocks"],
+            "gpu_launches": r["launches"],
+            "device_error_word": r["err"],
+            "e2e": {"value": round(world * T / r["e2e_s"], 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": T * shape.d_model * ab, "d2h_bytes_per_step": T * shape.d_model * ab,
+                    "api": "moe_layer_forward_host (pinned host x and y)"},
+            "cpu_baseline": cpu,
+        }
+        if r["sweep"]:
+            line["per_T"] = r["sweep"]
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

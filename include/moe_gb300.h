@@ -1,0 +1,232 @@
+/*
+ * moe_gb300.h -- C ABI of the routed ReLU^2 mixture-of-experts layer
+ * (NemotronH-style MoE feed-forward block), hand-written CUDA for sm_103a.
+ *
+ * The layer, for hidden rows x[T, d]:
+ *   (latent shapes)  x_e = bf16(x W_ld^T)                       [T, L]      else x_e = x
+ *   router           z = x W_r^T (FP32), s = sigmoid(z) (FP32),
+ *                    group-limited top-K on c = s + b, weights from s,
+ *                    normalised, times routed_scaling_factor
+ *   dispatch         per-expert counts, exclusive scan, routes sorted by
+ *                    (expert, token, slot)
+ *   experts          h = bf16(relu(bf16(x_e W_up,e^T))^2);  u = w * (h W_down,e^T)  (FP32)
+ *   combine          y_r[t] = sum of t's routed rows in ascending expert id (FP32)
+ *   shared + output  y_s = W_sd bf16(relu(bf16(W_su x))^2)  (FP32)
+ *                    y = bf16(y_r + y_s)                       (no latent)
+ *                    y = bf16(bf16(y_r) W_lu^T + y_s)          (latent)
+ * Sources: page "Nemotron Is Not One Circuit: Mamba, Attention, and MoE
+ * Routing" (sections "The Four Layer Kinds CKE Must Preserve", "The Router Is
+ * A Deterministic Algorithm", "The C Kernel Contract"); page "M6.1 - Routed
+ * Capacity: MoE Experts, Routers, and Token Dispatch" (sections 0x04A,
+ * 0x05A-0x05F); page "NemotronH (Nemotron 3.5 Lightning, Bolt, Super VL)"
+ * (section "Arithmetic"); page "Nemotron-3.5-Super 120B on an 8 GB GPU"
+ * (section "The only number that matters", latent experts; section "The
+ * engine, step by step", item 4, NVFP4 block scales).
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers unless stated otherwise, allocated and owned
+ *    by the caller; the library never allocates, frees or synchronises (except
+ *    moe_get_device_error and the _host convenience call).  Every call only
+ *    enqueues work on `stream` (a cudaStream_t passed as void*; NULL = the
+ *    legacy default stream) and returns.
+ *  - Row-major storage.  Weight matrices are stored [out, in] (the
+ *    nn.Linear orientation, page "M6.1 ...", section 0x04A).
+ *  - Every device pointer must be 16-byte aligned; every inner width
+ *    (d_model, d_latent, d_expert, d_shared) a multiple of 64.
+ *  - Argument and shape errors are returned before anything is enqueued.
+ *    A failed launch returns MOE_ERR_CUDA.  Conditions only the device can see
+ *    (an expert id out of range, a non-finite router score) set bits of the
+ *    device error word held in the workspace; read it with
+ *    moe_get_device_error.  Kernels never trap or assert.
+ *  - Outputs are overwritten, never accumulated into.
+ *  - Results are bit-identical from run to run for the same inputs and T
+ *    (no floating-point atomics; every sum has a fixed order).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t moe_status_t;
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape or parameter */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid but not built (e.g. a width not a multiple of 64) */
+  MOE_ERR_WORKSPACE = 3,    /* workspace smaller than moe_workspace_bytes() */
+  MOE_ERR_CUDA = 4,         /* a CUDA call or launch failed */
+  MOE_ERR_DEVICE = 5        /* moe_get_device_error found a device-side error bit */
+};
+
+/* device error word bits (moe_get_device_error) */
+enum {
+  MOE_DEVERR_EXPERT_ID = 1,      /* an expert id outside [0, n_experts) reached dispatch */
+  MOE_DEVERR_NONFINITE = 2,      /* a router score was NaN (ranked last, never chosen before a finite one) */
+  MOE_DEVERR_SCHEDULE = 4        /* a tile schedule disagreed with the dispatch offsets */
+};
+
+typedef int32_t moe_dtype_t;
+enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1, MOE_DT_NVFP4 = 2 };
+
+typedef struct moe_config {
+  int32_t d_model;       /* d: hidden width */
+  int32_t d_latent;      /* L: latent width the experts act on; 0 = experts act on d */
+  int32_t n_experts;     /* E: routed experts, 1..1024 */
+  int32_t top_k;         /* K: experts per token, 1..min(E, 32) */
+  int32_t n_group;       /* G: equal contiguous expert groups (E % G == 0) */
+  int32_t topk_group;    /* TG: groups kept per token, 1..G */
+  int32_t d_expert;      /* I: routed expert intermediate width */
+  int32_t d_shared;      /* S: shared expert intermediate width; 0 = no shared expert */
+  int32_t norm_topk_prob;          /* 1: chosen weights normalised to sum 1 before scaling */
+  float routed_scaling_factor;     /* multiplies the (normalised) chosen weights */
+  moe_dtype_t act_dtype;           /* MOE_DT_BF16 or MOE_DT_F32 (activations, dense weights) */
+  moe_dtype_t expert_dtype;        /* MOE_DT_BF16, MOE_DT_F32 (with F32 activations) or MOE_DT_NVFP4 */
+} moe_config_t;
+
+/* Weights of one layer (device pointers, row-major [out, in]).  de = L if L>0 else d.
+ * Dense tensors use act_dtype; routed experts use expert_dtype.               */
+typedef struct moe_weights {
+  const float* w_router;      /* [E, d]  FP32 router matrix                                  */
+  const float* router_bias;   /* [E]     FP32 selection bias, or NULL (choice only)          */
+  const void* w_lat_down;     /* [L, d]  latent down (latent shapes only)                    */
+  const void* w_lat_up;       /* [d, L]  latent up   (latent shapes only)                    */
+  const void* w_up;           /* [E, I, de] expert up   (BF16/F32) or NVFP4 packed [E, I, de/2] u8   */
+  const void* w_down;         /* [E, de, I] expert down (BF16/F32) or NVFP4 packed [E, de, I/2] u8   */
+  const uint8_t* w_up_sf;     /* NVFP4: E4M3 block scales [E, I, de/16], one per 16 K-elements       */
+  const uint8_t* w_down_sf;   /* NVFP4: E4M3 block scales [E, de, I/16]                              */
+  const float* w_up_gs;       /* NVFP4: FP32 per-tensor scale [E]                                    */
+  const float* w_down_gs;     /* NVFP4: FP32 per-tensor scale [E]                                    */
+  const void* w_sh_up;        /* [S, d] shared expert up   (S > 0)                                    */
+  const void* w_sh_down;      /* [d, S] shared expert down (S > 0)                                    */
+} moe_weights_t;
+
+/* Library version, e.g. 100 for 0.1.0.  Never fails. */
+int32_t moe_version(void);
+
+/* Short static description of a status code.  Never fails. */
+const char* moe_status_string(moe_status_t s);
+
+/* Validates a configuration without touching any pointer. */
+moe_status_t moe_check_config(const moe_config_t* cfg);
+
+/* Bytes of device workspace moe_layer_forward needs for T tokens (0 on an
+ * invalid configuration).  The same workspace serves every step entry point;
+ * its first 256 bytes hold the device error word and the expert schedule that
+ * moe_dispatch leaves for moe_experts_up / moe_experts_down_combine. */
+size_t moe_workspace_bytes(const moe_config_t* cfg, int32_t T);
+
+/* Step 1: router (page "Nemotron Is Not One Circuit", sections "The Router Is
+ * A Deterministic Algorithm" and "The C Kernel Contract"; page "NemotronH ...",
+ * section "Arithmetic", router bullet).
+ *   x        [T, d] act_dtype hidden rows (BF16 values enter FP32 exactly)
+ *   logits   [T, E] FP32 out: z = x W_r^T, or NULL (kept in the workspace)
+ *   scores   [T, E] FP32 out: s = sigmoid(z), or NULL
+ *   topk_ids [T, K] int32 out: chosen experts, best biased score first,
+ *            equal scores to the lower id
+ *   topk_w   [T, K] FP32 out: s of the chosen experts, normalised (if
+ *            configured) then times routed_scaling_factor                   */
+moe_status_t moe_router(const moe_config_t* cfg, int32_t T, const void* x,
+                        const float* w_router, const float* router_bias,
+                        float* logits, float* scores, int32_t* topk_ids, float* topk_w,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/* Step 2: dispatch (page "M6.1 ...", sections 0x05A "The Route Row Is The
+ * Reversible Unit" and 0x05B).  Routes r = (token t, slot k) are laid out
+ * expert-contiguously, sorted by (expert, token, slot); no atomics.
+ *   topk_ids       [T, K] int32 in
+ *   x_e            [T, de] act_dtype rows to pack (x, or the latent rows), or NULL
+ *   counts         [E] int32 out: routes per expert
+ *   offsets        [E+1] int32 out: exclusive prefix sum of counts
+ *   route_token    [T*K] int32 out: token of each packed row
+ *   route_slot     [T*K] int32 out: slot of each packed row
+ *   token_slot_row [T, K] int32 out: packed row of route (t, k)
+ *   x_packed       [T*K, de] out: x_packed[j] = x_e[route_token[j]], or NULL
+ * Also leaves the expert schedule in the workspace header.                   */
+moe_status_t moe_dispatch(const moe_config_t* cfg, int32_t T, const int32_t* topk_ids,
+                          const void* x_e, int32_t* counts, int32_t* offsets,
+                          int32_t* route_token, int32_t* route_slot, int32_t* token_slot_row,
+                          void* x_packed, void* ws, size_t ws_bytes, void* stream);
+
+/* Step 3: expert up projections with squared ReLU, no gate (page "NemotronH
+ * ...", section "Arithmetic": bf16(relu(bf16(up x))^2)).
+ *   x_e         [T, de] rows the experts read (gathered through route_token),
+ *               ignored when x_packed is given
+ *   x_packed    [T*K, de] packed rows from moe_dispatch, or NULL
+ *   route_token, offsets: from moe_dispatch (same workspace)
+ *   h           [T*K, I] out, packed order; BF16 (F32 for F32 layers)        */
+moe_status_t moe_experts_up(const moe_config_t* cfg, int32_t T, const void* x_e,
+                            const void* x_packed, const int32_t* route_token,
+                            const int32_t* offsets, const moe_weights_t* w, void* h,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* Steps 4+5: expert down projections, times the routing weight, and the
+ * combine: y_routed[t] = sum over t's routes in ascending expert id of
+ * w_tk * (h_r W_down,e^T), all FP32 (page "NemotronH ...", section
+ * "Arithmetic"; page "M6.1 ...", section 0x05B, weighted scatter-add).
+ *   h              [T*K, I] from moe_experts_up
+ *   route_token, route_slot, token_slot_row, offsets: from moe_dispatch
+ *   topk_w         [T, K] FP32 from moe_router
+ *   y_routed       [T, de] FP32 out                                         */
+moe_status_t moe_experts_down_combine(const moe_config_t* cfg, int32_t T, const void* h,
+                                      const int32_t* offsets, const int32_t* route_token,
+                                      const int32_t* route_slot, const int32_t* token_slot_row,
+                                      const float* topk_w, const moe_weights_t* w,
+                                      float* y_routed, void* ws, size_t ws_bytes, void* stream);
+
+/* Latent down projection of latent shapes: x_l = bf16(x W_ld^T), FP32
+ * accumulation (page "Nemotron-3.5-Super 120B on an 8 GB GPU", section "The
+ * only number that matters": experts work in a 1024-wide latent space).
+ *   x [T, d] in, x_l [T, L] out (act_dtype).                                  */
+moe_status_t moe_latent_down(const moe_config_t* cfg, int32_t T, const void* x,
+                             const moe_weights_t* w, void* x_l,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* Shared expert and output (page "Nemotron Is Not One Circuit", section "The
+ * Four Layer Kinds CKE Must Preserve": routed experts + shared expert).
+ *   x        [T, d] hidden rows
+ *   y_routed [T, de] FP32 combined routed output, or NULL (treated as zero)
+ *   y        [T, d] act_dtype out: bf16(y_routed + y_s), or for latent shapes
+ *            bf16(bf16(y_routed) W_lu^T + y_s); y_s = 0 when S == 0        */
+moe_status_t moe_shared(const moe_config_t* cfg, int32_t T, const void* x,
+                        const moe_weights_t* w, const float* y_routed, void* y,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/* The whole layer, every step above on `stream`, intermediates in `ws`.
+ *   x [T, d] in; y [T, d] out (act_dtype).
+ *   topk_ids_out [T,K] / topk_w_out [T,K] / logits_out [T,E] / scores_out [T,E]:
+ *   optional copies of the router's results (NULL = not written).
+ * Clears the device error word first.                                        */
+moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x,
+                               const moe_weights_t* w, void* y,
+                               int32_t* topk_ids_out, float* topk_w_out,
+                               float* logits_out, float* scores_out,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, copies the device error word of `ws` to *code (host
+ * pointer) and returns MOE_ERR_DEVICE if any bit is set, else MOE_OK.         */
+moe_status_t moe_get_device_error(const void* ws, void* stream, int32_t* code);
+
+/* Enqueues a clear of the device error word. */
+moe_status_t moe_clear_device_error(void* ws, void* stream);
+
+/* Number of kernel launches this library has enqueued in this process (a host
+ * counter, incremented once per kernel launch; memset and copy operations are
+ * not counted).  Never fails. */
+int64_t moe_launch_count(void);
+
+/* End-to-end convenience call with HOST buffers: copies x_host [T, d] to
+ * x_dev, runs moe_layer_forward, copies y to y_host and synchronises the
+ * stream.  x_dev / y_dev / ws are caller-owned device buffers; the host
+ * buffers should be pinned for asynchronous copies.                          */
+moe_status_t moe_layer_forward_host(const moe_config_t* cfg, int32_t T, const void* x_host,
+                                    void* x_dev, const moe_weights_t* w, void* y_dev,
+                                    void* y_host, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

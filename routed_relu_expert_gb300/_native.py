@@ -1,0 +1,101 @@
+"""ctypes binding of the C ABI declared in include/moe_gb300.h.
+
+Argument marshalling only: every step of the layer runs in the CUDA library.
+If the shared library is missing the import of any entry point fails loudly;
+there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libmoe_gb300.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(6)
+MOE_DEVERR_EXPERT_ID, MOE_DEVERR_NONFINITE, MOE_DEVERR_SCHEDULE = 1, 2, 4
+MOE_DT_F32, MOE_DT_BF16, MOE_DT_NVFP4 = 0, 1, 2
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [
+        ("d_model", ctypes.c_int32),
+        ("d_latent", ctypes.c_int32),
+        ("n_experts", ctypes.c_int32),
+        ("top_k", ctypes.c_int32),
+        ("n_group", ctypes.c_int32),
+        ("topk_group", ctypes.c_int32),
+        ("d_expert", ctypes.c_int32),
+        ("d_shared", ctypes.c_int32),
+        ("norm_topk_prob", ctypes.c_int32),
+        ("routed_scaling_factor", ctypes.c_float),
+        ("act_dtype", ctypes.c_int32),
+        ("expert_dtype", ctypes.c_int32),
+    ]
+
+
+class MoeWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "w_router", "router_bias", "w_lat_down", "w_lat_up", "w_up", "w_down",
+        "w_up_sf", "w_down_sf", "w_up_gs", "w_down_gs", "w_sh_up", "w_sh_down")]
+
+
+EXPORTS = (
+    "moe_version", "moe_status_string", "moe_check_config", "moe_workspace_bytes", "moe_router",
+    "moe_dispatch", "moe_experts_up", "moe_experts_down_combine", "moe_latent_down", "moe_shared",
+    "moe_layer_forward", "moe_get_device_error", "moe_clear_device_error", "moe_layer_forward_host",
+    "moe_launch_count",
+)
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                           "(run python -m routed_relu_expert_gb300.build)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.c_void_p
+    I32 = ctypes.c_int32
+    S = ctypes.c_size_t
+    CFG = ctypes.POINTER(MoeConfig)
+    W = ctypes.POINTER(MoeWeights)
+    sig = {
+        "moe_version": (I32, []),
+        "moe_status_string": (ctypes.c_char_p, [I32]),
+        "moe_check_config": (I32, [CFG]),
+        "moe_workspace_bytes": (S, [CFG, I32]),
+        "moe_router": (I32, [CFG, I32, P, P, P, P, P, P, P, P, S, P]),
+        "moe_dispatch": (I32, [CFG, I32, P, P, P, P, P, P, P, P, P, S, P]),
+        "moe_experts_up": (I32, [CFG, I32, P, P, P, P, W, P, P, S, P]),
+        "moe_experts_down_combine": (I32, [CFG, I32, P, P, P, P, P, P, W, P, P, S, P]),
+        "moe_latent_down": (I32, [CFG, I32, P, W, P, P, S, P]),
+        "moe_shared": (I32, [CFG, I32, P, W, P, P, P, S, P]),
+        "moe_layer_forward": (I32, [CFG, I32, P, W, P, P, P, P, P, P, S, P]),
+        "moe_get_device_error": (I32, [P, P, ctypes.POINTER(I32)]),
+        "moe_clear_device_error": (I32, [P, P]),
+        "moe_layer_forward_host": (I32, [CFG, I32, P, P, W, P, P, P, S, P]),
+        "moe_launch_count": (ctypes.c_int64, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = load().moe_status_string(status).decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+        self.status = status
+
+
+def check(status: int, where: str) -> None:
+    if status != MOE_OK:
+        raise MoEError(status, where)

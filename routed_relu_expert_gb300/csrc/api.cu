@@ -1,0 +1,411 @@
+// C ABI of the routed ReLU^2 MoE layer: argument checks, workspace layout and
+// the order of the steps.  Every kernel launch goes to the caller's stream.
+#include "internal.h"
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+using namespace moe;
+
+namespace moe {
+static std::atomic<int64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace moe
+
+namespace {
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kMaxGroups = 32;
+constexpr int64_t kMaxRoutes = (int64_t)1 << 28;
+
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+inline int act_bytes(const moe_config_t* c) { return c->act_dtype == MOE_DT_F32 ? 4 : 2; }
+inline int de_of(const moe_config_t* c) { return c->d_latent > 0 ? c->d_latent : c->d_model; }
+
+struct Layout {
+  size_t hdr, logits, scores, ids, topw, counts, offsets, active, tile_prefix;
+  size_t route_token, route_slot, tsr, x_l, x_packed, h, u, y_r, y_rl, hs, ys, tile_counts, total;
+};
+
+inline size_t take(size_t& off, size_t bytes) {
+  off = (off + 255) & ~(size_t)255;
+  const size_t o = off;
+  off += bytes;
+  return o;
+}
+
+Layout make_layout(const moe_config_t* c, int32_t T) {
+  Layout L{};
+  const size_t t = (size_t)T, E = c->n_experts, K = c->top_k, R = t * K;
+  const size_t de = de_of(c), ab = act_bytes(c);
+  size_t off = 0;
+  L.hdr = take(off, sizeof(WsHeader));
+  L.logits = take(off, t * E * 4);
+  L.scores = take(off, t * E * 4);
+  L.ids = take(off, R * 4);
+  L.topw = take(off, R * 4);
+  L.counts = take(off, E * 4);
+  L.offsets = take(off, (E + 1) * 4);
+  L.active = take(off, E * 4);
+  L.tile_prefix = take(off, (E + 1) * 4);
+  L.route_token = take(off, R * 4);
+  L.route_slot = take(off, R * 4);
+  L.tsr = take(off, R * 4);
+  L.x_l = take(off, c->d_latent > 0 ? t * c->d_latent * ab : 0);
+  L.x_packed = take(off, R * de * ab);
+  L.h = take(off, R * (size_t)c->d_expert * ab);
+  L.u = take(off, R * de * 4);
+  L.y_r = take(off, t * de * 4);
+  L.y_rl = take(off, c->d_latent > 0 ? t * de * ab : 0);
+  L.hs = take(off, t * (size_t)c->d_shared * ab);
+  L.ys = take(off, t * (size_t)c->d_model * 4);
+  L.tile_counts = take(off, dispatch_tile_count_elems(T, c->top_k, c->n_experts) * 4);
+  L.total = (off + 255) & ~(size_t)255;
+  return L;
+}
+
+moe_status_t check_config(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  const int E = c->n_experts, K = c->top_k, G = c->n_group, TG = c->topk_group;
+  if (c->d_model <= 0 || c->d_expert <= 0 || c->d_latent < 0 || c->d_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || E > kMaxExperts) return MOE_ERR_INVALID_ARG;
+  if (K < 1 || K > E || K > kMaxTopK) return MOE_ERR_INVALID_ARG;
+  if (G < 1 || G > kMaxGroups || E % G != 0 || TG < 1 || TG > G) return MOE_ERR_INVALID_ARG;
+  if (G > 1 && E / G < 2) return MOE_ERR_INVALID_ARG;          // a group score needs two members
+  if ((int64_t)K > (int64_t)TG * (E / G)) return MOE_ERR_INVALID_ARG;
+  if (c->norm_topk_prob != 0 && c->norm_topk_prob != 1) return MOE_ERR_INVALID_ARG;
+  if (!std::isfinite(c->routed_scaling_factor)) return MOE_ERR_INVALID_ARG;
+  if (c->act_dtype != MOE_DT_F32 && c->act_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->expert_dtype != MOE_DT_F32 && c->expert_dtype != MOE_DT_BF16 && c->expert_dtype != MOE_DT_NVFP4)
+    return MOE_ERR_INVALID_ARG;
+  if ((c->expert_dtype == MOE_DT_F32) != (c->act_dtype == MOE_DT_F32)) return MOE_ERR_UNSUPPORTED;
+  if (c->d_model % 64 || c->d_expert % 64 || c->d_latent % 64 || c->d_shared % 64) return MOE_ERR_UNSUPPORTED;
+  if (c->expert_dtype == MOE_DT_NVFP4) return MOE_ERR_UNSUPPORTED;   // NVFP4 kernels: not built yet
+  return MOE_OK;
+}
+
+moe_status_t check_common(const moe_config_t* c, int32_t T, const void* ws, size_t ws_bytes) {
+  moe_status_t st = check_config(c);
+  if (st != MOE_OK) return st;
+  if (T < 0 || (int64_t)T * c->top_k > kMaxRoutes) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < make_layout(c, T).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+#define REQ(p) do { if (!(p) || !aligned16(p)) return MOE_ERR_INVALID_ARG; } while (0)
+#define OPT(p) do { if ((p) && !aligned16(p)) return MOE_ERR_INVALID_ARG; } while (0)
+#define CU(x) do { if ((x) != cudaSuccess) return MOE_ERR_CUDA; } while (0)
+
+inline int wfmt_of(const moe_config_t* c) {
+  return c->expert_dtype == MOE_DT_F32 ? WF_F32 : (c->expert_dtype == MOE_DT_NVFP4 ? WF_NVFP4 : WF_BF16);
+}
+inline int dense_fmt(const moe_config_t* c) { return c->act_dtype == MOE_DT_F32 ? WF_F32 : WF_BF16; }
+
+GemvArgs dense_args(const void* W, int N, int K, const void* X, int rows, void* out, int64_t out_ld) {
+  GemvArgs a{};
+  a.W = W; a.N = N; a.K = K; a.X = X; a.x_ld = K; a.dense_rows = rows;
+  a.out = out; a.out_ld = out_ld;
+  return a;
+}
+
+struct Ptrs {
+  char* base;
+  Layout L;
+  template <class T> T* at(size_t o) const { return reinterpret_cast<T*>(base + o); }
+  WsHeader* hdr() const { return at<WsHeader>(L.hdr); }
+};
+
+// ---- steps -----------------------------------------------------------------
+moe_status_t run_router(const moe_config_t* c, int T, const void* x, const float* w_router, const float* bias,
+                        float* logits, float* scores, int32_t* ids, float* w, const Ptrs& P, cudaStream_t s) {
+  CU(launch_router_logits(x, c->act_dtype, T, c->d_model, w_router, c->n_experts, logits, s));
+  CU(launch_router_select(logits, T, c->n_experts, bias, c->n_group, c->topk_group, c->top_k,
+                          c->norm_topk_prob, c->routed_scaling_factor, scores, ids, w, &P.hdr()->err, s));
+  return MOE_OK;
+}
+
+moe_status_t run_dispatch(const moe_config_t* c, int T, const int32_t* ids, const void* x_e, int32_t* counts,
+                          int32_t* offsets, int32_t* rt, int32_t* rs, int32_t* tsr, void* x_packed,
+                          const Ptrs& P, cudaStream_t s) {
+  DispatchArgs a{};
+  a.ids = ids; a.T = T; a.K = c->top_k; a.E = c->n_experts;
+  a.counts = counts; a.offsets = offsets; a.route_token = rt; a.route_slot = rs; a.token_slot_row = tsr;
+  a.active = P.at<int32_t>(P.L.active);
+  a.hdr = P.hdr();
+  a.tile_counts = P.at<int32_t>(P.L.tile_counts);
+  a.tile_prefix = P.at<int32_t>(P.L.tile_prefix);
+  a.tile_rows = 0;
+  a.x_e = x_e; a.x_packed = x_e ? x_packed : nullptr;
+  a.de = de_of(c); a.elem_bytes = act_bytes(c);
+  CU(launch_dispatch(a, s));
+  return MOE_OK;
+}
+
+moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x_packed, const int32_t* rt,
+                    const int32_t* offsets, const moe_weights_t* w, void* h, const Ptrs& P, cudaStream_t s) {
+  const int de = de_of(c), I = c->d_expert;
+  GemvArgs a{};
+  a.W = w->w_up; a.w_seg_stride = (int64_t)I * de; a.N = I; a.K = de;
+  a.X = x_packed ? x_packed : x_e; a.x_ld = de; a.gather = x_packed ? nullptr : rt;
+  a.offsets = offsets; a.active = P.at<int32_t>(P.L.active); a.hdr = P.hdr();
+  a.out = h; a.out_ld = I; a.err = &P.hdr()->err;
+  const int segs = (int)std::min<int64_t>(c->n_experts, (int64_t)T * c->top_k);
+  CU(launch_gemv(a, wfmt_of(c), c->act_dtype, EPI_RELU2, c->act_dtype == MOE_DT_F32, T, segs, s));
+  return MOE_OK;
+}
+
+moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t* offsets, const int32_t* rt,
+                      const int32_t* rs, const float* topw, const moe_weights_t* w, float* u, const Ptrs& P,
+                      cudaStream_t s) {
+  const int de = de_of(c), I = c->d_expert;
+  GemvArgs a{};
+  a.W = w->w_down; a.w_seg_stride = (int64_t)de * I; a.N = de; a.K = I;
+  a.X = h; a.x_ld = I;
+  a.offsets = offsets; a.active = P.at<int32_t>(P.L.active); a.hdr = P.hdr();
+  a.out = u; a.out_ld = de;
+  a.topw = topw; a.route_token = rt; a.route_slot = rs; a.top_k = c->top_k; a.err = &P.hdr()->err;
+  const int segs = (int)std::min<int64_t>(c->n_experts, (int64_t)T * c->top_k);
+  CU(launch_gemv(a, wfmt_of(c), c->act_dtype, EPI_SCALE, true, T, segs, s));
+  return MOE_OK;
+}
+
+moe_status_t run_latent_down(const moe_config_t* c, int T, const void* x, const moe_weights_t* w, void* x_l,
+                             cudaStream_t s) {
+  GemvArgs a = dense_args(w->w_lat_down, c->d_latent, c->d_model, x, T, x_l, c->d_latent);
+  CU(launch_gemv(a, dense_fmt(c), c->act_dtype, EPI_STORE, false, T, 1, s));
+  return MOE_OK;
+}
+
+// shared expert + output; y_rl = act-typed routed latent rows (latent shapes, may be null)
+moe_status_t run_shared(const moe_config_t* c, int T, const void* x, const moe_weights_t* w, const float* y_r,
+                        const void* y_rl, void* y, const Ptrs& P, cudaStream_t s) {
+  const int d = c->d_model, S = c->d_shared;
+  const bool latent = c->d_latent > 0;
+  const bool f32 = c->act_dtype == MOE_DT_F32;
+  if (S > 0) {
+    void* hs = P.at<void>(P.L.hs);
+    GemvArgs up = dense_args(w->w_sh_up, S, d, x, T, hs, S);
+    CU(launch_gemv(up, dense_fmt(c), c->act_dtype, EPI_RELU2, f32, T, 1, s));
+    GemvArgs dn = dense_args(w->w_sh_down, d, S, hs, T, nullptr, d);
+    if (!latent) {
+      dn.out = y; dn.add_src = y_r; dn.add_ld = d;
+      CU(launch_gemv(dn, dense_fmt(c), c->act_dtype, EPI_ADD, f32, T, 1, s));
+      return MOE_OK;
+    }
+    dn.out = P.at<void>(P.L.ys);
+    CU(launch_gemv(dn, dense_fmt(c), c->act_dtype, EPI_STORE, true, T, 1, s));
+  } else if (!latent) {
+    // no shared expert: y = act(y_r); a combine over one row per token is a cast
+    CU(launch_cast(y_r, (int64_t)T * d, y, c->act_dtype, s));
+    return MOE_OK;
+  }
+  // latent up: y = act(act(y_r) W_lu^T + y_s)
+  const void* yl = y_rl;
+  if (!yl) {
+    void* tmp = P.at<void>(P.L.y_rl);
+    CU(launch_cast(y_r, (int64_t)T * c->d_latent, tmp, c->act_dtype, s));
+    yl = tmp;
+  }
+  GemvArgs lu = dense_args(w->w_lat_up, d, c->d_latent, yl, T, y, d);
+  lu.add_src = S > 0 ? P.at<float>(P.L.ys) : nullptr;
+  lu.add_ld = d;
+  CU(launch_gemv(lu, dense_fmt(c), c->act_dtype, EPI_ADD, f32, T, 1, s));
+  return MOE_OK;
+}
+
+moe_status_t check_weights(const moe_config_t* c, const moe_weights_t* w, bool experts, bool router, bool dense) {
+  if (!w) return MOE_ERR_INVALID_ARG;
+  if (router) { REQ(w->w_router); OPT(w->router_bias); }
+  if (experts) { REQ(w->w_up); REQ(w->w_down); }
+  if (dense) {
+    if (c->d_latent > 0) { REQ(w->w_lat_down); REQ(w->w_lat_up); }
+    if (c->d_shared > 0) { REQ(w->w_sh_up); REQ(w->w_sh_down); }
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+// ============================================================================
+extern "C" {
+
+int32_t moe_version(void) { return 100; }
+
+int64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE: return "device-side error flag set";
+    default: return "unknown status";
+  }
+}
+
+moe_status_t moe_check_config(const moe_config_t* cfg) { return check_config(cfg); }
+
+size_t moe_workspace_bytes(const moe_config_t* cfg, int32_t T) {
+  if (check_config(cfg) != MOE_OK || T < 0) return 0;
+  return make_layout(cfg, T).total;
+}
+
+moe_status_t moe_router(const moe_config_t* cfg, int32_t T, const void* x, const float* w_router,
+                        const float* router_bias, float* logits, float* scores, int32_t* topk_ids, float* topk_w,
+                        void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_common(cfg, T, ws, ws_bytes);
+  if (st != MOE_OK || T == 0) return st;
+  REQ(x); REQ(w_router); OPT(router_bias); OPT(logits); OPT(scores); REQ(topk_ids); REQ(topk_w);
+  Ptrs P{(char*)ws, make_layout(cfg, T)};
+  return run_router(cfg, T, x, w_router, router_bias, logits ? logits : P.at<float>(P.L.logits),
+                    scores ? scores : P.at<float>(P.L.scores), topk_ids, topk_w, P, (cudaStream_t)stream);
+}
+
+moe_status_t moe_dispatch(const moe_config_t* cfg, int32_t T, const int32_t* topk_ids, const void* x_e,
+                          int32_t* counts, int32_t* offsets, int32_t* route_token, int32_t* route_slot,
+                          int32_t* token_slot_row, void* x_packed, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_common(cfg, T, ws, ws_bytes);
+  if (st != MOE_OK || T == 0) return st;
+  REQ(topk_ids); OPT(x_e); REQ(counts); REQ(offsets); REQ(route_token); REQ(route_slot); REQ(token_slot_row);
+  OPT(x_packed);
+  if (x_packed && !x_e) return MOE_ERR_INVALID_ARG;
+  Ptrs P{(char*)ws, make_layout(cfg, T)};
+  return run_dispatch(cfg, T, topk_ids, x_e, counts, offsets, route_token, route_slot, token_slot_row, x_packed,
+                      P, (cudaStream_t)stream);
+}
+
+moe_status_t moe_experts_up(const moe_config_t* cfg, int32_t T, const void* x_e, const void* x_packed,
+                            const int32_t* route_token, const int32_t* offsets, const moe_weights_t* w, void* h,
+                            void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_common(cfg, T, ws, ws_bytes);
+  if (st != MOE_OK || T == 0) return st;
+  if ((st = check_weights(cfg, w, true, false, false)) != MOE_OK) return st;
+  OPT(x_e); OPT(x_packed); REQ(route_token); REQ(offsets); REQ(h);
+  if (!x_e && !x_packed) return MOE_ERR_INVALID_ARG;
+  Ptrs P{(char*)ws, make_layout(cfg, T)};
+  return run_up(cfg, T, x_e, x_packed, route_token, offsets, w, h, P, (cudaStream_t)stream);
+}
+
+moe_status_t moe_experts_down_combine(const moe_config_t* cfg, int32_t T, const void* h, const int32_t* offsets,
+                                      const int32_t* route_token, const int32_t* route_slot,
+                                      const int32_t* token_slot_row, const float* topk_w, const moe_weights_t* w,
+                                      float* y_routed, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_common(cfg, T, ws, ws_bytes);
+  if (st != MOE_OK || T == 0) return st;
+  if ((st = check_weights(cfg, w, true, false, false)) != MOE_OK) return st;
+  REQ(h); REQ(offsets); REQ(route_token); REQ(route_slot); REQ(token_slot_row); REQ(topk_w); REQ(y_routed);
+  Ptrs P{(char*)ws, make_layout(cfg, T)};
+  cudaStream_t s = (cudaStream_t)stream;
+  float* u = P.at<float>(P.L.u);
+  if ((st = run_down(cfg, T, h, offsets, route_token, route_slot, topk_w, w, u, P, s)) != MOE_OK) return st;
+  CU(launch_combine(u, token_slot_row, T, cfg->top_k, de_of(cfg), y_routed, nullptr, cfg->act_dtype, s));
+  return MOE_OK;
+}
+
+moe_status_t moe_latent_down(const moe_config_t* cfg, int32_t T, const void* x, const moe_weights_t* w, void* x_l,
+                             void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_common(cfg, T, ws, ws_bytes);
+  if (st != MOE_OK || T == 0) return st;
+  if (cfg->d_latent <= 0) return MOE_ERR_INVALID_ARG;
+  if (!w) return MOE_ERR_INVALID_ARG;
+  REQ(x); REQ(w->w_lat_down); REQ(x_l);
+  return run_latent_down(cfg, T, x, w, x_l, (cudaStream_t)stream);
+}
+
+moe_status_t moe_shared(const moe_config_t* cfg, int32_t T, const void* x, const moe_weights_t* w,
+                        const float* y_routed, void* y, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_common(cfg, T, ws, ws_bytes);
+  if (st != MOE_OK || T == 0) return st;
+  if ((st = check_weights(cfg, w, false, false, true)) != MOE_OK) return st;
+  REQ(x); OPT(y_routed); REQ(y);
+  Ptrs P{(char*)ws, make_layout(cfg, T)};
+  cudaStream_t s = (cudaStream_t)stream;
+  const float* yr = y_routed;
+  if (!yr) {
+    // no routed output: treat as zero
+    float* z = P.at<float>(P.L.y_r);
+    CU(cudaMemsetAsync(z, 0, (size_t)T * de_of(cfg) * 4, s));
+    yr = z;
+  }
+  return run_shared(cfg, T, x, w, yr, nullptr, y, P, s);
+}
+
+moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x, const moe_weights_t* w, void* y,
+                               int32_t* topk_ids_out, float* topk_w_out, float* logits_out, float* scores_out,
+                               void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_common(cfg, T, ws, ws_bytes);
+  if (st != MOE_OK || T == 0) return st;
+  if ((st = check_weights(cfg, w, true, true, true)) != MOE_OK) return st;
+  REQ(x); REQ(y); OPT(topk_ids_out); OPT(topk_w_out); OPT(logits_out); OPT(scores_out);
+  Ptrs P{(char*)ws, make_layout(cfg, T)};
+  cudaStream_t s = (cudaStream_t)stream;
+  CU(cudaMemsetAsync(P.hdr(), 0, sizeof(WsHeader), s));
+  const void* x_e = x;
+  if (cfg->d_latent > 0) {
+    void* xl = P.at<void>(P.L.x_l);
+    if ((st = run_latent_down(cfg, T, x, w, xl, s)) != MOE_OK) return st;
+    x_e = xl;
+  }
+  float* logits = logits_out ? logits_out : P.at<float>(P.L.logits);
+  float* scores = scores_out ? scores_out : P.at<float>(P.L.scores);
+  int32_t* ids = topk_ids_out ? topk_ids_out : P.at<int32_t>(P.L.ids);
+  float* topw = topk_w_out ? topk_w_out : P.at<float>(P.L.topw);
+  if ((st = run_router(cfg, T, x, w->w_router, w->router_bias, logits, scores, ids, topw, P, s)) != MOE_OK)
+    return st;
+  int32_t* offsets = P.at<int32_t>(P.L.offsets);
+  int32_t* rt = P.at<int32_t>(P.L.route_token);
+  int32_t* rs = P.at<int32_t>(P.L.route_slot);
+  int32_t* tsr = P.at<int32_t>(P.L.tsr);
+  if ((st = run_dispatch(cfg, T, ids, x_e, P.at<int32_t>(P.L.counts), offsets, rt, rs, tsr, nullptr, P, s)) !=
+      MOE_OK)
+    return st;
+  void* h = P.at<void>(P.L.h);
+  if ((st = run_up(cfg, T, x_e, nullptr, rt, offsets, w, h, P, s)) != MOE_OK) return st;
+  float* u = P.at<float>(P.L.u);
+  if ((st = run_down(cfg, T, h, offsets, rt, rs, topw, w, u, P, s)) != MOE_OK) return st;
+  float* y_r = P.at<float>(P.L.y_r);
+  void* y_rl = cfg->d_latent > 0 ? P.at<void>(P.L.y_rl) : nullptr;
+  CU(launch_combine(u, tsr, T, cfg->top_k, de_of(cfg), y_r, y_rl, cfg->act_dtype, s));
+  return run_shared(cfg, T, x, w, y_r, y_rl, y, P, s);
+}
+
+moe_status_t moe_get_device_error(const void* ws, void* stream, int32_t* code) {
+  if (!ws || !code) return MOE_ERR_INVALID_ARG;
+  int32_t v = 0;
+  CU(cudaMemcpyAsync(&v, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, (cudaStream_t)stream));
+  CU(cudaStreamSynchronize((cudaStream_t)stream));
+  *code = v;
+  return v ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+moe_status_t moe_clear_device_error(void* ws, void* stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  CU(cudaMemsetAsync(ws, 0, sizeof(int32_t), (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_forward_host(const moe_config_t* cfg, int32_t T, const void* x_host, void* x_dev,
+                                    const moe_weights_t* w, void* y_dev, void* y_host, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  moe_status_t st = check_common(cfg, T, ws, ws_bytes);
+  if (st != MOE_OK || T == 0) return st;
+  if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  REQ(x_dev); REQ(y_dev);
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t bytes = (size_t)T * cfg->d_model * act_bytes(cfg);
+  CU(cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, s));
+  st = moe_layer_forward(cfg, T, x_dev, w, y_dev, nullptr, nullptr, nullptr, nullptr, ws, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  CU(cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, s));
+  CU(cudaStreamSynchronize(s));
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,99 @@
+// Combine: y_r[t] = sum of token t's routed rows u[row] in ascending expert id,
+// FP32, one fixed order (page "NemotronH (Nemotron 3.5 Lightning, Bolt, Super
+// VL)", section "Arithmetic": the weighted sum in fp32 in ascending expert id;
+// page "Nemotron-3.5-Super 120B on an 8 GB GPU", section "How we know it's
+// right": a per-(token, expert) buffer summed in a fixed order instead of
+// atomics).  Packed rows are expert-contiguous, so ascending packed row is
+// ascending expert id.
+#include "internal.h"
+
+#include <algorithm>
+#include <climits>
+
+namespace moe {
+
+namespace {
+
+template <bool ACT_F32>
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ u, const int32_t* __restrict__ tsr,
+                                                      int K, int de, float* __restrict__ y_r,
+                                                      void* __restrict__ y_act) {
+  __shared__ int rows[32];
+  const int t = blockIdx.x;
+  if (threadIdx.x < K) {
+    const int r = tsr[(int64_t)t * K + threadIdx.x];
+    // rank among the token's rows (rows are distinct; invalid = -1 sorts last)
+    const unsigned key = r < 0 ? UINT_MAX : (unsigned)r;
+    int rank = 0;
+    for (int j = 0; j < K; ++j) {
+      const int rj = tsr[(int64_t)t * K + j];
+      const unsigned kj = rj < 0 ? UINT_MAX : (unsigned)rj;
+      rank += (kj < key) || (kj == key && j < (int)threadIdx.x);
+    }
+    rows[rank] = r;
+  }
+  __syncthreads();
+  const int nv = de / 4;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < K; ++i) {
+      const int r = rows[i];
+      if (r < 0) continue;
+      const float4 q = reinterpret_cast<const float4*>(u + (int64_t)r * de)[v];
+      acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+    }
+    if (y_r) reinterpret_cast<float4*>(y_r + (int64_t)t * de)[v] = acc;
+    if (y_act) {
+      if (ACT_F32) {
+        reinterpret_cast<float4*>(reinterpret_cast<float*>(y_act) + (int64_t)t * de)[v] = acc;
+      } else {
+        uint2 p;
+        p.x = (uint32_t)bf16_bits(acc.x) | ((uint32_t)bf16_bits(acc.y) << 16);
+        p.y = (uint32_t)bf16_bits(acc.z) | ((uint32_t)bf16_bits(acc.w) << 16);
+        reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(y_act) + (int64_t)t * de)[v] = p;
+      }
+    }
+  }
+}
+
+template <bool ACT_F32>
+__global__ void cast_kernel(const float* __restrict__ src, int64_t n4, void* __restrict__ dst) {
+  for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < n4; v += (int64_t)gridDim.x * blockDim.x) {
+    const float4 q = reinterpret_cast<const float4*>(src)[v];
+    if (ACT_F32) {
+      reinterpret_cast<float4*>(dst)[v] = q;
+    } else {
+      uint2 p;
+      p.x = (uint32_t)bf16_bits(q.x) | ((uint32_t)bf16_bits(q.y) << 16);
+      p.y = (uint32_t)bf16_bits(q.z) | ((uint32_t)bf16_bits(q.w) << 16);
+      reinterpret_cast<uint2*>(dst)[v] = p;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_cast(const float* src, int64_t n, void* dst, int act, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t n4 = n / 4;
+  const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(n4, 256), 4096);
+  if (act == MOE_DT_F32)
+    cast_kernel<true><<<grid, 256, 0, s>>>(src, n4, dst);
+  else
+    cast_kernel<false><<<grid, 256, 0, s>>>(src, n4, dst);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* u, const int32_t* token_slot_row, int T, int K, int de, float* y_r,
+                           void* y_act, int act, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (act == MOE_DT_F32)
+    combine_kernel<true><<<T, 256, 0, s>>>(u, token_slot_row, K, de, y_r, y_act);
+  else
+    combine_kernel<false><<<T, 256, 0, s>>>(u, token_slot_row, K, de, y_r, y_act);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

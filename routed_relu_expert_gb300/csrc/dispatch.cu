@@ -1,0 +1,273 @@
+// Dispatch: per-expert route counts, exclusive scan, and the stable
+// expert-contiguous layout of routes sorted by (expert, token, slot)
+// (page "M6.1 - Routed Capacity: MoE Experts, Routers, and Token Dispatch",
+// section 0x05A "The Route Row Is The Reversible Unit": offsets are the
+// prefix sum of counts; section 0x05B: X_packed[j] = H[a_pi(j)]).
+//
+// Atomic-free: a warp walks a contiguous range of routes 32 at a time; lanes
+// holding the same expert find each other with __match_any_sync, the lowest
+// such lane adds the group size to the warp's private histogram row, and a
+// lane's rank inside its group is the popcount of lower peers.  Per-expert
+// bases are exclusive scans over (tile, warp) in index order, so route r lands
+// after every earlier route of the same expert: the order is (expert, r) =
+// (expert, token, slot) because a token names an expert at most once.
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = 32;
+constexpr int kTileTokens = 256;   // tokens per CTA in the multi-CTA path
+
+// exclusive scan of one int per thread over a 1024-thread block
+__device__ int block_exclusive_scan(int v, int* tmp32, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) tmp32[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = tmp32[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    tmp32[lane] = w;  // inclusive
+  }
+  __syncthreads();
+  const int base = warp ? tmp32[warp - 1] : 0;
+  if (total) *total = tmp32[31];
+  __syncthreads();
+  return base + x - v;
+}
+
+// Histogram of routes [r0, r1) into hist[warp][E] (warp-private rows).
+__device__ void warp_histograms(const int32_t* __restrict__ ids, int r0, int r1, int E, int* hist,
+                                int32_t* err) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n = r1 - r0;
+  const int per = (int)ceil_div(ceil_div(n, kWarps), 32) * 32;
+  const int b = r0 + warp * per, bend = min(r1, b + per);
+  for (int base = b; base < bend; base += 32) {
+    const int r = base + lane;
+    int e = -1;
+    if (r < bend) {
+      e = ids[r];
+      if (e < 0 || e >= E) { set_error(err, MOE_DEVERR_EXPERT_ID); e = -1; }
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) hist[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// Scatter of routes [r0, r1) using per-warp running bases hist[warp][E].
+__device__ void warp_scatter(const int32_t* __restrict__ ids, int r0, int r1, int E, int K, int* hist,
+                             int32_t* route_token, int32_t* route_slot, int32_t* token_slot_row,
+                             const void* x_e, void* x_packed, int de, int elem_bytes) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n = r1 - r0;
+  const int per = (int)ceil_div(ceil_div(n, kWarps), 32) * 32;
+  const int b = r0 + warp * per, bend = min(r1, b + per);
+  const int row_vecs = de * elem_bytes / 16;
+  for (int base = b; base < bend; base += 32) {
+    const int r = base + lane;
+    int e = -1;
+    if (r < bend) {
+      e = ids[r];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    int pos = -1;
+    if (e >= 0) pos = hist[warp * E + e] + __popc(peers & lanemask_lt());
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) hist[warp * E + e] += __popc(peers);
+    __syncwarp();
+    if (r < bend) {
+      token_slot_row[r] = pos;
+      if (pos >= 0) {
+        route_token[pos] = r / K;
+        route_slot[pos] = r % K;
+      }
+    }
+    if (x_packed) {
+      // copy the gathered rows: the whole warp moves one 16-byte column slice set per route
+      for (int i = 0; i < 32; ++i) {
+        const int p = __shfl_sync(0xffffffffu, pos, i);
+        const int rr = base + i;
+        if (rr >= bend || p < 0) continue;
+        const int tok = rr / K;
+        const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(x_e) +
+                                                          (int64_t)tok * de * elem_bytes);
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<char*>(x_packed) + (int64_t)p * de * elem_bytes);
+        for (int v = lane; v < row_vecs; v += 32) dst[v] = src[v];
+      }
+    }
+  }
+}
+
+// Experts with routes, in ascending id, and the tensor-core tile prefix.
+__device__ void write_schedule(const DispatchArgs& a, int e, int total, int off, int* tmp32) {
+  const int has = (e < a.E && total > 0) ? 1 : 0;
+  int n_active = 0;
+  const int pos = block_exclusive_scan(has, tmp32, &n_active);
+  if (has) a.active[pos] = e;
+  int tiles = 0;
+  if (a.tile_rows > 0 && e < a.E) tiles = (int)ceil_div(total, a.tile_rows);
+  int n_tiles = 0;
+  const int tpos = block_exclusive_scan(tiles, tmp32, &n_tiles);
+  if (a.tile_prefix && e < a.E) a.tile_prefix[e] = tpos;
+  if (a.tile_prefix && e == a.E - 1) a.tile_prefix[a.E] = tpos + tiles;
+  // largest count: reduce via shuffles + shared
+  int m = (e < a.E) ? total : 0;
+#pragma unroll
+  for (int off2 = 16; off2 > 0; off2 >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off2));
+  if ((threadIdx.x & 31) == 0) tmp32[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int mm = 0;
+    for (int w = 0; w < kWarps; ++w) mm = max(mm, tmp32[w]);
+    a.hdr->n_active = n_active;
+    a.hdr->n_tiles = n_tiles;
+    a.hdr->max_rows = mm;
+  }
+  if (e < a.E) {
+    a.counts[e] = total;
+    a.offsets[e] = off;
+    if (e == a.E - 1) a.offsets[a.E] = off + total;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// single CTA (few routes)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) dispatch_single(const DispatchArgs a) {
+  extern __shared__ int sm[];
+  int* hist = sm;                      // [32][E]
+  int* tmp32 = sm + kWarps * a.E;      // [32]
+  const int R = a.T * a.K;
+  for (int i = threadIdx.x; i < kWarps * a.E; i += kThreads) hist[i] = 0;
+  __syncthreads();
+  warp_histograms(a.ids, 0, R, a.E, hist, &a.hdr->err);
+  __syncthreads();
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < a.E) {
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = hist[w * a.E + e];
+      hist[w * a.E + e] = total;
+      total += c;
+    }
+  }
+  const int off = block_exclusive_scan(e < a.E ? total : 0, tmp32, nullptr);
+  if (e < a.E)
+    for (int w = 0; w < kWarps; ++w) hist[w * a.E + e] += off;
+  write_schedule(a, e, total, off, tmp32);
+  __syncthreads();
+  warp_scatter(a.ids, 0, R, a.E, a.K, hist, a.route_token, a.route_slot, a.token_slot_row, a.x_e,
+               a.x_packed, a.de, a.elem_bytes);
+}
+
+// ---------------------------------------------------------------------------
+// multi CTA (many routes): count per token tile, one scan CTA, scatter
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) dispatch_count(const DispatchArgs a) {
+  extern __shared__ int sm[];
+  int* hist = sm;
+  const int tile = blockIdx.x;
+  const int r0 = tile * kTileTokens * a.K;
+  const int r1 = min(a.T, (tile + 1) * kTileTokens) * a.K;
+  for (int i = threadIdx.x; i < kWarps * a.E; i += kThreads) hist[i] = 0;
+  __syncthreads();
+  warp_histograms(a.ids, r0, r1, a.E, hist, &a.hdr->err);
+  __syncthreads();
+  for (int e = threadIdx.x; e < a.E; e += kThreads) {
+    int s = 0;
+    for (int w = 0; w < kWarps; ++w) s += hist[w * a.E + e];
+    a.tile_counts[(int64_t)tile * a.E + e] = s;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) dispatch_scan(const DispatchArgs a, int n_tiles) {
+  __shared__ int tmp32[32];
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < a.E) {
+    for (int tl = 0; tl < n_tiles; ++tl) {
+      const int c = a.tile_counts[(int64_t)tl * a.E + e];
+      a.tile_counts[(int64_t)tl * a.E + e] = total;
+      total += c;
+    }
+  }
+  const int off = block_exclusive_scan(e < a.E ? total : 0, tmp32, nullptr);
+  if (e < a.E)
+    for (int tl = 0; tl < n_tiles; ++tl) a.tile_counts[(int64_t)tl * a.E + e] += off;
+  write_schedule(a, e, total, off, tmp32);
+}
+
+__global__ void __launch_bounds__(kThreads) dispatch_scatter(const DispatchArgs a) {
+  extern __shared__ int sm[];
+  int* hist = sm;
+  const int tile = blockIdx.x;
+  const int r0 = tile * kTileTokens * a.K;
+  const int r1 = min(a.T, (tile + 1) * kTileTokens) * a.K;
+  for (int i = threadIdx.x; i < kWarps * a.E; i += kThreads) hist[i] = 0;
+  __syncthreads();
+  warp_histograms(a.ids, r0, r1, a.E, hist, nullptr);
+  __syncthreads();
+  for (int e = threadIdx.x; e < a.E; e += kThreads) {
+    int run = a.tile_counts[(int64_t)tile * a.E + e];
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = hist[w * a.E + e];
+      hist[w * a.E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  warp_scatter(a.ids, r0, r1, a.E, a.K, hist, a.route_token, a.route_slot, a.token_slot_row, a.x_e,
+               a.x_packed, a.de, a.elem_bytes);
+}
+
+constexpr int kSingleMaxRoutes = 4096;
+
+}  // namespace
+
+size_t dispatch_tile_count_elems(int T, int K, int E) {
+  (void)K;
+  return (size_t)ceil_div(T, kTileTokens) * (size_t)E;
+}
+
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
+  const int R = a.T * a.K;
+  if (R <= 0) return cudaSuccess;
+  if (R <= kSingleMaxRoutes) {
+    const size_t smem = (size_t)(kWarps * a.E + 32) * sizeof(int);
+    cudaError_t e = cudaFuncSetAttribute(dispatch_single, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dispatch_single<<<1, kThreads, smem, s>>>(a);
+    count_launches(1);
+    return cudaGetLastError();
+  }
+  const int n_tiles = (int)ceil_div(a.T, kTileTokens);
+  const size_t smem = (size_t)(kWarps * a.E) * sizeof(int);
+  cudaError_t e = cudaFuncSetAttribute(dispatch_count, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(dispatch_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dispatch_count<<<n_tiles, kThreads, smem, s>>>(a);
+  count_launches(1);
+  dispatch_scan<<<1, kThreads, 0, s>>>(a, n_tiles);
+  count_launches(1);
+  dispatch_scatter<<<n_tiles, kThreads, smem, s>>>(a);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

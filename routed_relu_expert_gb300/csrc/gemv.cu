@@ -1,0 +1,233 @@
+// Weight-streaming grouped GEMV for small row counts (decode).
+//
+// Every active expert's matrix (or one dense matrix) is read from HBM exactly
+// once per call for all of that expert's rows: a CTA owns 16 output features
+// of one segment, its 8 warps split the reduction dimension into 32-wide
+// chunks, and the partial sums are added in a fixed warp order through shared
+// memory (deterministic, no atomics).  Weight rows are fetched with 128-bit
+// streaming loads; each thread's 16 bytes of row g and row g+8 feed two
+// m16n8k16 MMAs whose k positions are a consistent permutation of the chunk
+// (the same permutation is applied to the activation operand), so no shuffle
+// or shared-memory staging is needed between the load and the MMA.
+//
+// The expert bank of page "NemotronH (Nemotron 3.5 Lightning, Bolt, Super
+// VL)", section "How the engine runs it" (a group's CTA decodes an expert's
+// tiles once for all of its rows) is the prior art; here the grouping comes
+// from the dispatch offsets and the split is over features and K.
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+
+struct Seg {
+  int id, row0, nrows;
+};
+
+__device__ __forceinline__ bool resolve_segment(const GemvArgs& a, int rows_per_cta, Seg& s) {
+  if (a.offsets) {
+    const int j = blockIdx.y;
+    if (j >= a.hdr->n_active) return false;
+    s.id = a.active[j];
+    s.row0 = a.offsets[s.id];
+    s.nrows = a.offsets[s.id + 1] - s.row0;
+  } else {
+    s.id = 0;
+    s.row0 = 0;
+    s.nrows = a.dense_rows;
+  }
+  const int rb = blockIdx.z * rows_per_cta;
+  if (rb >= s.nrows) return false;
+  s.row0 += rb;
+  s.nrows = min(s.nrows - rb, rows_per_cta);
+  return true;
+}
+
+template <int EPI, bool OUT_F32, bool ACT_F32>
+__device__ __forceinline__ void epilogue(const GemvArgs& a, int seg, int row, int f, float v) {
+  if (a.W_gs) v *= a.W_gs[seg];
+  const int64_t o = (int64_t)row * a.out_ld + f;
+  float r;
+  if (EPI == EPI_RELU2) {
+    if (ACT_F32) {
+      const float u = fmaxf(v, 0.f);
+      r = u * u;
+    } else {
+      const float u = fmaxf(round_bf16(v), 0.f);
+      r = u * u;                    // exact in FP32: product of two 8-bit significands
+    }
+  } else if (EPI == EPI_SCALE) {
+    const int t = a.route_token[row], k = a.route_slot[row];
+    r = a.topw[(int64_t)t * a.top_k + k] * v;
+  } else if (EPI == EPI_ADD) {
+    r = v + (a.add_src ? a.add_src[(int64_t)row * a.add_ld + f] : 0.f);
+  } else {
+    r = v;
+  }
+  if (OUT_F32 || ACT_F32) {
+    reinterpret_cast<float*>(a.out)[o] = r;
+  } else {
+    reinterpret_cast<bf16*>(a.out)[o] = __float2bfloat16_rn(r);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// BF16 weights, BF16 activations: NT chunks of 8 rows per CTA (rows <= 8*NT)
+// ---------------------------------------------------------------------------
+template <int NT, int EPI, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads) gemv_bf16_kernel(const GemvArgs a) {
+  constexpr int U = NT <= 2 ? 4 : 2;      // chunks in flight per warp
+  __shared__ float red[kWarps][NT][128];
+
+  Seg sg;
+  if (!resolve_segment(a, NT * 8, sg)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int f0 = blockIdx.x * 16;
+  const int K = a.K;
+
+  const bf16* W = reinterpret_cast<const bf16*>(a.W) + sg.id * a.w_seg_stride + (int64_t)f0 * K;
+  const bf16* wg = W + (int64_t)g * K + 8 * t4;
+  const bf16* wg8 = W + (int64_t)(g + 8) * K + 8 * t4;
+
+  const bf16* xr[NT];
+  bool xv[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int r = j * 8 + g;
+    xv[j] = r < sg.nrows;
+    int64_t row = 0;
+    if (xv[j]) row = a.gather ? a.gather[sg.row0 + r] : (sg.row0 + r);
+    xr[j] = reinterpret_cast<const bf16*>(a.X) + row * a.x_ld + 8 * t4;
+  }
+
+  float acc[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+  const int nchunks = K >> 5;
+  for (int c = warp; c < nchunks; c += kWarps * U) {
+    uint4 A0[U], A1[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int cc = c + kWarps * u;
+      if (cc < nchunks) {
+        A0[u] = ldg_stream(wg + cc * 32);
+        A1[u] = ldg_stream(wg8 + cc * 32);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int cc = c + kWarps * u;
+      if (cc < nchunks) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          if (j * 8 < sg.nrows) {
+            uint4 B = make_uint4(0, 0, 0, 0);
+            if (xv[j]) B = ldg_keep(xr[j] + cc * 32);
+            mma_bf16_16816(acc[j], A0[u].x, A1[u].x, A0[u].y, A1[u].y, B.x, B.y);
+            mma_bf16_16816(acc[j], A0[u].z, A1[u].z, A0[u].w, A1[u].w, B.z, B.w);
+          }
+        }
+      }
+    }
+  }
+
+  // acc[j][0]: (feature g, row 2t), [1]: (g, 2t+1), [2]: (g+8, 2t), [3]: (g+8, 2t+1)
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    red[warp][j][g * 8 + 2 * t4] = acc[j][0];
+    red[warp][j][g * 8 + 2 * t4 + 1] = acc[j][1];
+    red[warp][j][(g + 8) * 8 + 2 * t4] = acc[j][2];
+    red[warp][j][(g + 8) * 8 + 2 * t4 + 1] = acc[j][3];
+  }
+  __syncthreads();
+  for (int o = threadIdx.x; o < NT * 128; o += kThreads) {
+    const int j = o >> 7, idx = o & 127;
+    const int f = idx >> 3, r = j * 8 + (idx & 7);
+    if (r < sg.nrows) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) v += red[w][j][idx];
+      epilogue<EPI, OUT_F32, false>(a, sg.id, sg.row0 + r, f0 + f, v);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// FP32 weights and activations (small FP32 layers): plain FMA dot products.
+// A CTA owns 64 features of one segment and up to 64 rows.
+// ---------------------------------------------------------------------------
+template <int EPI>
+__global__ void __launch_bounds__(kThreads) gemv_f32_kernel(const GemvArgs a) {
+  Seg sg;
+  if (!resolve_segment(a, 64, sg)) return;
+  const int fl = threadIdx.x & 63, rg = threadIdx.x >> 6;
+  const int f = blockIdx.x * 64 + fl;
+  if (f >= a.N) return;
+  const float* w = reinterpret_cast<const float*>(a.W) + sg.id * a.w_seg_stride + (int64_t)f * a.K;
+  for (int r = rg; r < sg.nrows; r += 4) {
+    const int64_t row = a.gather ? a.gather[sg.row0 + r] : (sg.row0 + r);
+    const float* x = reinterpret_cast<const float*>(a.X) + row * a.x_ld;
+    float acc = 0.f;
+    for (int k = 0; k < a.K; k += 4) {
+      const float4 wv = *reinterpret_cast<const float4*>(w + k);
+      const float4 xv = *reinterpret_cast<const float4*>(x + k);
+      acc = fmaf(wv.x, xv.x, acc);
+      acc = fmaf(wv.y, xv.y, acc);
+      acc = fmaf(wv.z, xv.z, acc);
+      acc = fmaf(wv.w, xv.w, acc);
+    }
+    epilogue<EPI, true, true>(a, sg.id, sg.row0 + r, f, acc);
+  }
+}
+
+template <int NT, int EPI, bool OUT_F32>
+cudaError_t launch_bf16(const GemvArgs& a, int max_rows, int segs, cudaStream_t s) {
+  dim3 grid(a.N / 16, segs, (unsigned)ceil_div(max_rows, NT * 8));
+  gemv_bf16_kernel<NT, EPI, OUT_F32><<<grid, kThreads, 0, s>>>(a);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+template <int EPI, bool OUT_F32>
+cudaError_t pick_nt(const GemvArgs& a, int max_rows, int segs, cudaStream_t s) {
+  if (max_rows <= 8) return launch_bf16<1, EPI, OUT_F32>(a, max_rows, segs, s);
+  if (max_rows <= 16) return launch_bf16<2, EPI, OUT_F32>(a, max_rows, segs, s);
+  if (max_rows <= 32) return launch_bf16<4, EPI, OUT_F32>(a, max_rows, segs, s);
+  return launch_bf16<8, EPI, OUT_F32>(a, max_rows, segs, s);
+}
+
+}  // namespace
+
+cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_f32, int max_rows,
+                        int segs, cudaStream_t s) {
+  if (max_rows <= 0 || segs <= 0) return cudaSuccess;
+  if (wfmt == WF_F32) {
+    dim3 grid((unsigned)ceil_div(a.N, 64), segs, (unsigned)ceil_div(max_rows, 64));
+    switch (epi) {
+      case EPI_RELU2: gemv_f32_kernel<EPI_RELU2><<<grid, kThreads, 0, s>>>(a); break;
+      case EPI_SCALE: gemv_f32_kernel<EPI_SCALE><<<grid, kThreads, 0, s>>>(a); break;
+      case EPI_STORE: gemv_f32_kernel<EPI_STORE><<<grid, kThreads, 0, s>>>(a); break;
+      default: gemv_f32_kernel<EPI_ADD><<<grid, kThreads, 0, s>>>(a); break;
+    }
+    count_launches(1);
+    return cudaGetLastError();
+  }
+  if (wfmt != WF_BF16 || act != MOE_DT_BF16) return cudaErrorNotSupported;
+  switch (epi) {
+    case EPI_RELU2: return pick_nt<EPI_RELU2, false>(a, max_rows, segs, s);
+    case EPI_SCALE: return pick_nt<EPI_SCALE, true>(a, max_rows, segs, s);
+    case EPI_STORE:
+      return out_f32 ? pick_nt<EPI_STORE, true>(a, max_rows, segs, s)
+                     : pick_nt<EPI_STORE, false>(a, max_rows, segs, s);
+    default:
+      return out_f32 ? pick_nt<EPI_ADD, true>(a, max_rows, segs, s)
+                     : pick_nt<EPI_ADD, false>(a, max_rows, segs, s);
+  }
+}
+
+}  // namespace moe

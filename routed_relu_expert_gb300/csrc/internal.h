@@ -1,0 +1,90 @@
+// Internal launchers shared between the translation units of the library.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// host-side count of kernel launches (moe_launch_count)
+void count_launches(int n);
+
+// epilogues of the streaming GEMV / grouped GEMM kernels
+enum Epi : int {
+  EPI_RELU2 = 0,  // out = bf16(relu(bf16(v))^2)            (F32 layers: relu(v)^2)
+  EPI_SCALE = 1,  // out(f32) = topk_w[route] * v            (expert down: routed row u)
+  EPI_STORE = 2,  // out = bf16(v)                           (F32 out: v)
+  EPI_ADD = 3     // out = bf16(v + add_src[row, f])         (F32 out: v + add)
+};
+
+// Weight formats of the streamed matrix
+enum WFmt : int { WF_BF16 = 0, WF_F32 = 1, WF_NVFP4 = 2 };
+
+// One "grouped" matrix-times-rows product: for every segment (an active
+// expert, or one dense segment) out[rows, N] = X[rows, K] W_seg[N, K]^T.
+struct GemvArgs {
+  const void* W;            // [segments][N][K] (NVFP4: packed bytes [segments][N][K/2])
+  const uint8_t* W_sf;      // NVFP4 block scales [segments][N][K/16]
+  const float* W_gs;        // NVFP4 per-tensor scales [segments]
+  int64_t w_seg_stride;     // elements (bytes for NVFP4) between segments
+  int64_t sf_seg_stride;    // bytes between segments' scales
+  int N, K;
+  const void* X;            // activation rows, row stride x_ld elements
+  int64_t x_ld;
+  const int32_t* gather;    // X row of logical row r (route_token) or nullptr
+  const int32_t* offsets;   // [E+1] segment rows (grouped) or nullptr (dense)
+  const int32_t* active;    // [E] active expert list (grouped)
+  const WsHeader* hdr;      // n_active (grouped)
+  int dense_rows;           // rows of the dense segment
+  void* out;                // out rows [rows, out_ld]
+  int64_t out_ld;
+  const float* add_src;     // EPI_ADD source [rows, add_ld] f32 (nullable: adds 0)
+  int64_t add_ld;
+  const float* topw;        // EPI_SCALE: [T, K] routing weights
+  const int32_t* route_token;
+  const int32_t* route_slot;
+  int top_k;
+  int32_t* err;
+};
+
+// act: MOE_DT_BF16 / MOE_DT_F32 activation type of X and of non-f32 outputs.
+// out_f32: output element type is f32 (else act type).
+cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_f32,
+                        int max_rows, int grid_segments, cudaStream_t s);
+
+// router
+cudaError_t launch_router_logits(const void* x, int act, int T, int d, const float* w_router, int E,
+                                 float* logits, cudaStream_t s);
+cudaError_t launch_router_select(const float* logits, int T, int E, const float* bias, int G, int TG,
+                                 int K, int norm, float rsf, float* scores, int32_t* ids, float* w,
+                                 int32_t* err, cudaStream_t s);
+
+// dispatch
+struct DispatchArgs {
+  const int32_t* ids;
+  int T, K, E;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* route_token;
+  int32_t* route_slot;
+  int32_t* token_slot_row;
+  int32_t* active;          // [E]
+  WsHeader* hdr;
+  int32_t* tile_counts;     // [n_tiles, E] (multi-CTA path)
+  int32_t* tile_prefix;     // [E+1] tensor-core tile prefix (nullable)
+  int tile_rows;            // rows per tensor-core tile (0 = no tile prefix)
+  const void* x_e;          // pack source [T, de] (nullable)
+  void* x_packed;           // pack destination [R, de] (nullable)
+  int de;
+  int elem_bytes;
+};
+size_t dispatch_tile_count_elems(int T, int K, int E);
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
+
+// combine: y_r[t] = sum over t's packed rows in ascending order of u[row]
+cudaError_t launch_combine(const float* u, const int32_t* token_slot_row, int T, int K, int de,
+                           float* y_r, void* y_r_act, int act, cudaStream_t s);
+
+// dst (act dtype) = src (f32), n a multiple of 4
+cudaError_t launch_cast(const float* src, int64_t n, void* dst, int act, cudaStream_t s);
+
+}  // namespace moe

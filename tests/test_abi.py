@@ -1,0 +1,115 @@
+"""The C ABI library: it loads, exports every entry point the header declares,
+and rejects bad arguments on the host before enqueuing anything (no GPU
+needed: every call here returns before its first CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from routed_relu_expert_gb300 import build
+    build.build()
+    from routed_relu_expert_gb300 import _native
+    return _native.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_entry_point(lib):
+    names = _declared_functions()
+    assert "moe_layer_forward" in names and len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+    from routed_relu_expert_gb300 import EXPORTS
+    assert sorted(EXPORTS) == names
+
+
+def test_struct_layout_matches_header(lib):
+    from routed_relu_expert_gb300 import MoeConfig, MoeWeights
+    assert ctypes.sizeof(MoeConfig) == 12 * 4
+    assert ctypes.sizeof(MoeWeights) == 12 * 8
+
+
+def _cfg(**kw):
+    from routed_relu_expert_gb300 import make_config
+    base = dict(d_model=256, n_experts=8, top_k=2, d_expert=128, d_shared=256, routed_scaling_factor=2.5)
+    base.update(kw)
+    return make_config(**base)
+
+
+def test_config_validation(lib):
+    from routed_relu_expert_gb300 import _native as N
+    ok = _cfg()
+    assert lib.moe_check_config(ctypes.byref(ok)) == N.MOE_OK
+    bad = [
+        _cfg(top_k=9),                               # K > E
+        _cfg(n_experts=0),
+        _cfg(n_group=3),                             # E % G != 0
+        _cfg(n_group=4, topk_group=5),               # TG > G
+        _cfg(n_group=8, topk_group=1, top_k=2),      # groups of one expert
+        _cfg(n_group=4, topk_group=1, top_k=3),      # K > TG * E/G
+        _cfg(top_k=33, n_experts=64),
+        _cfg(norm_topk_prob=2),
+        _cfg(routed_scaling_factor=float("nan")),
+        _cfg(act_dtype=7),
+    ]
+    for c in bad:
+        assert lib.moe_check_config(ctypes.byref(c)) == N.MOE_ERR_INVALID_ARG
+    assert lib.moe_check_config(ctypes.byref(_cfg(d_model=250))) == N.MOE_ERR_UNSUPPORTED
+    # F32 experts need F32 activations
+    assert lib.moe_check_config(ctypes.byref(_cfg(expert_dtype=N.MOE_DT_F32))) == N.MOE_ERR_UNSUPPORTED
+
+
+def test_workspace_size_grows_with_tokens_and_rejects_short_buffers(lib):
+    from routed_relu_expert_gb300 import _native as N
+    c = _cfg()
+    sizes = [lib.moe_workspace_bytes(ctypes.byref(c), T) for T in (0, 1, 16, 1000)]
+    assert sizes[0] > 0 and sizes == sorted(sizes) and sizes[3] > sizes[2]
+    assert all(s % 256 == 0 for s in sizes)
+    assert lib.moe_workspace_bytes(ctypes.byref(_cfg(top_k=9)), 4) == 0
+    # a workspace one byte short is refused before any device work
+    fake = ctypes.c_void_p(1 << 20)            # never dereferenced: the size check comes first
+    w = N.MoeWeights()
+    st = lib.moe_layer_forward(ctypes.byref(c), 16, fake, ctypes.byref(w), fake, None, None, None, None,
+                               fake, ctypes.c_size_t(sizes[2] - 1), None)
+    assert st == N.MOE_ERR_WORKSPACE
+
+
+def test_null_and_misaligned_pointers_are_refused(lib):
+    from routed_relu_expert_gb300 import _native as N
+    c = _cfg()
+    n = lib.moe_workspace_bytes(ctypes.byref(c), 4)
+    ws = ctypes.c_void_p(1 << 20)
+    good = ctypes.c_void_p(1 << 21)
+    mis = ctypes.c_void_p((1 << 21) + 4)
+    w = N.MoeWeights()
+    args = lambda x, y: (ctypes.byref(c), 4, x, ctypes.byref(w), y, None, None, None, None, ws, n, None)
+    assert lib.moe_layer_forward(*args(None, good)) == N.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_forward(*args(mis, good)) == N.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_forward(*args(good, good)) == N.MOE_ERR_INVALID_ARG   # weights missing
+    assert lib.moe_router(ctypes.byref(c), 4, good, None, None, None, None, good, good, ws, n, None) == \
+        N.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch(ctypes.byref(c), 4, good, None, good, good, good, good, None, None, ws, n, None) == \
+        N.MOE_ERR_INVALID_ARG
+    assert lib.moe_latent_down(ctypes.byref(c), 4, good, ctypes.byref(w), good, ws, n, None) == \
+        N.MOE_ERR_INVALID_ARG                                                 # not a latent layer
+    # zero tokens: nothing to do, nothing touched
+    assert lib.moe_layer_forward(ctypes.byref(c), 0, None, ctypes.byref(w), None, None, None, None, None,
+                                 None, 0, None) == N.MOE_OK
+    assert lib.moe_get_device_error(None, None, None) == N.MOE_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.moe_status_string(s)
+    assert lib.moe_version() >= 100

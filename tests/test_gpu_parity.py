@@ -1,0 +1,212 @@
+"""GPU parity: the CUDA library against the CPU oracle on the same seeded inputs.
+
+Routing (expert ids and per-expert token lists) must match bit for bit, with
+the selection checked on the GPU's own FP32 scores; routing weights within
+1e-6; logits within 1e-5 of sum_i |x_i W_ei|; the layer output within
+2e-2 * RMS for BF16 layers (1e-4 * RMS for FP32 layers)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from synth import (NANO_DECODE, NANO_PREFILL, ROUTER_ONLY_GROUPED, SUPER_LATENT, TINY_FP32, make_weights,
+                   make_x, scaled)
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import routed_relu_expert_gb300 as M
+    from gpu_helpers import (check_output, check_router, device_weights, oracle_weights, run_gpu, to_np,
+                             tol_of)
+
+SMALL_NANO = scaled(NANO_DECODE, name="nano_scaled", d_model=512, n_experts=32, top_k=4, d_expert=320,
+                    d_shared=384, weight_seed=11, tokens=())
+SMALL_SUPER = scaled(SUPER_LATENT, name="super_scaled", d_model=512, d_latent=256, n_experts=64, top_k=6,
+                     n_group=8, topk_group=4, d_expert=320, d_shared=448, weight_seed=13, tokens=())
+
+
+def _parity(shape, T, sample=None, seed_stream=0):
+    w = device_weights(shape)
+    x = make_x(shape, T, "cuda", seed_stream)
+    g = to_np(run_gpu(shape, w, x))
+    assert g["err"] == 0
+    ow = oracle_weights(w)
+    x_np = x.float().cpu().numpy().astype(np.float64)
+    # routing on every token
+    ids_all, _ = check_router(shape, x_np, ow, g)
+    rows = None
+    if sample is not None and sample < T:
+        rng = np.random.default_rng(T)
+        rows = np.sort(rng.choice(T, sample, replace=False))
+    ids_o, w_o = check_router(shape, x_np, ow, g, rows)
+    err = check_output(shape, x_np, ow, ids_o, w_o, g["y"], tol_of(shape), rows)
+    return err, g
+
+
+@pytest.mark.parametrize("T", [16, 1, 5, 64, 100])
+def test_tiny_fp32_layer(T):
+    _parity(TINY_FP32, T)
+
+
+@pytest.mark.parametrize("T", [1, 7, 37, 64, 100, 300])
+def test_scaled_nano_layer(T):
+    _parity(SMALL_NANO, T)
+
+
+@pytest.mark.parametrize("T", [1, 13, 64, 200])
+def test_scaled_super_latent_layer(T):
+    _parity(SMALL_SUPER, T)
+
+
+@pytest.mark.parametrize("T", [1, 4, 16, 64])
+def test_nano_decode_full_size(T):
+    _parity(NANO_DECODE, T)
+
+
+def test_nano_prefill_2048_sampled():
+    _parity(NANO_PREFILL, 2048, sample=192)
+
+
+@pytest.mark.parametrize("T", [1, 16])
+def test_super_latent_full_size(T):
+    _parity(SUPER_LATENT, T)
+
+
+def test_super_latent_256_sampled():
+    _parity(SUPER_LATENT, 256, sample=48)
+
+
+def test_router_grouped_case_from_the_router_parity_test():
+    """128 experts, top-6, eight groups keeping three: the router parity case
+    of page "Nemotron Is Not One Circuit", section "What CKE Has Actually
+    Established"; exact ids and weights within 1e-6."""
+    shape = ROUTER_ONLY_GROUPED
+    w = device_weights(shape)
+    for T in (1, 64, 333):
+        x = make_x(shape, T, "cuda")
+        cfg = M.config_from(shape)
+        ws = M.new_workspace(cfg, T)
+        ids = torch.empty((T, shape.top_k), dtype=torch.int32, device="cuda")
+        topw = torch.empty((T, shape.top_k), dtype=torch.float32, device="cuda")
+        logits = torch.empty((T, shape.n_experts), dtype=torch.float32, device="cuda")
+        scores = torch.empty_like(logits)
+        M.moe_router(cfg, x, w["w_router"], w["bias"], ids, topw, ws, logits, scores)
+        torch.cuda.synchronize()
+        g = to_np({"ids": ids, "topw": topw, "logits": logits, "scores": scores})
+        ow = oracle_weights({"w_router": w["w_router"], "bias": w["bias"]})
+        check_router(shape, x.float().cpu().numpy().astype(np.float64), ow, g)
+
+
+@pytest.mark.parametrize("T,E,K", [(1, 8, 2), (64, 128, 6), (37, 512, 22), (2048, 128, 6), (700, 64, 6)])
+def test_dispatch_is_bit_exact(T, E, K):
+    from synth import MoEShape
+    shape = MoEShape("dispatch", 256, 0, E, K, 1, 1, 128, 0, 1.0, tokens=())
+    cfg = M.config_from(shape)
+    rng = np.random.default_rng(T + E)
+    p = rng.zipf(1.5, E).astype(np.float64)
+    p /= p.sum()
+    ids_np = np.stack([rng.choice(E, K, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    ids = torch.from_numpy(ids_np).cuda()
+    x = torch.randn((T, 256), device="cuda").to(torch.bfloat16)
+    ws = M.new_workspace(cfg, T)
+    R = T * K
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    rt = torch.empty(R, dtype=torch.int32, device="cuda")
+    rs = torch.empty(R, dtype=torch.int32, device="cuda")
+    tsr = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    xp = torch.empty((R, 256), dtype=torch.bfloat16, device="cuda")
+    M.moe_dispatch(cfg, ids, counts, offsets, rt, rs, tsr, ws, x_e=x, x_packed=xp)
+    torch.cuda.synchronize()
+    ref = O.dispatch(ids_np, E)
+    assert np.array_equal(counts.cpu().numpy(), ref["counts"])
+    assert np.array_equal(offsets.cpu().numpy(), ref["offsets"])
+    assert np.array_equal(rt.cpu().numpy(), ref["route_token"])
+    assert np.array_equal(rs.cpu().numpy(), ref["route_slot"])
+    assert np.array_equal(tsr.cpu().numpy(), ref["token_slot_row"])
+    assert torch.equal(xp, x[torch.from_numpy(ref["route_token"]).cuda()])
+    assert M.moe_get_device_error(ws) == 0
+
+
+def test_step_entry_points_reproduce_layer_forward_bit_for_bit():
+    for shape, T in ((SMALL_NANO, 37), (SMALL_SUPER, 13)):
+        w = device_weights(shape)
+        x = make_x(shape, T, "cuda", 3)
+        cfg = M.config_from(shape)
+        layer = M.MoELayer(cfg, w)
+        y_ref = layer.forward(x).clone()
+        E, K, de = shape.n_experts, shape.top_k, shape.d_e
+        ws = M.new_workspace(cfg, T)
+        ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+        topw = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        M.moe_router(cfg, x, w["w_router"], w["bias"], ids, topw, ws)
+        x_e = x
+        if shape.d_latent:
+            x_e = torch.empty((T, de), dtype=x.dtype, device="cuda")
+            M.moe_latent_down(cfg, x, layer.weights, x_e, ws)
+        counts = torch.empty(E, dtype=torch.int32, device="cuda")
+        offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+        rt = torch.empty(T * K, dtype=torch.int32, device="cuda")
+        rs = torch.empty(T * K, dtype=torch.int32, device="cuda")
+        tsr = torch.empty((T, K), dtype=torch.int32, device="cuda")
+        M.moe_dispatch(cfg, ids, counts, offsets, rt, rs, tsr, ws)
+        h = torch.empty((T * K, shape.d_expert), dtype=x.dtype, device="cuda")
+        M.moe_experts_up(cfg, T, rt, offsets, layer.weights, h, ws, x_e=x_e)
+        y_r = torch.empty((T, de), dtype=torch.float32, device="cuda")
+        M.moe_experts_down_combine(cfg, T, h, offsets, rt, rs, tsr, topw, layer.weights, y_r, ws)
+        y = torch.empty_like(x)
+        M.moe_shared(cfg, x, layer.weights, y, ws, y_routed=y_r)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_ref)
+
+
+def test_runs_are_bit_identical():
+    shape = NANO_DECODE
+    w = device_weights(shape)
+    x = make_x(shape, 64, "cuda", 5)
+    layer = M.MoELayer(M.config_from(shape), w)
+    ys = [layer.forward(x).clone() for _ in range(3)]
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[1], ys[2])
+
+
+def test_zero_tokens_is_a_no_op():
+    shape = SMALL_NANO
+    layer = M.MoELayer(M.config_from(shape), device_weights(shape))
+    x = torch.empty((0, shape.d_model), dtype=torch.bfloat16, device="cuda")
+    y = layer.forward(x)
+    assert y.shape == (0, shape.d_model)
+
+
+def test_nan_input_sets_the_nonfinite_bit_and_keeps_ids_in_range():
+    shape = SMALL_NANO
+    w = device_weights(shape)
+    x = make_x(shape, 8, "cuda")
+    x[3, 5] = float("nan")
+    g = run_gpu(shape, w, x)
+    assert g["err"] & M.MOE_DEVERR_NONFINITE
+    ids = g["ids"].cpu().numpy()
+    assert ids.min() >= 0 and ids.max() < shape.n_experts
+    assert all(len(set(r)) == shape.top_k for r in ids.tolist())
+
+
+def test_out_of_range_ids_are_flagged_and_skipped():
+    from synth import MoEShape
+    E, K, T = 16, 2, 10
+    shape = MoEShape("bad_ids", 256, 0, E, K, 1, 1, 128, 0, 1.0, tokens=())
+    cfg = M.config_from(shape)
+    ids_np = np.tile(np.array([[0, 1]], dtype=np.int32), (T, 1))
+    ids_np[4, 1] = E            # out of range
+    ids_np[6, 0] = -3
+    ids = torch.from_numpy(ids_np).cuda()
+    ws = M.new_workspace(cfg, T)
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    rt = torch.full((T * K,), -7, dtype=torch.int32, device="cuda")
+    rs = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    tsr = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    M.moe_clear_device_error(ws)
+    M.moe_dispatch(cfg, ids, counts, offsets, rt, rs, tsr, ws)
+    assert M.moe_get_device_error(ws) & M.MOE_DEVERR_EXPERT_ID
+    assert int(counts.sum()) == T * K - 2
+    t = tsr.cpu().numpy()
+    assert t[4, 1] == -1 and t[6, 0] == -1
