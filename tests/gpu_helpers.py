@@ -76,16 +76,18 @@ def run_gpu(shape: MoEShape, w: Dict[str, torch.Tensor], x: torch.Tensor):
 
 
 def check_router(shape: MoEShape, x_np: np.ndarray, ow: Dict, g: Dict, rows: Optional[np.ndarray] = None):
-    """Router checks on GPU outputs g (numpy): logits vs FP64, scores vs sigmoid
-    of the GPU's own logits, ids bit-exact and weights 1e-6 vs the oracle's
-    selection on the GPU's scores.  Returns the oracle's (ids, w)."""
+    """Router checks on GPU outputs g (numpy): logits vs FP64, scores within
+    4 ulp of the sigmoid of the GPU's own logits, ids bit-exact and weights
+    1e-6 vs the oracle's selection on the GPU's scores.  Returns the oracle's
+    (ids, w)."""
     rows = np.arange(x_np.shape[0]) if rows is None else rows
     z, zs = O.router_logits(x_np[rows], ow["w_router"])
     lg = g["logits"][rows].astype(np.float64)
     assert np.all(np.abs(lg - z) <= TOL_LOGIT * zs), f"logit error {np.max(np.abs(lg - z) / zs)}"
     s_ref = O.sigmoid_scores(g["logits"][rows])
     ulp = np.abs(g["scores"][rows].view(np.int32).astype(np.int64) - s_ref.view(np.int32).astype(np.int64))
-    assert ulp.max() <= 2, f"sigmoid differs by {ulp.max()} ulp"
+    # CUDA's expf is within 2 ulp; 1 + e and the division add one rounding each
+    assert ulp.max() <= 4, f"sigmoid differs by {ulp.max()} ulp"
     ids_o, w_o = O.route(g["scores"][rows], ow.get("bias"), shape.n_group, shape.topk_group, shape.top_k,
                          shape.norm_topk_prob, shape.routed_scaling_factor)
     mism = np.where(np.any(ids_o != g["ids"][rows], axis=1))[0]

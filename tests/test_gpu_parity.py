@@ -116,6 +116,7 @@ def test_dispatch_is_bit_exact(T, E, K):
     rs = torch.empty(R, dtype=torch.int32, device="cuda")
     tsr = torch.empty((T, K), dtype=torch.int32, device="cuda")
     xp = torch.empty((R, 256), dtype=torch.bfloat16, device="cuda")
+    M.moe_clear_device_error(ws)          # a fresh workspace holds garbage; step calls do not clear it
     M.moe_dispatch(cfg, ids, counts, offsets, rt, rs, tsr, ws, x_e=x, x_packed=xp)
     torch.cuda.synchronize()
     ref = O.dispatch(ids_np, E)
