@@ -218,6 +218,29 @@ moe_status_t moe_clear_device_error(void* ws, void* stream);
  * not counted).  Never fails. */
 int64_t moe_launch_count(void);
 
+/* Router step that allocates nothing and takes no workspace.  The pages have
+ * no counterpart: this serves callers that cannot allocate device memory at
+ * call time, such as code running after a host framework's memory pool has
+ * claimed the device, serving loops that forbid allocation once started, or
+ * work enqueued where cudaMalloc is not permitted.  Same arguments and
+ * results as moe_router without logits/scores outputs; its scratch (logits,
+ * scores and the error word) lives in a static device array of
+ * MOE_NOALLOC_MAX_ROUTER_ELEMS * 8 + 256 bytes that every GPU loading this
+ * library keeps until exit.
+ *   - Returns MOE_ERR_WORKSPACE, before enqueuing anything, when
+ *     T * n_experts > MOE_NOALLOC_MAX_ROUTER_ELEMS.
+ *   - The first call on a device looks the array up (cudaGetSymbolAddress,
+ *     once per device, with that device current): make it before any stream
+ *     capture.
+ *   - All calls share the array: calls whose work overlaps on the GPU race.
+ *     Each call clears the error word first; device error bits are not
+ *     reported by this entry point.
+ *   - Calls no allocation routine (no cudaMalloc/cudaFree).                  */
+#define MOE_NOALLOC_MAX_ROUTER_ELEMS 131072
+moe_status_t moe_router_noalloc(const moe_config_t* cfg, int32_t T, const void* x,
+                                const float* w_router, const float* router_bias,
+                                int32_t* topk_ids, float* topk_w, void* stream);
+
 /* End-to-end convenience call with HOST buffers: copies x_host [T, d] to
  * x_dev, runs moe_layer_forward, copies y to y_host and synchronises the
  * stream.  x_dev / y_dev / ws are caller-owned device buffers; the host

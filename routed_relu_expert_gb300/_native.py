@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libmoe_gb300.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(6)
 MOE_DEVERR_EXPERT_ID, MOE_DEVERR_NONFINITE, MOE_DEVERR_SCHEDULE = 1, 2, 4
 MOE_DT_F32, MOE_DT_BF16, MOE_DT_NVFP4 = 0, 1, 2
+MOE_NOALLOC_MAX_ROUTER_ELEMS = 131072
 
 
 class MoeConfig(ctypes.Structure):
@@ -44,7 +45,7 @@ EXPORTS = (
     "moe_version", "moe_status_string", "moe_check_config", "moe_workspace_bytes", "moe_router",
     "moe_dispatch", "moe_experts_up", "moe_experts_down_combine", "moe_latent_down", "moe_shared",
     "moe_layer_forward", "moe_get_device_error", "moe_clear_device_error", "moe_layer_forward_host",
-    "moe_launch_count",
+    "moe_launch_count", "moe_router_noalloc",
 )
 
 _lib = None
@@ -80,6 +81,7 @@ def load() -> ctypes.CDLL:
         "moe_clear_device_error": (I32, [P, P]),
         "moe_layer_forward_host": (I32, [CFG, I32, P, P, W, P, P, P, S, P]),
         "moe_launch_count": (ctypes.c_int64, []),
+        "moe_router_noalloc": (I32, [CFG, I32, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -104,6 +104,12 @@ def moe_router(cfg, x, w_router, bias, ids, topw, ws, logits=None, scores=None, 
                                 _p(ids), _p(topw), w, n, _s(stream)), "moe_router")
 
 
+def moe_router_noalloc(cfg, x, w_router, bias, ids, topw, stream=None):
+    """Router with no workspace (scratch in the library's static device array)."""
+    N.check(N.load().moe_router_noalloc(ctypes.byref(cfg), x.shape[0], _p(x), _p(w_router), _p(bias), _p(ids),
+                                        _p(topw), _s(stream)), "moe_router_noalloc")
+
+
 def moe_dispatch(cfg, ids, counts, offsets, route_token, route_slot, token_slot_row, ws, x_e=None,
                  x_packed=None, stream=None):
     T = ids.shape[0]
