@@ -75,15 +75,18 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, int seg, int row, in
 }
 
 // ---------------------------------------------------------------------------
-// BF16 weights, BF16 activations: NT chunks of 8 rows per CTA (rows <= 8*NT)
+// BF16 weights, BF16 activations.  A CTA handles its segment's rows in passes
+// of 16 (two 8-row MMA column blocks); a second pass finds the CTA's weight
+// tile still in L2, so HBM streams each weight once while registers stay low.
 // ---------------------------------------------------------------------------
-template <int NT, int EPI, bool OUT_F32>
-__global__ void __launch_bounds__(kThreads) gemv_bf16_kernel(const GemvArgs a) {
-  constexpr int U = NT <= 2 ? 4 : 2;      // chunks in flight per warp
+template <int EPI, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a) {
+  constexpr int NT = 2;                 // 8-row column blocks per pass
+  constexpr int U = 4;                  // 32-wide K chunks in flight per warp
   __shared__ float red[kWarps][NT][128];
 
   Seg sg;
-  if (!resolve_segment(a, NT * 8, sg)) return;
+  if (!resolve_segment(a, 1 << 30, sg)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int f0 = blockIdx.x * 16;
@@ -92,67 +95,70 @@ __global__ void __launch_bounds__(kThreads) gemv_bf16_kernel(const GemvArgs a) {
   const bf16* W = reinterpret_cast<const bf16*>(a.W) + sg.id * a.w_seg_stride + (int64_t)f0 * K;
   const bf16* wg = W + (int64_t)g * K + 8 * t4;
   const bf16* wg8 = W + (int64_t)(g + 8) * K + 8 * t4;
-
-  const bf16* xr[NT];
-  bool xv[NT];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    const int r = j * 8 + g;
-    xv[j] = r < sg.nrows;
-    int64_t row = 0;
-    if (xv[j]) row = a.gather ? a.gather[sg.row0 + r] : (sg.row0 + r);
-    xr[j] = reinterpret_cast<const bf16*>(a.X) + row * a.x_ld + 8 * t4;
-  }
-
-  float acc[NT][4];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-
   const int nchunks = K >> 5;
-  for (int c = warp; c < nchunks; c += kWarps * U) {
-    uint4 A0[U], A1[U];
+
+  for (int p0 = 0; p0 < sg.nrows; p0 += NT * 8) {
+    const int prow = min(sg.nrows - p0, NT * 8);
+    const bf16* xr[NT];
+    bool xv[NT];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int cc = c + kWarps * u;
-      if (cc < nchunks) {
-        A0[u] = ldg_stream(wg + cc * 32);
-        A1[u] = ldg_stream(wg8 + cc * 32);
-      }
+    for (int j = 0; j < NT; ++j) {
+      const int r = j * 8 + g;
+      xv[j] = r < prow;
+      int64_t row = 0;
+      if (xv[j]) row = a.gather ? a.gather[sg.row0 + p0 + r] : (sg.row0 + p0 + r);
+      xr[j] = reinterpret_cast<const bf16*>(a.X) + row * a.x_ld + 8 * t4;
     }
+    float acc[NT][4];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int cc = c + kWarps * u;
-      if (cc < nchunks) {
+    for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+    for (int c = warp; c < nchunks; c += kWarps * U) {
+      uint4 A0[U], A1[U];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          if (j * 8 < sg.nrows) {
-            uint4 B = make_uint4(0, 0, 0, 0);
-            if (xv[j]) B = ldg_keep(xr[j] + cc * 32);
-            mma_bf16_16816(acc[j], A0[u].x, A1[u].x, A0[u].y, A1[u].y, B.x, B.y);
-            mma_bf16_16816(acc[j], A0[u].z, A1[u].z, A0[u].w, A1[u].w, B.z, B.w);
+      for (int u = 0; u < U; ++u) {
+        const int cc = c + kWarps * u;
+        if (cc < nchunks) {
+          A0[u] = ldg_stream(wg + cc * 32);
+          A1[u] = ldg_stream(wg8 + cc * 32);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int cc = c + kWarps * u;
+        if (cc < nchunks) {
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            if (j * 8 < prow) {
+              uint4 B = make_uint4(0, 0, 0, 0);
+              if (xv[j]) B = ldg_keep(xr[j] + cc * 32);
+              mma_bf16_16816(acc[j], A0[u].x, A1[u].x, A0[u].y, A1[u].y, B.x, B.y);
+              mma_bf16_16816(acc[j], A0[u].z, A1[u].z, A0[u].w, A1[u].w, B.z, B.w);
+            }
           }
         }
       }
     }
-  }
 
-  // acc[j][0]: (feature g, row 2t), [1]: (g, 2t+1), [2]: (g+8, 2t), [3]: (g+8, 2t+1)
+    // acc[j][0]: (feature g, row 2t), [1]: (g, 2t+1), [2]: (g+8, 2t), [3]: (g+8, 2t+1)
+    if (p0 > 0) __syncthreads();      // previous pass has finished reading red
 #pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    red[warp][j][g * 8 + 2 * t4] = acc[j][0];
-    red[warp][j][g * 8 + 2 * t4 + 1] = acc[j][1];
-    red[warp][j][(g + 8) * 8 + 2 * t4] = acc[j][2];
-    red[warp][j][(g + 8) * 8 + 2 * t4 + 1] = acc[j][3];
-  }
-  __syncthreads();
-  for (int o = threadIdx.x; o < NT * 128; o += kThreads) {
-    const int j = o >> 7, idx = o & 127;
-    const int f = idx >> 3, r = j * 8 + (idx & 7);
-    if (r < sg.nrows) {
-      float v = 0.f;
+    for (int j = 0; j < NT; ++j) {
+      red[warp][j][g * 8 + 2 * t4] = acc[j][0];
+      red[warp][j][g * 8 + 2 * t4 + 1] = acc[j][1];
+      red[warp][j][(g + 8) * 8 + 2 * t4] = acc[j][2];
+      red[warp][j][(g + 8) * 8 + 2 * t4 + 1] = acc[j][3];
+    }
+    __syncthreads();
+    for (int o = threadIdx.x; o < NT * 128; o += kThreads) {
+      const int j = o >> 7, idx = o & 127;
+      const int f = idx >> 3, r = j * 8 + (idx & 7);
+      if (r < prow) {
+        float v = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) v += red[w][j][idx];
-      epilogue<EPI, OUT_F32, false>(a, sg.id, sg.row0 + r, f0 + f, v);
+        for (int w = 0; w < kWarps; ++w) v += red[w][j][idx];
+        epilogue<EPI, OUT_F32, false>(a, sg.id, sg.row0 + p0 + r, f0 + f, v);
+      }
     }
   }
 }
@@ -185,20 +191,13 @@ __global__ void __launch_bounds__(kThreads) gemv_f32_kernel(const GemvArgs a) {
   }
 }
 
-template <int NT, int EPI, bool OUT_F32>
-cudaError_t launch_bf16(const GemvArgs& a, int max_rows, int segs, cudaStream_t s) {
-  dim3 grid(a.N / 16, segs, (unsigned)ceil_div(max_rows, NT * 8));
-  gemv_bf16_kernel<NT, EPI, OUT_F32><<<grid, kThreads, 0, s>>>(a);
-  count_launches(1);
-  return cudaGetLastError();
-}
-
 template <int EPI, bool OUT_F32>
 cudaError_t pick_nt(const GemvArgs& a, int max_rows, int segs, cudaStream_t s) {
-  if (max_rows <= 8) return launch_bf16<1, EPI, OUT_F32>(a, max_rows, segs, s);
-  if (max_rows <= 16) return launch_bf16<2, EPI, OUT_F32>(a, max_rows, segs, s);
-  if (max_rows <= 32) return launch_bf16<4, EPI, OUT_F32>(a, max_rows, segs, s);
-  return launch_bf16<8, EPI, OUT_F32>(a, max_rows, segs, s);
+  (void)max_rows;
+  dim3 grid(a.N / 16, segs, 1);
+  gemv_bf16_kernel<EPI, OUT_F32><<<grid, kThreads, 0, s>>>(a);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 }  // namespace

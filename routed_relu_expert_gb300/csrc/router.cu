@@ -293,6 +293,8 @@ cudaError_t launch_router_logits(const void* x, int act, int T, int d, const flo
   if (T <= 0) return cudaSuccess;
   if (T <= 4) return launch_small<4>(x, act, T, d, w_router, E, logits, s);
   if (T <= 16) return launch_small<16>(x, act, T, d, w_router, E, logits, s);
+  if (T <= 32) return launch_small<32>(x, act, T, d, w_router, E, logits, s);
+  if (T <= 64) return launch_small<64>(x, act, T, d, w_router, E, logits, s);
   dim3 grid((unsigned)ceil_div(T, 64), (unsigned)ceil_div(E, 64));
   if (act == MOE_DT_F32)
     router_logits_tiled<true><<<grid, 256, 0, s>>>(x, T, d, w_router, E, logits);
