@@ -66,7 +66,8 @@ enum {
 enum {
   MOE_DEVERR_EXPERT_ID = 1,      /* an expert id outside [0, n_experts) reached dispatch */
   MOE_DEVERR_NONFINITE = 2,      /* a router score was NaN (ranked last, never chosen before a finite one) */
-  MOE_DEVERR_SCHEDULE = 4        /* a tile schedule disagreed with the dispatch offsets */
+  MOE_DEVERR_SCHEDULE = 4,       /* a tile schedule disagreed with the dispatch offsets */
+  MOE_DEVERR_TIMEOUT = 8         /* a kernel's bounded wait expired; that kernel stopped early */
 };
 
 typedef int32_t moe_dtype_t;

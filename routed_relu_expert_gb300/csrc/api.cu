@@ -21,6 +21,8 @@ constexpr int kMaxTopK = 32;
 constexpr int kMaxGroups = 32;
 constexpr int64_t kMaxRoutes = (int64_t)1 << 28;
 
+constexpr int kDecodeMaxT = 64;   // up to this many tokens: weight-streaming GEMV; above: tensor cores
+
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 inline int act_bytes(const moe_config_t* c) { return c->act_dtype == MOE_DT_F32 ? 4 : 2; }
 inline int de_of(const moe_config_t* c) { return c->d_latent > 0 ? c->d_latent : c->d_model; }
@@ -106,6 +108,30 @@ inline int wfmt_of(const moe_config_t* c) {
 }
 inline int dense_fmt(const moe_config_t* c) { return c->act_dtype == MOE_DT_F32 ? WF_F32 : WF_BF16; }
 
+// tensor-core path: BF16 layers with more than kDecodeMaxT tokens
+inline bool use_tc(const moe_config_t* c, int T) {
+  return c->act_dtype == MOE_DT_BF16 && c->expert_dtype == MOE_DT_BF16 && T > kDecodeMaxT;
+}
+
+// Rows per tensor-core tile: 256, halved while the estimated tile count stays
+// below two per SM (so moderate token counts still fill the GPU).
+int choose_bn(int64_t rows_per_seg, int64_t segs, int N) {
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t m_tiles = ceil_div(N, 128);
+  int bn = 256;
+  while (bn > 16 && ceil_div(std::max<int64_t>(rows_per_seg, 1), bn) * segs * m_tiles < 2 * (int64_t)sms) bn >>= 1;
+  return bn;
+}
+
+// dense product out[T, N] = X[T, K] W[N, K]^T through the GEMV or the tensor cores
+cudaError_t run_dense(const moe_config_t* c, const GemvArgs& a, int epi, bool out_f32, int T, cudaStream_t s) {
+  if (use_tc(c, T))
+    return launch_gemm_tc(a, epi, out_f32, a.N, T, 0, choose_bn(T, 1, a.N), s);
+  return launch_gemv(a, dense_fmt(c), c->act_dtype, epi, out_f32, T, 1, s);
+}
+
 GemvArgs dense_args(const void* W, int N, int K, const void* X, int rows, void* out, int64_t out_ld) {
   GemvArgs a{};
   a.W = W; a.N = N; a.K = K; a.X = X; a.x_ld = K; a.dense_rows = rows;
@@ -155,6 +181,12 @@ moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x
   a.offsets = offsets; a.active = P.at<int32_t>(P.L.active); a.hdr = P.hdr();
   a.out = h; a.out_ld = I; a.err = &P.hdr()->err;
   const int segs = (int)std::min<int64_t>(c->n_experts, (int64_t)T * c->top_k);
+  if (use_tc(c, T) && x_packed) {
+    const int64_t R = (int64_t)T * c->top_k;
+    CU(launch_gemm_tc(a, EPI_RELU2, false, (int64_t)c->n_experts * I, R, c->n_experts,
+                      choose_bn(R / segs, segs, I), s));
+    return MOE_OK;
+  }
   CU(launch_gemv(a, wfmt_of(c), c->act_dtype, EPI_RELU2, c->act_dtype == MOE_DT_F32, T, segs, s));
   return MOE_OK;
 }
@@ -170,6 +202,12 @@ moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t
   a.out = u; a.out_ld = de;
   a.topw = topw; a.route_token = rt; a.route_slot = rs; a.top_k = c->top_k; a.err = &P.hdr()->err;
   const int segs = (int)std::min<int64_t>(c->n_experts, (int64_t)T * c->top_k);
+  if (use_tc(c, T)) {
+    const int64_t R = (int64_t)T * c->top_k;
+    CU(launch_gemm_tc(a, EPI_SCALE, true, (int64_t)c->n_experts * de, R, c->n_experts,
+                      choose_bn(R / segs, segs, de), s));
+    return MOE_OK;
+  }
   CU(launch_gemv(a, wfmt_of(c), c->act_dtype, EPI_SCALE, true, T, segs, s));
   return MOE_OK;
 }
@@ -177,7 +215,7 @@ moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t
 moe_status_t run_latent_down(const moe_config_t* c, int T, const void* x, const moe_weights_t* w, void* x_l,
                              cudaStream_t s) {
   GemvArgs a = dense_args(w->w_lat_down, c->d_latent, c->d_model, x, T, x_l, c->d_latent);
-  CU(launch_gemv(a, dense_fmt(c), c->act_dtype, EPI_STORE, false, T, 1, s));
+  CU(run_dense(c, a, EPI_STORE, false, T, s));
   return MOE_OK;
 }
 
@@ -190,15 +228,15 @@ moe_status_t run_shared(const moe_config_t* c, int T, const void* x, const moe_w
   if (S > 0) {
     void* hs = P.at<void>(P.L.hs);
     GemvArgs up = dense_args(w->w_sh_up, S, d, x, T, hs, S);
-    CU(launch_gemv(up, dense_fmt(c), c->act_dtype, EPI_RELU2, f32, T, 1, s));
+    CU(run_dense(c, up, EPI_RELU2, f32, T, s));
     GemvArgs dn = dense_args(w->w_sh_down, d, S, hs, T, nullptr, d);
     if (!latent) {
       dn.out = y; dn.add_src = y_r; dn.add_ld = d;
-      CU(launch_gemv(dn, dense_fmt(c), c->act_dtype, EPI_ADD, f32, T, 1, s));
+      CU(run_dense(c, dn, EPI_ADD, f32, T, s));
       return MOE_OK;
     }
     dn.out = P.at<void>(P.L.ys);
-    CU(launch_gemv(dn, dense_fmt(c), c->act_dtype, EPI_STORE, true, T, 1, s));
+    CU(run_dense(c, dn, EPI_STORE, true, T, s));
   } else if (!latent) {
     // no shared expert: y = act(y_r); a combine over one row per token is a cast
     CU(launch_cast(y_r, (int64_t)T * d, y, c->act_dtype, s));
@@ -214,7 +252,7 @@ moe_status_t run_shared(const moe_config_t* c, int T, const void* x, const moe_w
   GemvArgs lu = dense_args(w->w_lat_up, d, c->d_latent, yl, T, y, d);
   lu.add_src = S > 0 ? P.at<float>(P.L.ys) : nullptr;
   lu.add_ld = d;
-  CU(launch_gemv(lu, dense_fmt(c), c->act_dtype, EPI_ADD, f32, T, 1, s));
+  CU(run_dense(c, lu, EPI_ADD, f32, T, s));
   return MOE_OK;
 }
 
@@ -363,11 +401,12 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
   int32_t* rt = P.at<int32_t>(P.L.route_token);
   int32_t* rs = P.at<int32_t>(P.L.route_slot);
   int32_t* tsr = P.at<int32_t>(P.L.tsr);
-  if ((st = run_dispatch(cfg, T, ids, x_e, P.at<int32_t>(P.L.counts), offsets, rt, rs, tsr, nullptr, P, s)) !=
+  void* x_packed = use_tc(cfg, T) ? P.at<void>(P.L.x_packed) : nullptr;
+  if ((st = run_dispatch(cfg, T, ids, x_e, P.at<int32_t>(P.L.counts), offsets, rt, rs, tsr, x_packed, P, s)) !=
       MOE_OK)
     return st;
   void* h = P.at<void>(P.L.h);
-  if ((st = run_up(cfg, T, x_e, nullptr, rt, offsets, w, h, P, s)) != MOE_OK) return st;
+  if ((st = run_up(cfg, T, x_e, x_packed, rt, offsets, w, h, P, s)) != MOE_OK) return st;
   float* u = P.at<float>(P.L.u);
   if ((st = run_down(cfg, T, h, offsets, rt, rs, topw, w, u, P, s)) != MOE_OK) return st;
   float* y_r = P.at<float>(P.L.y_r);

@@ -1,0 +1,37 @@
+// Output stage shared by the streaming GEMV and the tensor-core grouped GEMM:
+// one accumulated value v = sum_k X[row, k] W[f, k] becomes one stored output.
+#pragma once
+
+#include "internal.h"
+
+namespace moe {
+
+template <int EPI, bool OUT_F32, bool ACT_F32>
+__device__ __forceinline__ void epilogue(const GemvArgs& a, int seg, int row, int f, float v) {
+  if (a.W_gs) v *= a.W_gs[seg];
+  const int64_t o = (int64_t)row * a.out_ld + f;
+  float r;
+  if (EPI == EPI_RELU2) {
+    if (ACT_F32) {
+      const float u = fmaxf(v, 0.f);
+      r = u * u;
+    } else {
+      const float u = fmaxf(round_bf16(v), 0.f);
+      r = u * u;                    // exact in FP32: product of two 8-bit significands
+    }
+  } else if (EPI == EPI_SCALE) {
+    const int t = a.route_token[row], k = a.route_slot[row];
+    r = a.topw[(int64_t)t * a.top_k + k] * v;
+  } else if (EPI == EPI_ADD) {
+    r = v + (a.add_src ? a.add_src[(int64_t)row * a.add_ld + f] : 0.f);
+  } else {
+    r = v;
+  }
+  if (OUT_F32 || ACT_F32) {
+    reinterpret_cast<float*>(a.out)[o] = r;
+  } else {
+    reinterpret_cast<bf16*>(a.out)[o] = __float2bfloat16_rn(r);
+  }
+}
+
+}  // namespace moe

@@ -14,7 +14,7 @@
 // VL)", section "How the engine runs it" (a group's CTA decodes an expert's
 // tiles once for all of its rows) is the prior art; here the grouping comes
 // from the dispatch offsets and the split is over features and K.
-#include "internal.h"
+#include "epilogue.cuh"
 
 namespace moe {
 
@@ -44,34 +44,6 @@ __device__ __forceinline__ bool resolve_segment(const GemvArgs& a, int rows_per_
   s.row0 += rb;
   s.nrows = min(s.nrows - rb, rows_per_cta);
   return true;
-}
-
-template <int EPI, bool OUT_F32, bool ACT_F32>
-__device__ __forceinline__ void epilogue(const GemvArgs& a, int seg, int row, int f, float v) {
-  if (a.W_gs) v *= a.W_gs[seg];
-  const int64_t o = (int64_t)row * a.out_ld + f;
-  float r;
-  if (EPI == EPI_RELU2) {
-    if (ACT_F32) {
-      const float u = fmaxf(v, 0.f);
-      r = u * u;
-    } else {
-      const float u = fmaxf(round_bf16(v), 0.f);
-      r = u * u;                    // exact in FP32: product of two 8-bit significands
-    }
-  } else if (EPI == EPI_SCALE) {
-    const int t = a.route_token[row], k = a.route_slot[row];
-    r = a.topw[(int64_t)t * a.top_k + k] * v;
-  } else if (EPI == EPI_ADD) {
-    r = v + (a.add_src ? a.add_src[(int64_t)row * a.add_ld + f] : 0.f);
-  } else {
-    r = v;
-  }
-  if (OUT_F32 || ACT_F32) {
-    reinterpret_cast<float*>(a.out)[o] = r;
-  } else {
-    reinterpret_cast<bf16*>(a.out)[o] = __float2bfloat16_rn(r);
-  }
 }
 
 // ---------------------------------------------------------------------------

@@ -51,6 +51,12 @@ struct GemvArgs {
 cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_f32,
                         int max_rows, int grid_segments, cudaStream_t s);
 
+// Tensor-core grouped GEMM (tcgen05): same arguments as launch_gemv; X rows must
+// be contiguous (no gather).  w_rows/x_rows: rows of the W and X matrices (TMA
+// extents); E: segments (0 = dense); bn: rows per tile (power of two, 16..256).
+cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_rows, int64_t x_rows, int E, int bn,
+                           cudaStream_t s);
+
 // router
 cudaError_t launch_router_logits(const void* x, int act, int T, int d, const float* w_router, int E,
                                  float* logits, cudaStream_t s);
