@@ -206,21 +206,24 @@ def run_ours(args, rank, world, dev):
     rt = torch.empty(R, dtype=torch.int32, device=dev)
     rs = torch.empty(R, dtype=torch.int32, device=dev)
     tsr = torch.empty((T, K_), dtype=torch.int32, device=dev)
-    M.moe_dispatch(cfg, ids, counts, offsets, rt, rs, tsr, ws)
+    xp = torch.empty((R, shape.d_e), dtype=x.dtype, device=dev) if T > 64 else None
+    M.moe_dispatch(cfg, ids, counts, offsets, rt, rs, tsr, ws, x_e=x_e if xp is not None else None, x_packed=xp)
     h = torch.empty((R, shape.d_expert), dtype=x.dtype, device=dev)
 
     def up(i):
-        M.moe_experts_up(cfg, T, rt, offsets, layers[i % n_rep].weights, h, ws, x_e=x_e)
+        M.moe_experts_up(cfg, T, rt, offsets, layers[i % n_rep].weights, h, ws, x_e=x_e, x_packed=xp)
 
     for i in range(3):
         up(i)
-    k_up = max(20, args.steps)
+    k_up = max(20, min(args.steps, 200))
     c0 = M.load().moe_launch_count()
     ms_up = timed(up, k_up) / k_up
     assert M.load().moe_launch_count() - c0 == k_up, "expert up is expected to be one launch"
     ab = 2
     up_bytes = n_active * shape.d_expert * shape.d_e * ab + R * shape.d_e * ab + R * shape.d_expert * ab
+    up_flops = 2 * R * shape.d_expert * shape.d_e
     achieved = up_bytes / (ms_up / 1e3) / 1e9
+    achieved_tf = up_flops / (ms_up / 1e3) / 1e12
 
     # end to end through the C ABI with host buffers (copies inside the timed region)
     xh = x.cpu().pin_memory()
@@ -257,13 +260,17 @@ def run_ours(args, rank, world, dev):
             layers[0].forward(xs, ys, ids_out=idss)
             na = int(torch.unique(idss).numel())
             bb = layer_bytes(shape, na, Ts)["total"]
+            ff = layer_flops(shape, Ts)
             sweep[str(Ts)] = {"ms_per_step": round(mss, 5), "tokens_per_s": round(Ts / (mss / 1e3), 1),
                               "experts_active": na, "hbm_gb_per_s": round(bb / (mss / 1e3) / 1e9, 1),
-                              "hbm_frac": round(bb / (mss / 1e3) / 1e9 / pk["hbm_gbs"], 3)}
+                              "hbm_frac": round(bb / (mss / 1e3) / 1e9 / pk["hbm_gbs"], 3),
+                              "tflops": round(ff / (mss / 1e3) / 1e12, 1),
+                              "tensor_frac": round(ff / (mss / 1e3) / 1e12 / pk["bf16_tflops_sustained"], 3)}
 
     return {
         "value": value, "ms_per_step": ms_step, "n_active": n_active, "bytes": lb, "clocks": clk,
         "launches": int(n1 - n0), "err": err, "ms_up": ms_up, "up_bytes": up_bytes, "achieved_up": achieved,
+        "up_flops": up_flops, "achieved_up_tf": achieved_tf, "flops": layer_flops(shape, T),
         "peaks": pk, "e2e_s": e2e_s, "n_rep": n_rep, "sweep": sweep, "shape": shape, "T": T,
         "rep_bytes": one,
     }
@@ -393,8 +400,21 @@ def main():
     lb = r["bytes"]
     ab = 2 if shape.act_dtype != 0 else 4
     if rank == 0:
-        frac_up = r["achieved_up"] / pk["hbm_gbs"]
         layer_gbs = lb["total"] / (r["ms_per_step"] / 1e3) / 1e9
+        layer_tf = r["flops"] / (r["ms_per_step"] / 1e3) / 1e12
+        # the dominant kernel's bound: whichever ideal time (bytes / bandwidth, FLOPs / peak) is larger
+        up_tensor = r["up_flops"] / (pk["bf16_tflops"] * 1e12) > r["up_bytes"] / (pk["hbm_gbs"] * 1e9)
+        if up_tensor:
+            roof = {"bound": "tensor", "achieved": round(r["achieved_up_tf"], 1), "peak": pk["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": round(r["achieved_up_tf"] / pk["bf16_tflops"], 4),
+                    "algorithmic_flops_per_launch": int(r["up_flops"])}
+        else:
+            roof = {"bound": "hbm", "achieved": round(r["achieved_up"], 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(r["achieved_up"] / pk["hbm_gbs"], 4)}
+        roof.update({"kernel": "grouped expert up projection (moe_experts_up)", "traffic": None,
+                     "algorithmic_bytes_per_launch": int(r["up_bytes"]), "avg_launch_ms": round(r["ms_up"], 5),
+                     "peak_source": pk["source"] + (" (cuBLAS bf16 burst)" if up_tensor else " (burst copy)")})
+        layer_tensor = r["flops"] / (pk["bf16_tflops_sustained"] * 1e12) > lb["total"] / (pk["hbm_gbs"] * 1e9)
         line = {
             "metric": "MoE-layer tokens/s", "value": round(r["value"], 1), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -407,14 +427,13 @@ def main():
                        "l2": f"weights rotate over {r['n_rep']} seeded replicas "
                              f"({r['rep_bytes'] / 1e9:.2f} GB each); no step reads the previous step's weights",
                        "experts_active": r["n_active"]},
-            "roofline": {"bound": "hbm", "kernel": "grouped expert up projection (moe_experts_up)",
-                         "achieved": round(r["achieved_up"], 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(frac_up, 4), "traffic": None,
-                         "algorithmic_bytes_per_launch": int(r["up_bytes"]),
-                         "avg_launch_ms": round(r["ms_up"], 5), "peak_source": pk["source"] + " (burst copy)"},
-            "layer_roofline": {"bound": "hbm", "bytes_per_step": int(lb["total"]),
-                               "achieved": round(layer_gbs, 1), "unit": "GB/s",
-                               "frac": round(layer_gbs / pk["hbm_gbs"], 4), "bytes_breakdown": lb},
+            "roofline": roof,
+            "layer_roofline": {"bound": "tensor" if layer_tensor else "hbm", "bytes_per_step": int(lb["total"]),
+                               "flops_per_step": int(r["flops"]),
+                               "hbm_gb_per_s": round(layer_gbs, 1), "hbm_frac": round(layer_gbs / pk["hbm_gbs"], 4),
+                               "tflops": round(layer_tf, 1),
+                               "tensor_frac": round(layer_tf / pk["bf16_tflops_sustained"], 4),
+                               "tensor_peak": "sustained", "bytes_breakdown": lb},
             "clocks": r["clocks"],
             "gpu_launches": r["launches"],
             "device_error_word": r["err"],

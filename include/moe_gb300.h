@@ -224,12 +224,16 @@ int64_t moe_launch_count(void);
  * call time, such as code running after a host framework's memory pool has
  * claimed the device, serving loops that forbid allocation once started, or
  * work enqueued where cudaMalloc is not permitted.  Same arguments and
- * results as moe_router without logits/scores outputs; its scratch (logits,
- * scores and the error word) lives in a static device array of
- * MOE_NOALLOC_MAX_ROUTER_ELEMS * 8 + 256 bytes that every GPU loading this
- * library keeps until exit.
+ * results as moe_router without logits/scores outputs (the same kernels,
+ * bit-identical results); its scratch (logits, scores, the BF16 split of the
+ * router matrix used above 64 BF16 tokens, and the error word) lives in a
+ * static device array of MOE_NOALLOC_MAX_ROUTER_ELEMS * 8 +
+ * MOE_NOALLOC_MAX_SPLIT_ELEMS * 2 + 256 bytes (about 15 MiB) that every GPU
+ * loading this library keeps until exit.
  *   - Returns MOE_ERR_WORKSPACE, before enqueuing anything, when
- *     T * n_experts > MOE_NOALLOC_MAX_ROUTER_ELEMS.
+ *     T * n_experts > MOE_NOALLOC_MAX_ROUTER_ELEMS, or when T > 64 BF16
+ *     tokens need the split router matrix and 3 * n_experts * d_model >
+ *     MOE_NOALLOC_MAX_SPLIT_ELEMS.
  *   - The first call on a device looks the array up (cudaGetSymbolAddress,
  *     once per device, with that device current): make it before any stream
  *     capture.
@@ -238,6 +242,7 @@ int64_t moe_launch_count(void);
  *     reported by this entry point.
  *   - Calls no allocation routine (no cudaMalloc/cudaFree).                  */
 #define MOE_NOALLOC_MAX_ROUTER_ELEMS 131072
+#define MOE_NOALLOC_MAX_SPLIT_ELEMS 7340032
 moe_status_t moe_router_noalloc(const moe_config_t* cfg, int32_t T, const void* x,
                                 const float* w_router, const float* router_bias,
                                 int32_t* topk_ids, float* topk_w, void* stream);

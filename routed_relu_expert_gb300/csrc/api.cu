@@ -28,7 +28,7 @@ inline int act_bytes(const moe_config_t* c) { return c->act_dtype == MOE_DT_F32 
 inline int de_of(const moe_config_t* c) { return c->d_latent > 0 ? c->d_latent : c->d_model; }
 
 struct Layout {
-  size_t hdr, logits, scores, ids, topw, counts, offsets, active, tile_prefix;
+  size_t hdr, logits, scores, ids, topw, counts, offsets, active, tile_prefix, w_split;
   size_t route_token, route_slot, tsr, x_l, x_packed, h, u, y_r, y_rl, hs, ys, tile_counts, total;
 };
 
@@ -53,6 +53,7 @@ Layout make_layout(const moe_config_t* c, int32_t T) {
   L.offsets = take(off, (E + 1) * 4);
   L.active = take(off, E * 4);
   L.tile_prefix = take(off, (E + 1) * 4);
+  L.w_split = take(off, E * 3 * (size_t)c->d_model * 2);
   L.route_token = take(off, R * 4);
   L.route_slot = take(off, R * 4);
   L.tsr = take(off, R * 4);
@@ -149,7 +150,8 @@ struct Ptrs {
 // ---- steps -----------------------------------------------------------------
 moe_status_t run_router(const moe_config_t* c, int T, const void* x, const float* w_router, const float* bias,
                         float* logits, float* scores, int32_t* ids, float* w, const Ptrs& P, cudaStream_t s) {
-  CU(launch_router_logits(x, c->act_dtype, T, c->d_model, w_router, c->n_experts, logits, s));
+  CU(launch_router_logits(x, c->act_dtype, T, c->d_model, w_router, c->n_experts, logits, s,
+                          P.at<void>(P.L.w_split)));
   CU(launch_router_select(logits, T, c->n_experts, bias, c->n_group, c->topk_group, c->top_k,
                           c->norm_topk_prob, c->routed_scaling_factor, scores, ids, w, &P.hdr()->err, s));
   return MOE_OK;

@@ -13,6 +13,8 @@
 // (expert, token, slot) because a token names an expert at most once.
 #include "internal.h"
 
+#include <algorithm>
+
 namespace moe {
 
 namespace {
@@ -70,13 +72,11 @@ __device__ void warp_histograms(const int32_t* __restrict__ ids, int r0, int r1,
 
 // Scatter of routes [r0, r1) using per-warp running bases hist[warp][E].
 __device__ void warp_scatter(const int32_t* __restrict__ ids, int r0, int r1, int E, int K, int* hist,
-                             int32_t* route_token, int32_t* route_slot, int32_t* token_slot_row,
-                             const void* x_e, void* x_packed, int de, int elem_bytes) {
+                             int32_t* route_token, int32_t* route_slot, int32_t* token_slot_row) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n = r1 - r0;
   const int per = (int)ceil_div(ceil_div(n, kWarps), 32) * 32;
   const int b = r0 + warp * per, bend = min(r1, b + per);
-  const int row_vecs = de * elem_bytes / 16;
   for (int base = b; base < bend; base += 32) {
     const int r = base + lane;
     int e = -1;
@@ -97,18 +97,29 @@ __device__ void warp_scatter(const int32_t* __restrict__ ids, int r0, int r1, in
         route_slot[pos] = r % K;
       }
     }
-    if (x_packed) {
-      // copy the gathered rows: the whole warp moves one 16-byte column slice set per route
-      for (int i = 0; i < 32; ++i) {
-        const int p = __shfl_sync(0xffffffffu, pos, i);
-        const int rr = base + i;
-        if (rr >= bend || p < 0) continue;
-        const int tok = rr / K;
-        const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(x_e) +
-                                                          (int64_t)tok * de * elem_bytes);
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<char*>(x_packed) + (int64_t)p * de * elem_bytes);
-        for (int v = lane; v < row_vecs; v += 32) dst[v] = src[v];
-      }
+  }
+}
+
+// x_packed[j] = x_e[route_token[j]]: one warp per packed row, every 16-byte
+// piece of the row loaded before any is stored.
+__global__ void __launch_bounds__(256) pack_rows_kernel(const uint4* __restrict__ x_e,
+                                                        const int32_t* __restrict__ route_token,
+                                                        const int32_t* __restrict__ offsets, int E, int row_vecs,
+                                                        uint4* __restrict__ x_packed) {
+  const int R = offsets[E];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int j = blockIdx.x * 8 + warp; j < R; j += gridDim.x * 8) {
+    const uint4* src = x_e + (int64_t)route_token[j] * row_vecs;
+    uint4* dst = x_packed + (int64_t)j * row_vecs;
+    constexpr int U = 6;
+    for (int v0 = lane; v0 < row_vecs; v0 += 32 * U) {
+      uint4 q[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (v0 + 32 * u < row_vecs) q[u] = __ldg(src + v0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (v0 + 32 * u < row_vecs) dst[v0 + 32 * u] = q[u];
     }
   }
 }
@@ -171,8 +182,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_single(const DispatchArgs a
     for (int w = 0; w < kWarps; ++w) hist[w * a.E + e] += off;
   write_schedule(a, e, total, off, tmp32);
   __syncthreads();
-  warp_scatter(a.ids, 0, R, a.E, a.K, hist, a.route_token, a.route_slot, a.token_slot_row, a.x_e,
-               a.x_packed, a.de, a.elem_bytes);
+  warp_scatter(a.ids, 0, R, a.E, a.K, hist, a.route_token, a.route_slot, a.token_slot_row);
 }
 
 // ---------------------------------------------------------------------------
@@ -231,11 +241,20 @@ __global__ void __launch_bounds__(kThreads) dispatch_scatter(const DispatchArgs 
     }
   }
   __syncthreads();
-  warp_scatter(a.ids, r0, r1, a.E, a.K, hist, a.route_token, a.route_slot, a.token_slot_row, a.x_e,
-               a.x_packed, a.de, a.elem_bytes);
+  warp_scatter(a.ids, r0, r1, a.E, a.K, hist, a.route_token, a.route_slot, a.token_slot_row);
 }
 
 constexpr int kSingleMaxRoutes = 4096;
+
+cudaError_t launch_pack(const DispatchArgs& a, cudaStream_t s) {
+  if (!a.x_packed || !a.x_e) return cudaSuccess;
+  const int R = a.T * a.K;
+  const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(R, 8), 16384);
+  pack_rows_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(a.x_e), a.route_token, a.offsets, a.E,
+                                        a.de * a.elem_bytes / 16, reinterpret_cast<uint4*>(a.x_packed));
+  count_launches(1);
+  return cudaGetLastError();
+}
 
 }  // namespace
 
@@ -253,7 +272,9 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     dispatch_single<<<1, kThreads, smem, s>>>(a);
     count_launches(1);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_pack(a, s);
   }
   const int n_tiles = (int)ceil_div(a.T, kTileTokens);
   const size_t smem = (size_t)(kWarps * a.E) * sizeof(int);
@@ -267,7 +288,9 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
   count_launches(1);
   dispatch_scatter<<<n_tiles, kThreads, smem, s>>>(a);
   count_launches(1);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_pack(a, s);
 }
 
 }  // namespace moe

@@ -181,9 +181,55 @@ __device__ __forceinline__ int box_index(int rows) {
   return i;
 }
 
+// Epilogue of 32 accumulator columns (rows row0+c0 .. +31) of one feature f.
+// Per-row inputs are fetched before any store: the routing weight of each
+// column by one lane and broadcast, the added term as 32 independent loads.
+template <int EPI, bool OUT_F32>
+__device__ __forceinline__ void tile_epilogue(const GemvArgs& a, const Tile& ti, int c0, int f, bool fv, int lane,
+                                              float (&v)[32]) {
+  const int nc = min(32, ti.rows - c0);
+  if (EPI == EPI_SCALE) {
+    float wl = 0.f;
+    if (lane < nc) {
+      const int r = ti.row0 + c0 + lane;
+      wl = a.topw[(int64_t)a.route_token[r] * a.top_k + a.route_slot[r]];
+    }
+#pragma unroll
+    for (int c = 0; c < 32; ++c) v[c] *= __shfl_sync(0xffffffffu, wl, c);
+  }
+  if (!fv) return;
+  if (a.W_gs) {
+    const float gs = a.W_gs[ti.seg];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) v[c] *= gs;
+  }
+  if (EPI == EPI_ADD && a.add_src) {
+    float add[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+      add[c] = c < nc ? a.add_src[(int64_t)(ti.row0 + c0 + c) * a.add_ld + f] : 0.f;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) v[c] += add[c];
+  }
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    if (c >= nc) break;
+    float r = v[c];
+    if (EPI == EPI_RELU2) {
+      const float u = fmaxf(round_bf16(r), 0.f);
+      r = u * u;
+    }
+    const int64_t o = (int64_t)(ti.row0 + c0 + c) * a.out_ld + f;
+    if (OUT_F32 || EPI == EPI_SCALE)
+      reinterpret_cast<float*>(a.out)[o] = r;
+    else
+      reinterpret_cast<bf16*>(a.out)[o] = __float2bfloat16_rn(r);
+  }
+}
+
 template <int EPI, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, int E, int m_tiles, int bn) {
+    tc_gemm_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, int E, int m_tiles, int bn, int b_period) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -275,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = base + stage * STAGE_BYTES;
           mbar_expect_tx(full_bar(stage), A_BYTES + bbytes);
           tma_load_2d(sa, &maps.a, kb * BK, a_row, full_bar(stage));
-          tma_load_2d(sa + A_BYTES, &maps.b[bi], kb * BK, ti.row0, full_bar(stage));
+          tma_load_2d(sa + A_BYTES, &maps.b[bi], (kb % b_period) * BK, ti.row0, full_bar(stage));
           pend[stage] = (int)phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -343,11 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = 0; c0 < ti.rows; c0 += 32) {
         float v[32];
         tmem_ld32(tb + (uint32_t)c0, v);
-        if (fv) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c0 + c < ti.rows) epilogue<EPI, OUT_F32, false>(a, ti.seg, ti.row0 + c0 + c, f, v[c]);
-        }
+        tile_epilogue<EPI, OUT_F32>(a, ti, c0, f, fv, lane, v);
       }
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
@@ -408,7 +450,8 @@ size_t smem_bytes(int E) {
 }
 
 template <int EPI, bool OUT_F32>
-cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, int bn, int grid, cudaStream_t s) {
+cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, int bn, int b_period, int grid,
+                     cudaStream_t s) {
   const size_t smem = smem_bytes(kMaxSegments);
   static bool attr_set = false;
   if (!attr_set) {
@@ -417,7 +460,7 @@ cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  tc_gemm_kernel<EPI, OUT_F32><<<grid, kThreads, smem, s>>>(maps, a, E, m_tiles, bn);
+  tc_gemm_kernel<EPI, OUT_F32><<<grid, kThreads, smem, s>>>(maps, a, E, m_tiles, bn, b_period);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -425,25 +468,28 @@ cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, 
 }  // namespace
 
 cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_rows, int64_t x_rows, int E, int bn,
-                           cudaStream_t s) {
+                           cudaStream_t s, int x_cols) {
   if (a.K % BK != 0 || bn < 16 || bn > BN_MAX || (bn & (bn - 1)) || E > kMaxSegments) return cudaErrorNotSupported;
+  if (x_cols <= 0) x_cols = a.K;
+  if (x_cols % BK != 0 || a.K % x_cols != 0) return cudaErrorNotSupported;
   TcMaps maps;
   if (!make_map(&maps.a, a.W, w_rows, a.K, a.K, BM)) return cudaErrorInvalidValue;
   for (int i = 0; i < N_BOX; ++i)
-    if (!make_map(&maps.b[i], a.X, x_rows, a.K, a.x_ld, 16 << i)) return cudaErrorInvalidValue;
+    if (!make_map(&maps.b[i], a.X, x_rows, x_cols, a.x_ld, 16 << i)) return cudaErrorInvalidValue;
   const int m_tiles = (a.N + BM - 1) / BM;
+  const int b_period = x_cols / BK;
   int grid = num_sms();
   if (!a.offsets) grid = (int)std::min<int64_t>(grid, ceil_div(a.dense_rows, bn) * m_tiles);
   if (grid <= 0) return cudaSuccess;
   switch (epi) {
-    case EPI_RELU2: return launch_t<EPI_RELU2, false>(maps, a, E, m_tiles, bn, grid, s);
-    case EPI_SCALE: return launch_t<EPI_SCALE, true>(maps, a, E, m_tiles, bn, grid, s);
+    case EPI_RELU2: return launch_t<EPI_RELU2, false>(maps, a, E, m_tiles, bn, b_period, grid, s);
+    case EPI_SCALE: return launch_t<EPI_SCALE, true>(maps, a, E, m_tiles, bn, b_period, grid, s);
     case EPI_STORE:
-      return out_f32 ? launch_t<EPI_STORE, true>(maps, a, E, m_tiles, bn, grid, s)
-                     : launch_t<EPI_STORE, false>(maps, a, E, m_tiles, bn, grid, s);
+      return out_f32 ? launch_t<EPI_STORE, true>(maps, a, E, m_tiles, bn, b_period, grid, s)
+                     : launch_t<EPI_STORE, false>(maps, a, E, m_tiles, bn, b_period, grid, s);
     default:
-      return out_f32 ? launch_t<EPI_ADD, true>(maps, a, E, m_tiles, bn, grid, s)
-                     : launch_t<EPI_ADD, false>(maps, a, E, m_tiles, bn, grid, s);
+      return out_f32 ? launch_t<EPI_ADD, true>(maps, a, E, m_tiles, bn, b_period, grid, s)
+                     : launch_t<EPI_ADD, false>(maps, a, E, m_tiles, bn, b_period, grid, s);
   }
 }
 

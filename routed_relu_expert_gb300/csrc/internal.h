@@ -54,12 +54,17 @@ cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_
 // Tensor-core grouped GEMM (tcgen05): same arguments as launch_gemv; X rows must
 // be contiguous (no gather).  w_rows/x_rows: rows of the W and X matrices (TMA
 // extents); E: segments (0 = dense); bn: rows per tile (power of two, 16..256).
+// x_cols < K (a divisor of K) re-reads X's first x_cols columns for every
+// x_cols-wide slice of W's K (used to multiply X by side-by-side split parts of
+// one matrix); 0 = K.
 cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_rows, int64_t x_rows, int E, int bn,
-                           cudaStream_t s);
+                           cudaStream_t s, int x_cols = 0);
 
 // router
+// w_split: scratch of E * 3d BF16 for the tensor-core path (many BF16 tokens);
+// nullptr keeps the FP32 SIMT kernels.
 cudaError_t launch_router_logits(const void* x, int act, int T, int d, const float* w_router, int E,
-                                 float* logits, cudaStream_t s);
+                                 float* logits, cudaStream_t s, void* w_split = nullptr);
 cudaError_t launch_router_select(const float* logits, int T, int E, const float* bias, int G, int TG,
                                  int K, int norm, float rsf, float* scores, int32_t* ids, float* w,
                                  int32_t* err, cudaStream_t s);

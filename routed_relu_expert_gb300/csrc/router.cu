@@ -6,6 +6,7 @@
 // ties to the lower id).
 #include "internal.h"
 
+#include <algorithm>
 #include <climits>
 
 namespace moe {
@@ -264,6 +265,27 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
   }
 }
 
+// W (FP32) -> [W1 | W2 | W3] (BF16, side by side along K): W1 = bf16(W),
+// W2 = bf16(W - W1), W3 = bf16(W - W1 - W2).  Each difference is exact in FP32
+// and each term keeps 8 more significand bits, so sum(x * Wi) with FP32
+// accumulation carries FP32-level precision for BF16 x (exact in BF16).
+__global__ void split_bf16x3_kernel(const float* __restrict__ w, int E, int d, bf16* __restrict__ out) {
+  const int64_t n = (int64_t)E * d;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = i / d, j = i - e * d;
+    const float v = w[i];
+    const bf16 w1 = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(w1);
+    const bf16 w2 = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(w2);
+    const bf16 w3 = __float2bfloat16_rn(r2);
+    bf16* row = out + e * 3 * (int64_t)d;
+    row[j] = w1;
+    row[d + j] = w2;
+    row[2 * (int64_t)d + j] = w3;
+  }
+}
+
 template <int P>
 cudaError_t launch_select_p(const float* logits, int T, int E, const float* bias, int G, int TG, int K,
                             int norm, float rsf, float* scores, int32_t* ids, float* w, int32_t* err,
@@ -289,8 +311,21 @@ cudaError_t launch_small(const void* x, int act, int T, int d, const float* w, i
 }  // namespace
 
 cudaError_t launch_router_logits(const void* x, int act, int T, int d, const float* w_router, int E,
-                                 float* logits, cudaStream_t s) {
+                                 float* logits, cudaStream_t s, void* w_split) {
   if (T <= 0) return cudaSuccess;
+  if (w_split && act == MOE_DT_BF16 && T > 64 && E % 32 == 0 && d % 64 == 0) {
+    const int64_t n = (int64_t)E * d;
+    split_bf16x3_kernel<<<(unsigned)std::min<int64_t>(ceil_div(n, 256), 2048), 256, 0, s>>>(
+        w_router, E, d, reinterpret_cast<bf16*>(w_split));
+    count_launches(1);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    GemvArgs a{};
+    a.W = w_split; a.N = E; a.K = 3 * d; a.X = x; a.x_ld = d; a.dense_rows = T;
+    a.out = logits; a.out_ld = E;
+    const int bn = T >= 64 * 152 ? 64 : 32;
+    return launch_gemm_tc(a, EPI_STORE, true, E, T, 0, bn, s, d);
+  }
   if (T <= 4) return launch_small<4>(x, act, T, d, w_router, E, logits, s);
   if (T <= 16) return launch_small<16>(x, act, T, d, w_router, E, logits, s);
   if (T <= 32) return launch_small<32>(x, act, T, d, w_router, E, logits, s);

@@ -2,19 +2,25 @@
 // memory, e.g. code that runs after its host framework's pool has claimed all
 // device memory, runtimes that forbid allocation once serving starts, or code
 // enqueued where cudaMalloc is not permitted.  The scratch the router needs
-// between its two kernels (logits, scores, the device error word) lives in a
-// fixed static device array of this file instead of a caller workspace.
+// between its kernels (logits, scores, the split router matrix, the device
+// error word) lives in a fixed static device array of this file instead of a
+// caller workspace.
 //
 // Properties the caller must know:
-//  - The array (MOE_NOALLOC_MAX_ROUTER_ELEMS * 8 + 256 bytes) exists on every
-//    GPU that loads the library, for the life of the process.
+//  - The array (MOE_NOALLOC_MAX_ROUTER_ELEMS * 8 + MOE_NOALLOC_MAX_SPLIT_ELEMS
+//    * 2 + 256 bytes, about 15 MiB) exists on every GPU that loads the
+//    library, for the life of the process.
+//  - It computes exactly what moe_router computes, by the same kernels: for
+//    more than 64 BF16 tokens that includes the BF16 split of the router
+//    matrix, which is why the array also holds E * 3d BF16 values.
 //  - The first call on a device looks up the array's device address with
 //    cudaGetSymbolAddress (once per device, with that device current); make
 //    that first call before any stream capture.
 //  - Every call shares the one array: two calls whose work overlaps on the GPU
 //    (different streams, no ordering between them) race on it.  The error
 //    word is cleared at the start of every call; logits and scores are fully
-//    rewritten by each call before they are read.
+//    rewritten by each call before they are read, and so is the split router
+//    matrix when it is used.
 //  - The error word stays in the array: this entry point does not report
 //    device-side error bits.
 #include "internal.h"
@@ -24,10 +30,13 @@
 namespace {
 
 constexpr int64_t kMaxElems = MOE_NOALLOC_MAX_ROUTER_ELEMS;
+constexpr int64_t kMaxSplit = MOE_NOALLOC_MAX_SPLIT_ELEMS;
 constexpr size_t kHeaderBytes = 256;
 
-// [0, 256): error word;  then logits [kMaxElems] f32;  then scores [kMaxElems] f32
-static __device__ __align__(256) unsigned char g_router_scratch[kHeaderBytes + 2 * kMaxElems * sizeof(float)];
+// [0, 256): error word;  logits [kMaxElems] f32;  scores [kMaxElems] f32;
+// split router matrix [kMaxSplit] bf16
+static __device__ __align__(256) unsigned char
+    g_router_scratch[kHeaderBytes + 2 * kMaxElems * sizeof(float) + kMaxSplit * 2];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
@@ -60,6 +69,8 @@ extern "C" moe_status_t moe_router_noalloc(const moe_config_t* cfg, int32_t T, c
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if ((int64_t)T * cfg->n_experts > kMaxElems) return MOE_ERR_WORKSPACE;   // beyond the static scratch
+  const bool needs_split = cfg->act_dtype == MOE_DT_BF16 && T > 64;
+  if (needs_split && (int64_t)3 * cfg->n_experts * cfg->d_model > kMaxSplit) return MOE_ERR_WORKSPACE;
   if (!x || !w_router || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(topk_ids) || !aligned16(topk_w) ||
       (router_bias && !aligned16(router_bias)))
@@ -69,9 +80,10 @@ extern "C" moe_status_t moe_router_noalloc(const moe_config_t* cfg, int32_t T, c
   int32_t* err = reinterpret_cast<int32_t*>(base);
   float* logits = reinterpret_cast<float*>(reinterpret_cast<char*>(base) + kHeaderBytes);
   float* scores = logits + kMaxElems;
+  void* split = reinterpret_cast<void*>(scores + kMaxElems);
   cudaStream_t s = (cudaStream_t)stream;
   if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (moe::launch_router_logits(x, cfg->act_dtype, T, cfg->d_model, w_router, cfg->n_experts, logits, s) !=
+  if (moe::launch_router_logits(x, cfg->act_dtype, T, cfg->d_model, w_router, cfg->n_experts, logits, s, split) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   if (moe::launch_router_select(logits, T, cfg->n_experts, router_bias, cfg->n_group, cfg->topk_group,

@@ -6,8 +6,9 @@ allocation once started, or they enqueue work where cudaMalloc is not
 permitted.  This entry point keeps its scratch in a static device array of the
 library instead of a workspace.  The test calls it through the C ABI and
 checks it against moe_router (the workspace entry point) on two calls in a
-row, with the tolerances the other router tests use (ids exact, weights within
-1e-6), and checks that an oversized call is refused before any work.
+row (it runs the same kernels, so ids must be equal and weights within the
+1e-6 the other router tests use), and checks that an oversized call is
+refused before any work.
 """
 import ctypes
 
