@@ -29,7 +29,7 @@ inline int de_of(const moe_config_t* c) { return c->d_latent > 0 ? c->d_latent :
 
 struct Layout {
   size_t hdr, logits, scores, ids, topw, counts, offsets, active, tile_prefix, w_split;
-  size_t route_token, route_slot, tsr, x_l, x_packed, h, u, y_r, y_rl, hs, ys, tile_counts, total;
+  size_t route_token, route_slot, tsr, x_l, x_packed, h, u, y_r, y_rl, hs, ys, tile_counts, w_deq, total;
 };
 
 inline size_t take(size_t& off, size_t bytes) {
@@ -66,6 +66,8 @@ Layout make_layout(const moe_config_t* c, int32_t T) {
   L.hs = take(off, t * (size_t)c->d_shared * ab);
   L.ys = take(off, t * (size_t)c->d_model * 4);
   L.tile_counts = take(off, dispatch_tile_count_elems(T, c->top_k, c->n_experts) * 4);
+  // NVFP4 experts on the tensor-core path: one expert-weight tensor dequantised to BF16
+  L.w_deq = take(off, (c->expert_dtype == MOE_DT_NVFP4 && T > kDecodeMaxT) ? E * (size_t)c->d_expert * de * 2 : 0);
   L.total = (off + 255) & ~(size_t)255;
   return L;
 }
@@ -86,7 +88,8 @@ moe_status_t check_config(const moe_config_t* c) {
     return MOE_ERR_INVALID_ARG;
   if ((c->expert_dtype == MOE_DT_F32) != (c->act_dtype == MOE_DT_F32)) return MOE_ERR_UNSUPPORTED;
   if (c->d_model % 64 || c->d_expert % 64 || c->d_latent % 64 || c->d_shared % 64) return MOE_ERR_UNSUPPORTED;
-  if (c->expert_dtype == MOE_DT_NVFP4) return MOE_ERR_UNSUPPORTED;   // NVFP4 kernels: not built yet
+  if (c->expert_dtype == MOE_DT_NVFP4 && (de_of(c) % 128 || c->d_expert % 128)) return MOE_ERR_UNSUPPORTED;
+  if (c->expert_dtype == MOE_DT_NVFP4 && c->act_dtype != MOE_DT_BF16) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -111,7 +114,7 @@ inline int dense_fmt(const moe_config_t* c) { return c->act_dtype == MOE_DT_F32 
 
 // tensor-core path: BF16 layers with more than kDecodeMaxT tokens
 inline bool use_tc(const moe_config_t* c, int T) {
-  return c->act_dtype == MOE_DT_BF16 && c->expert_dtype == MOE_DT_BF16 && T > kDecodeMaxT;
+  return c->act_dtype == MOE_DT_BF16 && c->expert_dtype != MOE_DT_F32 && T > kDecodeMaxT;
 }
 
 // Rows per tensor-core tile: 256, halved while the estimated tile count stays
@@ -177,14 +180,22 @@ moe_status_t run_dispatch(const moe_config_t* c, int T, const int32_t* ids, cons
 moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x_packed, const int32_t* rt,
                     const int32_t* offsets, const moe_weights_t* w, void* h, const Ptrs& P, cudaStream_t s) {
   const int de = de_of(c), I = c->d_expert;
+  const bool fp4 = c->expert_dtype == MOE_DT_NVFP4;
   GemvArgs a{};
-  a.W = w->w_up; a.w_seg_stride = (int64_t)I * de; a.N = I; a.K = de;
+  a.W = w->w_up; a.w_seg_stride = fp4 ? (int64_t)I * de / 2 : (int64_t)I * de; a.N = I; a.K = de;
+  if (fp4) { a.W_sf = w->w_up_sf; a.W_gs = w->w_up_gs; a.sf_seg_stride = (int64_t)I * de / 16; }
   a.X = x_packed ? x_packed : x_e; a.x_ld = de; a.gather = x_packed ? nullptr : rt;
   a.offsets = offsets; a.active = P.at<int32_t>(P.L.active); a.hdr = P.hdr();
   a.out = h; a.out_ld = I; a.err = &P.hdr()->err;
   const int segs = (int)std::min<int64_t>(c->n_experts, (int64_t)T * c->top_k);
   if (use_tc(c, T) && x_packed) {
     const int64_t R = (int64_t)T * c->top_k;
+    if (fp4) {
+      void* deq = P.at<void>(P.L.w_deq);
+      CU(launch_dequant_nvfp4((const uint8_t*)w->w_up, w->w_up_sf,
+                              (int64_t)c->n_experts * I * de, deq, s));
+      a.W = deq; a.w_seg_stride = (int64_t)I * de; a.W_sf = nullptr;
+    }
     CU(launch_gemm_tc(a, EPI_RELU2, false, (int64_t)c->n_experts * I, R, c->n_experts,
                       choose_bn(R / segs, segs, I), s));
     return MOE_OK;
@@ -197,8 +208,10 @@ moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t
                       const int32_t* rs, const float* topw, const moe_weights_t* w, float* u, const Ptrs& P,
                       cudaStream_t s) {
   const int de = de_of(c), I = c->d_expert;
+  const bool fp4 = c->expert_dtype == MOE_DT_NVFP4;
   GemvArgs a{};
-  a.W = w->w_down; a.w_seg_stride = (int64_t)de * I; a.N = de; a.K = I;
+  a.W = w->w_down; a.w_seg_stride = fp4 ? (int64_t)de * I / 2 : (int64_t)de * I; a.N = de; a.K = I;
+  if (fp4) { a.W_sf = w->w_down_sf; a.W_gs = w->w_down_gs; a.sf_seg_stride = (int64_t)de * I / 16; }
   a.X = h; a.x_ld = I;
   a.offsets = offsets; a.active = P.at<int32_t>(P.L.active); a.hdr = P.hdr();
   a.out = u; a.out_ld = de;
@@ -206,6 +219,11 @@ moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t
   const int segs = (int)std::min<int64_t>(c->n_experts, (int64_t)T * c->top_k);
   if (use_tc(c, T)) {
     const int64_t R = (int64_t)T * c->top_k;
+    if (fp4) {
+      void* deq = P.at<void>(P.L.w_deq);
+      CU(launch_dequant_nvfp4((const uint8_t*)w->w_down, w->w_down_sf, (int64_t)c->n_experts * de * I, deq, s));
+      a.W = deq; a.w_seg_stride = (int64_t)de * I; a.W_sf = nullptr;
+    }
     CU(launch_gemm_tc(a, EPI_SCALE, true, (int64_t)c->n_experts * de, R, c->n_experts,
                       choose_bn(R / segs, segs, de), s));
     return MOE_OK;
@@ -261,7 +279,14 @@ moe_status_t run_shared(const moe_config_t* c, int T, const void* x, const moe_w
 moe_status_t check_weights(const moe_config_t* c, const moe_weights_t* w, bool experts, bool router, bool dense) {
   if (!w) return MOE_ERR_INVALID_ARG;
   if (router) { REQ(w->w_router); OPT(w->router_bias); }
-  if (experts) { REQ(w->w_up); REQ(w->w_down); }
+  if (experts) {
+    REQ(w->w_up); REQ(w->w_down);
+    if (c->expert_dtype == MOE_DT_NVFP4) {
+      if (!w->w_up_sf || !w->w_down_sf) return MOE_ERR_INVALID_ARG;
+      REQ(w->w_up_gs); REQ(w->w_down_gs);
+      if (((uintptr_t)w->w_up_sf & 1u) || ((uintptr_t)w->w_down_sf & 1u)) return MOE_ERR_INVALID_ARG;
+    }
+  }
   if (dense) {
     if (c->d_latent > 0) { REQ(w->w_lat_down); REQ(w->w_lat_up); }
     if (c->d_shared > 0) { REQ(w->w_sh_up); REQ(w->w_sh_down); }

@@ -9,8 +9,8 @@ import pytest
 import torch
 
 from oracle import moe_oracle as O
-from synth import (NANO_DECODE, NANO_PREFILL, ROUTER_ONLY_GROUPED, SUPER_LATENT, TINY_FP32, make_weights,
-                   make_x, scaled)
+from synth import (NANO_DECODE, NANO_PREFILL, ROUTER_ONLY_GROUPED, SUPER_LATENT, SUPER_NVFP4, TINY_FP32,
+                   make_weights, make_x, scaled)
 
 pytestmark = pytest.mark.gpu
 
@@ -23,6 +23,9 @@ SMALL_NANO = scaled(NANO_DECODE, name="nano_scaled", d_model=512, n_experts=32, 
                     d_shared=384, weight_seed=11, tokens=())
 SMALL_SUPER = scaled(SUPER_LATENT, name="super_scaled", d_model=512, d_latent=256, n_experts=64, top_k=6,
                      n_group=8, topk_group=4, d_expert=320, d_shared=448, weight_seed=13, tokens=())
+SMALL_NVFP4 = scaled(SUPER_LATENT, name="nvfp4_scaled", d_model=512, d_latent=256, n_experts=64, top_k=6,
+                     n_group=8, topk_group=4, d_expert=384, d_shared=448, expert_dtype=2, weight_seed=19,
+                     tokens=())
 
 
 def _parity(shape, T, sample=None, seed_stream=0):
@@ -74,6 +77,20 @@ def test_super_latent_full_size(T):
 
 def test_super_latent_256_sampled():
     _parity(SUPER_LATENT, 256, sample=48)
+
+
+@pytest.mark.parametrize("T", [1, 9, 64, 65, 200])
+def test_scaled_nvfp4_layer(T):
+    _parity(SMALL_NVFP4, T)
+
+
+@pytest.mark.parametrize("T", [1, 64])
+def test_super_nvfp4_full_size(T):
+    _parity(SUPER_NVFP4, T)
+
+
+def test_super_nvfp4_8192_sampled():
+    _parity(SUPER_NVFP4, 8192, sample=24)
 
 
 def test_router_grouped_case_from_the_router_parity_test():
