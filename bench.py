@@ -220,7 +220,9 @@ def run_ours(args, rank, world, dev):
     ms_up = timed(up, k_up) / k_up
     assert M.load().moe_launch_count() - c0 == k_up, "expert up is expected to be one launch"
     ab = 2
-    up_bytes = n_active * shape.d_expert * shape.d_e * ab + R * shape.d_e * ab + R * shape.d_expert * ab
+    w_up_bytes = (shape.d_expert * shape.d_e // 2 + shape.d_expert * shape.d_e // 16 + 4
+                  if shape.expert_dtype == 2 else shape.d_expert * shape.d_e * ab)
+    up_bytes = n_active * w_up_bytes + R * shape.d_e * ab + R * shape.d_expert * ab
     up_flops = 2 * R * shape.d_expert * shape.d_e
     achieved = up_bytes / (ms_up / 1e3) / 1e9
     achieved_tf = up_flops / (ms_up / 1e3) / 1e12

@@ -16,6 +16,8 @@
 // from the dispatch offsets and the split is over features and K.
 #include "epilogue.cuh"
 
+#include <cuda_fp16.h>
+
 #include <algorithm>
 
 namespace moe {
@@ -141,96 +143,124 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a
 // NVFP4 weights (E2M1 values, one E4M3 scale per 16 K-elements, FP32 per-tensor
 // scale), BF16 activations.  A warp streams 128-wide K chunks: 16 bytes of row
 // g and of row g+8 per thread (32 values each) plus their two block scales.
-// Each byte (two values) becomes a BF16 pair through a 256-entry table kept in
-// 32 bank-private copies, then one exact BF16 multiply applies the block
-// scale (E2M1 x E4M3 needs at most 6 significant bits); the per-tensor scale
-// multiplies the FP32 result in the epilogue.  MMA k positions are the same
-// consistent permutation trick as the BF16 kernel: MMA i of a chunk takes this
-// thread's values 4i..4i+3 of each row and the matching activations.
+// MMA k positions are the same consistent permutation as the BF16 kernel: MMA
+// i of a chunk takes this thread's values 4i..4i+3 of each row and the
+// matching activations.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t e2m1_pair_bf16(uint32_t byte) {
-  const uint16_t mag[8] = {0x0000, 0x3F00, 0x3F80, 0x3FC0, 0x4000, 0x4040, 0x4080, 0x40C0};
-  const uint32_t lo = mag[byte & 7] | ((byte & 8u) << 12);
-  const uint32_t hi = mag[(byte >> 4) & 7] | (((byte >> 7) & 1u) << 15);
-  return lo | (hi << 16);
+// Each warp owns 16 features of the segment over the whole K, so partial sums
+// never leave registers; the next chunk's weight bytes are requested before
+// the current chunk is decoded.  Values are decoded by the hardware E2M1 and
+// E4M3 conversions to FP16 and the block scale is applied by an exact FP16
+// multiply (E2M1 x E4M3 spans 2^-10 .. 2688 with at most 6 significant bits);
+// the MMA runs in FP16 with the BF16 activations converted to FP16, which is
+// exact for magnitudes in [2^-14, 65504] (smaller ones keep FP16's subnormal
+// precision); accumulation is FP32 and the per-tensor scale multiplies the
+// FP32 result.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// E4M3 byte -> FP32: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent
-// field 0 is subnormal (M * 2^-9); 0x7F / 0xFF are NaN.
-__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
-  const uint32_t s = (b & 0x80u) << 24, E = (b >> 3) & 15u, M = b & 7u;
-  if (E == 15u && M == 7u) return __uint_as_float(0x7FC00000u | s);
-  if (E == 0u) return __uint_as_float(s | __float_as_uint((float)M * 0.001953125f));
-  return __uint_as_float(s | ((E + 120u) << 23) | (M << 20));
+// the 8 values of one 32-bit word of NVFP4 bytes as 4 FP16 pairs (byte j -> pair j,
+// its low nibble in the low half)
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
+
+// two E4M3 scale bytes (low byte first) as an FP16 pair
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t s16) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)s16));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+  return *reinterpret_cast<uint32_t*>(&h);
 }
 
 template <int EPI, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 3) gemv_nvfp4_kernel(const GemvArgs a) {
   constexpr int NT = 2;
-  constexpr int U = 2;
-  __shared__ uint32_t lut[256 * 32];
-  __shared__ float red[kWarps][NT][128];
-  for (int i = threadIdx.x; i < 256 * 32; i += kThreads) lut[i] = e2m1_pair_bf16((uint32_t)(i >> 5));
-  __syncthreads();
-
   Seg sg;
   if (!resolve_segment(a, 1 << 30, sg)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
-  const int f0 = blockIdx.x * 16;
   const int K = a.K;
   const int64_t rowb = K / 2, rows_sf = K / 16;
-  const uint8_t* W = reinterpret_cast<const uint8_t*>(a.W) + sg.id * a.w_seg_stride + (int64_t)f0 * rowb;
-  const uint8_t* SF = a.W_sf + sg.id * a.sf_seg_stride + (int64_t)f0 * rows_sf;
-  const uint8_t* wg = W + (int64_t)g * rowb + 16 * t4;
-  const uint8_t* wg8 = W + (int64_t)(g + 8) * rowb + 16 * t4;
-  const uint8_t* sg0 = SF + (int64_t)g * rows_sf + 2 * t4;
-  const uint8_t* sg8 = SF + (int64_t)(g + 8) * rows_sf + 2 * t4;
-  const uint32_t* lutl = lut + lane;
   const int nchunks = K >> 7;
 
-  for (int p0 = 0; p0 < sg.nrows; p0 += NT * 8) {
-    const int prow = min(sg.nrows - p0, NT * 8);
-    const bf16* xr[NT];
-    bool xv[NT];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const int r = j * 8 + g;
-      xv[j] = r < prow;
-      int64_t row = 0;
-      if (xv[j]) row = a.gather ? a.gather[sg.row0 + p0 + r] : (sg.row0 + p0 + r);
-      xr[j] = reinterpret_cast<const bf16*>(a.X) + row * a.x_ld + 32 * t4;
-    }
-    float acc[NT][4];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  for (int f0 = (blockIdx.x * kWarps + warp) * 16; f0 < a.N; f0 += gridDim.x * kWarps * 16) {
+    const uint8_t* W = reinterpret_cast<const uint8_t*>(a.W) + sg.id * a.w_seg_stride + (int64_t)f0 * rowb;
+    const uint8_t* SF = a.W_sf + sg.id * a.sf_seg_stride + (int64_t)f0 * rows_sf;
+    const uint8_t* wg = W + (int64_t)g * rowb + 16 * t4;
+    const uint8_t* wg8 = W + (int64_t)(g + 8) * rowb + 16 * t4;
+    const uint8_t* sg0 = SF + (int64_t)g * rows_sf + 2 * t4;
+    const uint8_t* sg8 = SF + (int64_t)(g + 8) * rows_sf + 2 * t4;
 
-    for (int c = warp; c < nchunks; c += kWarps * U) {
-      uint4 A0[U], A1[U];
-      uint32_t S0[U], S1[U];
+    for (int p0 = 0; p0 < sg.nrows; p0 += NT * 8) {
+      const int prow = min(sg.nrows - p0, NT * 8);
+      const bf16* xr[NT];
+      bool xv[NT];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int cc = c + kWarps * u;
-        if (cc < nchunks) {
-          A0[u] = ldg_stream(wg + cc * 64);
-          A1[u] = ldg_stream(wg8 + cc * 64);
-          S0[u] = *reinterpret_cast<const uint16_t*>(sg0 + cc * 8);
-          S1[u] = *reinterpret_cast<const uint16_t*>(sg8 + cc * 8);
-        }
+      for (int j = 0; j < NT; ++j) {
+        const int r = j * 8 + g;
+        xv[j] = r < prow;
+        int64_t row = 0;
+        if (xv[j]) row = a.gather ? a.gather[sg.row0 + p0 + r] : (sg.row0 + p0 + r);
+        xr[j] = reinterpret_cast<const bf16*>(a.X) + row * a.x_ld + 32 * t4;
       }
+      float acc[NT][4];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int cc = c + kWarps * u;
-        if (cc >= nchunks) continue;
-        // block scales of rows g / g+8 for values 0..15 and 16..31, as BF16 pairs
-        __nv_bfloat162 sc0[2], sc1[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          sc0[h] = __float2bfloat162_rn(e4m3_to_f32((S0[u] >> (8 * h)) & 0xFFu));
-          sc1[h] = __float2bfloat162_rn(e4m3_to_f32((S1[u] >> (8 * h)) & 0xFFu));
+      for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+      uint4 nA0 = ldg_stream(wg), nA1 = ldg_stream(wg8);
+      uint32_t nS0 = *reinterpret_cast<const uint16_t*>(sg0), nS1 = *reinterpret_cast<const uint16_t*>(sg8);
+      for (int cc = 0; cc < nchunks; ++cc) {
+        const uint4 A0 = nA0, A1 = nA1;
+        const uint32_t S0 = nS0, S1 = nS1;
+        if (cc + 1 < nchunks) {
+          nA0 = ldg_stream(wg + (cc + 1) * 64);
+          nA1 = ldg_stream(wg8 + (cc + 1) * 64);
+          nS0 = *reinterpret_cast<const uint16_t*>(sg0 + (cc + 1) * 8);
+          nS1 = *reinterpret_cast<const uint16_t*>(sg8 + (cc + 1) * 8);
         }
-        const uint32_t w0[4] = {A0[u].x, A0[u].y, A0[u].z, A0[u].w};
-        const uint32_t w1[4] = {A1[u].x, A1[u].y, A1[u].z, A1[u].w};
+        // block scales (values 0..15 and 16..31 of each row's 32) as {s, s} pairs
+        const uint32_t s0 = e4m3x2_to_f16x2(S0), s1 = e4m3x2_to_f16x2(S1);
+        const uint32_t sc0[2] = {__byte_perm(s0, 0, 0x1010), __byte_perm(s0, 0, 0x3232)};
+        const uint32_t sc1[2] = {__byte_perm(s1, 0, 0x1010), __byte_perm(s1, 0, 0x3232)};
+        // fa[i]: A fragment of MMA i = this thread's values 4i..4i+3 of rows g and g+8
+        uint32_t fa[8][4];
+        const uint32_t w0[4] = {A0.x, A0.y, A0.z, A0.w};
+        const uint32_t w1[4] = {A1.x, A1.y, A1.z, A1.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t p0v[4], p1v[4];
+          e2m1x8_to_f16x2(w0[q], p0v);     // values 8q .. 8q+7 of row g
+          e2m1x8_to_f16x2(w1[q], p1v);     // of row g+8
+          const int h = q >> 1;
+          fa[2 * q][0] = hmul2_f16(p0v[0], sc0[h]);
+          fa[2 * q][2] = hmul2_f16(p0v[1], sc0[h]);
+          fa[2 * q][1] = hmul2_f16(p1v[0], sc1[h]);
+          fa[2 * q][3] = hmul2_f16(p1v[1], sc1[h]);
+          fa[2 * q + 1][0] = hmul2_f16(p0v[2], sc0[h]);
+          fa[2 * q + 1][2] = hmul2_f16(p0v[3], sc0[h]);
+          fa[2 * q + 1][1] = hmul2_f16(p1v[2], sc1[h]);
+          fa[2 * q + 1][3] = hmul2_f16(p1v[3], sc1[h]);
+        }
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
           if (j * 8 >= prow) continue;
@@ -239,46 +269,25 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_nvfp4_kernel(const GemvArgs 
           for (int q = 0; q < 4; ++q) B[q] = xv[j] ? ldg_keep(xr[j] + cc * 128 + 8 * q) : make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            // bytes 2i, 2i+1 of this thread's 16 bytes of each row: values 4i .. 4i+3
-            const int wi = i >> 1, sh = (i & 1) * 16;
-            const uint32_t b0 = (w0[wi] >> sh) & 0xFFu, b1 = (w0[wi] >> (sh + 8)) & 0xFFu;
-            const uint32_t c0 = (w1[wi] >> sh) & 0xFFu, c1 = (w1[wi] >> (sh + 8)) & 0xFFu;
-            const int h = i >> 2;
-            __nv_bfloat162 v;
-            uint32_t a0, a1, a2, a3;
-            v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&lutl[b0 << 5]), sc0[h]);
-            a0 = *reinterpret_cast<uint32_t*>(&v);
-            v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&lutl[b1 << 5]), sc0[h]);
-            a2 = *reinterpret_cast<uint32_t*>(&v);
-            v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&lutl[c0 << 5]), sc1[h]);
-            a1 = *reinterpret_cast<uint32_t*>(&v);
-            v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&lutl[c1 << 5]), sc1[h]);
-            a3 = *reinterpret_cast<uint32_t*>(&v);
             const uint4& Bq = B[i >> 1];
-            const uint32_t bb0 = (i & 1) ? Bq.z : Bq.x, bb1 = (i & 1) ? Bq.w : Bq.y;
-            mma_bf16_16816(acc[j], a0, a1, a2, a3, bb0, bb1);
+            const uint32_t bb0 = bf16x2_to_f16x2((i & 1) ? Bq.z : Bq.x);
+            const uint32_t bb1 = bf16x2_to_f16x2((i & 1) ? Bq.w : Bq.y);
+            mma_f16_16816(acc[j], fa[i][0], fa[i][1], fa[i][2], fa[i][3], bb0, bb1);
           }
         }
       }
-    }
-
-    if (p0 > 0) __syncthreads();
+      // acc[j][0]: (feature g, row 2t), [1]: (g, 2t+1), [2]: (g+8, 2t), [3]: (g+8, 2t+1)
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      red[warp][j][g * 8 + 2 * t4] = acc[j][0];
-      red[warp][j][g * 8 + 2 * t4 + 1] = acc[j][1];
-      red[warp][j][(g + 8) * 8 + 2 * t4] = acc[j][2];
-      red[warp][j][(g + 8) * 8 + 2 * t4 + 1] = acc[j][3];
-    }
-    __syncthreads();
-    for (int o = threadIdx.x; o < NT * 128; o += kThreads) {
-      const int j = o >> 7, idx = o & 127;
-      const int f = idx >> 3, r = j * 8 + (idx & 7);
-      if (r < prow) {
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) v += red[w][j][idx];
-        epilogue<EPI, OUT_F32, false>(a, sg.id, sg.row0 + p0 + r, f0 + f, v);
+      for (int j = 0; j < NT; ++j) {
+        const int r0 = j * 8 + 2 * t4;
+        if (r0 < prow) {
+          epilogue<EPI, OUT_F32, false>(a, sg.id, sg.row0 + p0 + r0, f0 + g, acc[j][0]);
+          epilogue<EPI, OUT_F32, false>(a, sg.id, sg.row0 + p0 + r0, f0 + g + 8, acc[j][2]);
+        }
+        if (r0 + 1 < prow) {
+          epilogue<EPI, OUT_F32, false>(a, sg.id, sg.row0 + p0 + r0 + 1, f0 + g, acc[j][1]);
+          epilogue<EPI, OUT_F32, false>(a, sg.id, sg.row0 + p0 + r0 + 1, f0 + g + 8, acc[j][3]);
+        }
       }
     }
   }
@@ -286,13 +295,27 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_nvfp4_kernel(const GemvArgs 
 
 // NVFP4 -> BF16 of whole matrices (for the tensor-core path): each output is
 // E2M1 * E4M3 (exact in BF16); the per-tensor scale stays for the epilogue.
-__global__ void dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf, int64_t n_bytes,
-                                     uint32_t* __restrict__ out) {
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_bytes; i += (int64_t)gridDim.x * blockDim.x) {
-    const float s = e4m3_to_f32(sf[i >> 3]);
-    const uint32_t p = e2m1_pair_bf16(q[i]);
-    const float lo = __uint_as_float(p << 16) * s, hi = __uint_as_float(p & 0xFFFF0000u) * s;
-    out[i] = (uint32_t)bf16_bits(lo) | ((uint32_t)bf16_bits(hi) << 16);
+// A thread turns 16 bytes (32 values, two scale blocks) into 64 output bytes.
+__global__ void dequant_nvfp4_kernel(const uint4* __restrict__ q, const uint16_t* __restrict__ sf, int64_t n16,
+                                     uint4* __restrict__ out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 w = __ldg(q + i);
+    const uint32_t s = e4m3x2_to_f16x2(__ldg(sf + i));
+    const uint32_t sc[2] = {__byte_perm(s, 0, 0x1010), __byte_perm(s, 0, 0x3232)};
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t p[4];
+      e2m1x8_to_f16x2(ws[k], p);
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t v = hmul2_f16(p[j], sc[k >> 1]);
+        const float2 f = __half22float2(*reinterpret_cast<__half2*>(&v));
+        o[j] = (uint32_t)bf16_bits(f.x) | ((uint32_t)bf16_bits(f.y) << 16);
+      }
+      out[4 * i + k] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
 }
 
@@ -336,10 +359,10 @@ cudaError_t pick_nt(const GemvArgs& a, int max_rows, int segs, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_dequant_nvfp4(const uint8_t* q, const uint8_t* sf, int64_t n_values, void* out, cudaStream_t s) {
-  const int64_t n_bytes = n_values / 2;
-  if (n_bytes <= 0) return cudaSuccess;
-  dequant_nvfp4_kernel<<<(unsigned)std::min<int64_t>(ceil_div(n_bytes, 256), 16384), 256, 0, s>>>(
-      q, sf, n_bytes, reinterpret_cast<uint32_t*>(out));
+  const int64_t n16 = n_values / 32;
+  if (n16 <= 0) return cudaSuccess;
+  dequant_nvfp4_kernel<<<(unsigned)std::min<int64_t>(ceil_div(n16, 256), 16384), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint16_t*>(sf), n16, reinterpret_cast<uint4*>(out));
   count_launches(1);
   return cudaGetLastError();
 }
@@ -359,7 +382,8 @@ cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_
     return cudaGetLastError();
   }
   if (wfmt == WF_NVFP4 && act == MOE_DT_BF16) {
-    dim3 grid(a.N / 16, segs, 1);
+    // one warp per 16 features: a CTA's 8 warps cover 128 features
+    dim3 grid((unsigned)ceil_div(a.N / 16, kWarps), segs, 1);
     switch (epi) {
       case EPI_RELU2: gemv_nvfp4_kernel<EPI_RELU2, false><<<grid, kThreads, 0, s>>>(a); break;
       case EPI_SCALE: gemv_nvfp4_kernel<EPI_SCALE, true><<<grid, kThreads, 0, s>>>(a); break;
