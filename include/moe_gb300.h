@@ -25,10 +25,14 @@
  *
  * Conventions for every entry point:
  *  - Pointers are DEVICE pointers unless stated otherwise, allocated and owned
- *    by the caller; the library never allocates, frees or synchronises (except
- *    moe_get_device_error and the _host convenience call).  Every call only
- *    enqueues work on `stream` (a cudaStream_t passed as void*; NULL = the
- *    legacy default stream) and returns.
+ *    by the caller; the library never allocates device memory, frees or
+ *    synchronises (except moe_get_device_error and the _host convenience
+ *    call).  Every call only enqueues work on `stream` (a cudaStream_t passed
+ *    as void*; NULL = the legacy default stream) and returns.
+ *    moe_layer_forward runs the shared expert on a library-owned auxiliary
+ *    stream (one per device, created with two events on the first call),
+ *    forked from and joined back to `stream` by events, so the layer is
+ *    still ordered as one operation on `stream` (and capturable).
  *  - Row-major storage.  Weight matrices are stored [out, in] (the
  *    nn.Linear orientation, page "M6.1 ...", section 0x04A).
  *  - Every device pointer must be 16-byte aligned; every inner width

@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 using namespace moe;
 
@@ -276,6 +277,43 @@ moe_status_t run_shared(const moe_config_t* c, int T, const void* x, const moe_w
   return MOE_OK;
 }
 
+// One auxiliary stream and a fork/join event pair per device, created on first
+// use: moe_layer_forward runs the shared expert there, concurrently with the
+// router -> dispatch -> experts chain on the caller's stream.
+struct AuxStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_aux_mutex;
+AuxStream g_aux[kMaxDevices];
+
+bool aux_stream(AuxStream** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  AuxStream& a = g_aux[dev];
+  if (!a.s) {
+    if (cudaStreamCreateWithFlags(&a.s, cudaStreamNonBlocking) != cudaSuccess) return false;
+    if (cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess) return false;
+    if (cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) return false;
+  }
+  *out = &a;
+  return true;
+}
+
+// shared expert y_s[T, d] (FP32) = W_sd act(relu(act(W_su x))^2)
+moe_status_t run_shared_to_f32(const moe_config_t* c, int T, const void* x, const moe_weights_t* w, float* ys,
+                               const Ptrs& P, cudaStream_t s) {
+  const int d = c->d_model, S = c->d_shared;
+  const bool f32 = c->act_dtype == MOE_DT_F32;
+  void* hs = P.at<void>(P.L.hs);
+  GemvArgs up = dense_args(w->w_sh_up, S, d, x, T, hs, S);
+  CU(run_dense(c, up, EPI_RELU2, f32, T, s));
+  GemvArgs dn = dense_args(w->w_sh_down, d, S, hs, T, ys, d);
+  CU(run_dense(c, dn, EPI_STORE, true, T, s));
+  return MOE_OK;
+}
+
 moe_status_t check_weights(const moe_config_t* c, const moe_weights_t* w, bool experts, bool router, bool dense) {
   if (!w) return MOE_ERR_INVALID_ARG;
   if (router) { REQ(w->w_router); OPT(w->router_bias); }
@@ -412,6 +450,19 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
   Ptrs P{(char*)ws, make_layout(cfg, T)};
   cudaStream_t s = (cudaStream_t)stream;
   CU(cudaMemsetAsync(P.hdr(), 0, sizeof(WsHeader), s));
+  // fork: the shared expert runs on the auxiliary stream
+  const bool shared = cfg->d_shared > 0;
+  float* ys = P.at<float>(P.L.ys);
+  std::unique_lock<std::mutex> aux_lock(g_aux_mutex);
+  AuxStream* aux = nullptr;
+  if (shared) {
+    if (!aux_stream(&aux)) return MOE_ERR_CUDA;
+    CU(cudaEventRecord(aux->fork, s));
+    CU(cudaStreamWaitEvent(aux->s, aux->fork, 0));
+    if ((st = run_shared_to_f32(cfg, T, x, w, ys, P, aux->s)) != MOE_OK) return st;
+    CU(cudaEventRecord(aux->join, aux->s));
+  }
+  aux_lock.unlock();
   const void* x_e = x;
   if (cfg->d_latent > 0) {
     void* xl = P.at<void>(P.L.x_l);
@@ -436,10 +487,21 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
   if ((st = run_up(cfg, T, x_e, x_packed, rt, offsets, w, h, P, s)) != MOE_OK) return st;
   float* u = P.at<float>(P.L.u);
   if ((st = run_down(cfg, T, h, offsets, rt, rs, topw, w, u, P, s)) != MOE_OK) return st;
-  float* y_r = P.at<float>(P.L.y_r);
-  void* y_rl = cfg->d_latent > 0 ? P.at<void>(P.L.y_rl) : nullptr;
-  CU(launch_combine(u, tsr, T, cfg->top_k, de_of(cfg), y_r, y_rl, cfg->act_dtype, s));
-  return run_shared(cfg, T, x, w, y_r, y_rl, y, P, s);
+  if (cfg->d_latent == 0) {
+    // join, then y = act(sum of routed rows + y_s): the same two FP32 terms, one rounding
+    if (shared) CU(cudaStreamWaitEvent(s, aux->join, 0));
+    CU(launch_combine(u, tsr, T, cfg->top_k, de_of(cfg), nullptr, y, cfg->act_dtype, s, shared ? ys : nullptr));
+    return MOE_OK;
+  }
+  // latent: combined latent rows rounded once, then latent up + y_s
+  void* y_rl = P.at<void>(P.L.y_rl);
+  CU(launch_combine(u, tsr, T, cfg->top_k, de_of(cfg), nullptr, y_rl, cfg->act_dtype, s));
+  if (shared) CU(cudaStreamWaitEvent(s, aux->join, 0));
+  GemvArgs lu = dense_args(w->w_lat_up, cfg->d_model, cfg->d_latent, y_rl, T, y, cfg->d_model);
+  lu.add_src = shared ? ys : nullptr;
+  lu.add_ld = cfg->d_model;
+  CU(run_dense(cfg, lu, EPI_ADD, cfg->act_dtype == MOE_DT_F32, T, s));
+  return MOE_OK;
 }
 
 moe_status_t moe_get_device_error(const void* ws, void* stream, int32_t* code) {

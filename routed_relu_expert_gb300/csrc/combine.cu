@@ -17,7 +17,7 @@ namespace {
 template <bool ACT_F32>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ u, const int32_t* __restrict__ tsr,
                                                       int K, int de, float* __restrict__ y_r,
-                                                      void* __restrict__ y_act) {
+                                                      void* __restrict__ y_act, const float* __restrict__ add) {
   __shared__ int rows[32];
   const int t = blockIdx.x;
   if (threadIdx.x < K) {
@@ -43,6 +43,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
     }
     if (y_r) reinterpret_cast<float4*>(y_r + (int64_t)t * de)[v] = acc;
+    if (add) {
+      // output = routed sum + an FP32 term (the shared expert), then one rounding
+      const float4 q = reinterpret_cast<const float4*>(add + (int64_t)t * de)[v];
+      acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+    }
     if (y_act) {
       if (ACT_F32) {
         reinterpret_cast<float4*>(reinterpret_cast<float*>(y_act) + (int64_t)t * de)[v] = acc;
@@ -86,12 +91,12 @@ cudaError_t launch_cast(const float* src, int64_t n, void* dst, int act, cudaStr
 }
 
 cudaError_t launch_combine(const float* u, const int32_t* token_slot_row, int T, int K, int de, float* y_r,
-                           void* y_act, int act, cudaStream_t s) {
+                           void* y_act, int act, cudaStream_t s, const float* add) {
   if (T <= 0) return cudaSuccess;
   if (act == MOE_DT_F32)
-    combine_kernel<true><<<T, 256, 0, s>>>(u, token_slot_row, K, de, y_r, y_act);
+    combine_kernel<true><<<T, 256, 0, s>>>(u, token_slot_row, K, de, y_r, y_act, add);
   else
-    combine_kernel<false><<<T, 256, 0, s>>>(u, token_slot_row, K, de, y_r, y_act);
+    combine_kernel<false><<<T, 256, 0, s>>>(u, token_slot_row, K, de, y_r, y_act, add);
   count_launches(1);
   return cudaGetLastError();
 }

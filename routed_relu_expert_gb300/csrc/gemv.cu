@@ -62,7 +62,9 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a
   __shared__ float red[kWarps][NT][128];
 
   Seg sg;
-  if (!resolve_segment(a, 1 << 30, sg)) return;
+  // dense products split their 16-row passes over grid.z (CTAs of one feature
+  // tile run together, so the tile is read from HBM once); grouped ones loop
+  if (!resolve_segment(a, a.offsets ? (1 << 30) : NT * 8, sg)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int f0 = blockIdx.x * 16;
@@ -349,8 +351,7 @@ __global__ void __launch_bounds__(kThreads) gemv_f32_kernel(const GemvArgs a) {
 
 template <int EPI, bool OUT_F32>
 cudaError_t pick_nt(const GemvArgs& a, int max_rows, int segs, cudaStream_t s) {
-  (void)max_rows;
-  dim3 grid(a.N / 16, segs, 1);
+  dim3 grid(a.N / 16, segs, a.offsets ? 1u : (unsigned)ceil_div(max_rows, 16));
   gemv_bf16_kernel<EPI, OUT_F32><<<grid, kThreads, 0, s>>>(a);
   count_launches(1);
   return cudaGetLastError();

@@ -91,9 +91,10 @@ struct DispatchArgs {
 size_t dispatch_tile_count_elems(int T, int K, int E);
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
 
-// combine: y_r[t] = sum over t's packed rows in ascending order of u[row]
+// combine: y_r[t] = sum over t's packed rows in ascending order of u[row];
+// y_r_act[t] = act(y_r[t] + add[t]) (add nullable)
 cudaError_t launch_combine(const float* u, const int32_t* token_slot_row, int T, int K, int de,
-                           float* y_r, void* y_r_act, int act, cudaStream_t s);
+                           float* y_r, void* y_r_act, int act, cudaStream_t s, const float* add = nullptr);
 
 // NVFP4 matrix -> BF16 values E2M1 * E4M3 (per-tensor scale not applied);
 // n_values elements, 16 per scale byte.

@@ -14,54 +14,70 @@ namespace moe {
 namespace {
 
 // ---------------------------------------------------------------------------
-// logits, few tokens: one warp per expert row of W_r (streamed once), all
-// tokens' rows read through L1; per-lane FP32 FMA chains reduced by a fixed
-// shuffle tree.
+// logits, few tokens: a CTA computes EPC experts x TMAX tokens; its 8 warps are
+// EPC experts x (8 / EPC) interleaved K slices of 256, each lane an FP32 FMA
+// chain over 8 consecutive elements; lanes reduce by a fixed shuffle tree and
+// the K slices by a fixed order through shared memory.  W_r rows are streamed
+// once per token group; the token rows are shared by the CTA's experts in L1.
 // ---------------------------------------------------------------------------
-template <int TMAX, bool XF32>
+template <int TMAX, int EPC, bool XF32>
 __global__ void __launch_bounds__(256) router_logits_small(const void* __restrict__ X, int T, int d,
                                                            const float* __restrict__ Wr, int E,
                                                            float* __restrict__ logits) {
+  constexpr int KS = 8 / EPC;
+  __shared__ float red[8][TMAX];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 8 + warp;
-  if (e >= E) return;
+  const int ei = warp % EPC, ks = warp / EPC;
+  const int e = blockIdx.x * EPC + ei;
+  const int t0 = blockIdx.y * TMAX;
+  const int nt = min(TMAX, T - t0);
   float acc[TMAX];
 #pragma unroll
   for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
-  const float* w = Wr + (int64_t)e * d;
-  for (int k = lane * 8; k < d; k += 256) {
-    const uint4 wa = ldg_stream(w + k);
-    const uint4 wb = ldg_stream(w + k + 4);
-    const float wv[8] = {__uint_as_float(wa.x), __uint_as_float(wa.y), __uint_as_float(wa.z),
-                         __uint_as_float(wa.w), __uint_as_float(wb.x), __uint_as_float(wb.y),
-                         __uint_as_float(wb.z), __uint_as_float(wb.w)};
+  if (e < E) {
+    const float* w = Wr + (int64_t)e * d;
+    for (int k = ks * 256 + lane * 8; k < d; k += KS * 256) {
+      const uint4 wa = ldg_stream(w + k);
+      const uint4 wb = ldg_stream(w + k + 4);
+      const float wv[8] = {__uint_as_float(wa.x), __uint_as_float(wa.y), __uint_as_float(wa.z),
+                           __uint_as_float(wa.w), __uint_as_float(wb.x), __uint_as_float(wb.y),
+                           __uint_as_float(wb.z), __uint_as_float(wb.w)};
 #pragma unroll
-    for (int t = 0; t < TMAX; ++t) {
-      if (t < T) {
-        float xv[8];
-        if (XF32) {
-          const float* xp = reinterpret_cast<const float*>(X) + (int64_t)t * d + k;
-          const float4 a = *reinterpret_cast<const float4*>(xp);
-          const float4 b = *reinterpret_cast<const float4*>(xp + 4);
-          xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
-          xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
-        } else {
-          const uint4 q = ldg_keep(reinterpret_cast<const bf16*>(X) + (int64_t)t * d + k);
-          xv[0] = bf16_lo(q.x); xv[1] = bf16_hi(q.x); xv[2] = bf16_lo(q.y); xv[3] = bf16_hi(q.y);
-          xv[4] = bf16_lo(q.z); xv[5] = bf16_hi(q.z); xv[6] = bf16_lo(q.w); xv[7] = bf16_hi(q.w);
+      for (int t = 0; t < TMAX; ++t) {
+        if (t < nt) {
+          float xv[8];
+          if (XF32) {
+            const float* xp = reinterpret_cast<const float*>(X) + (int64_t)(t0 + t) * d + k;
+            const float4 a = *reinterpret_cast<const float4*>(xp);
+            const float4 b = *reinterpret_cast<const float4*>(xp + 4);
+            xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
+            xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
+          } else {
+            const uint4 q = ldg_keep(reinterpret_cast<const bf16*>(X) + (int64_t)(t0 + t) * d + k);
+            xv[0] = bf16_lo(q.x); xv[1] = bf16_hi(q.x); xv[2] = bf16_lo(q.y); xv[3] = bf16_hi(q.y);
+            xv[4] = bf16_lo(q.z); xv[5] = bf16_hi(q.z); xv[6] = bf16_lo(q.w); xv[7] = bf16_hi(q.w);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[t] = fmaf(xv[i], wv[i], acc[t]);
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[t] = fmaf(xv[i], wv[i], acc[t]);
       }
     }
   }
 #pragma unroll
   for (int t = 0; t < TMAX; ++t) {
-    if (t < T) {
-      float v = acc[t];
+    float v = acc[t];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane == 0) logits[(int64_t)t * E + e] = v;
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) red[warp][t] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < EPC * TMAX) {
+    const int eo = threadIdx.x / TMAX, t = threadIdx.x % TMAX;
+    const int ee = blockIdx.x * EPC + eo;
+    if (ee < E && t < nt) {
+      float v = 0.f;
+      for (int k2 = 0; k2 < KS; ++k2) v += red[k2 * EPC + eo][t];
+      logits[(int64_t)(t0 + t) * E + ee] = v;
     }
   }
 }
@@ -296,16 +312,25 @@ cudaError_t launch_select_p(const float* logits, int T, int E, const float* bias
   return cudaGetLastError();
 }
 
+template <int TMAX, int EPC>
+cudaError_t launch_small_t(const void* x, int act, int T, int d, const float* w, int E, float* logits,
+                           cudaStream_t s) {
+  dim3 grid((unsigned)ceil_div(E, EPC), (unsigned)ceil_div(T, TMAX));
+  if (act == MOE_DT_F32)
+    router_logits_small<TMAX, EPC, true><<<grid, 256, 0, s>>>(x, T, d, w, E, logits);
+  else
+    router_logits_small<TMAX, EPC, false><<<grid, 256, 0, s>>>(x, T, d, w, E, logits);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 template <int TMAX>
 cudaError_t launch_small(const void* x, int act, int T, int d, const float* w, int E, float* logits,
                          cudaStream_t s) {
-  const unsigned grid = (unsigned)ceil_div(E, 8);
-  if (act == MOE_DT_F32)
-    router_logits_small<TMAX, true><<<grid, 256, 0, s>>>(x, T, d, w, E, logits);
-  else
-    router_logits_small<TMAX, false><<<grid, 256, 0, s>>>(x, T, d, w, E, logits);
-  count_launches(1);
-  return cudaGetLastError();
+  // wide routers share each CTA's token rows among several experts
+  if (E >= 512) return launch_small_t<TMAX, 4>(x, act, T, d, w, E, logits, s);
+  if (E >= 256) return launch_small_t<TMAX, 2>(x, act, T, d, w, E, logits, s);
+  return launch_small_t<TMAX, 1>(x, act, T, d, w, E, logits, s);
 }
 
 }  // namespace
@@ -327,9 +352,7 @@ cudaError_t launch_router_logits(const void* x, int act, int T, int d, const flo
     return launch_gemm_tc(a, EPI_STORE, true, E, T, 0, bn, s, d);
   }
   if (T <= 4) return launch_small<4>(x, act, T, d, w_router, E, logits, s);
-  if (T <= 16) return launch_small<16>(x, act, T, d, w_router, E, logits, s);
-  if (T <= 32) return launch_small<32>(x, act, T, d, w_router, E, logits, s);
-  if (T <= 64) return launch_small<64>(x, act, T, d, w_router, E, logits, s);
+  if (T <= 64) return launch_small<8>(x, act, T, d, w_router, E, logits, s);
   dim3 grid((unsigned)ceil_div(T, 64), (unsigned)ceil_div(E, 64));
   if (act == MOE_DT_F32)
     router_logits_tiled<true><<<grid, 256, 0, s>>>(x, T, d, w_router, E, logits);
