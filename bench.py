@@ -40,6 +40,7 @@ def parse():
     ap.add_argument("--replicas", type=int, default=0, help="weight replicas (0 = enough to defeat L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="also time every token count of the workload")
+    ap.add_argument("--eager", action="store_true", help="time eager calls instead of CUDA-graph replays")
     return ap.parse_args()
 
 
@@ -150,11 +151,11 @@ def run_ours(args, rank, world, dev):
         L._ws = ws
     stream = torch.cuda.current_stream()
 
-    def step(i):
+    def eager_step(i):
         layers[i % n_rep].forward(x, y)
 
-    for i in range(args.warmup):
-        step(i)
+    for i in range(max(args.warmup, n_rep)):
+        eager_step(i)
     torch.cuda.synchronize()
     err = M.moe_get_device_error(ws)
 
@@ -176,14 +177,39 @@ def run_ours(args, rank, world, dev):
             torch.distributed.barrier()
         return ms
 
+    # one CUDA graph per replica: the whole layer (both streams) as one launch
+    graphs, per_step_launches = [], None
+    if not args.eager:
+        for r in range(n_rep):
+            g = torch.cuda.CUDAGraph()
+            c0 = M.load().moe_launch_count()
+            with torch.cuda.graph(g):
+                layers[r].forward(x, y)
+            per_step_launches = M.load().moe_launch_count() - c0
+            graphs.append(g)
+        for i in range(args.warmup):
+            graphs[i % n_rep].replay()
+        torch.cuda.synchronize()
+
+    def step(i):
+        if graphs:
+            graphs[i % n_rep].replay()
+        else:
+            eager_step(i)
+
     clocks = ClockSampler(torch.cuda.current_device() if not os.environ.get("CUDA_VISIBLE_DEVICES") else 0)
     clocks.start()
     n0 = M.load().moe_launch_count()
     ms = timed(step, args.steps)
     n1 = M.load().moe_launch_count()
     clk = clocks.stop()
+    launches = int(n1 - n0) if not graphs else int(per_step_launches) * args.steps
     ms_step = ms / args.steps
     value = world * T / (ms_step / 1e3)
+    ms_eager = None
+    if graphs:
+        ke = max(10, min(args.steps, 200))
+        ms_eager = timed(eager_step, ke) / ke
 
     # experts that received routes (same routing for every replica: router and bias are shared)
     ids = torch.empty((T, shape.top_k), dtype=torch.int32, device=dev)
@@ -254,8 +280,18 @@ def run_ours(args, rank, world, dev):
             for L in layers:
                 L._ws = wss
             f = lambda i: layers[i % n_rep].forward(xs, ys)
-            for i in range(5):
+            for i in range(max(5, n_rep)):
                 f(i)
+            if not args.eager:
+                gs = []
+                for r in range(n_rep):
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g):
+                        layers[r].forward(xs, ys)
+                    gs.append(g)
+                f = lambda i: gs[i % n_rep].replay()
+                for i in range(3):
+                    f(i)
             kk = max(50, args.steps // 2)
             mss = timed(f, kk) / kk
             idss = torch.empty((Ts, shape.top_k), dtype=torch.int32, device=dev)
@@ -271,7 +307,7 @@ def run_ours(args, rank, world, dev):
 
     return {
         "value": value, "ms_per_step": ms_step, "n_active": n_active, "bytes": lb, "clocks": clk,
-        "launches": int(n1 - n0), "err": err, "ms_up": ms_up, "up_bytes": up_bytes, "achieved_up": achieved,
+        "launches": launches, "err": err, "ms_eager": ms_eager, "graphs": bool(graphs), "ms_up": ms_up, "up_bytes": up_bytes, "achieved_up": achieved,
         "up_flops": up_flops, "achieved_up_tf": achieved_tf, "flops": layer_flops(shape, T),
         "peaks": pk, "e2e_s": e2e_s, "n_rep": n_rep, "sweep": sweep, "shape": shape, "T": T,
         "rep_bytes": one,
@@ -438,6 +474,9 @@ def main():
                                "tensor_peak": "sustained", "bytes_breakdown": lb},
             "clocks": r["clocks"],
             "gpu_launches": r["launches"],
+            "execution": ("CUDA graph of the layer per weight replica, replayed each step"
+                          if r["graphs"] else "eager C-ABI calls"),
+            "eager_ms_per_step": round(r["ms_eager"], 5) if r["ms_eager"] else None,
             "device_error_word": r["err"],
             "e2e": {"value": round(world * T / r["e2e_s"], 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": T * shape.d_model * ab, "d2h_bytes_per_step": T * shape.d_model * ab,
