@@ -18,6 +18,8 @@ template <bool ACT_F32>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ u, const int32_t* __restrict__ tsr,
                                                       int K, int de, float* __restrict__ y_r,
                                                       void* __restrict__ y_act, const float* __restrict__ add) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int rows[32];
   const int t = blockIdx.x;
   if (threadIdx.x < K) {
@@ -63,6 +65,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 
 template <bool ACT_F32>
 __global__ void cast_kernel(const float* __restrict__ src, int64_t n4, void* __restrict__ dst) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < n4; v += (int64_t)gridDim.x * blockDim.x) {
     const float4 q = reinterpret_cast<const float4*>(src)[v];
     if (ACT_F32) {
@@ -83,10 +87,9 @@ cudaError_t launch_cast(const float* src, int64_t n, void* dst, int act, cudaStr
   const int64_t n4 = n / 4;
   const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(n4, 256), 4096);
   if (act == MOE_DT_F32)
-    cast_kernel<true><<<grid, 256, 0, s>>>(src, n4, dst);
+    launch_k(cast_kernel<true>, grid, 256, 0, s, src, n4, dst);
   else
-    cast_kernel<false><<<grid, 256, 0, s>>>(src, n4, dst);
-  count_launches(1);
+    launch_k(cast_kernel<false>, grid, 256, 0, s, src, n4, dst);
   return cudaGetLastError();
 }
 
@@ -94,10 +97,9 @@ cudaError_t launch_combine(const float* u, const int32_t* token_slot_row, int T,
                            void* y_act, int act, cudaStream_t s, const float* add) {
   if (T <= 0) return cudaSuccess;
   if (act == MOE_DT_F32)
-    combine_kernel<true><<<T, 256, 0, s>>>(u, token_slot_row, K, de, y_r, y_act, add);
+    launch_k(combine_kernel<true>, T, 256, 0, s, u, token_slot_row, K, de, y_r, y_act, add);
   else
-    combine_kernel<false><<<T, 256, 0, s>>>(u, token_slot_row, K, de, y_r, y_act, add);
-  count_launches(1);
+    launch_k(combine_kernel<false>, T, 256, 0, s, u, token_slot_row, K, de, y_r, y_act, add);
   return cudaGetLastError();
 }
 

@@ -73,6 +73,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: every kernel of the library is launched so
+// that it may start while its predecessor on the stream finishes; it lets its
+// own successor launch early (trigger) and waits for the predecessor's results
+// to be complete and visible (wait) before reading any of them.  Both are
+// no-ops for a kernel launched without the attribute.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // small integer helpers
 // ---------------------------------------------------------------------------
 __host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }

@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(256) pack_rows_kernel(const uint4* __restrict_
                                                         const int32_t* __restrict__ route_token,
                                                         const int32_t* __restrict__ offsets, int E, int row_vecs,
                                                         uint4* __restrict__ x_packed) {
+  pdl_wait();
+  pdl_trigger();
   const int R = offsets[E];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int j = blockIdx.x * 8 + warp; j < R; j += gridDim.x * 8) {
@@ -160,6 +162,8 @@ __device__ void write_schedule(const DispatchArgs& a, int e, int total, int off,
 // single CTA (few routes)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) dispatch_single(const DispatchArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int sm[];
   int* hist = sm;                      // [32][E]
   int* tmp32 = sm + kWarps * a.E;      // [32]
@@ -189,6 +193,8 @@ __global__ void __launch_bounds__(kThreads) dispatch_single(const DispatchArgs a
 // multi CTA (many routes): count per token tile, one scan CTA, scatter
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) dispatch_count(const DispatchArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int sm[];
   int* hist = sm;
   const int tile = blockIdx.x;
@@ -206,6 +212,8 @@ __global__ void __launch_bounds__(kThreads) dispatch_count(const DispatchArgs a)
 }
 
 __global__ void __launch_bounds__(kThreads) dispatch_scan(const DispatchArgs a, int n_tiles) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int tmp32[32];
   const int e = threadIdx.x;
   int total = 0;
@@ -223,6 +231,8 @@ __global__ void __launch_bounds__(kThreads) dispatch_scan(const DispatchArgs a, 
 }
 
 __global__ void __launch_bounds__(kThreads) dispatch_scatter(const DispatchArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int sm[];
   int* hist = sm;
   const int tile = blockIdx.x;
@@ -250,9 +260,8 @@ cudaError_t launch_pack(const DispatchArgs& a, cudaStream_t s) {
   if (!a.x_packed || !a.x_e) return cudaSuccess;
   const int R = a.T * a.K;
   const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(R, 8), 16384);
-  pack_rows_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(a.x_e), a.route_token, a.offsets, a.E,
+  launch_k(pack_rows_kernel, grid, 256, 0, s, reinterpret_cast<const uint4*>(a.x_e), a.route_token, a.offsets, a.E,
                                         a.de * a.elem_bytes / 16, reinterpret_cast<uint4*>(a.x_packed));
-  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -270,8 +279,7 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
     const size_t smem = (size_t)(kWarps * a.E + 32) * sizeof(int);
     cudaError_t e = cudaFuncSetAttribute(dispatch_single, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dispatch_single<<<1, kThreads, smem, s>>>(a);
-    count_launches(1);
+    launch_k(dispatch_single, 1, kThreads, smem, s, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_pack(a, s);
@@ -282,12 +290,9 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(dispatch_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dispatch_count<<<n_tiles, kThreads, smem, s>>>(a);
-  count_launches(1);
-  dispatch_scan<<<1, kThreads, 0, s>>>(a, n_tiles);
-  count_launches(1);
-  dispatch_scatter<<<n_tiles, kThreads, smem, s>>>(a);
-  count_launches(1);
+  launch_k(dispatch_count, n_tiles, kThreads, smem, s, a);
+  launch_k(dispatch_scan, 1, kThreads, 0, s, a, n_tiles);
+  launch_k(dispatch_scatter, n_tiles, kThreads, smem, s, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_pack(a, s);

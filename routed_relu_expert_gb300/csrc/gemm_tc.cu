@@ -37,7 +37,8 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;           // 16 KB
 constexpr int B_BYTES = BN_MAX * BK * 2;       // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int N_BOX = 5;                       // B boxes of 16, 32, 64, 128, 256 rows
+constexpr int N_BOX = 5;                       // B boxes of 16, 32, 64, 128, 256 rows: a tile's rows,
+                                               // rounded up to 16, load as their binary decomposition
 constexpr int kThreads = 192;
 constexpr uint32_t TMEM_COLS = 512;            // two accumulators of BN_MAX columns
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
@@ -175,12 +176,6 @@ __device__ __forceinline__ void decode_tile(int t, const int* prefix, int E, int
   ti.rows = min(bn, count - nt * bn);
 }
 
-__device__ __forceinline__ int box_index(int rows) {
-  int i = 0;
-  while ((16 << i) < rows && i < N_BOX - 1) ++i;
-  return i;
-}
-
 // Epilogue of 32 accumulator columns (rows row0+c0 .. +31) of one feature f.
 // Per-row inputs are fetched before any store: the routing weight of each
 // column by one lane and broadcast, the added term as 32 independent loads.
@@ -247,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* prefix = scan_tmp + 8;                                          // [E+1]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
@@ -267,6 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
 
+  // barriers and TMEM are set up while the previous kernel finishes; its
+  // results (offsets, activations) are read only after this wait
+  pdl_wait();
   // row-tile prefix over segments (each segment: ceil(rows / bn) row tiles)
   int total_q;
   if (a.offsets) {
@@ -313,15 +312,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         Tile ti;
         decode_tile(t, prefix, E, m_tiles, bn, a, ti);
-        const int bi = box_index(ti.rows);
-        const uint32_t bbytes = (uint32_t)(16 << bi) * BK * 2;
+        const int r16 = (ti.rows + 15) & ~15;
+        const uint32_t bbytes = (uint32_t)r16 * BK * 2;
         const int a_row = ti.seg * a.N + ti.m0;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.err)) { ok = false; break; }
           const uint32_t sa = base + stage * STAGE_BYTES;
           mbar_expect_tx(full_bar(stage), A_BYTES + bbytes);
           tma_load_2d(sa, &maps.a, kb * BK, a_row, full_bar(stage));
-          tma_load_2d(sa + A_BYTES, &maps.b[bi], (kb % b_period) * BK, ti.row0, full_bar(stage));
+          int off = 0;
+#pragma unroll
+          for (int i = N_BOX - 1; i >= 0; --i) {
+            if (r16 & (16 << i)) {
+              tma_load_2d(sa + A_BYTES + off * (BK * 2), &maps.b[i], (kb % b_period) * BK, ti.row0 + off,
+                          full_bar(stage));
+              off += 16 << i;
+            }
+          }
           pend[stage] = (int)phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -460,8 +467,7 @@ cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  tc_gemm_kernel<EPI, OUT_F32><<<grid, kThreads, smem, s>>>(maps, a, E, m_tiles, bn, b_period);
-  count_launches(1);
+  launch_k(tc_gemm_kernel<EPI, OUT_F32>, grid, kThreads, smem, s, maps, a, E, m_tiles, bn, b_period);
   return cudaGetLastError();
 }
 

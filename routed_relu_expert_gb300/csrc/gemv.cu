@@ -57,6 +57,8 @@ __device__ __forceinline__ bool resolve_segment(const GemvArgs& a, int rows_per_
 // ---------------------------------------------------------------------------
 template <int EPI, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int NT = 2;                 // 8-row column blocks per pass
   constexpr int U = 4;                  // 32-wide K chunks in flight per warp
   __shared__ float red[kWarps][NT][128];
@@ -196,6 +198,8 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
 
 template <int EPI, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 3) gemv_nvfp4_kernel(const GemvArgs a) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int NT = 2;
   Seg sg;
   if (!resolve_segment(a, 1 << 30, sg)) return;
@@ -300,6 +304,8 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_nvfp4_kernel(const GemvArgs 
 // A thread turns 16 bytes (32 values, two scale blocks) into 64 output bytes.
 __global__ void dequant_nvfp4_kernel(const uint4* __restrict__ q, const uint16_t* __restrict__ sf, int64_t n16,
                                      uint4* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x) {
     const uint4 w = __ldg(q + i);
     const uint32_t s = e4m3x2_to_f16x2(__ldg(sf + i));
@@ -327,6 +333,8 @@ __global__ void dequant_nvfp4_kernel(const uint4* __restrict__ q, const uint16_t
 // ---------------------------------------------------------------------------
 template <int EPI>
 __global__ void __launch_bounds__(kThreads) gemv_f32_kernel(const GemvArgs a) {
+  pdl_wait();
+  pdl_trigger();
   Seg sg;
   if (!resolve_segment(a, 64, sg)) return;
   const int fl = threadIdx.x & 63, rg = threadIdx.x >> 6;
@@ -352,8 +360,7 @@ __global__ void __launch_bounds__(kThreads) gemv_f32_kernel(const GemvArgs a) {
 template <int EPI, bool OUT_F32>
 cudaError_t pick_nt(const GemvArgs& a, int max_rows, int segs, cudaStream_t s) {
   dim3 grid(a.N / 16, segs, a.offsets ? 1u : (unsigned)ceil_div(max_rows, 16));
-  gemv_bf16_kernel<EPI, OUT_F32><<<grid, kThreads, 0, s>>>(a);
-  count_launches(1);
+  launch_k(gemv_bf16_kernel<EPI, OUT_F32>, grid, kThreads, 0, s, a);
   return cudaGetLastError();
 }
 
@@ -362,9 +369,7 @@ cudaError_t pick_nt(const GemvArgs& a, int max_rows, int segs, cudaStream_t s) {
 cudaError_t launch_dequant_nvfp4(const uint8_t* q, const uint8_t* sf, int64_t n_values, void* out, cudaStream_t s) {
   const int64_t n16 = n_values / 32;
   if (n16 <= 0) return cudaSuccess;
-  dequant_nvfp4_kernel<<<(unsigned)std::min<int64_t>(ceil_div(n16, 256), 16384), 256, 0, s>>>(
-      reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint16_t*>(sf), n16, reinterpret_cast<uint4*>(out));
-  count_launches(1);
+  launch_k(dequant_nvfp4_kernel, (unsigned)std::min<int64_t>(ceil_div(n16, 256), 16384), 256, 0, s, reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint16_t*>(sf), n16, reinterpret_cast<uint4*>(out));
   return cudaGetLastError();
 }
 
@@ -374,23 +379,21 @@ cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_
   if (wfmt == WF_F32) {
     dim3 grid((unsigned)ceil_div(a.N, 64), segs, (unsigned)ceil_div(max_rows, 64));
     switch (epi) {
-      case EPI_RELU2: gemv_f32_kernel<EPI_RELU2><<<grid, kThreads, 0, s>>>(a); break;
-      case EPI_SCALE: gemv_f32_kernel<EPI_SCALE><<<grid, kThreads, 0, s>>>(a); break;
-      case EPI_STORE: gemv_f32_kernel<EPI_STORE><<<grid, kThreads, 0, s>>>(a); break;
-      default: gemv_f32_kernel<EPI_ADD><<<grid, kThreads, 0, s>>>(a); break;
+      case EPI_RELU2: launch_k(gemv_f32_kernel<EPI_RELU2>, grid, kThreads, 0, s, a); break;
+      case EPI_SCALE: launch_k(gemv_f32_kernel<EPI_SCALE>, grid, kThreads, 0, s, a); break;
+      case EPI_STORE: launch_k(gemv_f32_kernel<EPI_STORE>, grid, kThreads, 0, s, a); break;
+      default: launch_k(gemv_f32_kernel<EPI_ADD>, grid, kThreads, 0, s, a); break;
     }
-    count_launches(1);
     return cudaGetLastError();
   }
   if (wfmt == WF_NVFP4 && act == MOE_DT_BF16) {
     // one warp per 16 features: a CTA's 8 warps cover 128 features
     dim3 grid((unsigned)ceil_div(a.N / 16, kWarps), segs, 1);
     switch (epi) {
-      case EPI_RELU2: gemv_nvfp4_kernel<EPI_RELU2, false><<<grid, kThreads, 0, s>>>(a); break;
-      case EPI_SCALE: gemv_nvfp4_kernel<EPI_SCALE, true><<<grid, kThreads, 0, s>>>(a); break;
+      case EPI_RELU2: launch_k(gemv_nvfp4_kernel<EPI_RELU2, false>, grid, kThreads, 0, s, a); break;
+      case EPI_SCALE: launch_k(gemv_nvfp4_kernel<EPI_SCALE, true>, grid, kThreads, 0, s, a); break;
       default: return cudaErrorNotSupported;
     }
-    count_launches(1);
     return cudaGetLastError();
   }
   if (wfmt != WF_BF16 || act != MOE_DT_BF16) return cudaErrorNotSupported;

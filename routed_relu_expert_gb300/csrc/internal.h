@@ -8,6 +8,23 @@ namespace moe {
 // host-side count of kernel launches (moe_launch_count)
 void count_launches(int n);
 
+// Launch with programmatic stream serialisation (see pdl_wait / pdl_trigger).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  count_launches(1);
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // epilogues of the streaming GEMV / grouped GEMM kernels
 enum Epi : int {
   EPI_RELU2 = 0,  // out = bf16(relu(bf16(v))^2)            (F32 layers: relu(v)^2)

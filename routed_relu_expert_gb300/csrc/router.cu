@@ -24,6 +24,8 @@ template <int TMAX, int EPC, bool XF32>
 __global__ void __launch_bounds__(256) router_logits_small(const void* __restrict__ X, int T, int d,
                                                            const float* __restrict__ Wr, int E,
                                                            float* __restrict__ logits) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int KS = 8 / EPC;
   __shared__ float red[8][TMAX];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -90,6 +92,8 @@ template <bool XF32>
 __global__ void __launch_bounds__(256) router_logits_tiled(const void* __restrict__ X, int T, int d,
                                                            const float* __restrict__ Wr, int E,
                                                            float* __restrict__ logits) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float xs[16][64 + 4];
   __shared__ float ws[16][64 + 4];
   const int tid = threadIdx.x;
@@ -167,6 +171,8 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
                                                             int32_t* __restrict__ ids,
                                                             float* __restrict__ wout,
                                                             int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -248,31 +254,42 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
     }
   }
 
-  // top-K among experts of kept groups
+  // top-K among experts of kept groups: every lane keeps the best of its own
+  // remaining candidates; each round the warp takes the best lane-best and only
+  // the winning lane looks again among its values
   uint32_t taken = 0;
   float wsel = 0.f;          // lane k keeps the score of slot k
   int esel = 0;
   float wsum = 0.f;
-#pragma unroll 1
-  for (int k = 0; k < K; ++k) {
-    int bk = INT_MIN, be = INT_MAX;
-    float bs = 0.f;
+  int lk = INT_MIN, le = INT_MAX;
+  float ls = 0.f;
+  auto rescan = [&]() {
+    lk = INT_MIN; le = INT_MAX; ls = 0.f;
 #pragma unroll
     for (int j = 0; j < P; ++j) {
       const int e = lane + 32 * j;
       if (e < E && !((taken >> j) & 1u) && ((kept >> (e / gsz)) & 1u)) {
-        if (better(key[j], e, bk, be)) { bk = key[j]; be = e; bs = s[j]; }
+        if (better(key[j], e, lk, le)) { lk = key[j]; le = e; ls = s[j]; }
       }
     }
+  };
+  rescan();
+#pragma unroll 1
+  for (int k = 0; k < K; ++k) {
+    int bk = lk, be = le;
+    float bs = ls;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const int ok = __shfl_xor_sync(0xffffffffu, bk, off), oe = __shfl_xor_sync(0xffffffffu, be, off);
       const float os = __shfl_xor_sync(0xffffffffu, bs, off);
       if (better(ok, oe, bk, be)) { bk = ok; be = oe; bs = os; }
     }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
     if (lane == k) { wsel = bs; esel = be; }
     wsum += bs;              // slot order, FP32
+    if (be != INT_MAX && (be & 31) == lane) {
+      taken |= 1u << (be >> 5);
+      rescan();
+    }
   }
   if (lane < K) {
     const float wv = norm ? (wsel / wsum) * rsf : wsel * rsf;
@@ -286,6 +303,8 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
 // and each term keeps 8 more significand bits, so sum(x * Wi) with FP32
 // accumulation carries FP32-level precision for BF16 x (exact in BF16).
 __global__ void split_bf16x3_kernel(const float* __restrict__ w, int E, int d, bf16* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t n = (int64_t)E * d;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t e = i / d, j = i - e * d;
@@ -306,9 +325,8 @@ template <int P>
 cudaError_t launch_select_p(const float* logits, int T, int E, const float* bias, int G, int TG, int K,
                             int norm, float rsf, float* scores, int32_t* ids, float* w, int32_t* err,
                             cudaStream_t s) {
-  router_select_kernel<P><<<(unsigned)ceil_div(T, 8), 256, 0, s>>>(logits, T, E, bias, G, TG, K, norm, rsf,
+  launch_k(router_select_kernel<P>, (unsigned)ceil_div(T, 8), 256, 0, s, logits, T, E, bias, G, TG, K, norm, rsf,
                                                                    scores, ids, w, err);
-  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -317,10 +335,9 @@ cudaError_t launch_small_t(const void* x, int act, int T, int d, const float* w,
                            cudaStream_t s) {
   dim3 grid((unsigned)ceil_div(E, EPC), (unsigned)ceil_div(T, TMAX));
   if (act == MOE_DT_F32)
-    router_logits_small<TMAX, EPC, true><<<grid, 256, 0, s>>>(x, T, d, w, E, logits);
+    launch_k(router_logits_small<TMAX, EPC, true>, grid, 256, 0, s, x, T, d, w, E, logits);
   else
-    router_logits_small<TMAX, EPC, false><<<grid, 256, 0, s>>>(x, T, d, w, E, logits);
-  count_launches(1);
+    launch_k(router_logits_small<TMAX, EPC, false>, grid, 256, 0, s, x, T, d, w, E, logits);
   return cudaGetLastError();
 }
 
@@ -340,9 +357,7 @@ cudaError_t launch_router_logits(const void* x, int act, int T, int d, const flo
   if (T <= 0) return cudaSuccess;
   if (w_split && act == MOE_DT_BF16 && T > 64 && E % 32 == 0 && d % 64 == 0) {
     const int64_t n = (int64_t)E * d;
-    split_bf16x3_kernel<<<(unsigned)std::min<int64_t>(ceil_div(n, 256), 2048), 256, 0, s>>>(
-        w_router, E, d, reinterpret_cast<bf16*>(w_split));
-    count_launches(1);
+    launch_k(split_bf16x3_kernel, (unsigned)std::min<int64_t>(ceil_div(n, 256), 2048), 256, 0, s, w_router, E, d, reinterpret_cast<bf16*>(w_split));
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     GemvArgs a{};
@@ -355,10 +370,9 @@ cudaError_t launch_router_logits(const void* x, int act, int T, int d, const flo
   if (T <= 64) return launch_small<8>(x, act, T, d, w_router, E, logits, s);
   dim3 grid((unsigned)ceil_div(T, 64), (unsigned)ceil_div(E, 64));
   if (act == MOE_DT_F32)
-    router_logits_tiled<true><<<grid, 256, 0, s>>>(x, T, d, w_router, E, logits);
+    launch_k(router_logits_tiled<true>, grid, 256, 0, s, x, T, d, w_router, E, logits);
   else
-    router_logits_tiled<false><<<grid, 256, 0, s>>>(x, T, d, w_router, E, logits);
-  count_launches(1);
+    launch_k(router_logits_tiled<false>, grid, 256, 0, s, x, T, d, w_router, E, logits);
   return cudaGetLastError();
 }
 
