@@ -256,6 +256,9 @@ __global__ void __launch_bounds__(kThreads) dispatch_scatter(const DispatchArgs 
 
 constexpr int kSingleMaxRoutes = 4096;
 
+// the dynamic shared-memory limits are raised once, to the largest expert count
+bool g_attr_single = false, g_attr_multi = false;
+
 cudaError_t launch_pack(const DispatchArgs& a, cudaStream_t s) {
   if (!a.x_packed || !a.x_e) return cudaSuccess;
   const int R = a.T * a.K;
@@ -277,8 +280,13 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
   if (R <= kSingleMaxRoutes) {
     const size_t smem = (size_t)(kWarps * a.E + 32) * sizeof(int);
-    cudaError_t e = cudaFuncSetAttribute(dispatch_single, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (!g_attr_single) {
+      e = cudaFuncSetAttribute(dispatch_single, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)((kWarps * 1024 + 32) * sizeof(int)));
+      if (e != cudaSuccess) return e;
+      g_attr_single = true;
+    }
     launch_k(dispatch_single, 1, kThreads, smem, s, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -286,10 +294,15 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
   }
   const int n_tiles = (int)ceil_div(a.T, kTileTokens);
   const size_t smem = (size_t)(kWarps * a.E) * sizeof(int);
-  cudaError_t e = cudaFuncSetAttribute(dispatch_count, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(dispatch_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (!g_attr_multi) {
+    const int most = (int)(kWarps * 1024 * sizeof(int));
+    e = cudaFuncSetAttribute(dispatch_count, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dispatch_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e != cudaSuccess) return e;
+    g_attr_multi = true;
+  }
   launch_k(dispatch_count, n_tiles, kThreads, smem, s, a);
   launch_k(dispatch_scan, 1, kThreads, 0, s, a, n_tiles);
   launch_k(dispatch_scatter, n_tiles, kThreads, smem, s, a);

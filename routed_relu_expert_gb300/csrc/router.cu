@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(256) router_logits_small(const void* __restric
   for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
   if (e < E) {
     const float* w = Wr + (int64_t)e * d;
+#pragma unroll 2
     for (int k = ks * 256 + lane * 8; k < d; k += KS * 256) {
       const uint4 wa = ldg_stream(w + k);
       const uint4 wb = ldg_stream(w + k + 4);
@@ -199,45 +200,52 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
   }
   if (__any_sync(0xffffffffu, any_nan) && lane == 0) set_error(err, MOE_DEVERR_NONFINITE);
 
+  // group of each held expert (one division per held value)
+  const int gsz = E / G;
+  int grp[P];
+#pragma unroll
+  for (int j = 0; j < P; ++j) grp[j] = (lane + 32 * j) / gsz;
+
   // group limit: keep the TG groups with the largest sum of their two largest c
   uint32_t kept = 0xffffffffu;
-  const int gsz = E / G;
   if (G > 1 && TG < G) {
     float gsum[32];
 #pragma unroll
-    for (int g = 0; g < 32; ++g) {
-      gsum[g] = 0.f;
-      if (g < G) {
-        int k1 = INT_MIN, e1 = INT_MAX, k2 = INT_MIN, e2 = INT_MAX;
-        float v1 = 0.f, v2 = 0.f;
+    for (int g = 0; g < 32; ++g) gsum[g] = 0.f;
+#pragma unroll 1
+    for (int g = 0; g < G; ++g) {
+      int k1 = INT_MIN, e1 = INT_MAX, k2 = INT_MIN, e2 = INT_MAX;
+      float v1 = 0.f, v2 = 0.f;
 #pragma unroll
-        for (int j = 0; j < P; ++j) {
-          const int e = lane + 32 * j;
-          if (e < E && e / gsz == g) {
-            if (better(key[j], e, k1, e1)) {
-              k2 = k1; e2 = e1; v2 = v1;
-              k1 = key[j]; e1 = e; v1 = c[j];
-            } else if (better(key[j], e, k2, e2)) {
-              k2 = key[j]; e2 = e; v2 = c[j];
-            }
+      for (int j = 0; j < P; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E && grp[j] == g) {
+          if (better(key[j], e, k1, e1)) {
+            k2 = k1; e2 = e1; v2 = v1;
+            k1 = key[j]; e1 = e; v1 = c[j];
+          } else if (better(key[j], e, k2, e2)) {
+            k2 = key[j]; e2 = e; v2 = c[j];
           }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const int ok1 = __shfl_xor_sync(0xffffffffu, k1, off), oe1 = __shfl_xor_sync(0xffffffffu, e1, off);
-          const int ok2 = __shfl_xor_sync(0xffffffffu, k2, off), oe2 = __shfl_xor_sync(0xffffffffu, e2, off);
-          const float ov1 = __shfl_xor_sync(0xffffffffu, v1, off), ov2 = __shfl_xor_sync(0xffffffffu, v2, off);
-          // merge two sorted pairs into the top two
-          if (better(ok1, oe1, k1, e1)) {
-            if (better(k1, e1, ok2, oe2)) { k2 = k1; e2 = e1; v2 = v1; }
-            else { k2 = ok2; e2 = oe2; v2 = ov2; }
-            k1 = ok1; e1 = oe1; v1 = ov1;
-          } else if (better(ok1, oe1, k2, e2)) {
-            k2 = ok1; e2 = oe1; v2 = ov1;
-          }
-        }
-        gsum[g] = v1 + v2;
       }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const int ok1 = __shfl_xor_sync(0xffffffffu, k1, off), oe1 = __shfl_xor_sync(0xffffffffu, e1, off);
+        const int ok2 = __shfl_xor_sync(0xffffffffu, k2, off), oe2 = __shfl_xor_sync(0xffffffffu, e2, off);
+        const float ov1 = __shfl_xor_sync(0xffffffffu, v1, off), ov2 = __shfl_xor_sync(0xffffffffu, v2, off);
+        // merge two sorted pairs into the top two
+        if (better(ok1, oe1, k1, e1)) {
+          if (better(k1, e1, ok2, oe2)) { k2 = k1; e2 = e1; v2 = v1; }
+          else { k2 = ok2; e2 = oe2; v2 = ov2; }
+          k1 = ok1; e1 = oe1; v1 = ov1;
+        } else if (better(ok1, oe1, k2, e2)) {
+          k2 = ok1; e2 = oe1; v2 = ov1;
+        }
+      }
+      // (g is warp-uniform: the select below keeps gsum in registers)
+#pragma unroll
+      for (int gg = 0; gg < 32; ++gg)
+        if (gg == g) gsum[gg] = v1 + v2;
     }
     kept = 0;
 #pragma unroll 1
@@ -268,7 +276,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
 #pragma unroll
     for (int j = 0; j < P; ++j) {
       const int e = lane + 32 * j;
-      if (e < E && !((taken >> j) & 1u) && ((kept >> (e / gsz)) & 1u)) {
+      if (e < E && !((taken >> j) & 1u) && ((kept >> grp[j]) & 1u)) {
         if (better(key[j], e, lk, le)) { lk = key[j]; le = e; ls = s[j]; }
       }
     }
@@ -345,7 +353,6 @@ template <int TMAX>
 cudaError_t launch_small(const void* x, int act, int T, int d, const float* w, int E, float* logits,
                          cudaStream_t s) {
   // wide routers share each CTA's token rows among several experts
-  if (E >= 512) return launch_small_t<TMAX, 4>(x, act, T, d, w, E, logits, s);
   if (E >= 256) return launch_small_t<TMAX, 2>(x, act, T, d, w, E, logits, s);
   return launch_small_t<TMAX, 1>(x, act, T, d, w, E, logits, s);
 }
