@@ -30,7 +30,7 @@ inline int de_of(const moe_config_t* c) { return c->d_latent > 0 ? c->d_latent :
 
 struct Layout {
   size_t hdr, logits, scores, ids, topw, counts, offsets, active, tile_prefix, w_split;
-  size_t route_token, route_slot, tsr, x_l, x_packed, h, u, y_r, y_rl, hs, ys, tile_counts, w_deq, total;
+  size_t route_token, route_slot, tsr, x_l, x_packed, h, u, y_r, y_rl, hs, ys, tile_counts, total;
 };
 
 inline size_t take(size_t& off, size_t bytes) {
@@ -67,8 +67,6 @@ Layout make_layout(const moe_config_t* c, int32_t T) {
   L.hs = take(off, t * (size_t)c->d_shared * ab);
   L.ys = take(off, t * (size_t)c->d_model * 4);
   L.tile_counts = take(off, dispatch_tile_count_elems(T, c->top_k, c->n_experts) * 4);
-  // NVFP4 experts on the tensor-core path: one expert-weight tensor dequantised to BF16
-  L.w_deq = take(off, (c->expert_dtype == MOE_DT_NVFP4 && T > kDecodeMaxT) ? E * (size_t)c->d_expert * de * 2 : 0);
   L.total = (off + 255) & ~(size_t)255;
   return L;
 }
@@ -191,12 +189,7 @@ moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x
   const int segs = (int)std::min<int64_t>(c->n_experts, (int64_t)T * c->top_k);
   if (use_tc(c, T) && x_packed) {
     const int64_t R = (int64_t)T * c->top_k;
-    if (fp4) {
-      void* deq = P.at<void>(P.L.w_deq);
-      CU(launch_dequant_nvfp4((const uint8_t*)w->w_up, w->w_up_sf,
-                              (int64_t)c->n_experts * I * de, deq, s));
-      a.W = deq; a.w_seg_stride = (int64_t)I * de; a.W_sf = nullptr;
-    }
+    // (NVFP4 weights are converted to BF16 inside the tensor-core kernel)
     CU(launch_gemm_tc(a, EPI_RELU2, false, (int64_t)c->n_experts * I, R, c->n_experts,
                       choose_bn(R / segs, segs, I), s));
     return MOE_OK;
@@ -220,11 +213,6 @@ moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t
   const int segs = (int)std::min<int64_t>(c->n_experts, (int64_t)T * c->top_k);
   if (use_tc(c, T)) {
     const int64_t R = (int64_t)T * c->top_k;
-    if (fp4) {
-      void* deq = P.at<void>(P.L.w_deq);
-      CU(launch_dequant_nvfp4((const uint8_t*)w->w_down, w->w_down_sf, (int64_t)c->n_experts * de * I, deq, s));
-      a.W = deq; a.w_seg_stride = (int64_t)de * I; a.W_sf = nullptr;
-    }
     CU(launch_gemm_tc(a, EPI_SCALE, true, (int64_t)c->n_experts * de, R, c->n_experts,
                       choose_bn(R / segs, segs, de), s));
     return MOE_OK;

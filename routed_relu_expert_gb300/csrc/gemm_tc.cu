@@ -21,9 +21,11 @@
 // Super VL)", section "Super VL", prefill bullet; section "Lightning",
 // prefill bullet) is the prior art; here all experts' tiles form one launch.
 #include "epilogue.cuh"
+#include "nvfp4.cuh"
 
 #include <cuda.h>
 
+#include <cstring>
 #include <mutex>
 
 namespace moe {
@@ -39,7 +41,9 @@ constexpr int B_BYTES = BN_MAX * BK * 2;       // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int N_BOX = 5;                       // B boxes of 16, 32, 64, 128, 256 rows: a tile's rows,
                                                // rounded up to 16, load as their binary decomposition
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;                  // TMA, MMA, 4 epilogue warps
+constexpr int kConvThreads = 128;              // NVFP4 A converters: one thread per tile row
+constexpr int kThreadsFp4 = kThreads + kConvThreads;
 constexpr uint32_t TMEM_COLS = 512;            // two accumulators of BN_MAX columns
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr int kMaxSegments = 1024;
@@ -222,9 +226,14 @@ __device__ __forceinline__ void tile_epilogue(const GemvArgs& a, const Tile& ti,
   }
 }
 
-template <int EPI, bool OUT_F32>
-__global__ void __launch_bounds__(kThreads, 1)
+// FP4A: the A operand (weights) is NVFP4 (a.W packed bytes, a.W_sf E4M3 block
+// scales) and warps 6..9 turn each 128 x 64 stage into BF16 in shared memory
+// (value * block scale, exact), in the 128-byte-swizzled layout TMA would have
+// written; the per-tensor scale is applied by the epilogue.
+template <int EPI, bool OUT_F32, bool FP4A>
+__global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, int E, int m_tiles, int bn, int b_period) {
+  constexpr int NTHR = FP4A ? kThreadsFp4 : kThreads;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -236,10 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + i); };
   auto tempty_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 + i); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  auto afull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };   // FP4A: A tile converted
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* scan_tmp = reinterpret_cast<int*>(tmem_holder + 4);          // [8]
-  int* prefix = scan_tmp + 8;                                          // [E+1]
+  int* scan_tmp = reinterpret_cast<int*>(tmem_holder + 4);          // [16]
+  int* prefix = scan_tmp + 16;                                         // [E+1]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_trigger();
@@ -253,6 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(i), 128);
     }
     mbar_init(drain_bar, 1);
+    if (FP4A)
+      for (int s = 0; s < STAGES; ++s) mbar_init(afull_bar(s), kConvThreads);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -269,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // row-tile prefix over segments (each segment: ceil(rows / bn) row tiles)
   int total_q;
   if (a.offsets) {
-    const int per = (E + kThreads - 1) / kThreads;
+    const int per = (E + NTHR - 1) / NTHR;
     const int e0 = threadIdx.x * per;
     int local = 0;
     for (int e = e0; e < min(E, e0 + per); ++e) local += (a.offsets[e + 1] - a.offsets[e] + bn - 1) / bn;
@@ -288,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefix[e] = run;
       run += (a.offsets[e + 1] - a.offsets[e] + bn - 1) / bn;
     }
-    if (threadIdx.x == kThreads - 1) prefix[E] = wbase + x;
+    if (threadIdx.x == NTHR - 1) prefix[E] = wbase + x;
     // (e0 >= E for the last threads: they still write prefix[E] correctly as the block total)
   } else {
     total_q = (a.dense_rows + bn - 1) / bn;
@@ -318,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.err)) { ok = false; break; }
           const uint32_t sa = base + stage * STAGE_BYTES;
-          mbar_expect_tx(full_bar(stage), A_BYTES + bbytes);
-          tma_load_2d(sa, &maps.a, kb * BK, a_row, full_bar(stage));
+          mbar_expect_tx(full_bar(stage), (FP4A ? 0u : (uint32_t)A_BYTES) + bbytes);
+          if (!FP4A) tma_load_2d(sa, &maps.a, kb * BK, a_row, full_bar(stage));
           int off = 0;
 #pragma unroll
           for (int i = N_BOX - 1; i >= 0; --i) {
@@ -358,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem_base + (uint32_t)(acc * BN_MAX);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
+          if (FP4A && !mbar_wait(afull_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = base + stage * STAGE_BYTES;
           const uint64_t da = smem_desc_sw128(sa), db = smem_desc_sw128(sa + A_BYTES);
@@ -380,7 +393,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
+  } else if (FP4A && warp >= kThreads / 32) {
+    // ------- NVFP4 A converters: warps 6..9; thread = tile row, 64 values per stage -------
+    const int r = threadIdx.x - kThreads;            // tile row
+    const int64_t rowb = a.K / 2, rows_sf = a.K / 16;
+    const uint8_t* Wq = reinterpret_cast<const uint8_t*>(a.W);
+    // flat sequence of (tile, k block) items; loads run two items ahead
+    struct Item { uint4 q0, q1; uint32_t sc; };
+    int ft = blockIdx.x, fkb = 0;                    // fetch cursor and its tile
+    Tile fti;
+    if (ft < total) decode_tile(ft, prefix, E, m_tiles, bn, a, fti);
+    auto fetch_next = [&](Item& it) {
+      const int f = fti.m0 + r;
+      if (f < a.N) {
+        const int64_t row = (int64_t)fti.seg * a.N + f;
+        const uint8_t* src = Wq + row * rowb + fkb * (BK / 2);
+        it.q0 = ldg_stream(src);
+        it.q1 = ldg_stream(src + 16);
+        it.sc = __ldg(reinterpret_cast<const uint32_t*>(a.W_sf + row * rows_sf + fkb * (BK / 16)));
+      } else {
+        it.q0 = it.q1 = make_uint4(0, 0, 0, 0);
+        it.sc = 0;
+      }
+      if (++fkb == nkb) {
+        fkb = 0;
+        ft += gridDim.x;
+        if (ft < total) decode_tile(ft, prefix, E, m_tiles, bn, a, fti);
+      }
+    };
+    Item cur, nxt;
+    cur.q0 = cur.q1 = nxt.q0 = nxt.q1 = make_uint4(0, 0, 0, 0);
+    cur.sc = nxt.sc = 0;
+    if (ft < total) fetch_next(cur);
+    if (ft < total) fetch_next(nxt);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        Item nn = cur;
+        if (ft < total) fetch_next(nn);
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.err)) { ok = false; break; }
+        const uint32_t s0 = e4m3x2_to_f16x2(cur.sc & 0xFFFFu), s1 = e4m3x2_to_f16x2(cur.sc >> 16);
+        const uint32_t sc[4] = {__byte_perm(s0, 0, 0x1010), __byte_perm(s0, 0, 0x3232),
+                                __byte_perm(s1, 0, 0x1010), __byte_perm(s1, 0, 0x3232)};
+        const uint32_t w[8] = {cur.q0.x, cur.q0.y, cur.q0.z, cur.q0.w, cur.q1.x, cur.q1.y, cur.q1.z, cur.q1.w};
+        uint8_t* dst = gbase + stage * STAGE_BYTES + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {            // 16-byte chunk c = values 8c .. 8c+7
+          uint32_t p[4];
+          e2m1x8_to_f16x2(w[c], p);
+          uint4 o;
+          o.x = f16x2_to_bf16x2(hmul2_f16(p[0], sc[c >> 1]));
+          o.y = f16x2_to_bf16x2(hmul2_f16(p[1], sc[c >> 1]));
+          o.z = f16x2_to_bf16x2(hmul2_f16(p[2], sc[c >> 1]));
+          o.w = f16x2_to_bf16x2(hmul2_f16(p[3], sc[c >> 1]));
+          *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) = o;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(afull_bar(stage));
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        cur = nxt;
+        nxt = nn;
+      }
+    }
+  } else if (warp >= 2 && warp < 6) {
     // ---------------- epilogue: warps 2..5, TMEM lane quarter = warp % 4 ----------------
     const int q = warp & 3;
     int acc = 0;
@@ -453,22 +530,22 @@ int num_sms() {
 }
 
 size_t smem_bytes(int E) {
-  return 1024 + (size_t)STAGES * STAGE_BYTES + (2 * STAGES + 5) * 8 + 16 + (8 + E + 1) * sizeof(int) + 64;
+  return 1024 + (size_t)STAGES * STAGE_BYTES + (3 * STAGES + 5) * 8 + 16 + (16 + E + 1) * sizeof(int) + 64;
 }
 
-template <int EPI, bool OUT_F32>
+template <int EPI, bool OUT_F32, bool FP4A>
 cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, int bn, int b_period, int grid,
                      cudaStream_t s) {
   const size_t smem = smem_bytes(kMaxSegments);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, OUT_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, OUT_F32, FP4A>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  launch_k(tc_gemm_kernel<EPI, OUT_F32>, grid, kThreads, smem, s, maps, a, E, m_tiles, bn, b_period);
-  return cudaGetLastError();
+  return launch_k(tc_gemm_kernel<EPI, OUT_F32, FP4A>, grid, FP4A ? kThreadsFp4 : kThreads, smem, s, maps, a, E,
+                  m_tiles, bn, b_period);
 }
 
 }  // namespace
@@ -478,8 +555,10 @@ cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_r
   if (a.K % BK != 0 || bn < 16 || bn > BN_MAX || (bn & (bn - 1)) || E > kMaxSegments) return cudaErrorNotSupported;
   if (x_cols <= 0) x_cols = a.K;
   if (x_cols % BK != 0 || a.K % x_cols != 0) return cudaErrorNotSupported;
+  const bool fp4 = a.W_sf != nullptr;       // NVFP4 weights: converted in the kernel
   TcMaps maps;
-  if (!make_map(&maps.a, a.W, w_rows, a.K, a.K, BM)) return cudaErrorInvalidValue;
+  memset(&maps, 0, sizeof(maps));
+  if (!fp4 && !make_map(&maps.a, a.W, w_rows, a.K, a.K, BM)) return cudaErrorInvalidValue;
   for (int i = 0; i < N_BOX; ++i)
     if (!make_map(&maps.b[i], a.X, x_rows, x_cols, a.x_ld, 16 << i)) return cudaErrorInvalidValue;
   const int m_tiles = (a.N + BM - 1) / BM;
@@ -487,15 +566,22 @@ cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_r
   int grid = num_sms();
   if (!a.offsets) grid = (int)std::min<int64_t>(grid, ceil_div(a.dense_rows, bn) * m_tiles);
   if (grid <= 0) return cudaSuccess;
+  if (fp4) {
+    switch (epi) {
+      case EPI_RELU2: return launch_t<EPI_RELU2, false, true>(maps, a, E, m_tiles, bn, b_period, grid, s);
+      case EPI_SCALE: return launch_t<EPI_SCALE, true, true>(maps, a, E, m_tiles, bn, b_period, grid, s);
+      default: return cudaErrorNotSupported;
+    }
+  }
   switch (epi) {
-    case EPI_RELU2: return launch_t<EPI_RELU2, false>(maps, a, E, m_tiles, bn, b_period, grid, s);
-    case EPI_SCALE: return launch_t<EPI_SCALE, true>(maps, a, E, m_tiles, bn, b_period, grid, s);
+    case EPI_RELU2: return launch_t<EPI_RELU2, false, false>(maps, a, E, m_tiles, bn, b_period, grid, s);
+    case EPI_SCALE: return launch_t<EPI_SCALE, true, false>(maps, a, E, m_tiles, bn, b_period, grid, s);
     case EPI_STORE:
-      return out_f32 ? launch_t<EPI_STORE, true>(maps, a, E, m_tiles, bn, b_period, grid, s)
-                     : launch_t<EPI_STORE, false>(maps, a, E, m_tiles, bn, b_period, grid, s);
+      return out_f32 ? launch_t<EPI_STORE, true, false>(maps, a, E, m_tiles, bn, b_period, grid, s)
+                     : launch_t<EPI_STORE, false, false>(maps, a, E, m_tiles, bn, b_period, grid, s);
     default:
-      return out_f32 ? launch_t<EPI_ADD, true>(maps, a, E, m_tiles, bn, b_period, grid, s)
-                     : launch_t<EPI_ADD, false>(maps, a, E, m_tiles, bn, b_period, grid, s);
+      return out_f32 ? launch_t<EPI_ADD, true, false>(maps, a, E, m_tiles, bn, b_period, grid, s)
+                     : launch_t<EPI_ADD, false, false>(maps, a, E, m_tiles, bn, b_period, grid, s);
   }
 }
 

@@ -15,6 +15,7 @@
 // tiles once for all of its rows) is the prior art; here the grouping comes
 // from the dispatch offsets and the split is over features and K.
 #include "epilogue.cuh"
+#include "nvfp4.cuh"
 
 #include <cuda_fp16.h>
 
@@ -169,28 +170,6 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// the 8 values of one 32-bit word of NVFP4 bytes as 4 FP16 pairs (byte j -> pair j,
-// its low nibble in the low half)
-__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&o)[4]) {
-  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
-      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-      : "r"(w));
-}
-
-// two E4M3 scale bytes (low byte first) as an FP16 pair
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t s16) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)s16));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
-  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
   return *reinterpret_cast<uint32_t*>(&h);
@@ -299,34 +278,6 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_nvfp4_kernel(const GemvArgs 
   }
 }
 
-// NVFP4 -> BF16 of whole matrices (for the tensor-core path): each output is
-// E2M1 * E4M3 (exact in BF16); the per-tensor scale stays for the epilogue.
-// A thread turns 16 bytes (32 values, two scale blocks) into 64 output bytes.
-__global__ void dequant_nvfp4_kernel(const uint4* __restrict__ q, const uint16_t* __restrict__ sf, int64_t n16,
-                                     uint4* __restrict__ out) {
-  pdl_wait();
-  pdl_trigger();
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x) {
-    const uint4 w = __ldg(q + i);
-    const uint32_t s = e4m3x2_to_f16x2(__ldg(sf + i));
-    const uint32_t sc[2] = {__byte_perm(s, 0, 0x1010), __byte_perm(s, 0, 0x3232)};
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint32_t p[4];
-      e2m1x8_to_f16x2(ws[k], p);
-      uint32_t o[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t v = hmul2_f16(p[j], sc[k >> 1]);
-        const float2 f = __half22float2(*reinterpret_cast<__half2*>(&v));
-        o[j] = (uint32_t)bf16_bits(f.x) | ((uint32_t)bf16_bits(f.y) << 16);
-      }
-      out[4 * i + k] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------
 // FP32 weights and activations (small FP32 layers): plain FMA dot products.
 // A CTA owns 64 features of one segment and up to 64 rows.
@@ -365,13 +316,6 @@ cudaError_t pick_nt(const GemvArgs& a, int max_rows, int segs, cudaStream_t s) {
 }
 
 }  // namespace
-
-cudaError_t launch_dequant_nvfp4(const uint8_t* q, const uint8_t* sf, int64_t n_values, void* out, cudaStream_t s) {
-  const int64_t n16 = n_values / 32;
-  if (n16 <= 0) return cudaSuccess;
-  launch_k(dequant_nvfp4_kernel, (unsigned)std::min<int64_t>(ceil_div(n16, 256), 16384), 256, 0, s, reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint16_t*>(sf), n16, reinterpret_cast<uint4*>(out));
-  return cudaGetLastError();
-}
 
 cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_f32, int max_rows,
                         int segs, cudaStream_t s) {

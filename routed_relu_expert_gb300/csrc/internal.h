@@ -113,10 +113,6 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const float* u, const int32_t* token_slot_row, int T, int K, int de,
                            float* y_r, void* y_r_act, int act, cudaStream_t s, const float* add = nullptr);
 
-// NVFP4 matrix -> BF16 values E2M1 * E4M3 (per-tensor scale not applied);
-// n_values elements, 16 per scale byte.
-cudaError_t launch_dequant_nvfp4(const uint8_t* q, const uint8_t* sf, int64_t n_values, void* out, cudaStream_t s);
-
 // dst (act dtype) = src (f32), n a multiple of 4
 cudaError_t launch_cast(const float* src, int64_t n, void* dst, int act, cudaStream_t s);
 
