@@ -116,22 +116,10 @@ inline bool use_tc(const moe_config_t* c, int T) {
   return c->act_dtype == MOE_DT_BF16 && c->expert_dtype != MOE_DT_F32 && T > kDecodeMaxT;
 }
 
-// Rows per tensor-core tile: 256, halved while the estimated tile count stays
-// below two per SM (so moderate token counts still fill the GPU).
-int choose_bn(int64_t rows_per_seg, int64_t segs, int N) {
-  int sms = 0, dev = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t m_tiles = ceil_div(N, 128);
-  int bn = 256;
-  while (bn > 16 && ceil_div(std::max<int64_t>(rows_per_seg, 1), bn) * segs * m_tiles < 2 * (int64_t)sms) bn >>= 1;
-  return bn;
-}
-
 // dense product out[T, N] = X[T, K] W[N, K]^T through the GEMV or the tensor cores
 cudaError_t run_dense(const moe_config_t* c, const GemvArgs& a, int epi, bool out_f32, int T, cudaStream_t s) {
   if (use_tc(c, T))
-    return launch_gemm_tc(a, epi, out_f32, a.N, T, 0, choose_bn(T, 1, a.N), s);
+    return launch_gemm_tc(a, epi, out_f32, a.N, T, 0, tc_tile_rows(T, 1, a.N), s);
   return launch_gemv(a, dense_fmt(c), c->act_dtype, epi, out_f32, T, 1, s);
 }
 
@@ -191,7 +179,7 @@ moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x
     const int64_t R = (int64_t)T * c->top_k;
     // (NVFP4 weights are converted to BF16 inside the tensor-core kernel)
     CU(launch_gemm_tc(a, EPI_RELU2, false, (int64_t)c->n_experts * I, R, c->n_experts,
-                      choose_bn(R / segs, segs, I), s));
+                      tc_tile_rows(R / segs, segs, I), s));
     return MOE_OK;
   }
   CU(launch_gemv(a, wfmt_of(c), c->act_dtype, EPI_RELU2, c->act_dtype == MOE_DT_F32, T, segs, s));
@@ -214,7 +202,7 @@ moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t
   if (use_tc(c, T)) {
     const int64_t R = (int64_t)T * c->top_k;
     CU(launch_gemm_tc(a, EPI_SCALE, true, (int64_t)c->n_experts * de, R, c->n_experts,
-                      choose_bn(R / segs, segs, de), s));
+                      tc_tile_rows(R / segs, segs, de), s));
     return MOE_OK;
   }
   CU(launch_gemv(a, wfmt_of(c), c->act_dtype, EPI_SCALE, true, T, segs, s));

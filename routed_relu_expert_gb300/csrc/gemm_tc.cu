@@ -1,16 +1,29 @@
 // Tensor-core grouped GEMM for segments with many rows (prefill):
 //   out[row, f] = epilogue( sum_k X[row, k] * W_seg[f, k] )
-// computed as D^T = W_tile (A, 128 features x K) * X_tile^T (B, up to 256 rows)
+// computed as D^T = W_tile (A, features x K) * X_tile^T (B, up to 256 rows)
 // with tcgen05.mma (kind::f16, BF16 in, FP32 accumulate in TMEM).
 //
-// One persistent CTA per SM walks the tile list (segment, 128-feature tile,
-// row tile).  Warp 0 streams A and B tiles with TMA (128-byte swizzle,
-// K-major, 64 K-elements per stage) through a 4-stage shared-memory ring;
-// one thread of warp 1 issues the MMAs; warps 2-5 read the accumulator from
-// TMEM and run the epilogue, which overlaps the next tile's MMAs through two
-// TMEM accumulators.  Row tiles end at segment boundaries: rows a tile loads
-// beyond its segment are computed and discarded, and the MMA N is the row
-// count rounded up to 16, so small tail tiles cost little.
+// Persistent kernel: one CTA per SM, or one CTA pair per two SMs, walks the
+// tile list (segment, feature tile, row tile).  Warps 0 and 6 stream the A and
+// the B tiles with TMA (128-byte swizzle, K-major, 64 K-elements per stage)
+// through a shared-memory ring: one TMA box per operand and stage, each issued
+// by its own warp, since one issuing thread sustains only about one box per
+// 300-400 cycles.  One thread of warp 1 issues the MMAs; warps 2-5 read the
+// accumulator from TMEM and run the epilogue, which overlaps the next tile's
+// MMAs through two TMEM accumulators.  Row tiles end at segment boundaries:
+// rows a tile loads beyond its segment are computed and discarded, and the MMA
+// N is the row count rounded up to 16, so small tail tiles cost little.
+//
+// CG = 2 (a cluster of two CTAs on two SMs, tcgen05 cta_group::2): the tile is
+// 256 features x N rows.  Each CTA stages its own 128 features of A and half
+// of the N rows of B; the even CTA issues M = 256 MMAs that read both CTAs'
+// shared memory and write 128 TMEM lanes in each.  Per SM this halves the B
+// bytes staged per MMA, so a stage carries 32 KB instead of 48 KB for the same
+// tensor work: the L2-to-SM copy rate (about 60-68 bytes per cycle per SM),
+// not the tensor pipe, bounds the single-CTA form.  The even CTA's "full" barrier counts both CTAs' TMA
+// bytes; MMA completion is signalled to both CTAs' "empty" and "accumulator
+// full" barriers by a multicast commit; the odd CTA's epilogue and converter
+// threads arrive on the even CTA's barriers remotely.
 //
 // Every wait on an mbarrier gives up after a time limit: the waiter sets
 // MOE_DEVERR_TIMEOUT and an abort flag that stops the other roles, the
@@ -32,25 +45,38 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128;                        // features per tile (MMA M)
+constexpr int BM = 128;                        // features per CTA (TMEM lanes)
 constexpr int BK = 64;                         // K per stage: one 128-byte swizzle row
 constexpr int BN_MAX = 256;                    // rows per tile (MMA N at most)
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;           // 16 KB
-constexpr int B_BYTES = BN_MAX * BK * 2;       // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int N_BOX = 5;                       // B boxes of 16, 32, 64, 128, 256 rows: a tile's rows,
-                                               // rounded up to 16, load as their binary decomposition
-constexpr int kThreads = 192;                  // TMA, MMA, 4 epilogue warps
+constexpr int N_BMAP = 16;                     // B boxes of 1..16 x (16 / CG) rows: every tile's B
+                                               // half loads as one box
+constexpr int kThreads = 224;                  // A TMA, MMA, 4 epilogue warps, B TMA
+constexpr int kBWarp = 6;
 constexpr int kConvThreads = 128;              // NVFP4 A converters: one thread per tile row
 constexpr int kThreadsFp4 = kThreads + kConvThreads;
 constexpr uint32_t TMEM_COLS = 512;            // two accumulators of BN_MAX columns
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr int kMaxSegments = 1024;
 
+// ring geometry per CTA group size (CG = CTAs that share one MMA)
+template <int CG>
+struct Ring {
+  static constexpr int TILE_M = BM * CG;                  // features per tile
+  static constexpr int B_ROWS = BN_MAX / CG;              // B rows one CTA stages
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB (CG 1), 32 KB (CG 2)
+  static constexpr int STAGES = CG == 2 ? 6 : 4;
+  static constexpr int BOX0 = 16 / CG;                    // B box height step (rows)
+  // unused bytes after the ring, so that no operand read of the last stage can
+  // leave the allocation whatever the split of B between the two CTAs
+  static constexpr int SLACK = CG == 2 ? B_BYTES : 0;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES + SLACK;
+};
+
 struct TcMaps {
   CUtensorMap a;
-  CUtensorMap b[N_BOX];
+  CUtensorMap b[N_BMAP];                         // b[i]: boxes of (i + 1) * BOX0 rows
 };
 
 // ---------------------------------------------------------------------------
@@ -83,13 +109,27 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// the same with cluster-scope acquire: for barriers the peer CTA arrives on
+__device__ __forceinline__ bool mbar_try_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase of `parity` to complete; false if this thread
 // gave up or another role raised the abort flag.
+template <bool CL = false>
 __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
-  if (mbar_try(bar, parity)) return true;
+  auto probe = [&]() { return CL ? mbar_try_cl(bar, parity) : mbar_try(bar, parity); };
+  if (probe()) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (mbar_try(bar, parity)) return true;
+    if (probe()) return true;
     if (*abort_flag) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
       set_error(err, MOE_DEVERR_TIMEOUT);
@@ -97,6 +137,28 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_fla
       return false;
     }
   }
+}
+
+// ---- cluster (CTA pair) helpers ----
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// address of the same shared-memory offset in CTA 0 of the cluster
+__device__ __forceinline__ uint32_t map_to_rank0(uint32_t addr) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(addr));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
@@ -107,17 +169,44 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// pair form: the copy lands in this CTA's shared memory and completes its
+// bytes on an mbarrier of either CTA of the pair (here: CTA 0's)
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+template <int CG>
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if (CG == 2)
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+// arrive on `bar` when this thread's MMAs so far are complete; CG 2: on the
+// barrier at the same offset in each CTA of `mask`
+template <int CG>
+__device__ __forceinline__ void tc_commit(uint32_t bar, uint16_t mask = 3) {
+  if (CG == 2)
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // 32 consecutive FP32 accumulator columns of this thread's TMEM lane
@@ -159,8 +248,8 @@ struct Tile {
   int seg, m0, row0, rows;
 };
 
-__device__ __forceinline__ void decode_tile(int t, const int* prefix, int E, int m_tiles, int bn, const GemvArgs& a,
-                                            Tile& ti) {
+__device__ __forceinline__ void decode_tile(int t, const int* prefix, int E, int m_tiles, int tile_m, int bn,
+                                            const GemvArgs& a, Tile& ti) {
   const int q = t / m_tiles, m = t - q * m_tiles;
   int seg = 0, nt = q, base = 0, count = a.dense_rows;
   if (a.offsets) {
@@ -175,7 +264,7 @@ __device__ __forceinline__ void decode_tile(int t, const int* prefix, int E, int
     count = a.offsets[lo + 1] - base;
   }
   ti.seg = seg;
-  ti.m0 = m * BM;
+  ti.m0 = m * tile_m;
   ti.row0 = base + nt * bn;
   ti.rows = min(bn, count - nt * bn);
 }
@@ -227,52 +316,71 @@ __device__ __forceinline__ void tile_epilogue(const GemvArgs& a, const Tile& ti,
 }
 
 // FP4A: the A operand (weights) is NVFP4 (a.W packed bytes, a.W_sf E4M3 block
-// scales) and warps 6..9 turn each 128 x 64 stage into BF16 in shared memory
+// scales) and warps 7..10 turn each 128 x 64 stage into BF16 in shared memory
 // (value * block scale, exact), in the 128-byte-swizzled layout TMA would have
 // written; the per-tensor scale is applied by the epilogue.
-template <int EPI, bool OUT_F32, bool FP4A>
+template <int EPI, bool OUT_F32, bool FP4A, int CG>
 __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, int E, int m_tiles, int bn, int b_period) {
+  using G = Ring<CG>;
   constexpr int NTHR = FP4A ? kThreadsFp4 : kThreads;
+  constexpr int STAGES = G::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + G::RING_BYTES);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
   auto tfull_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + i); };
   auto tempty_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 + i); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  auto afull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };   // FP4A: A tile converted
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
+  auto afull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };   // FP4A: this CTA's A converted
+  auto pafull_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + 5 + s); };  // FP4A, CG 2: the peer's A converted
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 4 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* scan_tmp = reinterpret_cast<int*>(tmem_holder + 4);          // [16]
   int* prefix = scan_tmp + 16;                                         // [E+1]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CG 2: rank 0 of the pair issues the MMAs and owns the barriers both CTAs'
+  // copies and drains arrive on; both walk the same tile sequence
+  const uint32_t rank = CG == 2 ? cluster_rank() : 0u;
+  const int unit = CG == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int n_units = CG == 2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  auto at_leader = [&](uint32_t bar) { return CG == 2 ? map_to_rank0(bar) : bar; };
   pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), FP4A ? 1 : 2);      // the A and B producers of CTA 0
       mbar_init(empty_bar(s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull_bar(i), 1);
-      mbar_init(tempty_bar(i), 128);
+      mbar_init(tempty_bar(i), 128 * CG);
     }
     mbar_init(drain_bar, 1);
     if (FP4A)
-      for (int s = 0; s < STAGES; ++s) mbar_init(afull_bar(s), kConvThreads);
+      for (int s = 0; s < STAGES; ++s) {
+        mbar_init(afull_bar(s), kConvThreads);
+        mbar_init(pafull_bar(s), 1);
+      }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (CG == 2) {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
 
   // barriers and TMEM are set up while the previous kernel finishes; its
@@ -307,46 +415,46 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (CG == 2) cluster_sync();      // the peer's barriers exist before any remote arrive or copy
   tc_fence_after();
   if (a.offsets) total_q = prefix[E];
   const uint32_t tmem_base = *tmem_holder;
   const int total = total_q * m_tiles;
   const int nkb = a.K / BK;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
+  if (warp == 0 || warp == kBWarp) {
+    const bool is_a = warp == 0;
+    if (lane == 0 && !(is_a && FP4A)) {
+      // ------- TMA producers: warp 0 the A (weight) tile, warp 6 the B (row) tile;
+      // each CTA loads its own operand halves -------
       int pend[STAGES];
       for (int s = 0; s < STAGES; ++s) pend[s] = -1;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int t = unit; t < total && ok; t += n_units) {
         Tile ti;
-        decode_tile(t, prefix, E, m_tiles, bn, a, ti);
+        decode_tile(t, prefix, E, m_tiles, G::TILE_M, bn, a, ti);
         const int r16 = (ti.rows + 15) & ~15;
-        const uint32_t bbytes = (uint32_t)r16 * BK * 2;
-        const int a_row = ti.seg * a.N + ti.m0;
+        const int hb = r16 / CG;                             // B rows this CTA loads
+        const CUtensorMap* map = is_a ? &maps.a : &maps.b[hb / G::BOX0 - 1];
+        const uint32_t tx = is_a ? (uint32_t)CG * A_BYTES : (uint32_t)r16 * BK * 2;
+        const int row = is_a ? ti.seg * a.N + ti.m0 + BM * (int)rank : ti.row0 + hb * (int)rank;
+        const uint32_t dst0 = base + (is_a ? 0u : (uint32_t)A_BYTES);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.err)) { ok = false; break; }
-          const uint32_t sa = base + stage * STAGE_BYTES;
-          mbar_expect_tx(full_bar(stage), (FP4A ? 0u : (uint32_t)A_BYTES) + bbytes);
-          if (!FP4A) tma_load_2d(sa, &maps.a, kb * BK, a_row, full_bar(stage));
-          int off = 0;
-#pragma unroll
-          for (int i = N_BOX - 1; i >= 0; --i) {
-            if (r16 & (16 << i)) {
-              tma_load_2d(sa + A_BYTES + off * (BK * 2), &maps.b[i], (kb % b_period) * BK, ti.row0 + off,
-                          full_bar(stage));
-              off += 16 << i;
-            }
-          }
+          if (rank == 0) mbar_expect_tx(full_bar(stage), tx);
+          const int col = is_a ? kb * BK : (kb % b_period) * BK;
+          const uint32_t dst = dst0 + stage * G::STAGE_BYTES;
+          if (CG == 2) tma_load_2d_pair(dst, map, col, row, at_leader(full_bar(stage)));
+          else tma_load_2d(dst, map, col, row, full_bar(stage));
           pend[stage] = (int)phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
-      if (!ok) {
-        // copies still in flight must land before the CTA leaves
+      if (!ok && rank == 0) {
+        // copies still in flight (both CTAs' count on these barriers) must land
+        // before the CTA leaves
         for (int s = 0; s < STAGES; ++s) {
           if (pend[s] < 0) continue;
           const uint64_t t0 = globaltimer();
@@ -356,55 +464,69 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer ----------------
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true, issued = false;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int t = unit; t < total && ok; t += n_units) {
         Tile ti;
-        decode_tile(t, prefix, E, m_tiles, bn, a, ti);
-        const uint32_t idesc = idesc_bf16(BM, (ti.rows + 15) & ~15);
-        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, a.err)) { ok = false; break; }
+        decode_tile(t, prefix, E, m_tiles, G::TILE_M, bn, a, ti);
+        const uint32_t idesc = idesc_bf16(G::TILE_M, (ti.rows + 15) & ~15);
+        if (!mbar_wait<CG == 2>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, a.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN_MAX);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
           if (FP4A && !mbar_wait(afull_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
+          if (FP4A && CG == 2 && !mbar_wait<true>(pafull_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sa = base + stage * STAGE_BYTES;
+          const uint32_t sa = base + stage * G::STAGE_BYTES;
           const uint64_t da = smem_desc_sw128(sa), db = smem_desc_sw128(sa + A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc_mma(d, da + 2u * k, db + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            tc_mma<CG>(d, da + 2u * k, db + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
           issued = true;
-          tc_commit(empty_bar(stage));
+          tc_commit<CG>(empty_bar(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(tfull_bar(acc));
+        tc_commit<CG>(tfull_bar(acc));
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
       if (!ok && issued) {
         // MMAs still reading shared memory / writing TMEM must finish first
-        tc_commit(drain_bar);
+        tc_commit<CG>(drain_bar, 1);
         const uint64_t t0 = globaltimer();
         while (!mbar_try(drain_bar, 0u) && globaltimer() - t0 < kWaitLimitNs) {
         }
       }
+    } else if (FP4A && CG == 2 && lane == 0) {
+      // ---- odd CTA: relay "A converted" to the even CTA, one arrive per stage ----
+      // (the converters' own arrives are CTA-local, so their release does not
+      // wait on the global loads they keep in flight)
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = unit; t < total && ok; t += n_units)
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(afull_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
+          mbar_arrive_cluster(at_leader(pafull_bar(stage)));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
     }
   } else if (FP4A && warp >= kThreads / 32) {
-    // ------- NVFP4 A converters: warps 6..9; thread = tile row, 64 values per stage -------
+    // ------- NVFP4 A converters: warps 7..10; thread = tile row, 64 values per stage -------
     const int r = threadIdx.x - kThreads;            // tile row
     const int64_t rowb = a.K / 2, rows_sf = a.K / 16;
     const uint8_t* Wq = reinterpret_cast<const uint8_t*>(a.W);
     // flat sequence of (tile, k block) items; loads run two items ahead
     struct Item { uint4 q0, q1; uint32_t sc; };
-    int ft = blockIdx.x, fkb = 0;                    // fetch cursor and its tile
+    int ft = unit, fkb = 0;                          // fetch cursor and its tile
     Tile fti;
-    if (ft < total) decode_tile(ft, prefix, E, m_tiles, bn, a, fti);
+    if (ft < total) decode_tile(ft, prefix, E, m_tiles, G::TILE_M, bn, a, fti);
     auto fetch_next = [&](Item& it) {
-      const int f = fti.m0 + r;
+      const int f = fti.m0 + BM * (int)rank + r;
       if (f < a.N) {
         const int64_t row = (int64_t)fti.seg * a.N + f;
         const uint8_t* src = Wq + row * rowb + fkb * (BK / 2);
@@ -417,8 +539,8 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
       }
       if (++fkb == nkb) {
         fkb = 0;
-        ft += gridDim.x;
-        if (ft < total) decode_tile(ft, prefix, E, m_tiles, bn, a, fti);
+        ft += n_units;
+        if (ft < total) decode_tile(ft, prefix, E, m_tiles, G::TILE_M, bn, a, fti);
       }
     };
     Item cur, nxt;
@@ -429,7 +551,7 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int t = unit; t < total && ok; t += n_units) {
       for (int kb = 0; kb < nkb; ++kb) {
         Item nn = cur;
         if (ft < total) fetch_next(nn);
@@ -438,7 +560,7 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
         const uint32_t sc[4] = {__byte_perm(s0, 0, 0x1010), __byte_perm(s0, 0, 0x3232),
                                 __byte_perm(s1, 0, 0x1010), __byte_perm(s1, 0, 0x3232)};
         const uint32_t w[8] = {cur.q0.x, cur.q0.y, cur.q0.z, cur.q0.w, cur.q1.x, cur.q1.y, cur.q1.z, cur.q1.w};
-        uint8_t* dst = gbase + stage * STAGE_BYTES + r * 128;
+        uint8_t* dst = gbase + stage * G::STAGE_BYTES + r * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {            // 16-byte chunk c = values 8c .. 8c+7
           uint32_t p[4];
@@ -462,12 +584,12 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
     const int q = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int t = unit; t < total; t += n_units) {
       Tile ti;
-      decode_tile(t, prefix, E, m_tiles, bn, a, ti);
+      decode_tile(t, prefix, E, m_tiles, G::TILE_M, bn, a, ti);
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, a.err)) break;
       tc_fence_after();
-      const int f = ti.m0 + 32 * q + lane;
+      const int f = ti.m0 + BM * (int)rank + 32 * q + lane;
       const bool fv = f < a.N;
       const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN_MAX);
       for (int c0 = 0; c0 < ti.rows; c0 += 32) {
@@ -475,18 +597,27 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
         tmem_ld32(tb + (uint32_t)c0, v);
         tile_epilogue<EPI, OUT_F32>(a, ti, c0, f, fv, lane, v);
       }
+      // TMEM reads are complete (tcgen05.wait::ld); the stores need no ordering
+      // with the next MMAs, so the peer's arrive is relaxed
       tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
+      if (rank == 0) mbar_arrive(tempty_bar(acc));
+      else mbar_arrive_cluster_relaxed(at_leader(tempty_bar(acc)));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
   }
   tc_fence_before();
   __syncthreads();
+  if (CG == 2) cluster_sync();      // no CTA leaves while its peer may still touch its memory
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
-                 : "memory");
+    if (CG == 2)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                   : "memory");
   }
+  if (CG == 2) cluster_sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -522,6 +653,49 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps of one product (A: weights, 128-row boxes; B: rows, boxes of
+// 1..16 x 16/cg rows), encoded once per distinct set of pointers and extents.
+struct MapKey {
+  const void* w;
+  int64_t w_rows;
+  int k;
+  const void* x;
+  int64_t x_rows;
+  int x_cols;
+  int64_t x_ld;
+  int cg;
+  bool operator==(const MapKey& o) const {
+    return w == o.w && w_rows == o.w_rows && k == o.k && x == o.x && x_rows == o.x_rows && x_cols == o.x_cols &&
+           x_ld == o.x_ld && cg == o.cg;
+  }
+};
+
+bool get_maps(const MapKey& key, TcMaps& out) {
+  constexpr int kSlots = 16;
+  static std::mutex mu;
+  static MapKey keys[kSlots];
+  static TcMaps maps[kSlots];
+  static bool used[kSlots] = {};
+  static int next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < kSlots; ++i)
+    if (used[i] && keys[i] == key) {
+      out = maps[i];
+      return true;
+    }
+  TcMaps m;
+  memset(&m, 0, sizeof(m));
+  if (key.w && !make_map(&m.a, key.w, key.w_rows, key.k, key.k, BM)) return false;
+  for (int i = 0; i < N_BMAP; ++i)
+    if (!make_map(&m.b[i], key.x, key.x_rows, key.x_cols, key.x_ld, (i + 1) * (16 / key.cg))) return false;
+  keys[next] = key;
+  maps[next] = m;
+  used[next] = true;
+  next = (next + 1) % kSlots;
+  out = m;
+  return true;
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -529,26 +703,105 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
+template <int CG>
 size_t smem_bytes(int E) {
-  return 1024 + (size_t)STAGES * STAGE_BYTES + (3 * STAGES + 5) * 8 + 16 + (16 + E + 1) * sizeof(int) + 64;
+  return 1024 + (size_t)Ring<CG>::RING_BYTES + (4 * Ring<CG>::STAGES + 5) * 8 + 16 + (16 + E + 1) * sizeof(int) + 64;
 }
 
-template <int EPI, bool OUT_F32, bool FP4A>
-cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, int bn, int b_period, int grid,
-                     cudaStream_t s) {
-  const size_t smem = smem_bytes(kMaxSegments);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, OUT_F32, FP4A>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
+// Largest number of CTA pairs (clusters of 2) resident at once; 0 if unknown.
+template <class K>
+int max_pairs(K kernel, size_t smem, int threads) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
   }
-  return launch_k(tc_gemm_kernel<EPI, OUT_F32, FP4A>, grid, FP4A ? kThreadsFp4 : kThreads, smem, s, maps, a, E,
-                  m_tiles, bn, b_period);
+  return n;
 }
+
+template <int EPI, bool OUT_F32, bool FP4A, int CG>
+cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, int bn, int b_period, int units,
+                     cudaStream_t s) {
+  auto kernel = tc_gemm_kernel<EPI, OUT_F32, FP4A, CG>;
+  const size_t smem = smem_bytes<CG>(kMaxSegments);
+  const int threads = FP4A ? kThreadsFp4 : kThreads;
+  static int unit_cap = -1;           // CTAs (CG 1) or CTA pairs (CG 2) resident at once
+  if (unit_cap < 0) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (CG == 2) {
+      const int p = max_pairs(kernel, smem, threads);
+      unit_cap = p > 0 ? p : num_sms() / 2;
+    } else {
+      unit_cap = num_sms();
+    }
+  }
+  units = std::max(1, std::min(units, unit_cap));
+  if (CG == 1) return launch_k(kernel, units, threads, smem, s, maps, a, E, m_tiles, bn, b_period);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * units);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  count_launches(1);
+  return cudaLaunchKernelEx(&cfg, kernel, maps, a, E, m_tiles, bn, b_period);
+}
+
+template <int CG>
+cudaError_t launch_cg(const TcMaps& maps, const GemvArgs& a, int epi, bool out_f32, bool fp4, int E, int m_tiles,
+                      int bn, int b_period, int units, cudaStream_t s) {
+  if (fp4) {
+    switch (epi) {
+      case EPI_RELU2: return launch_t<EPI_RELU2, false, true, CG>(maps, a, E, m_tiles, bn, b_period, units, s);
+      case EPI_SCALE: return launch_t<EPI_SCALE, true, true, CG>(maps, a, E, m_tiles, bn, b_period, units, s);
+      default: return cudaErrorNotSupported;
+    }
+  }
+  switch (epi) {
+    case EPI_RELU2: return launch_t<EPI_RELU2, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, s);
+    case EPI_SCALE: return launch_t<EPI_SCALE, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, s);
+    case EPI_STORE:
+      return out_f32 ? launch_t<EPI_STORE, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, s)
+                     : launch_t<EPI_STORE, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, s);
+    default:
+      return out_f32 ? launch_t<EPI_ADD, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, s)
+                     : launch_t<EPI_ADD, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, s);
+  }
+}
+
+// CTA pairs for products with more than one 128-feature tile per segment
+inline int pick_cg(int N) { return N > BM ? 2 : 1; }
 
 }  // namespace
+
+int tc_tile_rows(int64_t rows_per_seg, int64_t segs, int N) {
+  const int cg = pick_cg(N);
+  const int64_t m_tiles = ceil_div(N, (int64_t)BM * cg);
+  const int64_t units = num_sms() / cg;
+  int bn = BN_MAX;
+  while (bn > 16 && ceil_div(std::max<int64_t>(rows_per_seg, 1), bn) * segs * m_tiles < 2 * units) bn >>= 1;
+  return bn;
+}
 
 cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_rows, int64_t x_rows, int E, int bn,
                            cudaStream_t s, int x_cols) {
@@ -556,33 +809,17 @@ cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_r
   if (x_cols <= 0) x_cols = a.K;
   if (x_cols % BK != 0 || a.K % x_cols != 0) return cudaErrorNotSupported;
   const bool fp4 = a.W_sf != nullptr;       // NVFP4 weights: converted in the kernel
+  const int cg = pick_cg(a.N);
   TcMaps maps;
-  memset(&maps, 0, sizeof(maps));
-  if (!fp4 && !make_map(&maps.a, a.W, w_rows, a.K, a.K, BM)) return cudaErrorInvalidValue;
-  for (int i = 0; i < N_BOX; ++i)
-    if (!make_map(&maps.b[i], a.X, x_rows, x_cols, a.x_ld, 16 << i)) return cudaErrorInvalidValue;
-  const int m_tiles = (a.N + BM - 1) / BM;
+  if (!get_maps(MapKey{fp4 ? nullptr : a.W, w_rows, a.K, a.X, x_rows, x_cols, a.x_ld, cg}, maps))
+    return cudaErrorInvalidValue;
+  const int m_tiles = (a.N + BM * cg - 1) / (BM * cg);
   const int b_period = x_cols / BK;
-  int grid = num_sms();
-  if (!a.offsets) grid = (int)std::min<int64_t>(grid, ceil_div(a.dense_rows, bn) * m_tiles);
-  if (grid <= 0) return cudaSuccess;
-  if (fp4) {
-    switch (epi) {
-      case EPI_RELU2: return launch_t<EPI_RELU2, false, true>(maps, a, E, m_tiles, bn, b_period, grid, s);
-      case EPI_SCALE: return launch_t<EPI_SCALE, true, true>(maps, a, E, m_tiles, bn, b_period, grid, s);
-      default: return cudaErrorNotSupported;
-    }
-  }
-  switch (epi) {
-    case EPI_RELU2: return launch_t<EPI_RELU2, false, false>(maps, a, E, m_tiles, bn, b_period, grid, s);
-    case EPI_SCALE: return launch_t<EPI_SCALE, true, false>(maps, a, E, m_tiles, bn, b_period, grid, s);
-    case EPI_STORE:
-      return out_f32 ? launch_t<EPI_STORE, true, false>(maps, a, E, m_tiles, bn, b_period, grid, s)
-                     : launch_t<EPI_STORE, false, false>(maps, a, E, m_tiles, bn, b_period, grid, s);
-    default:
-      return out_f32 ? launch_t<EPI_ADD, true, false>(maps, a, E, m_tiles, bn, b_period, grid, s)
-                     : launch_t<EPI_ADD, false, false>(maps, a, E, m_tiles, bn, b_period, grid, s);
-  }
+  int units = num_sms() / cg;
+  if (!a.offsets) units = (int)std::min<int64_t>(units, ceil_div(a.dense_rows, bn) * m_tiles);
+  if (units <= 0) return cudaSuccess;
+  if (cg == 2) return launch_cg<2>(maps, a, epi, out_f32, fp4, E, m_tiles, bn, b_period, units, s);
+  return launch_cg<1>(maps, a, epi, out_f32, fp4, E, m_tiles, bn, b_period, units, s);
 }
 
 }  // namespace moe

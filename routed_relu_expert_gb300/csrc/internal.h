@@ -76,6 +76,10 @@ cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_
 // one matrix); 0 = K.
 cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_rows, int64_t x_rows, int E, int bn,
                            cudaStream_t s, int x_cols = 0);
+// Rows per tile for launch_gemm_tc: the largest power of two (16..256) that
+// still gives every SM about two tiles, for segments of rows_per_seg rows and
+// N output features.
+int tc_tile_rows(int64_t rows_per_seg, int64_t segs, int N);
 
 // router
 // w_split: scratch of E * 3d BF16 for the tensor-core path (many BF16 tokens);
