@@ -68,15 +68,19 @@ struct Ring {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB (CG 1), 32 KB (CG 2)
   static constexpr int STAGES = CG == 2 ? 6 : 4;
   static constexpr int BOX0 = 16 / CG;                    // B box height step (rows)
-  // unused bytes after the ring, so that no operand read of the last stage can
-  // leave the allocation whatever the split of B between the two CTAs
-  static constexpr int SLACK = CG == 2 ? B_BYTES : 0;
-  static constexpr int RING_BYTES = STAGES * STAGE_BYTES + SLACK;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
 };
+
+// epilogue staging after the ring: per epilogue warp one 32 x 32 output chunk
+// (FP32 at most) and the routing weights of one tile's rows
+constexpr int STG_BYTES = 32 * 32 * 4;
+constexpr int WROW_BYTES = BN_MAX * 4;
+constexpr int EPI_SMEM = 4 * (STG_BYTES + WROW_BYTES);
 
 struct TcMaps {
   CUtensorMap a;
   CUtensorMap b[N_BMAP];                         // b[i]: boxes of (i + 1) * BOX0 rows
+  CUtensorMap out;                               // output, boxes of 32 rows x 32 features
 };
 
 // ---------------------------------------------------------------------------
@@ -168,6 +172,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+
+// shared -> global tensor store of one box; completion tracked by bulk groups
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // pair form: the copy lands in this CTA's shared memory and completes its
 // bytes on an mbarrier of either CTA of the pair (here: CTA 0's)
@@ -269,23 +284,24 @@ __device__ __forceinline__ void decode_tile(int t, const int* prefix, int E, int
   ti.rows = min(bn, count - nt * bn);
 }
 
-// Epilogue of 32 accumulator columns (rows row0+c0 .. +31) of one feature f.
-// Per-row inputs are fetched before any store: the routing weight of each
-// column by one lane and broadcast, the added term as 32 independent loads.
+// Epilogue of 32 accumulator columns (rows row0+c0 .. +31) of one feature f;
+// the warp's 32 lanes hold features f0 .. f0+31 (all valid or all beyond N).
+// The routing weight of each row (EPI_SCALE) was fetched at the start of the
+// tile into `wrow`.  A full chunk of 32 rows is staged in shared memory as
+// [row][32 features] and written by one TMA store (a few wide writes instead of
+// 32 two- or four-byte stores per thread); a partial chunk, or an output
+// without a tensor map, is stored element by element.
 template <int EPI, bool OUT_F32>
-__device__ __forceinline__ void tile_epilogue(const GemvArgs& a, const Tile& ti, int c0, int f, bool fv, int lane,
-                                              float (&v)[32]) {
+__device__ __forceinline__ void tile_epilogue(const GemvArgs& a, const CUtensorMap* out_map, const Tile& ti, int c0,
+                                              int f0, int lane, const float* wrow, uint8_t* stg, float (&v)[32]) {
+  constexpr bool F32 = OUT_F32 || EPI == EPI_SCALE;
   const int nc = min(32, ti.rows - c0);
+  const int f = f0 + lane;
+  if (f0 >= a.N) return;
   if (EPI == EPI_SCALE) {
-    float wl = 0.f;
-    if (lane < nc) {
-      const int r = ti.row0 + c0 + lane;
-      wl = a.topw[(int64_t)a.route_token[r] * a.top_k + a.route_slot[r]];
-    }
 #pragma unroll
-    for (int c = 0; c < 32; ++c) v[c] *= __shfl_sync(0xffffffffu, wl, c);
+    for (int c = 0; c < 32; ++c) v[c] *= wrow[c0 + c];
   }
-  if (!fv) return;
   if (a.W_gs) {
     const float gs = a.W_gs[ti.seg];
 #pragma unroll
@@ -301,17 +317,34 @@ __device__ __forceinline__ void tile_epilogue(const GemvArgs& a, const Tile& ti,
   }
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
-    if (c >= nc) break;
-    float r = v[c];
     if (EPI == EPI_RELU2) {
-      const float u = fmaxf(round_bf16(r), 0.f);
-      r = u * u;
+      const float u = fmaxf(round_bf16(v[c]), 0.f);
+      v[c] = u * u;
     }
+  }
+  if (out_map && nc == 32) {
+    if (lane == 0) bulk_wait_read_all();   // the previous chunk's store has left the staging buffer
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      if (F32)
+        reinterpret_cast<float*>(stg)[c * 32 + lane] = v[c];
+      else
+        reinterpret_cast<bf16*>(stg)[c * 32 + lane] = __float2bfloat16_rn(v[c]);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) tma_store_2d(out_map, smem_u32(stg), f0, ti.row0 + c0);
+    return;
+  }
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    if (c >= nc) break;
     const int64_t o = (int64_t)(ti.row0 + c0 + c) * a.out_ld + f;
-    if (OUT_F32 || EPI == EPI_SCALE)
-      reinterpret_cast<float*>(a.out)[o] = r;
+    if (F32)
+      reinterpret_cast<float*>(a.out)[o] = v[c];
     else
-      reinterpret_cast<bf16*>(a.out)[o] = __float2bfloat16_rn(r);
+      reinterpret_cast<bf16*>(a.out)[o] = __float2bfloat16_rn(v[c]);
   }
 }
 
@@ -321,7 +354,8 @@ __device__ __forceinline__ void tile_epilogue(const GemvArgs& a, const Tile& ti,
 // written; the per-tensor scale is applied by the epilogue.
 template <int EPI, bool OUT_F32, bool FP4A, int CG>
 __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, int E, int m_tiles, int bn, int b_period) {
+    tc_gemm_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, int E, int m_tiles, int bn, int b_period,
+                   int tma_out) {
   using G = Ring<CG>;
   constexpr int NTHR = FP4A ? kThreadsFp4 : kThreads;
   constexpr int STAGES = G::STAGES;
@@ -329,7 +363,8 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + G::RING_BYTES);
+  uint8_t* epi_smem = gbase + G::RING_BYTES;                        // 4 x (staging, row weights)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + G::RING_BYTES + EPI_SMEM);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -582,20 +617,31 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
   } else if (warp >= 2 && warp < 6) {
     // ---------------- epilogue: warps 2..5, TMEM lane quarter = warp % 4 ----------------
     const int q = warp & 3;
+    uint8_t* stg = epi_smem + q * (STG_BYTES + WROW_BYTES);
+    float* wrow = reinterpret_cast<float*>(stg + STG_BYTES);
+    const CUtensorMap* out_map = tma_out ? &maps.out : nullptr;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = unit; t < total; t += n_units) {
       Tile ti;
       decode_tile(t, prefix, E, m_tiles, G::TILE_M, bn, a, ti);
+      if (EPI == EPI_SCALE) {
+        // routing weights of the tile's rows, fetched while the MMAs run
+        __syncwarp();
+        for (int r = lane; r < ti.rows; r += 32) {
+          const int row = ti.row0 + r;
+          wrow[r] = a.topw[(int64_t)a.route_token[row] * a.top_k + a.route_slot[row]];
+        }
+        __syncwarp();
+      }
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, a.err)) break;
       tc_fence_after();
-      const int f = ti.m0 + BM * (int)rank + 32 * q + lane;
-      const bool fv = f < a.N;
+      const int f0 = ti.m0 + BM * (int)rank + 32 * q;
       const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN_MAX);
       for (int c0 = 0; c0 < ti.rows; c0 += 32) {
         float v[32];
         tmem_ld32(tb + (uint32_t)c0, v);
-        tile_epilogue<EPI, OUT_F32>(a, ti, c0, f, fv, lane, v);
+        tile_epilogue<EPI, OUT_F32>(a, out_map, ti, c0, f0, lane, wrow, stg, v);
       }
       // TMEM reads are complete (tcgen05.wait::ld); the stores need no ordering
       // with the next MMAs, so the peer's arrive is relaxed
@@ -604,6 +650,7 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
       else mbar_arrive_cluster_relaxed(at_leader(tempty_bar(acc)));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
+    if (lane == 0) bulk_wait_all();        // this warp's output stores are complete
   }
   tc_fence_before();
   __syncthreads();
@@ -664,23 +711,44 @@ struct MapKey {
   int x_cols;
   int64_t x_ld;
   int cg;
+  const void* out;                 // output [x_rows, out_ld], n features per row
+  int64_t out_ld;
+  int n;
+  int out_f32;
   bool operator==(const MapKey& o) const {
     return w == o.w && w_rows == o.w_rows && k == o.k && x == o.x && x_rows == o.x_rows && x_cols == o.x_cols &&
-           x_ld == o.x_ld && cg == o.cg;
+           x_ld == o.x_ld && cg == o.cg && out == o.out && out_ld == o.out_ld && n == o.n && out_f32 == o.out_f32;
   }
 };
 
-bool get_maps(const MapKey& key, TcMaps& out) {
+// output map for the epilogue's TMA stores; false (element stores instead) if
+// the output's base or row pitch is not 16-byte aligned
+bool make_out_map(CUtensorMap* m, const void* ptr, int64_t rows, int n, int64_t ld, bool f32) {
+  EncodeTiledFn fn = encode_fn();
+  const int es = f32 ? 4 : 2;
+  if (!fn || !ptr || (reinterpret_cast<uintptr_t>(ptr) & 15) || (ld * es) % 16 || n % 32) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)n, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t el[2] = {1, 1};
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+            strides, box, el, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool get_maps(const MapKey& key, TcMaps& out, int& tma_out) {
   constexpr int kSlots = 16;
   static std::mutex mu;
   static MapKey keys[kSlots];
   static TcMaps maps[kSlots];
+  static int outs[kSlots];
   static bool used[kSlots] = {};
   static int next = 0;
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < kSlots; ++i)
     if (used[i] && keys[i] == key) {
       out = maps[i];
+      tma_out = outs[i];
       return true;
     }
   TcMaps m;
@@ -688,11 +756,14 @@ bool get_maps(const MapKey& key, TcMaps& out) {
   if (key.w && !make_map(&m.a, key.w, key.w_rows, key.k, key.k, BM)) return false;
   for (int i = 0; i < N_BMAP; ++i)
     if (!make_map(&m.b[i], key.x, key.x_rows, key.x_cols, key.x_ld, (i + 1) * (16 / key.cg))) return false;
+  const int to = make_out_map(&m.out, key.out, key.x_rows, key.n, key.out_ld, key.out_f32 != 0) ? 1 : 0;
   keys[next] = key;
   maps[next] = m;
+  outs[next] = to;
   used[next] = true;
   next = (next + 1) % kSlots;
   out = m;
+  tma_out = to;
   return true;
 }
 
@@ -705,7 +776,8 @@ int num_sms() {
 
 template <int CG>
 size_t smem_bytes(int E) {
-  return 1024 + (size_t)Ring<CG>::RING_BYTES + (4 * Ring<CG>::STAGES + 5) * 8 + 16 + (16 + E + 1) * sizeof(int) + 64;
+  return 1024 + (size_t)Ring<CG>::RING_BYTES + EPI_SMEM + (4 * Ring<CG>::STAGES + 5) * 8 + 16 + (16 + E + 1) * sizeof(int) +
+         64;
 }
 
 // Largest number of CTA pairs (clusters of 2) resident at once; 0 if unknown.
@@ -732,7 +804,7 @@ int max_pairs(K kernel, size_t smem, int threads) {
 
 template <int EPI, bool OUT_F32, bool FP4A, int CG>
 cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, int bn, int b_period, int units,
-                     cudaStream_t s) {
+                     int tma_out, cudaStream_t s) {
   auto kernel = tc_gemm_kernel<EPI, OUT_F32, FP4A, CG>;
   const size_t smem = smem_bytes<CG>(kMaxSegments);
   const int threads = FP4A ? kThreadsFp4 : kThreads;
@@ -748,7 +820,7 @@ cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, 
     }
   }
   units = std::max(1, std::min(units, unit_cap));
-  if (CG == 1) return launch_k(kernel, units, threads, smem, s, maps, a, E, m_tiles, bn, b_period);
+  if (CG == 1) return launch_k(kernel, units, threads, smem, s, maps, a, E, m_tiles, bn, b_period, tma_out);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * units);
   cfg.blockDim = dim3(threads);
@@ -764,28 +836,28 @@ cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, 
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   count_launches(1);
-  return cudaLaunchKernelEx(&cfg, kernel, maps, a, E, m_tiles, bn, b_period);
+  return cudaLaunchKernelEx(&cfg, kernel, maps, a, E, m_tiles, bn, b_period, tma_out);
 }
 
 template <int CG>
 cudaError_t launch_cg(const TcMaps& maps, const GemvArgs& a, int epi, bool out_f32, bool fp4, int E, int m_tiles,
-                      int bn, int b_period, int units, cudaStream_t s) {
+                      int bn, int b_period, int units, int to, cudaStream_t s) {
   if (fp4) {
     switch (epi) {
-      case EPI_RELU2: return launch_t<EPI_RELU2, false, true, CG>(maps, a, E, m_tiles, bn, b_period, units, s);
-      case EPI_SCALE: return launch_t<EPI_SCALE, true, true, CG>(maps, a, E, m_tiles, bn, b_period, units, s);
+      case EPI_RELU2: return launch_t<EPI_RELU2, false, true, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
+      case EPI_SCALE: return launch_t<EPI_SCALE, true, true, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
       default: return cudaErrorNotSupported;
     }
   }
   switch (epi) {
-    case EPI_RELU2: return launch_t<EPI_RELU2, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, s);
-    case EPI_SCALE: return launch_t<EPI_SCALE, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, s);
+    case EPI_RELU2: return launch_t<EPI_RELU2, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
+    case EPI_SCALE: return launch_t<EPI_SCALE, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
     case EPI_STORE:
-      return out_f32 ? launch_t<EPI_STORE, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, s)
-                     : launch_t<EPI_STORE, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, s);
+      return out_f32 ? launch_t<EPI_STORE, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s)
+                     : launch_t<EPI_STORE, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
     default:
-      return out_f32 ? launch_t<EPI_ADD, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, s)
-                     : launch_t<EPI_ADD, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, s);
+      return out_f32 ? launch_t<EPI_ADD, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s)
+                     : launch_t<EPI_ADD, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
   }
 }
 
@@ -805,21 +877,26 @@ int tc_tile_rows(int64_t rows_per_seg, int64_t segs, int N) {
 
 cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_rows, int64_t x_rows, int E, int bn,
                            cudaStream_t s, int x_cols) {
-  if (a.K % BK != 0 || bn < 16 || bn > BN_MAX || (bn & (bn - 1)) || E > kMaxSegments) return cudaErrorNotSupported;
+  if (a.K % BK != 0 || a.N % 32 != 0 || bn < 16 || bn > BN_MAX || (bn & (bn - 1)) || E > kMaxSegments)
+    return cudaErrorNotSupported;
   if (x_cols <= 0) x_cols = a.K;
   if (x_cols % BK != 0 || a.K % x_cols != 0) return cudaErrorNotSupported;
   const bool fp4 = a.W_sf != nullptr;       // NVFP4 weights: converted in the kernel
   const int cg = pick_cg(a.N);
   TcMaps maps;
-  if (!get_maps(MapKey{fp4 ? nullptr : a.W, w_rows, a.K, a.X, x_rows, x_cols, a.x_ld, cg}, maps))
+  int to = 0;
+  const bool of32 = out_f32 || epi == EPI_SCALE;
+  if (!get_maps(MapKey{fp4 ? nullptr : a.W, w_rows, a.K, a.X, x_rows, x_cols, a.x_ld, cg, a.out, a.out_ld, a.N,
+                       of32 ? 1 : 0},
+                maps, to))
     return cudaErrorInvalidValue;
   const int m_tiles = (a.N + BM * cg - 1) / (BM * cg);
   const int b_period = x_cols / BK;
   int units = num_sms() / cg;
   if (!a.offsets) units = (int)std::min<int64_t>(units, ceil_div(a.dense_rows, bn) * m_tiles);
   if (units <= 0) return cudaSuccess;
-  if (cg == 2) return launch_cg<2>(maps, a, epi, out_f32, fp4, E, m_tiles, bn, b_period, units, s);
-  return launch_cg<1>(maps, a, epi, out_f32, fp4, E, m_tiles, bn, b_period, units, s);
+  if (cg == 2) return launch_cg<2>(maps, a, epi, out_f32, fp4, E, m_tiles, bn, b_period, units, to, s);
+  return launch_cg<1>(maps, a, epi, out_f32, fp4, E, m_tiles, bn, b_period, units, to, s);
 }
 
 }  // namespace moe
