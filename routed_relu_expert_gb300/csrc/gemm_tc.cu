@@ -59,16 +59,19 @@ constexpr uint32_t TMEM_COLS = 512;            // two accumulators of BN_MAX col
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr int kMaxSegments = 1024;
 
-// ring geometry per CTA group size (CG = CTAs that share one MMA)
-template <int CG>
+// ring geometry per CTA group size (CG = CTAs that share one MMA); FP4A: a
+// second ring of raw NVFP4 weight bytes feeds the converters
+template <int CG, bool FP4A = false>
 struct Ring {
   static constexpr int TILE_M = BM * CG;                  // features per tile
   static constexpr int B_ROWS = BN_MAX / CG;              // B rows one CTA stages
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB (CG 1), 32 KB (CG 2)
-  static constexpr int STAGES = CG == 2 ? 6 : 4;
+  static constexpr int STAGES = FP4A ? (CG == 2 ? 5 : 3) : (CG == 2 ? 6 : 4);
   static constexpr int BOX0 = 16 / CG;                    // B box height step (rows)
   static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int RAW_STAGES = FP4A ? 8 : 0;         // 128 rows x 32 packed bytes each
+  static constexpr int RAW_BYTES = RAW_STAGES * BM * (BK / 2);
 };
 
 // epilogue staging after the ring: per epilogue warp one 32 x 32 output chunk
@@ -356,7 +359,7 @@ template <int EPI, bool OUT_F32, bool FP4A, int CG>
 __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, int E, int m_tiles, int bn, int b_period,
                    int tma_out) {
-  using G = Ring<CG>;
+  using G = Ring<CG, FP4A>;
   constexpr int NTHR = FP4A ? kThreadsFp4 : kThreads;
   constexpr int STAGES = G::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -364,7 +367,8 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   uint8_t* epi_smem = gbase + G::RING_BYTES;                        // 4 x (staging, row weights)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + G::RING_BYTES + EPI_SMEM);
+  uint8_t* raw_smem = epi_smem + EPI_SMEM;                            // FP4A: packed weight ring
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw_smem + G::RAW_BYTES);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -373,7 +377,10 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
   auto afull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };   // FP4A: this CTA's A converted
   auto pafull_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + 5 + s); };  // FP4A, CG 2: the peer's A converted
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 4 * STAGES + 5);
+  constexpr int RS = G::RAW_STAGES;
+  auto rfull_bar = [&](int s) { return bar0 + 8u * (4 * STAGES + 5 + s); };        // FP4A: raw bytes landed
+  auto rempty_bar = [&](int s) { return bar0 + 8u * (4 * STAGES + 5 + RS + s); };  // FP4A: raw slot read
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 4 * STAGES + 5 + 2 * RS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* scan_tmp = reinterpret_cast<int*>(tmem_holder + 4);          // [16]
   int* prefix = scan_tmp + 16;                                         // [E+1]
@@ -396,11 +403,16 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
       mbar_init(tempty_bar(i), 128 * CG);
     }
     mbar_init(drain_bar, 1);
-    if (FP4A)
+    if (FP4A) {
       for (int s = 0; s < STAGES; ++s) {
         mbar_init(afull_bar(s), kConvThreads);
         mbar_init(pafull_bar(s), 1);
       }
+      for (int s = 0; s < RS; ++s) {
+        mbar_init(rfull_bar(s), 1);
+        mbar_init(rempty_bar(s), kConvThreads);
+      }
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -457,9 +469,38 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
   const int total = total_q * m_tiles;
   const int nkb = a.K / BK;
 
-  if (warp == 0 || warp == kBWarp) {
+  if (FP4A && warp == 0) {
+    if (lane == 0) {
+      // ------- FP4A: packed weight bytes of this CTA's 128 rows, one box per k-block -------
+      int rs = 0;
+      uint32_t rphase = 0;
+      bool ok = true;
+      int pend[RS > 0 ? RS : 1];
+      for (int s = 0; s < RS; ++s) pend[s] = -1;
+      for (int t = unit; t < total && ok; t += n_units) {
+        Tile ti;
+        decode_tile(t, prefix, E, m_tiles, G::TILE_M, bn, a, ti);
+        const int row = ti.seg * a.N + ti.m0 + BM * (int)rank;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(rempty_bar(rs), rphase ^ 1u, abort_flag, a.err)) { ok = false; break; }
+          mbar_expect_tx(rfull_bar(rs), BM * (BK / 2));
+          tma_load_2d(smem_u32(raw_smem) + rs * (BM * (BK / 2)), &maps.a, kb * (BK / 2), row, rfull_bar(rs));
+          pend[rs] = (int)rphase;
+          if (++rs == RS) { rs = 0; rphase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < RS; ++s) {
+          if (pend[s] < 0) continue;
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try(rfull_bar(s), (uint32_t)pend[s]) && globaltimer() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 0 || warp == kBWarp) {
     const bool is_a = warp == 0;
-    if (lane == 0 && !(is_a && FP4A)) {
+    if (lane == 0) {
       // ------- TMA producers: warp 0 the A (weight) tile, warp 6 the B (row) tile;
       // each CTA loads its own operand halves -------
       int pend[STAGES];
@@ -552,66 +593,73 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
     }
   } else if (FP4A && warp >= kThreads / 32) {
     // ------- NVFP4 A converters: warps 7..10; thread = tile row, 64 values per stage -------
+    // packed bytes come from the raw ring (TMA, warp 0); the E4M3 block scales
+    // (4 bytes per row and stage) are loaded here, kSP stages ahead
+    constexpr int kSP = 6;
     const int r = threadIdx.x - kThreads;            // tile row
-    const int64_t rowb = a.K / 2, rows_sf = a.K / 16;
-    const uint8_t* Wq = reinterpret_cast<const uint8_t*>(a.W);
-    // flat sequence of (tile, k block) items; loads run two items ahead
-    struct Item { uint4 q0, q1; uint32_t sc; };
-    int ft = unit, fkb = 0;                          // fetch cursor and its tile
+    const int64_t rows_sf = a.K / 16;
+    int ft = unit, fkb = 0;                          // scale fetch cursor and its tile
     Tile fti;
     if (ft < total) decode_tile(ft, prefix, E, m_tiles, G::TILE_M, bn, a, fti);
-    auto fetch_next = [&](Item& it) {
+    auto fetch_scale = [&]() -> uint32_t {
+      uint32_t v = 0;
+      if (ft >= total) return v;
       const int f = fti.m0 + BM * (int)rank + r;
       if (f < a.N) {
         const int64_t row = (int64_t)fti.seg * a.N + f;
-        const uint8_t* src = Wq + row * rowb + fkb * (BK / 2);
-        it.q0 = ldg_stream(src);
-        it.q1 = ldg_stream(src + 16);
-        it.sc = __ldg(reinterpret_cast<const uint32_t*>(a.W_sf + row * rows_sf + fkb * (BK / 16)));
-      } else {
-        it.q0 = it.q1 = make_uint4(0, 0, 0, 0);
-        it.sc = 0;
+        v = __ldg(reinterpret_cast<const uint32_t*>(a.W_sf + row * rows_sf + fkb * (BK / 16)));
       }
       if (++fkb == nkb) {
         fkb = 0;
         ft += n_units;
         if (ft < total) decode_tile(ft, prefix, E, m_tiles, G::TILE_M, bn, a, fti);
       }
+      return v;
     };
-    Item cur, nxt;
-    cur.q0 = cur.q1 = nxt.q0 = nxt.q1 = make_uint4(0, 0, 0, 0);
-    cur.sc = nxt.sc = 0;
-    if (ft < total) fetch_next(cur);
-    if (ft < total) fetch_next(nxt);
-    int stage = 0;
-    uint32_t phase = 0;
+    uint32_t scq[kSP];
+#pragma unroll
+    for (int i = 0; i < kSP; ++i) scq[i] = fetch_scale();
+    int stage = 0, rs = 0;
+    uint32_t phase = 0, rphase = 0;
     bool ok = true;
     for (int t = unit; t < total && ok; t += n_units) {
       for (int kb = 0; kb < nkb; ++kb) {
-        Item nn = cur;
-        if (ft < total) fetch_next(nn);
+        const uint32_t sc_word = scq[0];
+#pragma unroll
+        for (int i = 0; i < kSP - 1; ++i) scq[i] = scq[i + 1];
+        scq[kSP - 1] = fetch_scale();
+        if (!mbar_wait(rfull_bar(rs), rphase, abort_flag, a.err)) { ok = false; break; }
+        const uint4* src = reinterpret_cast<const uint4*>(raw_smem + rs * (BM * (BK / 2)) + r * (BK / 2));
+        const uint4 q0 = src[0], q1 = src[1];
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.err)) { ok = false; break; }
-        const uint32_t s0 = e4m3x2_to_f16x2(cur.sc & 0xFFFFu), s1 = e4m3x2_to_f16x2(cur.sc >> 16);
+        // block scales as BF16 pairs (exact), one per 16 values
+        const uint32_t s0 = f16x2_to_bf16x2(e4m3x2_to_f16x2(sc_word & 0xFFFFu));
+        const uint32_t s1 = f16x2_to_bf16x2(e4m3x2_to_f16x2(sc_word >> 16));
         const uint32_t sc[4] = {__byte_perm(s0, 0, 0x1010), __byte_perm(s0, 0, 0x3232),
                                 __byte_perm(s1, 0, 0x1010), __byte_perm(s1, 0, 0x3232)};
-        const uint32_t w[8] = {cur.q0.x, cur.q0.y, cur.q0.z, cur.q0.w, cur.q1.x, cur.q1.y, cur.q1.z, cur.q1.w};
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
         uint8_t* dst = gbase + stage * G::STAGE_BYTES + r * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {            // 16-byte chunk c = values 8c .. 8c+7
           uint32_t p[4];
-          e2m1x8_to_f16x2(w[c], p);
-          uint4 o;
-          o.x = f16x2_to_bf16x2(hmul2_f16(p[0], sc[c >> 1]));
-          o.y = f16x2_to_bf16x2(hmul2_f16(p[1], sc[c >> 1]));
-          o.z = f16x2_to_bf16x2(hmul2_f16(p[2], sc[c >> 1]));
-          o.w = f16x2_to_bf16x2(hmul2_f16(p[3], sc[c >> 1]));
+          e2m1x8_to_bf16x2(w[c], p);
+          uint4 o;                               // value x scale: at most 6 significant bits, exact
+          o.x = hmul2_bf16(p[0], sc[c >> 1]);
+          o.y = hmul2_bf16(p[1], sc[c >> 1]);
+          o.z = hmul2_bf16(p[2], sc[c >> 1]);
+          o.w = hmul2_bf16(p[3], sc[c >> 1]);
           *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) = o;
         }
+        // order this thread's shared-memory accesses (the raw bytes read, the
+        // converted row written) before the async-proxy accesses that follow the
+        // arrives: the MMA reading the row and the next TMA copy into the raw
+        // slot (releasing the slot before this fence let that copy overwrite
+        // bytes still being read)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_arrive(afull_bar(stage));
+        mbar_arrive(rempty_bar(rs));
+        if (++rs == RS) { rs = 0; rphase ^= 1u; }
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        cur = nxt;
-        nxt = nn;
       }
     }
   } else if (warp >= 2 && warp < 6) {
@@ -715,11 +763,26 @@ struct MapKey {
   int64_t out_ld;
   int n;
   int out_f32;
+  int fp4;                         // w: packed NVFP4 bytes [w_rows, k / 2]
   bool operator==(const MapKey& o) const {
     return w == o.w && w_rows == o.w_rows && k == o.k && x == o.x && x_rows == o.x_rows && x_cols == o.x_cols &&
-           x_ld == o.x_ld && cg == o.cg && out == o.out && out_ld == o.out_ld && n == o.n && out_f32 == o.out_f32;
+           x_ld == o.x_ld && cg == o.cg && out == o.out && out_ld == o.out_ld && n == o.n && out_f32 == o.out_f32 &&
+           fp4 == o.fp4;
   }
 };
+
+// packed NVFP4 weights [rows, k / 2] bytes: boxes of 128 rows x 32 bytes (64 values)
+bool make_packed_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t k) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)(k / 2), (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(k / 2)};
+  cuuint32_t box[2] = {BK / 2, BM};
+  cuuint32_t el[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, el,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // output map for the epilogue's TMA stores; false (element stores instead) if
 // the output's base or row pitch is not 16-byte aligned
@@ -753,7 +816,8 @@ bool get_maps(const MapKey& key, TcMaps& out, int& tma_out) {
     }
   TcMaps m;
   memset(&m, 0, sizeof(m));
-  if (key.w && !make_map(&m.a, key.w, key.w_rows, key.k, key.k, BM)) return false;
+  if (key.fp4 ? !make_packed_map(&m.a, key.w, key.w_rows, key.k) : !make_map(&m.a, key.w, key.w_rows, key.k, key.k, BM))
+    return false;
   for (int i = 0; i < N_BMAP; ++i)
     if (!make_map(&m.b[i], key.x, key.x_rows, key.x_cols, key.x_ld, (i + 1) * (16 / key.cg))) return false;
   const int to = make_out_map(&m.out, key.out, key.x_rows, key.n, key.out_ld, key.out_f32 != 0) ? 1 : 0;
@@ -774,10 +838,11 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-template <int CG>
+template <int CG, bool FP4A>
 size_t smem_bytes(int E) {
-  return 1024 + (size_t)Ring<CG>::RING_BYTES + EPI_SMEM + (4 * Ring<CG>::STAGES + 5) * 8 + 16 + (16 + E + 1) * sizeof(int) +
-         64;
+  using G = Ring<CG, FP4A>;
+  return 1024 + (size_t)G::RING_BYTES + EPI_SMEM + G::RAW_BYTES + (4 * G::STAGES + 5 + 2 * G::RAW_STAGES) * 8 + 16 +
+         (16 + E + 1) * sizeof(int) + 64;
 }
 
 // Largest number of CTA pairs (clusters of 2) resident at once; 0 if unknown.
@@ -806,7 +871,7 @@ template <int EPI, bool OUT_F32, bool FP4A, int CG>
 cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, int bn, int b_period, int units,
                      int tma_out, cudaStream_t s) {
   auto kernel = tc_gemm_kernel<EPI, OUT_F32, FP4A, CG>;
-  const size_t smem = smem_bytes<CG>(kMaxSegments);
+  const size_t smem = smem_bytes<CG, FP4A>(kMaxSegments);
   const int threads = FP4A ? kThreadsFp4 : kThreads;
   static int unit_cap = -1;           // CTAs (CG 1) or CTA pairs (CG 2) resident at once
   if (unit_cap < 0) {
@@ -886,8 +951,8 @@ cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_r
   TcMaps maps;
   int to = 0;
   const bool of32 = out_f32 || epi == EPI_SCALE;
-  if (!get_maps(MapKey{fp4 ? nullptr : a.W, w_rows, a.K, a.X, x_rows, x_cols, a.x_ld, cg, a.out, a.out_ld, a.N,
-                       of32 ? 1 : 0},
+  if (!get_maps(MapKey{a.W, w_rows, a.K, a.X, x_rows, x_cols, a.x_ld, cg, a.out, a.out_ld, a.N, of32 ? 1 : 0,
+                       fp4 ? 1 : 0},
                 maps, to))
     return cudaErrorInvalidValue;
   const int m_tiles = (a.N + BM * cg - 1) / (BM * cg);
