@@ -22,8 +22,9 @@
 // tensor work: the L2-to-SM copy rate (about 60-68 bytes per cycle per SM),
 // not the tensor pipe, bounds the single-CTA form.  The even CTA's "full" barrier counts both CTAs' TMA
 // bytes; MMA completion is signalled to both CTAs' "empty" and "accumulator
-// full" barriers by a multicast commit; the odd CTA's epilogue and converter
-// threads arrive on the even CTA's barriers remotely.
+// full" barriers by a multicast commit; the odd CTA's epilogue threads arrive
+// on the even CTA's "accumulator empty" barrier remotely.  NVFP4 weights run
+// on single CTAs (see pick_cg).
 //
 // Every wait on an mbarrier gives up after a time limit: the waiter sets
 // MOE_DEVERR_TIMEOUT and an abort flag that stops the other roles, the
@@ -53,7 +54,8 @@ constexpr int N_BMAP = 16;                     // B boxes of 1..16 x (16 / CG) r
                                                // half loads as one box
 constexpr int kThreads = 224;                  // A TMA, MMA, 4 epilogue warps, B TMA
 constexpr int kBWarp = 6;
-constexpr int kConvThreads = 128;              // NVFP4 A converters: one thread per tile row
+constexpr int kConvThreads = 256;              // NVFP4 A converters: two threads per tile row
+constexpr int kConvChunks = 8 * BM / kConvThreads;   // 16-byte output chunks (8 values) per thread
 constexpr int kThreadsFp4 = kThreads + kConvThreads;
 constexpr uint32_t TMEM_COLS = 512;            // two accumulators of BN_MAX columns
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
@@ -160,9 +162,6 @@ __device__ __forceinline__ uint32_t map_to_rank0(uint32_t addr) {
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
@@ -359,6 +358,7 @@ template <int EPI, bool OUT_F32, bool FP4A, int CG>
 __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, int E, int m_tiles, int bn, int b_period,
                    int tma_out) {
+  static_assert(!(FP4A && CG == 2), "NVFP4 weights run on single CTAs");
   using G = Ring<CG, FP4A>;
   constexpr int NTHR = FP4A ? kThreadsFp4 : kThreads;
   constexpr int STAGES = G::STAGES;
@@ -376,7 +376,6 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
   auto tempty_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 + i); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
   auto afull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };   // FP4A: this CTA's A converted
-  auto pafull_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + 5 + s); };  // FP4A, CG 2: the peer's A converted
   constexpr int RS = G::RAW_STAGES;
   auto rfull_bar = [&](int s) { return bar0 + 8u * (4 * STAGES + 5 + s); };        // FP4A: raw bytes landed
   auto rempty_bar = [&](int s) { return bar0 + 8u * (4 * STAGES + 5 + RS + s); };  // FP4A: raw slot read
@@ -404,10 +403,7 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
     }
     mbar_init(drain_bar, 1);
     if (FP4A) {
-      for (int s = 0; s < STAGES; ++s) {
-        mbar_init(afull_bar(s), kConvThreads);
-        mbar_init(pafull_bar(s), 1);
-      }
+      for (int s = 0; s < STAGES; ++s) mbar_init(afull_bar(s), kConvThreads);
       for (int s = 0; s < RS; ++s) {
         mbar_init(rfull_bar(s), 1);
         mbar_init(rempty_bar(s), kConvThreads);
@@ -555,7 +551,6 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
           if (FP4A && !mbar_wait(afull_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
-          if (FP4A && CG == 2 && !mbar_wait<true>(pafull_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = base + stage * G::STAGE_BYTES;
           const uint64_t da = smem_desc_sw128(sa), db = smem_desc_sw128(sa + A_BYTES);
@@ -577,26 +572,15 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
         while (!mbar_try(drain_bar, 0u) && globaltimer() - t0 < kWaitLimitNs) {
         }
       }
-    } else if (FP4A && CG == 2 && lane == 0) {
-      // ---- odd CTA: relay "A converted" to the even CTA, one arrive per stage ----
-      // (the converters' own arrives are CTA-local, so their release does not
-      // wait on the global loads they keep in flight)
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int t = unit; t < total && ok; t += n_units)
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(afull_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
-          mbar_arrive_cluster(at_leader(pafull_bar(stage)));
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
     }
   } else if (FP4A && warp >= kThreads / 32) {
-    // ------- NVFP4 A converters: warps 7..10; thread = tile row, 64 values per stage -------
+    // ------- NVFP4 A converters: warps 7..14; two threads per tile row, 32 values each -------
     // packed bytes come from the raw ring (TMA, warp 0); the E4M3 block scales
     // (4 bytes per row and stage) are loaded here, kSP stages ahead
     constexpr int kSP = 6;
-    const int r = threadIdx.x - kThreads;            // tile row
+    const int ct = threadIdx.x - kThreads;
+    const int r = ct % BM;                           // tile row
+    const int hf = ct / BM;                          // half of the row's 64 values
     const int64_t rows_sf = a.K / 16;
     int ft = unit, fkb = 0;                          // scale fetch cursor and its tile
     Tile fti;
@@ -629,18 +613,16 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
         for (int i = 0; i < kSP - 1; ++i) scq[i] = scq[i + 1];
         scq[kSP - 1] = fetch_scale();
         if (!mbar_wait(rfull_bar(rs), rphase, abort_flag, a.err)) { ok = false; break; }
-        const uint4* src = reinterpret_cast<const uint4*>(raw_smem + rs * (BM * (BK / 2)) + r * (BK / 2));
-        const uint4 q0 = src[0], q1 = src[1];
+        const uint4 q = reinterpret_cast<const uint4*>(raw_smem + rs * (BM * (BK / 2)) + r * (BK / 2))[hf];
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.err)) { ok = false; break; }
-        // block scales as BF16 pairs (exact), one per 16 values
-        const uint32_t s0 = f16x2_to_bf16x2(e4m3x2_to_f16x2(sc_word & 0xFFFFu));
-        const uint32_t s1 = f16x2_to_bf16x2(e4m3x2_to_f16x2(sc_word >> 16));
-        const uint32_t sc[4] = {__byte_perm(s0, 0, 0x1010), __byte_perm(s0, 0, 0x3232),
-                                __byte_perm(s1, 0, 0x1010), __byte_perm(s1, 0, 0x3232)};
-        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        // this half's two block scales as BF16 pairs (exact), one per 16 values
+        const uint32_t s2 = f16x2_to_bf16x2(e4m3x2_to_f16x2((sc_word >> (16 * hf)) & 0xFFFFu));
+        const uint32_t sc[2] = {__byte_perm(s2, 0, 0x1010), __byte_perm(s2, 0, 0x3232)};
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
         uint8_t* dst = gbase + stage * G::STAGE_BYTES + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {            // 16-byte chunk c = values 8c .. 8c+7
+        for (int c = 0; c < kConvChunks; ++c) {  // 16-byte chunk cc = values 8cc .. 8cc+7
+          const int cc = hf * kConvChunks + c;
           uint32_t p[4];
           e2m1x8_to_bf16x2(w[c], p);
           uint4 o;                               // value x scale: at most 6 significant bits, exact
@@ -648,7 +630,7 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
           o.y = hmul2_bf16(p[1], sc[c >> 1]);
           o.z = hmul2_bf16(p[2], sc[c >> 1]);
           o.w = hmul2_bf16(p[3], sc[c >> 1]);
-          *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) = o;
+          *reinterpret_cast<uint4*>(dst + ((cc ^ (r & 7)) << 4)) = o;
         }
         // order this thread's shared-memory accesses (the raw bytes read, the
         // converted row written) before the async-proxy accesses that follow the
@@ -908,11 +890,14 @@ template <int CG>
 cudaError_t launch_cg(const TcMaps& maps, const GemvArgs& a, int epi, bool out_f32, bool fp4, int E, int m_tiles,
                       int bn, int b_period, int units, int to, cudaStream_t s) {
   if (fp4) {
-    switch (epi) {
-      case EPI_RELU2: return launch_t<EPI_RELU2, false, true, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
-      case EPI_SCALE: return launch_t<EPI_SCALE, true, true, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
-      default: return cudaErrorNotSupported;
+    if constexpr (CG == 1) {
+      switch (epi) {
+        case EPI_RELU2: return launch_t<EPI_RELU2, false, true, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
+        case EPI_SCALE: return launch_t<EPI_SCALE, true, true, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
+        default: return cudaErrorNotSupported;
+      }
     }
+    return cudaErrorNotSupported;
   }
   switch (epi) {
     case EPI_RELU2: return launch_t<EPI_RELU2, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
@@ -926,13 +911,16 @@ cudaError_t launch_cg(const TcMaps& maps, const GemvArgs& a, int epi, bool out_f
   }
 }
 
-// CTA pairs for products with more than one 128-feature tile per segment
-inline int pick_cg(int N) { return N > BM ? 2 : 1; }
+// CTA pairs for BF16 products with more than one 128-feature tile per
+// segment.  NVFP4 weights stay on single CTAs: a pair's MMA would wait for the
+// peer CTA's converted rows, and that cross-CTA hand-off cost more than the
+// halved B traffic saves.
+inline int pick_cg(int N, bool fp4) { return !fp4 && N > BM ? 2 : 1; }
 
 }  // namespace
 
 int tc_tile_rows(int64_t rows_per_seg, int64_t segs, int N) {
-  const int cg = pick_cg(N);
+  const int cg = pick_cg(N, false);
   const int64_t m_tiles = ceil_div(N, (int64_t)BM * cg);
   const int64_t units = num_sms() / cg;
   int bn = BN_MAX;
@@ -947,7 +935,7 @@ cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_r
   if (x_cols <= 0) x_cols = a.K;
   if (x_cols % BK != 0 || a.K % x_cols != 0) return cudaErrorNotSupported;
   const bool fp4 = a.W_sf != nullptr;       // NVFP4 weights: converted in the kernel
-  const int cg = pick_cg(a.N);
+  const int cg = pick_cg(a.N, fp4);
   TcMaps maps;
   int to = 0;
   const bool of32 = out_f32 || epi == EPI_SCALE;
