@@ -34,4 +34,34 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, int seg, int row, in
   }
 }
 
+// The same with the segment's per-tensor scale (1 if none) and, for
+// EPI_SCALE, the row's routing weight, both fetched earlier by the caller so
+// that their load latency overlaps the weight stream.
+template <int EPI, bool OUT_F32, bool ACT_F32>
+__device__ __forceinline__ void epilogue_pre(const GemvArgs& a, int row, int f, float v, float gs, float wr) {
+  v *= gs;
+  const int64_t o = (int64_t)row * a.out_ld + f;
+  float r;
+  if (EPI == EPI_RELU2) {
+    const float u = ACT_F32 ? fmaxf(v, 0.f) : fmaxf(round_bf16(v), 0.f);
+    r = u * u;
+  } else if (EPI == EPI_SCALE) {
+    r = wr * v;
+  } else if (EPI == EPI_ADD) {
+    r = v + (a.add_src ? a.add_src[(int64_t)row * a.add_ld + f] : 0.f);
+  } else {
+    r = v;
+  }
+  if (OUT_F32 || ACT_F32) {
+    reinterpret_cast<float*>(a.out)[o] = r;
+  } else {
+    reinterpret_cast<bf16*>(a.out)[o] = __float2bfloat16_rn(r);
+  }
+}
+
+// routing weight of packed row `row` (EPI_SCALE)
+__device__ __forceinline__ float route_weight(const GemvArgs& a, int row) {
+  return a.topw[(int64_t)a.route_token[row] * a.top_k + a.route_slot[row]];
+}
+
 }  // namespace moe

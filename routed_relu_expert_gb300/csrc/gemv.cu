@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a
   constexpr int NT = 2;                 // 8-row column blocks per pass
   constexpr int U = 4;                  // 32-wide K chunks in flight per warp
   __shared__ float red[kWarps][NT][128];
+  __shared__ float wrs[2][NT * 8];      // routing weights of a pass's rows (EPI_SCALE)
 
   Seg sg;
   // dense products split their 16-row passes over grid.z (CTAs of one feature
@@ -78,8 +79,11 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a
   const bf16* wg8 = W + (int64_t)(g + 8) * K + 8 * t4;
   const int nchunks = K >> 5;
 
-  for (int p0 = 0; p0 < sg.nrows; p0 += NT * 8) {
+  for (int p0 = 0, pi = 0; p0 < sg.nrows; p0 += NT * 8, ++pi) {
     const int prow = min(sg.nrows - p0, NT * 8);
+    // the pass's routing weights, read after the K loop (double-buffered by
+    // pass parity: the pass before the previous one has finished with them)
+    if (EPI == EPI_SCALE && threadIdx.x < prow) wrs[pi & 1][threadIdx.x] = route_weight(a, sg.row0 + p0 + threadIdx.x);
     const bf16* xr[NT];
     bool xv[NT];
 #pragma unroll
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a
         float v = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) v += red[w][j][idx];
-        epilogue<EPI, OUT_F32, false>(a, sg.id, sg.row0 + p0 + r, f0 + f, v);
+        epilogue_pre<EPI, OUT_F32, false>(a, sg.row0 + p0 + r, f0 + f, v, 1.f, EPI == EPI_SCALE ? wrs[pi & 1][r] : 0.f);
       }
     }
   }
@@ -279,6 +283,165 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_nvfp4_kernel(const GemvArgs 
 }
 
 // ---------------------------------------------------------------------------
+// NVFP4 weights, bulk-copied.  A CTA owns 16 features of one segment.  Their
+// packed rows (16 x K/2 contiguous bytes) and block scales (16 x K/16) are
+// brought into shared memory by two cp.async.bulk copies on one mbarrier, so
+// the CTA's whole weight tile is in flight at once whatever the register
+// budget; the 4 warps then split K into 128-wide chunks exactly as above
+// (same decode, same MMA k permutation) and add their partial sums in a fixed
+// warp order.  Row passes of 16 re-read the tile from shared memory.
+// ---------------------------------------------------------------------------
+constexpr int kBulkWarps = 4;
+constexpr int kBulkThreads = kBulkWarps * 32;
+constexpr uint64_t kBulkWaitNs = 4000000000ull;
+constexpr size_t kBulkSmemMax = 160 * 1024;
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+size_t nvfp4_bulk_smem(int K) {
+  return (size_t)16 * (K / 2) + (size_t)16 * (K / 16) + (size_t)kBulkWarps * 2 * 128 * sizeof(float) + 16;
+}
+
+template <int EPI, bool OUT_F32>
+__global__ void __launch_bounds__(kBulkThreads, 8) gemv_nvfp4_bulk_kernel(const GemvArgs a) {
+  extern __shared__ __align__(16) uint8_t bsm[];
+  pdl_wait();
+  pdl_trigger();
+  constexpr int NT = 2;
+  Seg sg;
+  if (!resolve_segment(a, 1 << 30, sg)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int K = a.K;
+  const int rowb = K / 2, rows_sf = K / 16;
+  const int nchunks = K >> 7;
+  const int f0 = blockIdx.x * 16;
+  uint8_t* ws = bsm;                                             // [16][K/2] packed values
+  uint8_t* ss = bsm + 16 * rowb;                                 // [16][K/16] E4M3 scales
+  float* red = reinterpret_cast<float*>(ss + 16 * rows_sf);      // [warps][NT][128]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(red + kBulkWarps * NT * 128);
+  const uint32_t b = smem_u32(bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const uint32_t wbytes = 16u * rowb, sbytes = 16u * rows_sf;
+    mbar_expect_tx(b, wbytes + sbytes);
+    bulk_g2s(smem_u32(ws), reinterpret_cast<const uint8_t*>(a.W) + sg.id * a.w_seg_stride + (int64_t)f0 * rowb, wbytes,
+             b);
+    bulk_g2s(smem_u32(ss), a.W_sf + sg.id * a.sf_seg_stride + (int64_t)f0 * rows_sf, sbytes, b);
+  }
+  // the segment's per-tensor scale and the rows' routing weights load while
+  // the weight tile is in flight
+  const float gs = a.W_gs ? a.W_gs[sg.id] : 1.f;
+  __shared__ float wrs[2][16];
+  if (EPI == EPI_SCALE && threadIdx.x < min(sg.nrows, 16)) wrs[0][threadIdx.x] = route_weight(a, sg.row0 + threadIdx.x);
+  __syncthreads();
+  bool ok = mbar_try(b, 0);
+  if (!ok) {
+    const uint64_t t0 = globaltimer();
+    while (!(ok = mbar_try(b, 0)) && globaltimer() - t0 < kBulkWaitNs) {
+    }
+  }
+  if (!ok) {
+    // the copies never completed: report, and keep the CTA alive (bounded)
+    // while they may still land in its shared memory
+    if (threadIdx.x == 0) {
+      set_error(a.err, MOE_DEVERR_TIMEOUT);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try(b, 0) && globaltimer() - t0 < kBulkWaitNs) {
+      }
+    }
+    return;
+  }
+
+  for (int p0 = 0, pi = 0; p0 < sg.nrows; p0 += NT * 8, ++pi) {
+    const int prow = min(sg.nrows - p0, NT * 8);
+    if (EPI == EPI_SCALE && pi > 0 && threadIdx.x < prow) wrs[pi & 1][threadIdx.x] = route_weight(a, sg.row0 + p0 + threadIdx.x);
+    const bf16* xr[NT];
+    bool xv[NT];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int r = j * 8 + g;
+      xv[j] = r < prow;
+      int64_t row = 0;
+      if (xv[j]) row = a.gather ? a.gather[sg.row0 + p0 + r] : (sg.row0 + p0 + r);
+      xr[j] = reinterpret_cast<const bf16*>(a.X) + row * a.x_ld + 32 * t4;
+    }
+    float acc[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+    for (int cc = warp; cc < nchunks; cc += kBulkWarps) {
+      const uint4 A0 = *reinterpret_cast<const uint4*>(ws + g * rowb + cc * 64 + 16 * t4);
+      const uint4 A1 = *reinterpret_cast<const uint4*>(ws + (g + 8) * rowb + cc * 64 + 16 * t4);
+      const uint32_t S0 = *reinterpret_cast<const uint16_t*>(ss + g * rows_sf + cc * 8 + 2 * t4);
+      const uint32_t S1 = *reinterpret_cast<const uint16_t*>(ss + (g + 8) * rows_sf + cc * 8 + 2 * t4);
+      const uint32_t s0 = e4m3x2_to_f16x2(S0), s1 = e4m3x2_to_f16x2(S1);
+      const uint32_t sc0[2] = {__byte_perm(s0, 0, 0x1010), __byte_perm(s0, 0, 0x3232)};
+      const uint32_t sc1[2] = {__byte_perm(s1, 0, 0x1010), __byte_perm(s1, 0, 0x3232)};
+      uint32_t fa[8][4];
+      const uint32_t w0[4] = {A0.x, A0.y, A0.z, A0.w};
+      const uint32_t w1[4] = {A1.x, A1.y, A1.z, A1.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t p0v[4], p1v[4];
+        e2m1x8_to_f16x2(w0[q], p0v);
+        e2m1x8_to_f16x2(w1[q], p1v);
+        const int h = q >> 1;
+        fa[2 * q][0] = hmul2_f16(p0v[0], sc0[h]);
+        fa[2 * q][2] = hmul2_f16(p0v[1], sc0[h]);
+        fa[2 * q][1] = hmul2_f16(p1v[0], sc1[h]);
+        fa[2 * q][3] = hmul2_f16(p1v[1], sc1[h]);
+        fa[2 * q + 1][0] = hmul2_f16(p0v[2], sc0[h]);
+        fa[2 * q + 1][2] = hmul2_f16(p0v[3], sc0[h]);
+        fa[2 * q + 1][1] = hmul2_f16(p1v[2], sc1[h]);
+        fa[2 * q + 1][3] = hmul2_f16(p1v[3], sc1[h]);
+      }
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        if (j * 8 >= prow) continue;
+        uint4 B[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) B[q] = xv[j] ? ldg_keep(xr[j] + cc * 128 + 8 * q) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4& Bq = B[i >> 1];
+          const uint32_t bb0 = bf16x2_to_f16x2((i & 1) ? Bq.z : Bq.x);
+          const uint32_t bb1 = bf16x2_to_f16x2((i & 1) ? Bq.w : Bq.y);
+          mma_f16_16816(acc[j], fa[i][0], fa[i][1], fa[i][2], fa[i][3], bb0, bb1);
+        }
+      }
+    }
+
+    // acc[j][0]: (feature g, row 2t), [1]: (g, 2t+1), [2]: (g+8, 2t), [3]: (g+8, 2t+1)
+    if (p0 > 0) __syncthreads();      // previous pass has finished reading red
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      float* rw = red + (warp * NT + j) * 128;
+      rw[g * 8 + 2 * t4] = acc[j][0];
+      rw[g * 8 + 2 * t4 + 1] = acc[j][1];
+      rw[(g + 8) * 8 + 2 * t4] = acc[j][2];
+      rw[(g + 8) * 8 + 2 * t4 + 1] = acc[j][3];
+    }
+    __syncthreads();
+    for (int o = threadIdx.x; o < NT * 128; o += kBulkThreads) {
+      const int j = o >> 7, idx = o & 127;
+      const int f = idx >> 3, r = j * 8 + (idx & 7);
+      if (r < prow) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kBulkWarps; ++w) v += red[(w * NT + j) * 128 + idx];
+        epilogue_pre<EPI, OUT_F32, false>(a, sg.row0 + p0 + r, f0 + f, v, gs, EPI == EPI_SCALE ? wrs[pi & 1][r] : 0.f);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // FP32 weights and activations (small FP32 layers): plain FMA dot products.
 // A CTA owns 64 features of one segment and up to 64 rows.
 // ---------------------------------------------------------------------------
@@ -327,6 +490,29 @@ cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_
       case EPI_SCALE: launch_k(gemv_f32_kernel<EPI_SCALE>, grid, kThreads, 0, s, a); break;
       case EPI_STORE: launch_k(gemv_f32_kernel<EPI_STORE>, grid, kThreads, 0, s, a); break;
       default: launch_k(gemv_f32_kernel<EPI_ADD>, grid, kThreads, 0, s, a); break;
+    }
+    return cudaGetLastError();
+  }
+  const bool bulk_ok = a.offsets && nvfp4_bulk_smem(a.K) <= kBulkSmemMax &&
+                       !(reinterpret_cast<uintptr_t>(a.W) & 15) && !(reinterpret_cast<uintptr_t>(a.W_sf) & 15);
+  if (wfmt == WF_NVFP4 && act == MOE_DT_BF16 && bulk_ok) {
+    // one CTA per 16 features of each active segment, weight tile bulk-copied
+    const size_t smem = nvfp4_bulk_smem(a.K);
+    static bool attr_set = false;
+    if (!attr_set) {
+      cudaError_t e1 = cudaFuncSetAttribute(gemv_nvfp4_bulk_kernel<EPI_RELU2, false>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmemMax);
+      cudaError_t e2 = cudaFuncSetAttribute(gemv_nvfp4_bulk_kernel<EPI_SCALE, true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmemMax);
+      if (e1 != cudaSuccess) return e1;
+      if (e2 != cudaSuccess) return e2;
+      attr_set = true;
+    }
+    dim3 grid((unsigned)(a.N / 16), segs, 1);
+    switch (epi) {
+      case EPI_RELU2: launch_k(gemv_nvfp4_bulk_kernel<EPI_RELU2, false>, grid, kBulkThreads, smem, s, a); break;
+      case EPI_SCALE: launch_k(gemv_nvfp4_bulk_kernel<EPI_SCALE, true>, grid, kBulkThreads, smem, s, a); break;
+      default: return cudaErrorNotSupported;
     }
     return cudaGetLastError();
   }
