@@ -230,10 +230,10 @@ int64_t moe_launch_count(void);
  * work enqueued where cudaMalloc is not permitted.  Same arguments and
  * results as moe_router without logits/scores outputs (the same kernels,
  * bit-identical results); its scratch (logits, scores, the BF16 split of the
- * router matrix used above 64 BF16 tokens, and the error word) lives in a
- * static device array of MOE_NOALLOC_MAX_ROUTER_ELEMS * 8 +
- * MOE_NOALLOC_MAX_SPLIT_ELEMS * 2 + 256 bytes (about 15 MiB) that every GPU
- * loading this library keeps until exit.
+ * router matrix and the four K-split logit slabs used above 64 BF16 tokens,
+ * and the error word) lives in a static device array of
+ * MOE_NOALLOC_MAX_ROUTER_ELEMS * 24 + MOE_NOALLOC_MAX_SPLIT_ELEMS * 2 + 256
+ * bytes (about 17 MiB) that every GPU loading this library keeps until exit.
  *   - Returns MOE_ERR_WORKSPACE, before enqueuing anything, when
  *     T * n_experts > MOE_NOALLOC_MAX_ROUTER_ELEMS, or when T > 64 BF16
  *     tokens need the split router matrix and 3 * n_experts * d_model >

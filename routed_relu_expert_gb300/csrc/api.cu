@@ -29,7 +29,7 @@ inline int act_bytes(const moe_config_t* c) { return c->act_dtype == MOE_DT_F32 
 inline int de_of(const moe_config_t* c) { return c->d_latent > 0 ? c->d_latent : c->d_model; }
 
 struct Layout {
-  size_t hdr, logits, scores, ids, topw, counts, offsets, active, tile_prefix, w_split;
+  size_t hdr, logits, logit_parts, scores, ids, topw, counts, offsets, active, tile_prefix, w_split;
   size_t route_token, route_slot, tsr, x_l, x_packed, h, u, y_r, y_rl, hs, ys, tile_counts, total;
 };
 
@@ -47,6 +47,7 @@ Layout make_layout(const moe_config_t* c, int32_t T) {
   size_t off = 0;
   L.hdr = take(off, sizeof(WsHeader));
   L.logits = take(off, t * E * 4);
+  L.logit_parts = take(off, T > 64 ? (size_t)kRouterParts * t * E * 4 : 0);   // K-split router logits
   L.scores = take(off, t * E * 4);
   L.ids = take(off, R * 4);
   L.topw = take(off, R * 4);
@@ -140,10 +141,14 @@ struct Ptrs {
 // ---- steps -----------------------------------------------------------------
 moe_status_t run_router(const moe_config_t* c, int T, const void* x, const float* w_router, const float* bias,
                         float* logits, float* scores, int32_t* ids, float* w, const Ptrs& P, cudaStream_t s) {
+  float* parts = T > 64 ? P.at<float>(P.L.logit_parts) : nullptr;
+  int nparts = 1;
   CU(launch_router_logits(x, c->act_dtype, T, c->d_model, w_router, c->n_experts, logits, s,
-                          P.at<void>(P.L.w_split)));
-  CU(launch_router_select(logits, T, c->n_experts, bias, c->n_group, c->topk_group, c->top_k,
-                          c->norm_topk_prob, c->routed_scaling_factor, scores, ids, w, &P.hdr()->err, s));
+                          P.at<void>(P.L.w_split), parts, &nparts));
+  const bool split = nparts > 1;
+  CU(launch_router_select(split ? parts : logits, nparts, (int64_t)T * c->n_experts, split ? logits : nullptr, T,
+                          c->n_experts, bias, c->n_group, c->topk_group, c->top_k, c->norm_topk_prob,
+                          c->routed_scaling_factor, scores, ids, w, &P.hdr()->err, s));
   return MOE_OK;
 }
 

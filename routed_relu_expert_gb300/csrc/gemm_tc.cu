@@ -239,10 +239,16 @@ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
 // ---------------------------------------------------------------------------
 struct Tile {
   int seg, m0, row0, rows;
+  int kb0, kb1;        // k-blocks [kb0, kb1) of this unit (all of K unless split)
+  int orow0;           // first output row (row0 shifted by the unit's K-part slab)
 };
 
+// unit t -> (K part, row tile, feature tile); parts outermost, so units that
+// run together share their K range
 __device__ __forceinline__ void decode_tile(int t, const int* prefix, int E, int m_tiles, int tile_m, int bn,
-                                            const GemvArgs& a, Tile& ti) {
+                                            const GemvArgs& a, int per_part, int ksplit, int nkb, Tile& ti) {
+  const int ks = t / per_part;
+  t -= ks * per_part;
   const int q = t / m_tiles, m = t - q * m_tiles;
   int seg = 0, nt = q, base = 0, count = a.dense_rows;
   if (a.offsets) {
@@ -260,6 +266,9 @@ __device__ __forceinline__ void decode_tile(int t, const int* prefix, int E, int
   ti.m0 = m * tile_m;
   ti.row0 = base + nt * bn;
   ti.rows = min(bn, count - nt * bn);
+  ti.kb0 = (int)((int64_t)ks * nkb / ksplit);
+  ti.kb1 = (int)((int64_t)(ks + 1) * nkb / ksplit);
+  ti.orow0 = ti.row0 + ks * a.dense_rows;   // K parts: dense products only
 }
 
 // Epilogue of 32 accumulator columns (rows row0+c0 .. +31) of one feature f;
@@ -312,13 +321,13 @@ __device__ __forceinline__ void tile_epilogue(const GemvArgs& a, const CUtensorM
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
-    if (lane == 0) tma_store_2d(out_map, smem_u32(stg), f0, ti.row0 + c0);
+    if (lane == 0) tma_store_2d(out_map, smem_u32(stg), f0, ti.orow0 + c0);
     return;
   }
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
     if (c >= nc) break;
-    const int64_t o = (int64_t)(ti.row0 + c0 + c) * a.out_ld + f;
+    const int64_t o = (int64_t)(ti.orow0 + c0 + c) * a.out_ld + f;
     if (F32)
       reinterpret_cast<float*>(a.out)[o] = v[c];
     else
@@ -333,7 +342,7 @@ __device__ __forceinline__ void tile_epilogue(const GemvArgs& a, const CUtensorM
 template <int EPI, bool OUT_F32, bool FP4A, int CG>
 __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, int E, int m_tiles, int bn, int b_period,
-                   int tma_out) {
+                   int tma_out, int ksplit) {
   static_assert(!(FP4A && CG == 2), "NVFP4 weights run on single CTAs");
   using G = Ring<CG, FP4A>;
   constexpr int NTHR = FP4A ? kThreadsFp4 : kThreads;
@@ -438,7 +447,8 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
   tc_fence_after();
   if (a.offsets) total_q = prefix[E];
   const uint32_t tmem_base = *tmem_holder;
-  const int total = total_q * m_tiles;
+  const int per_part = total_q * m_tiles;
+  const int total = per_part * ksplit;
   const int nkb = a.K / BK;
 
   if (FP4A && warp == 0) {
@@ -451,9 +461,9 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
       for (int s = 0; s < RS; ++s) pend[s] = -1;
       for (int t = unit; t < total && ok; t += n_units) {
         Tile ti;
-        decode_tile(t, prefix, E, m_tiles, G::TILE_M, bn, a, ti);
+        decode_tile(t, prefix, E, m_tiles, G::TILE_M, bn, a, per_part, ksplit, nkb, ti);
         const int row = ti.seg * a.N + ti.m0 + BM * (int)rank;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
           if (!mbar_wait(rempty_bar(rs), rphase ^ 1u, abort_flag, a.err)) { ok = false; break; }
           mbar_expect_tx(rfull_bar(rs), BM * (BK / 2));
           tma_load_2d(smem_u32(raw_smem) + rs * (BM * (BK / 2)), &maps.a, kb * (BK / 2), row, rfull_bar(rs));
@@ -482,14 +492,14 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
       bool ok = true;
       for (int t = unit; t < total && ok; t += n_units) {
         Tile ti;
-        decode_tile(t, prefix, E, m_tiles, G::TILE_M, bn, a, ti);
+        decode_tile(t, prefix, E, m_tiles, G::TILE_M, bn, a, per_part, ksplit, nkb, ti);
         const int r16 = (ti.rows + 15) & ~15;
         const int hb = r16 / CG;                             // B rows this CTA loads
         const CUtensorMap* map = is_a ? &maps.a : &maps.b[hb / G::BOX0 - 1];
         const uint32_t tx = is_a ? (uint32_t)CG * A_BYTES : (uint32_t)r16 * BK * 2;
         const int row = is_a ? ti.seg * a.N + ti.m0 + BM * (int)rank : ti.row0 + hb * (int)rank;
         const uint32_t dst0 = base + (is_a ? 0u : (uint32_t)A_BYTES);
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.err)) { ok = false; break; }
           if (rank == 0) mbar_expect_tx(full_bar(stage), tx);
           const int col = is_a ? kb * BK : (kb % b_period) * BK;
@@ -519,12 +529,12 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
       bool ok = true, issued = false;
       for (int t = unit; t < total && ok; t += n_units) {
         Tile ti;
-        decode_tile(t, prefix, E, m_tiles, G::TILE_M, bn, a, ti);
+        decode_tile(t, prefix, E, m_tiles, G::TILE_M, bn, a, per_part, ksplit, nkb, ti);
         const uint32_t idesc = idesc_bf16(G::TILE_M, (ti.rows + 15) & ~15);
         if (!mbar_wait<CG == 2>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, a.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN_MAX);
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
           if (FP4A && !mbar_wait(afull_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
           tc_fence_after();
@@ -532,7 +542,7 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
           const uint64_t da = smem_desc_sw128(sa), db = smem_desc_sw128(sa + A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc_mma<CG>(d, da + 2u * k, db + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            tc_mma<CG>(d, da + 2u * k, db + 2u * k, idesc, (kb != ti.kb0 || k != 0) ? 1u : 0u);
           issued = true;
           tc_commit<CG>(empty_bar(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -560,7 +570,7 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
     const int64_t rows_sf = a.K / 16;
     int ft = unit, fkb = 0;                          // scale fetch cursor and its tile
     Tile fti;
-    if (ft < total) decode_tile(ft, prefix, E, m_tiles, G::TILE_M, bn, a, fti);
+    if (ft < total) decode_tile(ft, prefix, E, m_tiles, G::TILE_M, bn, a, per_part, ksplit, nkb, fti);
     auto fetch_scale = [&]() -> uint32_t {
       uint32_t v = 0;
       if (ft >= total) return v;
@@ -572,7 +582,7 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
       if (++fkb == nkb) {
         fkb = 0;
         ft += n_units;
-        if (ft < total) decode_tile(ft, prefix, E, m_tiles, G::TILE_M, bn, a, fti);
+        if (ft < total) decode_tile(ft, prefix, E, m_tiles, G::TILE_M, bn, a, per_part, ksplit, nkb, fti);
       }
       return v;
     };
@@ -582,7 +592,7 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
     int stage = 0, rs = 0;
     uint32_t phase = 0, rphase = 0;
     bool ok = true;
-    for (int t = unit; t < total && ok; t += n_units) {
+    for (int t = unit; t < total && ok; t += n_units) {        // (NVFP4 products are never split in K)
       for (int kb = 0; kb < nkb; ++kb) {
         const uint32_t sc_word = scq[0];
 #pragma unroll
@@ -630,7 +640,7 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
     uint32_t acc_phase = 0;
     for (int t = unit; t < total; t += n_units) {
       Tile ti;
-      decode_tile(t, prefix, E, m_tiles, G::TILE_M, bn, a, ti);
+      decode_tile(t, prefix, E, m_tiles, G::TILE_M, bn, a, per_part, ksplit, nkb, ti);
       if (EPI == EPI_SCALE) {
         // routing weights of the tile's rows, fetched while the MMAs run
         __syncwarp();
@@ -722,10 +732,11 @@ struct MapKey {
   int n;
   int out_f32;
   int fp4;                         // w: packed NVFP4 bytes [w_rows, k / 2]
+  int64_t out_rows;                // rows of the output (K parts stack their slabs)
   bool operator==(const MapKey& o) const {
     return w == o.w && w_rows == o.w_rows && k == o.k && x == o.x && x_rows == o.x_rows && x_cols == o.x_cols &&
            x_ld == o.x_ld && cg == o.cg && out == o.out && out_ld == o.out_ld && n == o.n && out_f32 == o.out_f32 &&
-           fp4 == o.fp4;
+           fp4 == o.fp4 && out_rows == o.out_rows;
   }
 };
 
@@ -778,7 +789,7 @@ bool get_maps(const MapKey& key, TcMaps& out, int& tma_out) {
     return false;
   for (int i = 0; i < N_BMAP; ++i)
     if (!make_map(&m.b[i], key.x, key.x_rows, key.x_cols, key.x_ld, (i + 1) * (16 / key.cg))) return false;
-  const int to = make_out_map(&m.out, key.out, key.x_rows, key.n, key.out_ld, key.out_f32 != 0) ? 1 : 0;
+  const int to = make_out_map(&m.out, key.out, key.out_rows, key.n, key.out_ld, key.out_f32 != 0) ? 1 : 0;
   keys[next] = key;
   maps[next] = m;
   outs[next] = to;
@@ -827,7 +838,7 @@ int max_pairs(K kernel, size_t smem, int threads) {
 
 template <int EPI, bool OUT_F32, bool FP4A, int CG>
 cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, int bn, int b_period, int units,
-                     int tma_out, cudaStream_t s) {
+                     int tma_out, int ksplit, cudaStream_t s) {
   auto kernel = tc_gemm_kernel<EPI, OUT_F32, FP4A, CG>;
   const size_t smem = smem_bytes<CG, FP4A>(kMaxSegments);
   const int threads = FP4A ? kThreadsFp4 : kThreads;
@@ -843,7 +854,7 @@ cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, 
     }
   }
   units = std::max(1, std::min(units, unit_cap));
-  if (CG == 1) return launch_k(kernel, units, threads, smem, s, maps, a, E, m_tiles, bn, b_period, tma_out);
+  if (CG == 1) return launch_k(kernel, units, threads, smem, s, maps, a, E, m_tiles, bn, b_period, tma_out, ksplit);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * units);
   cfg.blockDim = dim3(threads);
@@ -859,31 +870,31 @@ cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, 
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   count_launches(1);
-  return cudaLaunchKernelEx(&cfg, kernel, maps, a, E, m_tiles, bn, b_period, tma_out);
+  return cudaLaunchKernelEx(&cfg, kernel, maps, a, E, m_tiles, bn, b_period, tma_out, ksplit);
 }
 
 template <int CG>
 cudaError_t launch_cg(const TcMaps& maps, const GemvArgs& a, int epi, bool out_f32, bool fp4, int E, int m_tiles,
-                      int bn, int b_period, int units, int to, cudaStream_t s) {
+                      int bn, int b_period, int units, int to, int ks, cudaStream_t s) {
   if (fp4) {
     if constexpr (CG == 1) {
       switch (epi) {
-        case EPI_RELU2: return launch_t<EPI_RELU2, false, true, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
-        case EPI_SCALE: return launch_t<EPI_SCALE, true, true, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
+        case EPI_RELU2: return launch_t<EPI_RELU2, false, true, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
+        case EPI_SCALE: return launch_t<EPI_SCALE, true, true, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
         default: return cudaErrorNotSupported;
       }
     }
     return cudaErrorNotSupported;
   }
   switch (epi) {
-    case EPI_RELU2: return launch_t<EPI_RELU2, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
-    case EPI_SCALE: return launch_t<EPI_SCALE, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
+    case EPI_RELU2: return launch_t<EPI_RELU2, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
+    case EPI_SCALE: return launch_t<EPI_SCALE, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
     case EPI_STORE:
-      return out_f32 ? launch_t<EPI_STORE, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s)
-                     : launch_t<EPI_STORE, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
+      return out_f32 ? launch_t<EPI_STORE, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s)
+                     : launch_t<EPI_STORE, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
     default:
-      return out_f32 ? launch_t<EPI_ADD, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s)
-                     : launch_t<EPI_ADD, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, s);
+      return out_f32 ? launch_t<EPI_ADD, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s)
+                     : launch_t<EPI_ADD, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
   }
 }
 
@@ -905,8 +916,11 @@ int tc_tile_rows(int64_t rows_per_seg, int64_t segs, int N) {
 }
 
 cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_rows, int64_t x_rows, int E, int bn,
-                           cudaStream_t s, int x_cols) {
+                           cudaStream_t s, int x_cols, int ksplit) {
   if (a.K % BK != 0 || a.N % 32 != 0 || bn < 16 || bn > BN_MAX || (bn & (bn - 1)) || E > kMaxSegments)
+    return cudaErrorNotSupported;
+  // K parts: dense FP32 stores only, at least one k-block each
+  if (ksplit < 1 || ksplit > a.K / BK || (ksplit > 1 && (a.offsets || epi != EPI_STORE || !out_f32 || a.W_sf)))
     return cudaErrorNotSupported;
   if (x_cols <= 0) x_cols = a.K;
   if (x_cols % BK != 0 || a.K % x_cols != 0) return cudaErrorNotSupported;
@@ -916,16 +930,16 @@ cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_r
   int to = 0;
   const bool of32 = out_f32 || epi == EPI_SCALE;
   if (!get_maps(MapKey{a.W, w_rows, a.K, a.X, x_rows, x_cols, a.x_ld, cg, a.out, a.out_ld, a.N, of32 ? 1 : 0,
-                       fp4 ? 1 : 0},
+                       fp4 ? 1 : 0, x_rows * ksplit},
                 maps, to))
     return cudaErrorInvalidValue;
   const int m_tiles = (a.N + BM * cg - 1) / (BM * cg);
   const int b_period = x_cols / BK;
   int units = num_sms() / cg;
-  if (!a.offsets) units = (int)std::min<int64_t>(units, ceil_div(a.dense_rows, bn) * m_tiles);
+  if (!a.offsets) units = (int)std::min<int64_t>(units, ceil_div(a.dense_rows, bn) * m_tiles * ksplit);
   if (units <= 0) return cudaSuccess;
-  if (cg == 2) return launch_cg<2>(maps, a, epi, out_f32, fp4, E, m_tiles, bn, b_period, units, to, s);
-  return launch_cg<1>(maps, a, epi, out_f32, fp4, E, m_tiles, bn, b_period, units, to, s);
+  if (cg == 2) return launch_cg<2>(maps, a, epi, out_f32, fp4, E, m_tiles, bn, b_period, units, to, ksplit, s);
+  return launch_cg<1>(maps, a, epi, out_f32, fp4, E, m_tiles, bn, b_period, units, to, ksplit, s);
 }
 
 }  // namespace moe

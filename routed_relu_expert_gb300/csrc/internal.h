@@ -74,8 +74,11 @@ cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_
 // x_cols < K (a divisor of K) re-reads X's first x_cols columns for every
 // x_cols-wide slice of W's K (used to multiply X by side-by-side split parts of
 // one matrix); 0 = K.
+// ksplit > 1 (dense FP32 stores only) splits K into that many parts, each a
+// separate output slab [x_rows, out_ld] after the previous one; the caller adds
+// the slabs in part order.
 cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_rows, int64_t x_rows, int E, int bn,
-                           cudaStream_t s, int x_cols = 0);
+                           cudaStream_t s, int x_cols = 0, int ksplit = 1);
 // Rows per tile for launch_gemm_tc: the largest power of two (16..256) that
 // still gives every SM about two tiles, for segments of rows_per_seg rows and
 // N output features.
@@ -83,12 +86,18 @@ int tc_tile_rows(int64_t rows_per_seg, int64_t segs, int N);
 
 // router
 // w_split: scratch of E * 3d BF16 for the tensor-core path (many BF16 tokens);
-// nullptr keeps the FP32 SIMT kernels.
+// nullptr keeps the FP32 SIMT kernels.  parts: scratch of kRouterParts * T * E
+// FP32 for K-split tensor-core logits (nullptr: no split).  *nparts receives
+// the number of logit slabs written (1: `logits` itself; more: `parts`, slab p
+// at p * T * E), which the selection kernel adds in order.
+constexpr int kRouterParts = 4;
 cudaError_t launch_router_logits(const void* x, int act, int T, int d, const float* w_router, int E,
-                                 float* logits, cudaStream_t s, void* w_split = nullptr);
-cudaError_t launch_router_select(const float* logits, int T, int E, const float* bias, int G, int TG,
-                                 int K, int norm, float rsf, float* scores, int32_t* ids, float* w,
-                                 int32_t* err, cudaStream_t s);
+                                 float* logits, cudaStream_t s, void* w_split, float* parts, int* nparts);
+// logits: slab 0 of nparts slabs part_stride floats apart; their sum (part
+// order) is the logit, written to logits_out when it is not nullptr
+cudaError_t launch_router_select(const float* logits, int nparts, int64_t part_stride, float* logits_out, int T,
+                                 int E, const float* bias, int G, int TG, int K, int norm, float rsf, float* scores,
+                                 int32_t* ids, float* w, int32_t* err, cudaStream_t s);
 
 // dispatch
 struct DispatchArgs {

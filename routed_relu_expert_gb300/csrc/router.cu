@@ -198,7 +198,9 @@ __device__ __forceinline__ void top2_merge(Top2& t, int span) {
 }
 
 template <int P>
-__global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits, int T, int E,
+__global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits, int nparts,
+                                                            int64_t part_stride, float* __restrict__ logits_out,
+                                                            int T, int E,
                                                             const float* __restrict__ bias, int G, int TG,
                                                             int K, int norm, float rsf,
                                                             float* __restrict__ scores,
@@ -220,7 +222,10 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
   for (int j = 0; j < P; ++j) {
     const int e = e0 + j;
     if (e < E) {
-      const float z = zrow[e];
+      // logits split over K parts are added here, in part order
+      float z = zrow[e];
+      for (int p = 1; p < nparts; ++p) z += zrow[p * part_stride + e];
+      if (logits_out) logits_out[(int64_t)t * E + e] = z;
       const float sv = 1.0f / (1.0f + expf(-z));
       s[j] = sv;
       srow[e] = sv;
@@ -364,11 +369,11 @@ __global__ void split_bf16x3_kernel(const float* __restrict__ w, int E, int d, b
 }
 
 template <int P>
-cudaError_t launch_select_p(const float* logits, int T, int E, const float* bias, int G, int TG, int K,
-                            int norm, float rsf, float* scores, int32_t* ids, float* w, int32_t* err,
-                            cudaStream_t s) {
-  launch_k(router_select_kernel<P>, (unsigned)ceil_div(T, 8), 256, 0, s, logits, T, E, bias, G, TG, K, norm, rsf,
-                                                                   scores, ids, w, err);
+cudaError_t launch_select_p(const float* logits, int nparts, int64_t part_stride, float* logits_out, int T, int E,
+                            const float* bias, int G, int TG, int K, int norm, float rsf, float* scores, int32_t* ids,
+                            float* w, int32_t* err, cudaStream_t s) {
+  launch_k(router_select_kernel<P>, (unsigned)ceil_div(T, 8), 256, 0, s, logits, nparts, part_stride, logits_out, T,
+           E, bias, G, TG, K, norm, rsf, scores, ids, w, err);
   return cudaGetLastError();
 }
 
@@ -394,7 +399,8 @@ cudaError_t launch_small(const void* x, int act, int T, int d, const float* w, i
 }  // namespace
 
 cudaError_t launch_router_logits(const void* x, int act, int T, int d, const float* w_router, int E,
-                                 float* logits, cudaStream_t s, void* w_split) {
+                                 float* logits, cudaStream_t s, void* w_split, float* parts, int* nparts) {
+  *nparts = 1;
   if (T <= 0) return cudaSuccess;
   if (w_split && act == MOE_DT_BF16 && T > 64 && E % 32 == 0 && d % 64 == 0) {
     const int64_t n = (int64_t)E * d;
@@ -403,9 +409,19 @@ cudaError_t launch_router_logits(const void* x, int act, int T, int d, const flo
     if (err != cudaSuccess) return err;
     GemvArgs a{};
     a.W = w_split; a.N = E; a.K = 3 * d; a.X = x; a.x_ld = d; a.dense_rows = T;
-    a.out = logits; a.out_ld = E;
-    const int bn = T >= 64 * 152 ? 64 : 32;
-    return launch_gemm_tc(a, EPI_STORE, true, E, T, 0, bn, s, d);
+    a.out_ld = E;
+    // full 256-row tiles; the K = 3d reduction is split into up to kRouterParts
+    // parts when the row x expert tiles alone cannot fill the GPU (the
+    // selection kernel adds the parts)
+    const int bn = 256;
+    int ks = 1;
+    if (parts) {
+      const int64_t tiles = ceil_div(T, bn) * ceil_div(E, 256);
+      ks = (int)std::min<int64_t>(kRouterParts, std::max<int64_t>(1, ceil_div(2 * 152, tiles)));
+    }
+    a.out = ks > 1 ? parts : logits;
+    *nparts = ks;
+    return launch_gemm_tc(a, EPI_STORE, true, E, T, 0, bn, s, d, ks);
   }
   if (T <= 4) return launch_small<4>(x, act, T, d, w_router, E, logits, s);
   if (T <= 64) return launch_small<8>(x, act, T, d, w_router, E, logits, s);
@@ -417,17 +433,21 @@ cudaError_t launch_router_logits(const void* x, int act, int T, int d, const flo
   return cudaGetLastError();
 }
 
-cudaError_t launch_router_select(const float* logits, int T, int E, const float* bias, int G, int TG, int K,
-                                 int norm, float rsf, float* scores, int32_t* ids, float* w, int32_t* err,
-                                 cudaStream_t s) {
+cudaError_t launch_router_select(const float* logits, int nparts, int64_t part_stride, float* logits_out, int T,
+                                 int E, const float* bias, int G, int TG, int K, int norm, float rsf, float* scores,
+                                 int32_t* ids, float* w, int32_t* err, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int P = (int)ceil_div(E, 32);
-  if (P <= 1) return launch_select_p<1>(logits, T, E, bias, G, TG, K, norm, rsf, scores, ids, w, err, s);
-  if (P <= 2) return launch_select_p<2>(logits, T, E, bias, G, TG, K, norm, rsf, scores, ids, w, err, s);
-  if (P <= 4) return launch_select_p<4>(logits, T, E, bias, G, TG, K, norm, rsf, scores, ids, w, err, s);
-  if (P <= 8) return launch_select_p<8>(logits, T, E, bias, G, TG, K, norm, rsf, scores, ids, w, err, s);
-  if (P <= 16) return launch_select_p<16>(logits, T, E, bias, G, TG, K, norm, rsf, scores, ids, w, err, s);
-  return launch_select_p<32>(logits, T, E, bias, G, TG, K, norm, rsf, scores, ids, w, err, s);
+#define MOE_SELECT(PP) \
+  return launch_select_p<PP>(logits, nparts, part_stride, logits_out, T, E, bias, G, TG, K, norm, rsf, scores, ids, w, \
+                             err, s)
+  if (P <= 1) MOE_SELECT(1);
+  if (P <= 2) MOE_SELECT(2);
+  if (P <= 4) MOE_SELECT(4);
+  if (P <= 8) MOE_SELECT(8);
+  if (P <= 16) MOE_SELECT(16);
+  MOE_SELECT(32);
+#undef MOE_SELECT
 }
 
 }  // namespace moe

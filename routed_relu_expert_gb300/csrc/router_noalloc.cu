@@ -2,17 +2,18 @@
 // memory, e.g. code that runs after its host framework's pool has claimed all
 // device memory, runtimes that forbid allocation once serving starts, or code
 // enqueued where cudaMalloc is not permitted.  The scratch the router needs
-// between its kernels (logits, scores, the split router matrix, the device
-// error word) lives in a fixed static device array of this file instead of a
-// caller workspace.
+// between its kernels (logits, scores, the K-split partial logits, the split
+// router matrix, the device error word) lives in a fixed static device array of
+// this file instead of a caller workspace.
 //
 // Properties the caller must know:
-//  - The array (MOE_NOALLOC_MAX_ROUTER_ELEMS * 8 + MOE_NOALLOC_MAX_SPLIT_ELEMS
-//    * 2 + 256 bytes, about 15 MiB) exists on every GPU that loads the
+//  - The array (MOE_NOALLOC_MAX_ROUTER_ELEMS * 24 + MOE_NOALLOC_MAX_SPLIT_ELEMS
+//    * 2 + 256 bytes, about 17 MiB) exists on every GPU that loads the
 //    library, for the life of the process.
 //  - It computes exactly what moe_router computes, by the same kernels: for
 //    more than 64 BF16 tokens that includes the BF16 split of the router
-//    matrix, which is why the array also holds E * 3d BF16 values.
+//    matrix (E * 3d BF16 values) and the logits split over up to four K parts
+//    (four logit-sized slabs), both held in the array.
 //  - The first call on a device looks up the array's device address with
 //    cudaGetSymbolAddress (once per device, with that device current); make
 //    that first call before any stream capture.
@@ -34,9 +35,10 @@ constexpr int64_t kMaxSplit = MOE_NOALLOC_MAX_SPLIT_ELEMS;
 constexpr size_t kHeaderBytes = 256;
 
 // [0, 256): error word;  logits [kMaxElems] f32;  scores [kMaxElems] f32;
-// split router matrix [kMaxSplit] bf16
+// K-split logit slabs [kRouterParts * kMaxElems] f32;  split router matrix
+// [kMaxSplit] bf16
 static __device__ __align__(256) unsigned char
-    g_router_scratch[kHeaderBytes + 2 * kMaxElems * sizeof(float) + kMaxSplit * 2];
+    g_router_scratch[kHeaderBytes + (2 + moe::kRouterParts) * kMaxElems * sizeof(float) + kMaxSplit * 2];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
@@ -80,15 +82,19 @@ extern "C" moe_status_t moe_router_noalloc(const moe_config_t* cfg, int32_t T, c
   int32_t* err = reinterpret_cast<int32_t*>(base);
   float* logits = reinterpret_cast<float*>(reinterpret_cast<char*>(base) + kHeaderBytes);
   float* scores = logits + kMaxElems;
-  void* split = reinterpret_cast<void*>(scores + kMaxElems);
+  float* parts = scores + kMaxElems;
+  void* split = reinterpret_cast<void*>(parts + moe::kRouterParts * kMaxElems);
   cudaStream_t s = (cudaStream_t)stream;
   if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (moe::launch_router_logits(x, cfg->act_dtype, T, cfg->d_model, w_router, cfg->n_experts, logits, s, split) !=
-      cudaSuccess)
+  int nparts = 1;
+  if (moe::launch_router_logits(x, cfg->act_dtype, T, cfg->d_model, w_router, cfg->n_experts, logits, s, split,
+                                T > 64 ? parts : nullptr, &nparts) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (moe::launch_router_select(logits, T, cfg->n_experts, router_bias, cfg->n_group, cfg->topk_group,
-                                cfg->top_k, cfg->norm_topk_prob, cfg->routed_scaling_factor, scores, topk_ids,
-                                topk_w, err, s) != cudaSuccess)
+  const bool ks = nparts > 1;
+  if (moe::launch_router_select(ks ? parts : logits, nparts, (int64_t)T * cfg->n_experts, ks ? logits : nullptr, T,
+                                cfg->n_experts, router_bias, cfg->n_group, cfg->topk_group, cfg->top_k,
+                                cfg->norm_topk_prob, cfg->routed_scaling_factor, scores, topk_ids, topk_w, err,
+                                s) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
