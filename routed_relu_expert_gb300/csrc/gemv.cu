@@ -78,6 +78,20 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a
   const bf16* wg = W + (int64_t)g * K + 8 * t4;
   const bf16* wg8 = W + (int64_t)(g + 8) * K + 8 * t4;
   const int nchunks = K >> 5;
+  uint4 A0[U], A1[U];
+  auto load_round = [&](int c) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int cc = c + kWarps * u;
+      if (cc < nchunks) {
+        A0[u] = ldg_stream(wg + cc * 32);
+        A1[u] = ldg_stream(wg8 + cc * 32);
+      }
+    }
+  };
+  // the first round of weight loads goes out before the row gathers below,
+  // whose dependent loads would otherwise delay it
+  load_round(warp);
 
   for (int p0 = 0, pi = 0; p0 < sg.nrows; p0 += NT * 8, ++pi) {
     const int prow = min(sg.nrows - p0, NT * 8);
@@ -99,15 +113,7 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a
     for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
     for (int c = warp; c < nchunks; c += kWarps * U) {
-      uint4 A0[U], A1[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int cc = c + kWarps * u;
-        if (cc < nchunks) {
-          A0[u] = ldg_stream(wg + cc * 32);
-          A1[u] = ldg_stream(wg8 + cc * 32);
-        }
-      }
+      if (p0 > 0 || c != warp) load_round(c);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int cc = c + kWarps * u;
