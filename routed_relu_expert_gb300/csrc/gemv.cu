@@ -32,15 +32,27 @@ struct Seg {
   int id, row0, nrows;
 };
 
-__device__ __forceinline__ bool resolve_segment(const GemvArgs& a, int rows_per_cta, Seg& s) {
+// segment of this CTA: the expert id first (one level of dependent loads, so a
+// caller can start its weight stream), then the rows
+__device__ __forceinline__ bool resolve_id(const GemvArgs& a, Seg& s) {
   if (a.offsets) {
     const int j = blockIdx.y;
-    if (j >= a.hdr->n_active) return false;
-    s.id = a.active[j];
+    // both loads go out together (active[] has a slot for every launched j)
+    const int n_active = a.hdr->n_active;
+    const int id = a.active[j];
+    if (j >= n_active) return false;
+    s.id = id;
+  } else {
+    s.id = 0;
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool resolve_rows(const GemvArgs& a, int rows_per_cta, Seg& s) {
+  if (a.offsets) {
     s.row0 = a.offsets[s.id];
     s.nrows = a.offsets[s.id + 1] - s.row0;
   } else {
-    s.id = 0;
     s.row0 = 0;
     s.nrows = a.dense_rows;
   }
@@ -49,6 +61,10 @@ __device__ __forceinline__ bool resolve_segment(const GemvArgs& a, int rows_per_
   s.row0 += rb;
   s.nrows = min(s.nrows - rb, rows_per_cta);
   return true;
+}
+
+__device__ __forceinline__ bool resolve_segment(const GemvArgs& a, int rows_per_cta, Seg& s) {
+  return resolve_id(a, s) && resolve_rows(a, rows_per_cta, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -66,9 +82,7 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a
   __shared__ float wrs[2][NT * 8];      // routing weights of a pass's rows (EPI_SCALE)
 
   Seg sg;
-  // dense products split their 16-row passes over grid.z (CTAs of one feature
-  // tile run together, so the tile is read from HBM once); grouped ones loop
-  if (!resolve_segment(a, a.offsets ? (1 << 30) : NT * 8, sg)) return;
+  if (!resolve_id(a, sg)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int f0 = blockIdx.x * 16;
@@ -89,9 +103,13 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a
       }
     }
   };
-  // the first round of weight loads goes out before the row gathers below,
-  // whose dependent loads would otherwise delay it
+  // the first round of weight loads goes out before the row lookups and
+  // gathers below, whose dependent loads would otherwise delay it
   load_round(warp);
+  // dense products split their 16-row passes over grid.z (CTAs of one feature
+  // tile run together, so the tile is read from HBM once; z < ceil(rows/16),
+  // so no CTA returns here after loading); grouped ones loop
+  if (!resolve_rows(a, a.offsets ? (1 << 30) : NT * 8, sg)) return;
 
   for (int p0 = 0, pi = 0; p0 < sg.nrows; p0 += NT * 8, ++pi) {
     const int prow = min(sg.nrows - p0, NT * 8);
@@ -319,7 +337,7 @@ __global__ void __launch_bounds__(kBulkThreads, 8) gemv_nvfp4_bulk_kernel(const 
   pdl_trigger();
   constexpr int NT = 2;
   Seg sg;
-  if (!resolve_segment(a, 1 << 30, sg)) return;
+  if (!resolve_id(a, sg)) return;       // grouped only: the copy needs the expert id alone
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int K = a.K;
@@ -340,8 +358,10 @@ __global__ void __launch_bounds__(kBulkThreads, 8) gemv_nvfp4_bulk_kernel(const 
              b);
     bulk_g2s(smem_u32(ss), a.W_sf + sg.id * a.sf_seg_stride + (int64_t)f0 * rows_sf, sbytes, b);
   }
-  // the segment's per-tensor scale and the rows' routing weights load while
-  // the weight tile is in flight
+  // the rows, the segment's per-tensor scale and the rows' routing weights
+  // load while the weight tile is in flight (an active expert has rows, so no
+  // CTA leaves here with its copy outstanding)
+  resolve_rows(a, 1 << 30, sg);
   const float gs = a.W_gs ? a.W_gs[sg.id] : 1.f;
   __shared__ float wrs[2][16];
   if (EPI == EPI_SCALE && threadIdx.x < min(sg.nrows, 16)) wrs[0][threadIdx.x] = route_weight(a, sg.row0 + threadIdx.x);
