@@ -14,10 +14,16 @@ namespace moe {
 
 namespace {
 
+// grid (T, column blocks of 128 float4s): each thread owns one float4 column of
+// one token and loads all of that column's routed rows before adding them in
+// row order, so a token's K loads are in flight together
+constexpr int kCombineThreads = 128;
+
 template <bool ACT_F32>
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ u, const int32_t* __restrict__ tsr,
-                                                      int K, int de, float* __restrict__ y_r,
-                                                      void* __restrict__ y_act, const float* __restrict__ add) {
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* __restrict__ u,
+                                                                  const int32_t* __restrict__ tsr, int K, int de,
+                                                                  float* __restrict__ y_r, void* __restrict__ y_act,
+                                                                  const float* __restrict__ add) {
   pdl_wait();
   pdl_trigger();
   __shared__ int rows[32];
@@ -34,31 +40,41 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     }
     rows[rank] = r;
   }
-  __syncthreads();
   const int nv = de / 4;
-  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < K; ++i) {
-      const int r = rows[i];
-      if (r < 0) continue;
-      const float4 q = reinterpret_cast<const float4*>(u + (int64_t)r * de)[v];
-      acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+  const int v = blockIdx.y * kCombineThreads + threadIdx.x;
+  float4 extra = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (add && v < nv) extra = reinterpret_cast<const float4*>(add + (int64_t)t * de)[v];
+  __syncthreads();
+  if (v >= nv) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int B = 8;                   // rows loaded ahead of their adds
+  for (int i0 = 0; i0 < K; i0 += B) {
+    float4 q[B];
+#pragma unroll
+    for (int i = 0; i < B; ++i) {
+      const int r = i0 + i < K ? rows[i0 + i] : -1;
+      q[i] = r >= 0 ? reinterpret_cast<const float4*>(u + (int64_t)r * de)[v] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (y_r) reinterpret_cast<float4*>(y_r + (int64_t)t * de)[v] = acc;
-    if (add) {
-      // output = routed sum + an FP32 term (the shared expert), then one rounding
-      const float4 q = reinterpret_cast<const float4*>(add + (int64_t)t * de)[v];
-      acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
-    }
-    if (y_act) {
-      if (ACT_F32) {
-        reinterpret_cast<float4*>(reinterpret_cast<float*>(y_act) + (int64_t)t * de)[v] = acc;
-      } else {
-        uint2 p;
-        p.x = (uint32_t)bf16_bits(acc.x) | ((uint32_t)bf16_bits(acc.y) << 16);
-        p.y = (uint32_t)bf16_bits(acc.z) | ((uint32_t)bf16_bits(acc.w) << 16);
-        reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(y_act) + (int64_t)t * de)[v] = p;
+#pragma unroll
+    for (int i = 0; i < B; ++i) {
+      if (i0 + i < K && rows[i0 + i] >= 0) {
+        acc.x += q[i].x; acc.y += q[i].y; acc.z += q[i].z; acc.w += q[i].w;
       }
+    }
+  }
+  if (y_r) reinterpret_cast<float4*>(y_r + (int64_t)t * de)[v] = acc;
+  if (add) {
+    // output = routed sum + an FP32 term (the shared expert), then one rounding
+    acc.x += extra.x; acc.y += extra.y; acc.z += extra.z; acc.w += extra.w;
+  }
+  if (y_act) {
+    if (ACT_F32) {
+      reinterpret_cast<float4*>(reinterpret_cast<float*>(y_act) + (int64_t)t * de)[v] = acc;
+    } else {
+      uint2 p;
+      p.x = (uint32_t)bf16_bits(acc.x) | ((uint32_t)bf16_bits(acc.y) << 16);
+      p.y = (uint32_t)bf16_bits(acc.z) | ((uint32_t)bf16_bits(acc.w) << 16);
+      reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(y_act) + (int64_t)t * de)[v] = p;
     }
   }
 }
@@ -96,10 +112,11 @@ cudaError_t launch_cast(const float* src, int64_t n, void* dst, int act, cudaStr
 cudaError_t launch_combine(const float* u, const int32_t* token_slot_row, int T, int K, int de, float* y_r,
                            void* y_act, int act, cudaStream_t s, const float* add) {
   if (T <= 0) return cudaSuccess;
+  const dim3 grid((unsigned)T, (unsigned)ceil_div(de / 4, kCombineThreads));
   if (act == MOE_DT_F32)
-    launch_k(combine_kernel<true>, T, 256, 0, s, u, token_slot_row, K, de, y_r, y_act, add);
+    launch_k(combine_kernel<true>, grid, kCombineThreads, 0, s, u, token_slot_row, K, de, y_r, y_act, add);
   else
-    launch_k(combine_kernel<false>, T, 256, 0, s, u, token_slot_row, K, de, y_r, y_act, add);
+    launch_k(combine_kernel<false>, grid, kCombineThreads, 0, s, u, token_slot_row, K, de, y_r, y_act, add);
   return cudaGetLastError();
 }
 
