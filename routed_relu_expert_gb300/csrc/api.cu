@@ -139,22 +139,37 @@ struct Ptrs {
 };
 
 // ---- steps -----------------------------------------------------------------
-moe_status_t run_router(const moe_config_t* c, int T, const void* x, const float* w_router, const float* bias,
-                        float* logits, float* scores, int32_t* ids, float* w, const Ptrs& P, cudaStream_t s) {
+// router logits; the selection's arguments (the logits may be split over K parts)
+moe_status_t run_logits(const moe_config_t* c, int T, const void* x, const float* w_router, const float* bias,
+                        float* logits, float* scores, int32_t* ids, float* w, const Ptrs& P, cudaStream_t s,
+                        SelectArgs& sa) {
   float* parts = T > 64 ? P.at<float>(P.L.logit_parts) : nullptr;
   int nparts = 1;
   CU(launch_router_logits(x, c->act_dtype, T, c->d_model, w_router, c->n_experts, logits, s,
                           P.at<void>(P.L.w_split), parts, &nparts));
   const bool split = nparts > 1;
-  CU(launch_router_select(split ? parts : logits, nparts, (int64_t)T * c->n_experts, split ? logits : nullptr, T,
-                          c->n_experts, bias, c->n_group, c->topk_group, c->top_k, c->norm_topk_prob,
-                          c->routed_scaling_factor, scores, ids, w, &P.hdr()->err, s));
+  sa = SelectArgs{split ? parts : logits, nparts, (int64_t)T * c->n_experts, split ? logits : nullptr, T,
+                  c->n_experts, bias, c->n_group, c->topk_group, c->top_k, c->norm_topk_prob,
+                  c->routed_scaling_factor, scores, ids, w, &P.hdr()->err};
   return MOE_OK;
 }
 
-moe_status_t run_dispatch(const moe_config_t* c, int T, const int32_t* ids, const void* x_e, int32_t* counts,
-                          int32_t* offsets, int32_t* rt, int32_t* rs, int32_t* tsr, void* x_packed,
-                          const Ptrs& P, cudaStream_t s) {
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t s) {
+  return launch_router_select(a.logits, a.nparts, a.part_stride, a.logits_out, a.T, a.E, a.bias, a.G, a.TG, a.K,
+                              a.norm, a.rsf, a.scores, a.ids, a.w, a.err, s);
+}
+
+moe_status_t run_router(const moe_config_t* c, int T, const void* x, const float* w_router, const float* bias,
+                        float* logits, float* scores, int32_t* ids, float* w, const Ptrs& P, cudaStream_t s) {
+  SelectArgs sa;
+  moe_status_t st = run_logits(c, T, x, w_router, bias, logits, scores, ids, w, P, s, sa);
+  if (st != MOE_OK) return st;
+  CU(launch_select(sa, s));
+  return MOE_OK;
+}
+
+DispatchArgs dispatch_args(const moe_config_t* c, int T, const int32_t* ids, const void* x_e, int32_t* counts,
+                           int32_t* offsets, int32_t* rt, int32_t* rs, int32_t* tsr, void* x_packed, const Ptrs& P) {
   DispatchArgs a{};
   a.ids = ids; a.T = T; a.K = c->top_k; a.E = c->n_experts;
   a.counts = counts; a.offsets = offsets; a.route_token = rt; a.route_slot = rs; a.token_slot_row = tsr;
@@ -165,7 +180,13 @@ moe_status_t run_dispatch(const moe_config_t* c, int T, const int32_t* ids, cons
   a.tile_rows = 0;
   a.x_e = x_e; a.x_packed = x_e ? x_packed : nullptr;
   a.de = de_of(c); a.elem_bytes = act_bytes(c);
-  CU(launch_dispatch(a, s));
+  return a;
+}
+
+moe_status_t run_dispatch(const moe_config_t* c, int T, const int32_t* ids, const void* x_e, int32_t* counts,
+                          int32_t* offsets, int32_t* rt, int32_t* rs, int32_t* tsr, void* x_packed,
+                          const Ptrs& P, cudaStream_t s) {
+  CU(launch_dispatch(dispatch_args(c, T, ids, x_e, counts, offsets, rt, rs, tsr, x_packed, P), s));
   return MOE_OK;
 }
 
@@ -454,16 +475,22 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
   float* scores = scores_out ? scores_out : P.at<float>(P.L.scores);
   int32_t* ids = topk_ids_out ? topk_ids_out : P.at<int32_t>(P.L.ids);
   float* topw = topk_w_out ? topk_w_out : P.at<float>(P.L.topw);
-  if ((st = run_router(cfg, T, x, w->w_router, w->router_bias, logits, scores, ids, topw, P, s)) != MOE_OK)
+  SelectArgs sa;
+  if ((st = run_logits(cfg, T, x, w->w_router, w->router_bias, logits, scores, ids, topw, P, s, sa)) != MOE_OK)
     return st;
   int32_t* offsets = P.at<int32_t>(P.L.offsets);
   int32_t* rt = P.at<int32_t>(P.L.route_token);
   int32_t* rs = P.at<int32_t>(P.L.route_slot);
   int32_t* tsr = P.at<int32_t>(P.L.tsr);
   void* x_packed = use_tc(cfg, T) ? P.at<void>(P.L.x_packed) : nullptr;
-  if ((st = run_dispatch(cfg, T, ids, x_e, P.at<int32_t>(P.L.counts), offsets, rt, rs, tsr, x_packed, P, s)) !=
-      MOE_OK)
-    return st;
+  const DispatchArgs da =
+      dispatch_args(cfg, T, ids, x_e, P.at<int32_t>(P.L.counts), offsets, rt, rs, tsr, x_packed, P);
+  if (select_dispatch_fits(T, cfg->top_k, da)) {
+    CU(launch_select_dispatch(sa, da, s));       // a few tokens: one kernel
+  } else {
+    CU(launch_select(sa, s));
+    CU(launch_dispatch(da, s));
+  }
   void* h = P.at<void>(P.L.h);
   if ((st = run_up(cfg, T, x_e, x_packed, rt, offsets, w, h, P, s)) != MOE_OK) return st;
   float* u = P.at<float>(P.L.u);

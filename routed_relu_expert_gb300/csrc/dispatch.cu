@@ -11,7 +11,7 @@
 // bases are exclusive scans over (tile, warp) in index order, so route r lands
 // after every earlier route of the same expert: the order is (expert, r) =
 // (expert, token, slot) because a token names an expert at most once.
-#include "internal.h"
+#include "select.cuh"
 
 #include <algorithm>
 
@@ -254,6 +254,94 @@ __global__ void __launch_bounds__(kThreads) dispatch_scatter(const DispatchArgs 
   warp_scatter(a.ids, r0, r1, a.E, a.K, hist, a.route_token, a.route_slot, a.token_slot_row);
 }
 
+// ---------------------------------------------------------------------------
+// a few tokens (T <= 8, T*K <= 256): selection and dispatch in one CTA.  Warp t
+// selects token t (the selection kernel's code), then every route r is placed
+// directly: its packed position is the number of routes ordered before it by
+// (expert, r); an expert's offset is the number of routes with a lower expert.
+// Same outputs as the selection kernel followed by dispatch_single.
+// ---------------------------------------------------------------------------
+constexpr int kTinyThreads = 256;
+constexpr int kTinyMaxRoutes = 256;
+constexpr int kTinyMaxTokens = kTinyThreads / 32;
+
+template <int P>
+__global__ void __launch_bounds__(kTinyThreads) select_dispatch_tiny(const SelectArgs sa, const DispatchArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int sid[kTinyMaxRoutes];     // expert of route r (-1: invalid)
+  __shared__ int first[kTinyMaxRoutes];   // route r is its expert's first route
+  __shared__ int cnt_max[kTinyThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < a.T)
+    select_token<P>(sa.logits, sa.nparts, sa.part_stride, sa.logits_out, warp, sa.E, sa.bias, sa.G, sa.TG, sa.K,
+                    sa.norm, sa.rsf, sa.scores, sa.ids, sa.w, sa.err, warp, lane);
+  __syncthreads();                        // this CTA's id writes are visible to it
+  const int R = a.T * a.K;
+  const int r = threadIdx.x;
+  int e = -1;
+  if (r < R) {
+    e = a.ids[r];
+    if (e < 0 || e >= a.E) {
+      set_error(&a.hdr->err, MOE_DEVERR_EXPERT_ID);
+      e = -1;
+    }
+    sid[r] = e;
+  }
+  __syncthreads();
+  if (r < R) {
+    int pos = -1;
+    bool is_first = e >= 0;
+    if (e >= 0) {
+      pos = 0;
+      for (int j = 0; j < R; ++j) {
+        const int ej = sid[j];
+        pos += (ej >= 0) && (ej < e || (ej == e && j < r));
+        is_first &= !(ej == e && j < r);
+      }
+    }
+    first[r] = is_first ? 1 : 0;
+    a.token_slot_row[r] = pos;
+    if (pos >= 0) {
+      a.route_token[pos] = r / a.K;
+      a.route_slot[pos] = r % a.K;
+    }
+  }
+  __syncthreads();
+  // per expert: count, offset; the active list (experts with routes, ascending)
+  int local_max = 0;
+  for (int x = threadIdx.x; x <= a.E; x += kTinyThreads) {
+    int below = 0, count = 0;
+    for (int j = 0; j < R; ++j) {
+      const int ej = sid[j];
+      below += (ej >= 0 && ej < x);
+      count += (ej == x);
+    }
+    a.offsets[x] = below;
+    if (x < a.E) {
+      a.counts[x] = count;
+      local_max = max(local_max, count);
+    }
+  }
+  if (r < R && first[r]) {
+    int idx = 0;                          // distinct experts below this one
+    for (int j = 0; j < R; ++j) idx += first[j] && sid[j] < e;
+    a.active[idx] = e;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) local_max = max(local_max, __shfl_xor_sync(0xffffffffu, local_max, off));
+  if (lane == 0) cnt_max[warp] = local_max;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int n_active = 0, mm = 0;
+    for (int j = 0; j < R; ++j) n_active += first[j];
+    for (int w = 0; w < kTinyThreads / 32; ++w) mm = max(mm, cnt_max[w]);
+    a.hdr->n_active = n_active;
+    a.hdr->n_tiles = 0;
+    a.hdr->max_rows = mm;
+  }
+}
+
 constexpr int kSingleMaxRoutes = 4096;
 
 // the dynamic shared-memory limits are raised once, to the largest expert count
@@ -269,6 +357,25 @@ cudaError_t launch_pack(const DispatchArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+bool select_dispatch_fits(int T, int K, const DispatchArgs& a) {
+  return T >= 1 && T <= kTinyMaxTokens && T * K <= kTinyMaxRoutes && a.tile_rows == 0 && !a.x_packed;
+}
+
+cudaError_t launch_select_dispatch(const SelectArgs& sa, const DispatchArgs& a, cudaStream_t s) {
+  if (!select_dispatch_fits(a.T, a.K, a)) return cudaErrorNotSupported;
+  const int P = (int)ceil_div(sa.E, 32);
+#define MOE_TINY(PP) \
+  launch_k(select_dispatch_tiny<PP>, 1, kTinyThreads, 0, s, sa, a); \
+  return cudaGetLastError()
+  if (P <= 1) { MOE_TINY(1); }
+  if (P <= 2) { MOE_TINY(2); }
+  if (P <= 4) { MOE_TINY(4); }
+  if (P <= 8) { MOE_TINY(8); }
+  if (P <= 16) { MOE_TINY(16); }
+  MOE_TINY(32);
+#undef MOE_TINY
+}
 
 size_t dispatch_tile_count_elems(int T, int K, int E) {
   (void)K;

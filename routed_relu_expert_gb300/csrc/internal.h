@@ -121,6 +121,27 @@ struct DispatchArgs {
 size_t dispatch_tile_count_elems(int T, int K, int E);
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
 
+// selection arguments (see launch_router_select)
+struct SelectArgs {
+  const float* logits;
+  int nparts;
+  int64_t part_stride;
+  float* logits_out;
+  int T, E;
+  const float* bias;
+  int G, TG, K, norm;
+  float rsf;
+  float* scores;
+  int32_t* ids;
+  float* w;
+  int32_t* err;
+};
+// Selection followed by dispatch in one single-CTA kernel, for a few tokens
+// (T <= 8, T*K <= 256) on the GEMV path (no tile schedule, no packed rows);
+// same results as launch_router_select + launch_dispatch.
+bool select_dispatch_fits(int T, int K, const DispatchArgs& a);
+cudaError_t launch_select_dispatch(const SelectArgs& sa, const DispatchArgs& a, cudaStream_t s);
+
 // combine: y_r[t] = sum over t's packed rows in ascending order of u[row];
 // y_r_act[t] = act(y_r[t] + add[t]) (add nullable)
 cudaError_t launch_combine(const float* u, const int32_t* token_slot_row, int T, int K, int de,

@@ -4,7 +4,7 @@
 // Kernel Contract"; page "NemotronH (Nemotron 3.5 Lightning, Bolt, Super VL)",
 // section "Arithmetic": fp32 logits, sigmoid, the bias for the choice only,
 // ties to the lower id).
-#include "internal.h"
+#include "select.cuh"
 
 #include <algorithm>
 #include <climits>
@@ -148,55 +148,6 @@ __global__ void __launch_bounds__(256) router_logits_tiled(const void* __restric
   }
 }
 
-// ---------------------------------------------------------------------------
-// selection: one warp per token; lane l holds the P consecutive experts
-// lP .. lP+P-1, so experts ascend with the lane and, where P divides the group
-// size, a group is a run of lanes.
-// Ordering key: larger biased score first, NaN after every number, equal keys
-// to the lower expert id.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ int order_key(float v) {
-  if (isnan(v)) return INT_MIN + 1;
-  v = v + 0.0f;  // -0 -> +0
-  const int b = __float_as_int(v);
-  return b >= 0 ? b : (b ^ 0x7FFFFFFF);
-}
-
-__device__ __forceinline__ bool better(int ka, int ea, int kb, int eb) {
-  return ka > kb || (ka == kb && ea < eb);
-}
-
-// top two (key, id, value) of a lane's candidates, then merged across the
-// lanes whose xor distance is below `span` (a power of two)
-struct Top2 {
-  int k1, e1, k2, e2;
-  float v1, v2;
-};
-__device__ __forceinline__ void top2_add(Top2& t, int k, int e, float v) {
-  if (better(k, e, t.k1, t.e1)) {
-    t.k2 = t.k1; t.e2 = t.e1; t.v2 = t.v1;
-    t.k1 = k; t.e1 = e; t.v1 = v;
-  } else if (better(k, e, t.k2, t.e2)) {
-    t.k2 = k; t.e2 = e; t.v2 = v;
-  }
-}
-__device__ __forceinline__ void top2_merge(Top2& t, int span) {
-  for (int off = span >> 1; off > 0; off >>= 1) {
-    Top2 o;
-    o.k1 = __shfl_xor_sync(0xffffffffu, t.k1, off); o.e1 = __shfl_xor_sync(0xffffffffu, t.e1, off);
-    o.k2 = __shfl_xor_sync(0xffffffffu, t.k2, off); o.e2 = __shfl_xor_sync(0xffffffffu, t.e2, off);
-    o.v1 = __shfl_xor_sync(0xffffffffu, t.v1, off); o.v2 = __shfl_xor_sync(0xffffffffu, t.v2, off);
-    // both inputs are ordered pairs: the result is the best two of the four
-    if (better(o.k1, o.e1, t.k1, t.e1)) {
-      if (better(t.k1, t.e1, o.k2, o.e2)) { t.k2 = t.k1; t.e2 = t.e1; t.v2 = t.v1; }
-      else { t.k2 = o.k2; t.e2 = o.e2; t.v2 = o.v2; }
-      t.k1 = o.k1; t.e1 = o.e1; t.v1 = o.v1;
-    } else if (better(o.k1, o.e1, t.k2, t.e2)) {
-      t.k2 = o.k1; t.e2 = o.e1; t.v2 = o.v1;
-    }
-  }
-}
-
 template <int P>
 __global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits, int nparts,
                                                             int64_t part_stride, float* __restrict__ logits_out,
@@ -212,137 +163,8 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
-  const int e0 = lane * P;
-  float s[P], c[P];
-  int key[P];
-  bool any_nan = false;
-  const float* zrow = logits + (int64_t)t * E;
-  float* srow = scores + (int64_t)t * E;
-#pragma unroll
-  for (int j = 0; j < P; ++j) {
-    const int e = e0 + j;
-    if (e < E) {
-      // logits split over K parts are added here, in part order
-      float z = zrow[e];
-      for (int p = 1; p < nparts; ++p) z += zrow[p * part_stride + e];
-      if (logits_out) logits_out[(int64_t)t * E + e] = z;
-      const float sv = 1.0f / (1.0f + expf(-z));
-      s[j] = sv;
-      srow[e] = sv;
-      const float cv = bias ? sv + bias[e] : sv;
-      c[j] = cv;
-      key[j] = order_key(cv);
-      any_nan |= isnan(cv);
-    } else {
-      s[j] = 0.f;
-      c[j] = 0.f;
-      key[j] = INT_MIN;  // not an expert: never chosen
-    }
-  }
-  if (__any_sync(0xffffffffu, any_nan) && lane == 0) set_error(err, MOE_DEVERR_NONFINITE);
-
-  // group limit: keep the TG groups with the largest sum of their two largest
-  // c (ties to the lower group); cand bit j = value j may be chosen
-  uint32_t cand = 0xffffffffu;
-  if (G > 1 && TG < G) {
-    const int gsz = E / G;
-    const int lpg = gsz / P;                       // lanes per group when P divides gsz
-    if (gsz % P == 0 && (lpg & (lpg - 1)) == 0) {
-      // each lane lies in one group g = lane / lpg: lane top two, merged over the group's lanes
-      const int g = lane / lpg;
-      Top2 tp{INT_MIN, INT_MAX, INT_MIN, INT_MAX, 0.f, 0.f};
-#pragma unroll
-      for (int j = 0; j < P; ++j)
-        if (e0 + j < E) top2_add(tp, key[j], e0 + j, c[j]);
-      top2_merge(tp, lpg);
-      const float gs = tp.v1 + tp.v2;
-      const int gk = order_key(gs);
-      // rank of this lane's group among all G group scores
-      int rank = 0;
-      for (int g2 = 0; g2 < G; ++g2) {
-        const int k2 = __shfl_sync(0xffffffffu, gk, g2 * lpg);
-        rank += better(k2, g2, gk, g) ? 1 : 0;
-      }
-      cand = (g < G && rank < TG) ? 0xffffffffu : 0u;
-    } else {
-      // general layout: one pass per group over every lane's values
-      __shared__ float gsum_sh[8][32];
-      float* gsum = gsum_sh[warp];
-      uint32_t kept = 0;
-#pragma unroll 1
-      for (int g = 0; g < G; ++g) {
-        Top2 tp{INT_MIN, INT_MAX, INT_MIN, INT_MAX, 0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < P; ++j) {
-          const int e = e0 + j;
-          if (e < E && e / gsz == g) top2_add(tp, key[j], e, c[j]);
-        }
-        top2_merge(tp, 32);
-        if (lane == 0) gsum[g] = tp.v1 + tp.v2;
-      }
-      __syncwarp();
-#pragma unroll 1
-      for (int n = 0; n < TG; ++n) {
-        int bk = INT_MIN, bg = INT_MAX;
-#pragma unroll 1
-        for (int g = 0; g < G; ++g) {
-          if (!((kept >> g) & 1u)) {
-            const int kg = order_key(gsum[g]);
-            if (better(kg, g, bk, bg)) { bk = kg; bg = g; }
-          }
-        }
-        kept |= 1u << bg;
-      }
-      cand = 0;
-#pragma unroll
-      for (int j = 0; j < P; ++j)
-        if (e0 + j < E && ((kept >> ((e0 + j) / gsz)) & 1u)) cand |= 1u << j;
-    }
-  }
-
-  // top-K: every lane keeps the best of its remaining candidates; each round
-  // the warp maximum of the lane keys (ties: the lowest lane, which holds the
-  // lowest ids) wins and only the winning lane looks again among its values
-  uint32_t taken = 0;
-  float wsel = 0.f;          // lane k keeps the score of slot k
-  int esel = 0;
-  float wsum = 0.f;
-  int lk = INT_MIN, lj = -1;
-  auto rescan = [&]() {
-    lk = INT_MIN; lj = -1;
-#pragma unroll
-    for (int j = 0; j < P; ++j) {
-      if (((cand & ~taken) >> j) & 1u && key[j] > lk && e0 + j < E) { lk = key[j]; lj = j; }
-    }
-  };
-  rescan();
-#pragma unroll 1
-  for (int k = 0; k < K; ++k) {
-    const int mk = __reduce_max_sync(0xffffffffu, lk);
-    const uint32_t hit = __ballot_sync(0xffffffffu, lk == mk && lj >= 0);
-    float ls = 0.f;
-#pragma unroll
-    for (int j = 0; j < P; ++j)
-      if (j == lj) ls = s[j];
-    int be = INT_MAX;
-    float bs = 0.f;
-    if (hit) {
-      const int src = __ffs(hit) - 1;
-      be = __shfl_sync(0xffffffffu, e0 + lj, src);
-      bs = __shfl_sync(0xffffffffu, ls, src);
-      if (lane == src) {
-        taken |= 1u << lj;
-        rescan();
-      }
-    }
-    if (lane == k) { wsel = bs; esel = be; }
-    wsum += bs;              // slot order, FP32
-  }
-  if (lane < K) {
-    const float wv = norm ? (wsel / wsum) * rsf : wsel * rsf;
-    ids[(int64_t)t * K + lane] = esel;
-    wout[(int64_t)t * K + lane] = wv;
-  }
+  select_token<P>(logits, nparts, part_stride, logits_out, t, E, bias, G, TG, K, norm, rsf, scores, ids, wout, err,
+                  warp, lane);
 }
 
 // W (FP32) -> [W1 | W2 | W3] (BF16, side by side along K): W1 = bf16(W),
