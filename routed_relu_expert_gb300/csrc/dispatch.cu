@@ -255,14 +255,14 @@ __global__ void __launch_bounds__(kThreads) dispatch_scatter(const DispatchArgs 
 }
 
 // ---------------------------------------------------------------------------
-// a few tokens (T <= 8, T*K <= 256): selection and dispatch in one CTA.  Warp t
+// a few tokens (T <= 16, T*K <= 256): selection and dispatch in one CTA.  Warp t
 // selects token t (the selection kernel's code), then every route r is placed
 // directly: its packed position is the number of routes ordered before it by
 // (expert, r); an expert's offset is the number of routes with a lower expert.
 // Same outputs as the selection kernel followed by dispatch_single.
 // ---------------------------------------------------------------------------
-constexpr int kTinyThreads = 256;
-constexpr int kTinyMaxRoutes = 256;
+constexpr int kTinyThreads = 512;
+constexpr int kTinyMaxRoutes = 256;   // the placement below is quadratic in the routes
 constexpr int kTinyMaxTokens = kTinyThreads / 32;
 
 template <int P>

@@ -137,7 +137,7 @@ struct SelectArgs {
   int32_t* err;
 };
 // Selection followed by dispatch in one single-CTA kernel, for a few tokens
-// (T <= 8, T*K <= 256) on the GEMV path (no tile schedule, no packed rows);
+// (T <= 16, T*K <= 256) on the GEMV path (no tile schedule, no packed rows);
 // same results as launch_router_select + launch_dispatch.
 bool select_dispatch_fits(int T, int K, const DispatchArgs& a);
 cudaError_t launch_select_dispatch(const SelectArgs& sa, const DispatchArgs& a, cudaStream_t s);

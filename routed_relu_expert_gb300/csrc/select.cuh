@@ -62,7 +62,7 @@ __device__ __forceinline__ void top2_merge(Top2& t, int span) {
 }
 
 // One token's selection, by one warp (lane = its lane, warp = its warp index in
-// the CTA, < 8).  logits: slab 0 of nparts slabs part_stride floats apart.
+// the CTA).  logits: slab 0 of nparts slabs part_stride floats apart.
 template <int P>
 __device__ __forceinline__ void select_token(const float* __restrict__ logits, int nparts, int64_t part_stride,
                                              float* __restrict__ logits_out, int t, int E,
@@ -123,7 +123,7 @@ __device__ __forceinline__ void select_token(const float* __restrict__ logits, i
       cand = (g < G && rank < TG) ? 0xffffffffu : 0u;
     } else {
       // general layout: one pass per group over every lane's values
-      __shared__ float gsum_sh[8][32];
+      __shared__ float gsum_sh[32][32];
       float* gsum = gsum_sh[warp];
       uint32_t kept = 0;
 #pragma unroll 1
