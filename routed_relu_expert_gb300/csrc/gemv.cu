@@ -307,18 +307,21 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_nvfp4_kernel(const GemvArgs 
 }
 
 // ---------------------------------------------------------------------------
-// NVFP4 weights, bulk-copied.  A CTA owns 16 features of one segment.  Their
-// packed rows (16 x K/2 contiguous bytes) and block scales (16 x K/16) are
-// brought into shared memory by two cp.async.bulk copies on one mbarrier, so
-// the CTA's whole weight tile is in flight at once whatever the register
-// budget; the 4 warps then split K into 128-wide chunks exactly as above
-// (same decode, same MMA k permutation) and add their partial sums in a fixed
-// warp order.  Row passes of 16 re-read the tile from shared memory.
+// NVFP4 weights, bulk-copied (grouped decode products).  A CTA's 4 warps form
+// groups of WPG warps; a group owns 16 features, a warp of the group every
+// WPG-th 128-wide K chunk (WPG = 1 for K <= 1536, else 2), so a CTA covers
+// 64 / WPG features.  Their packed rows (contiguous bytes) and block scales
+// arrive in two cp.async.bulk copies on one mbarrier, so the whole tile is in
+// flight at once whatever the register budget.  Each chunk is decoded exactly
+// as above (hardware E2M1 / E4M3 conversion, exact FP16 scale multiply, same
+// MMA k permutation) while the next chunk's activations load; a group's two
+// partial sums are added in a fixed order.  Row passes of 16 re-read the tile
+// from shared memory.
 // ---------------------------------------------------------------------------
 constexpr int kBulkWarps = 4;
 constexpr int kBulkThreads = kBulkWarps * 32;
 constexpr uint64_t kBulkWaitNs = 4000000000ull;
-constexpr size_t kBulkSmemMax = 160 * 1024;
+constexpr size_t kBulkSmemMax = 200 * 1024;
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -326,44 +329,50 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                : "memory");
 }
 
-size_t nvfp4_bulk_smem(int K) {
-  return (size_t)16 * (K / 2) + (size_t)16 * (K / 16) + (size_t)kBulkWarps * 2 * 128 * sizeof(float) + 16;
+inline int nvfp4_wpg(int K) { return K <= 1536 ? 1 : 2; }
+
+size_t nvfp4_bulk_smem(int K, int wpg) {
+  const int rows = 16 * kBulkWarps / wpg;
+  return (size_t)rows * (K / 2) + (size_t)rows * (K / 16) + (size_t)kBulkWarps * 2 * 128 * sizeof(float) + 16;
 }
 
-template <int EPI, bool OUT_F32>
-__global__ void __launch_bounds__(kBulkThreads, 8) gemv_nvfp4_bulk_kernel(const GemvArgs a) {
+template <int EPI, bool OUT_F32, int WPG>
+__global__ void __launch_bounds__(kBulkThreads) gemv_nvfp4_bulk_kernel(const GemvArgs a) {
   extern __shared__ __align__(16) uint8_t bsm[];
   pdl_wait();
   pdl_trigger();
   constexpr int NT = 2;
+  constexpr int ROWS = 16 * kBulkWarps / WPG;          // features of this CTA
   Seg sg;
   if (!resolve_id(a, sg)) return;       // grouped only: the copy needs the expert id alone
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
+  const int gi = warp / WPG, sub = warp % WPG;         // feature group, K share
   const int K = a.K;
   const int rowb = K / 2, rows_sf = K / 16;
   const int nchunks = K >> 7;
-  const int f0 = blockIdx.x * 16;
-  uint8_t* ws = bsm;                                             // [16][K/2] packed values
-  uint8_t* ss = bsm + 16 * rowb;                                 // [16][K/16] E4M3 scales
-  float* red = reinterpret_cast<float*>(ss + 16 * rows_sf);      // [warps][NT][128]
+  const int fc = blockIdx.x * ROWS;                    // first feature of the CTA
+  const int f0 = fc + 16 * gi;                         // first feature of this warp's group
+  uint8_t* ws = bsm;                                   // [ROWS][K/2] packed values
+  uint8_t* ss = bsm + ROWS * rowb;                     // [ROWS][K/16] E4M3 scales
+  float* red = reinterpret_cast<float*>(ss + ROWS * rows_sf);   // [warps][NT][4][32] (WPG 2)
   uint64_t* bar = reinterpret_cast<uint64_t*>(red + kBulkWarps * NT * 128);
   const uint32_t b = smem_u32(bar);
   if (threadIdx.x == 0) {
     mbar_init(b, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    const uint32_t wbytes = 16u * rowb, sbytes = 16u * rows_sf;
+    const uint32_t wbytes = (uint32_t)ROWS * rowb, sbytes = (uint32_t)ROWS * rows_sf;
     mbar_expect_tx(b, wbytes + sbytes);
-    bulk_g2s(smem_u32(ws), reinterpret_cast<const uint8_t*>(a.W) + sg.id * a.w_seg_stride + (int64_t)f0 * rowb, wbytes,
+    bulk_g2s(smem_u32(ws), reinterpret_cast<const uint8_t*>(a.W) + sg.id * a.w_seg_stride + (int64_t)fc * rowb, wbytes,
              b);
-    bulk_g2s(smem_u32(ss), a.W_sf + sg.id * a.sf_seg_stride + (int64_t)f0 * rows_sf, sbytes, b);
+    bulk_g2s(smem_u32(ss), a.W_sf + sg.id * a.sf_seg_stride + (int64_t)fc * rows_sf, sbytes, b);
   }
   // the rows, the segment's per-tensor scale and the rows' routing weights
   // load while the weight tile is in flight (an active expert has rows, so no
   // CTA leaves here with its copy outstanding)
   resolve_rows(a, 1 << 30, sg);
   const float gs = a.W_gs ? a.W_gs[sg.id] : 1.f;
-  __shared__ float wrs[2][16];
+  __shared__ float wrs[1][16];
   if (EPI == EPI_SCALE && threadIdx.x < min(sg.nrows, 16)) wrs[0][threadIdx.x] = route_weight(a, sg.row0 + threadIdx.x);
   __syncthreads();
   bool ok = mbar_try(b, 0);
@@ -383,10 +392,18 @@ __global__ void __launch_bounds__(kBulkThreads, 8) gemv_nvfp4_bulk_kernel(const 
     }
     return;
   }
+  const uint8_t* wrow = ws + (16 * gi) * rowb;
+  const uint8_t* srow = ss + (16 * gi) * rows_sf;
 
-  for (int p0 = 0, pi = 0; p0 < sg.nrows; p0 += NT * 8, ++pi) {
+  for (int p0 = 0; p0 < sg.nrows; p0 += NT * 8) {
     const int prow = min(sg.nrows - p0, NT * 8);
-    if (EPI == EPI_SCALE && pi > 0 && threadIdx.x < prow) wrs[pi & 1][threadIdx.x] = route_weight(a, sg.row0 + p0 + threadIdx.x);
+    if (p0 > 0) {
+      // every warp has finished the previous pass (its epilogue read wrs, its
+      // partial sums were read from red)
+      __syncthreads();
+      if (EPI == EPI_SCALE && threadIdx.x < prow) wrs[0][threadIdx.x] = route_weight(a, sg.row0 + p0 + threadIdx.x);
+      __syncthreads();
+    }
     const bf16* xr[NT];
     bool xv[NT];
 #pragma unroll
@@ -397,71 +414,91 @@ __global__ void __launch_bounds__(kBulkThreads, 8) gemv_nvfp4_bulk_kernel(const 
       if (xv[j]) row = a.gather ? a.gather[sg.row0 + p0 + r] : (sg.row0 + p0 + r);
       xr[j] = reinterpret_cast<const bf16*>(a.X) + row * a.x_ld + 32 * t4;
     }
+    const bool two = prow > 8;
     float acc[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-
-    for (int cc = warp; cc < nchunks; cc += kBulkWarps) {
-      const uint4 A0 = *reinterpret_cast<const uint4*>(ws + g * rowb + cc * 64 + 16 * t4);
-      const uint4 A1 = *reinterpret_cast<const uint4*>(ws + (g + 8) * rowb + cc * 64 + 16 * t4);
-      const uint32_t S0 = *reinterpret_cast<const uint16_t*>(ss + g * rows_sf + cc * 8 + 2 * t4);
-      const uint32_t S1 = *reinterpret_cast<const uint16_t*>(ss + (g + 8) * rows_sf + cc * 8 + 2 * t4);
+    // activations of the first chunk; later chunks load one chunk ahead
+    uint4 B0[4], B1[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) B0[q] = B1[q] = make_uint4(0, 0, 0, 0);
+    if (sub < nchunks) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (xv[0]) B0[q] = ldg_keep(xr[0] + sub * 128 + 8 * q);
+        if (two && xv[1]) B1[q] = ldg_keep(xr[1] + sub * 128 + 8 * q);
+      }
+    }
+    for (int cc = sub; cc < nchunks; cc += WPG) {
+      const int cn = cc + WPG;
+      uint4 N0[4], N1[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        N0[q] = N1[q] = make_uint4(0, 0, 0, 0);
+        if (cn < nchunks) {
+          if (xv[0]) N0[q] = ldg_keep(xr[0] + cn * 128 + 8 * q);
+          if (two && xv[1]) N1[q] = ldg_keep(xr[1] + cn * 128 + 8 * q);
+        }
+      }
+      const uint4 A0 = *reinterpret_cast<const uint4*>(wrow + g * rowb + cc * 64 + 16 * t4);
+      const uint4 A1 = *reinterpret_cast<const uint4*>(wrow + (g + 8) * rowb + cc * 64 + 16 * t4);
+      const uint32_t S0 = *reinterpret_cast<const uint16_t*>(srow + g * rows_sf + cc * 8 + 2 * t4);
+      const uint32_t S1 = *reinterpret_cast<const uint16_t*>(srow + (g + 8) * rows_sf + cc * 8 + 2 * t4);
       const uint32_t s0 = e4m3x2_to_f16x2(S0), s1 = e4m3x2_to_f16x2(S1);
       const uint32_t sc0[2] = {__byte_perm(s0, 0, 0x1010), __byte_perm(s0, 0, 0x3232)};
       const uint32_t sc1[2] = {__byte_perm(s1, 0, 0x1010), __byte_perm(s1, 0, 0x3232)};
-      uint32_t fa[8][4];
       const uint32_t w0[4] = {A0.x, A0.y, A0.z, A0.w};
       const uint32_t w1[4] = {A1.x, A1.y, A1.z, A1.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t p0v[4], p1v[4];
-        e2m1x8_to_f16x2(w0[q], p0v);
-        e2m1x8_to_f16x2(w1[q], p1v);
+        e2m1x8_to_f16x2(w0[q], p0v);     // values 8q .. 8q+7 of row g
+        e2m1x8_to_f16x2(w1[q], p1v);     // of row g+8
         const int h = q >> 1;
-        fa[2 * q][0] = hmul2_f16(p0v[0], sc0[h]);
-        fa[2 * q][2] = hmul2_f16(p0v[1], sc0[h]);
-        fa[2 * q][1] = hmul2_f16(p1v[0], sc1[h]);
-        fa[2 * q][3] = hmul2_f16(p1v[1], sc1[h]);
-        fa[2 * q + 1][0] = hmul2_f16(p0v[2], sc0[h]);
-        fa[2 * q + 1][2] = hmul2_f16(p0v[3], sc0[h]);
-        fa[2 * q + 1][1] = hmul2_f16(p1v[2], sc1[h]);
-        fa[2 * q + 1][3] = hmul2_f16(p1v[3], sc1[h]);
+        // MMA 2q: values 8q..8q+3, MMA 2q+1: 8q+4..8q+7 (this thread's k slots)
+        const uint32_t fa0[4] = {hmul2_f16(p0v[0], sc0[h]), hmul2_f16(p1v[0], sc1[h]), hmul2_f16(p0v[1], sc0[h]),
+                                 hmul2_f16(p1v[1], sc1[h])};
+        const uint32_t fa1[4] = {hmul2_f16(p0v[2], sc0[h]), hmul2_f16(p1v[2], sc1[h]), hmul2_f16(p0v[3], sc0[h]),
+                                 hmul2_f16(p1v[3], sc1[h])};
+        mma_f16_16816(acc[0], fa0[0], fa0[1], fa0[2], fa0[3], bf16x2_to_f16x2(B0[q].x), bf16x2_to_f16x2(B0[q].y));
+        mma_f16_16816(acc[0], fa1[0], fa1[1], fa1[2], fa1[3], bf16x2_to_f16x2(B0[q].z), bf16x2_to_f16x2(B0[q].w));
+        if (two) {
+          mma_f16_16816(acc[1], fa0[0], fa0[1], fa0[2], fa0[3], bf16x2_to_f16x2(B1[q].x), bf16x2_to_f16x2(B1[q].y));
+          mma_f16_16816(acc[1], fa1[0], fa1[1], fa1[2], fa1[3], bf16x2_to_f16x2(B1[q].z), bf16x2_to_f16x2(B1[q].w));
+        }
       }
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        if (j * 8 >= prow) continue;
-        uint4 B[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) B[q] = xv[j] ? ldg_keep(xr[j] + cc * 128 + 8 * q) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4& Bq = B[i >> 1];
-          const uint32_t bb0 = bf16x2_to_f16x2((i & 1) ? Bq.z : Bq.x);
-          const uint32_t bb1 = bf16x2_to_f16x2((i & 1) ? Bq.w : Bq.y);
-          mma_f16_16816(acc[j], fa[i][0], fa[i][1], fa[i][2], fa[i][3], bb0, bb1);
-        }
+      for (int q = 0; q < 4; ++q) {
+        B0[q] = N0[q];
+        B1[q] = N1[q];
       }
     }
 
     // acc[j][0]: (feature g, row 2t), [1]: (g, 2t+1), [2]: (g+8, 2t), [3]: (g+8, 2t+1)
-    if (p0 > 0) __syncthreads();      // previous pass has finished reading red
+    if (WPG > 1) {
+      if (sub != 0) {
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      float* rw = red + (warp * NT + j) * 128;
-      rw[g * 8 + 2 * t4] = acc[j][0];
-      rw[g * 8 + 2 * t4 + 1] = acc[j][1];
-      rw[(g + 8) * 8 + 2 * t4] = acc[j][2];
-      rw[(g + 8) * 8 + 2 * t4 + 1] = acc[j][3];
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) red[((warp * NT + j) * 4 + i) * 32 + lane] = acc[j][i];
+      }
+      __syncthreads();
     }
-    __syncthreads();
-    for (int o = threadIdx.x; o < NT * 128; o += kBulkThreads) {
-      const int j = o >> 7, idx = o & 127;
-      const int f = idx >> 3, r = j * 8 + (idx & 7);
-      if (r < prow) {
-        float v = 0.f;
+    if (sub == 0) {
 #pragma unroll
-        for (int w = 0; w < kBulkWarps; ++w) v += red[(w * NT + j) * 128 + idx];
-        epilogue_pre<EPI, OUT_F32, false>(a, sg.row0 + p0 + r, f0 + f, v, gs, EPI == EPI_SCALE ? wrs[pi & 1][r] : 0.f);
+      for (int j = 0; j < NT; ++j) {
+        float v[4] = {acc[j][0], acc[j][1], acc[j][2], acc[j][3]};
+#pragma unroll
+        for (int w = 1; w < WPG; ++w)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[i] += red[(((warp + w) * NT + j) * 4 + i) * 32 + lane];
+        const int r0 = j * 8 + 2 * t4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = r0 + (i & 1), f = f0 + g + (i >> 1) * 8;
+          if (r < prow)
+            epilogue_pre<EPI, OUT_F32, false>(a, sg.row0 + p0 + r, f, v[i], gs, EPI == EPI_SCALE ? wrs[0][r] : 0.f);
+        }
       }
     }
   }
@@ -519,27 +556,36 @@ cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_
     }
     return cudaGetLastError();
   }
-  const bool bulk_ok = a.offsets && nvfp4_bulk_smem(a.K) <= kBulkSmemMax &&
+  const int wpg = nvfp4_wpg(a.K);
+  const bool bulk_ok = a.offsets && nvfp4_bulk_smem(a.K, wpg) <= kBulkSmemMax && (a.N % (64 / wpg)) == 0 &&
                        !(reinterpret_cast<uintptr_t>(a.W) & 15) && !(reinterpret_cast<uintptr_t>(a.W_sf) & 15);
   if (wfmt == WF_NVFP4 && act == MOE_DT_BF16 && bulk_ok) {
-    // one CTA per 16 features of each active segment, weight tile bulk-copied
-    const size_t smem = nvfp4_bulk_smem(a.K);
+    // one CTA per 64 / WPG features of each active segment, weight tile bulk-copied
+    const size_t smem = nvfp4_bulk_smem(a.K, wpg);
     static bool attr_set = false;
     if (!attr_set) {
-      cudaError_t e1 = cudaFuncSetAttribute(gemv_nvfp4_bulk_kernel<EPI_RELU2, false>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmemMax);
-      cudaError_t e2 = cudaFuncSetAttribute(gemv_nvfp4_bulk_kernel<EPI_SCALE, true>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmemMax);
-      if (e1 != cudaSuccess) return e1;
-      if (e2 != cudaSuccess) return e2;
+      const void* ks[4] = {(const void*)gemv_nvfp4_bulk_kernel<EPI_RELU2, false, 1>,
+                           (const void*)gemv_nvfp4_bulk_kernel<EPI_RELU2, false, 2>,
+                           (const void*)gemv_nvfp4_bulk_kernel<EPI_SCALE, true, 1>,
+                           (const void*)gemv_nvfp4_bulk_kernel<EPI_SCALE, true, 2>};
+      for (const void* k : ks) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmemMax);
+        if (e != cudaSuccess) return e;
+      }
       attr_set = true;
     }
-    dim3 grid((unsigned)(a.N / 16), segs, 1);
-    switch (epi) {
-      case EPI_RELU2: launch_k(gemv_nvfp4_bulk_kernel<EPI_RELU2, false>, grid, kBulkThreads, smem, s, a); break;
-      case EPI_SCALE: launch_k(gemv_nvfp4_bulk_kernel<EPI_SCALE, true>, grid, kBulkThreads, smem, s, a); break;
-      default: return cudaErrorNotSupported;
+    dim3 grid((unsigned)(a.N / (64 / wpg)), segs, 1);
+#define MOE_NVB(E_, F_, W_) launch_k(gemv_nvfp4_bulk_kernel<E_, F_, W_>, grid, kBulkThreads, smem, s, a)
+    if (epi == EPI_RELU2) {
+      if (wpg == 1) MOE_NVB(EPI_RELU2, false, 1);
+      else MOE_NVB(EPI_RELU2, false, 2);
+    } else if (epi == EPI_SCALE) {
+      if (wpg == 1) MOE_NVB(EPI_SCALE, true, 1);
+      else MOE_NVB(EPI_SCALE, true, 2);
+    } else {
+      return cudaErrorNotSupported;
     }
+#undef MOE_NVB
     return cudaGetLastError();
   }
   if (wfmt == WF_NVFP4 && act == MOE_DT_BF16) {
