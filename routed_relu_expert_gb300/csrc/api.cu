@@ -284,7 +284,7 @@ moe_status_t run_shared(const moe_config_t* c, int T, const void* x, const moe_w
 // router -> dispatch -> experts chain on the caller's stream.
 struct AuxStream {
   cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, latent = nullptr;
 };
 constexpr int kMaxDevices = 64;
 std::mutex g_aux_mutex;
@@ -298,6 +298,7 @@ bool aux_stream(AuxStream** out) {
     if (cudaStreamCreateWithFlags(&a.s, cudaStreamNonBlocking) != cudaSuccess) return false;
     if (cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess) return false;
     if (cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) return false;
+    if (cudaEventCreateWithFlags(&a.latent, cudaEventDisableTiming) != cudaSuccess) return false;
   }
   *out = &a;
   return true;
@@ -452,25 +453,26 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
   Ptrs P{(char*)ws, make_layout(cfg, T)};
   cudaStream_t s = (cudaStream_t)stream;
   CU(cudaMemsetAsync(P.hdr(), 0, sizeof(WsHeader), s));
-  // fork: the shared expert runs on the auxiliary stream
+  // fork: the latent down projection and the shared expert run on the
+  // auxiliary stream, the router and the selection on the caller's stream
   const bool shared = cfg->d_shared > 0;
+  const bool latent = cfg->d_latent > 0;
   float* ys = P.at<float>(P.L.ys);
+  const void* x_e = latent ? P.at<void>(P.L.x_l) : x;
   std::unique_lock<std::mutex> aux_lock(g_aux_mutex);
   AuxStream* aux = nullptr;
-  if (shared) {
+  if (shared || latent) {
     if (!aux_stream(&aux)) return MOE_ERR_CUDA;
     CU(cudaEventRecord(aux->fork, s));
     CU(cudaStreamWaitEvent(aux->s, aux->fork, 0));
-    if ((st = run_shared_to_f32(cfg, T, x, w, ys, P, aux->s)) != MOE_OK) return st;
+    if (latent) {
+      if ((st = run_latent_down(cfg, T, x, w, const_cast<void*>(x_e), aux->s)) != MOE_OK) return st;
+      CU(cudaEventRecord(aux->latent, aux->s));
+    }
+    if (shared && (st = run_shared_to_f32(cfg, T, x, w, ys, P, aux->s)) != MOE_OK) return st;
     CU(cudaEventRecord(aux->join, aux->s));
   }
   aux_lock.unlock();
-  const void* x_e = x;
-  if (cfg->d_latent > 0) {
-    void* xl = P.at<void>(P.L.x_l);
-    if ((st = run_latent_down(cfg, T, x, w, xl, s)) != MOE_OK) return st;
-    x_e = xl;
-  }
   float* logits = logits_out ? logits_out : P.at<float>(P.L.logits);
   float* scores = scores_out ? scores_out : P.at<float>(P.L.scores);
   int32_t* ids = topk_ids_out ? topk_ids_out : P.at<int32_t>(P.L.ids);
@@ -489,22 +491,24 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
     CU(launch_select_dispatch(sa, da, s));       // a few tokens: one kernel
   } else {
     CU(launch_select(sa, s));
+    if (latent && x_packed) CU(cudaStreamWaitEvent(s, aux->latent, 0));   // the pack reads the latent rows
     CU(launch_dispatch(da, s));
   }
+  if (latent && !x_packed) CU(cudaStreamWaitEvent(s, aux->latent, 0));    // the up GEMV reads them
   void* h = P.at<void>(P.L.h);
   if ((st = run_up(cfg, T, x_e, x_packed, rt, offsets, w, h, P, s)) != MOE_OK) return st;
   float* u = P.at<float>(P.L.u);
   if ((st = run_down(cfg, T, h, offsets, rt, rs, topw, w, u, P, s)) != MOE_OK) return st;
   if (cfg->d_latent == 0) {
     // join, then y = act(sum of routed rows + y_s): the same two FP32 terms, one rounding
-    if (shared) CU(cudaStreamWaitEvent(s, aux->join, 0));
+    if (aux) CU(cudaStreamWaitEvent(s, aux->join, 0));
     CU(launch_combine(u, tsr, T, cfg->top_k, de_of(cfg), nullptr, y, cfg->act_dtype, s, shared ? ys : nullptr));
     return MOE_OK;
   }
   // latent: combined latent rows rounded once, then latent up + y_s
   void* y_rl = P.at<void>(P.L.y_rl);
   CU(launch_combine(u, tsr, T, cfg->top_k, de_of(cfg), nullptr, y_rl, cfg->act_dtype, s));
-  if (shared) CU(cudaStreamWaitEvent(s, aux->join, 0));
+  if (aux) CU(cudaStreamWaitEvent(s, aux->join, 0));
   GemvArgs lu = dense_args(w->w_lat_up, cfg->d_model, cfg->d_latent, y_rl, T, y, cfg->d_model);
   lu.add_src = shared ? ys : nullptr;
   lu.add_ld = cfg->d_model;

@@ -75,18 +75,27 @@ __device__ __forceinline__ void select_token(const float* __restrict__ logits, i
   bool any_nan = false;
   const float* zrow = logits + (int64_t)t * E;
   float* srow = scores + (int64_t)t * E;
+  // every load first (logits, their K parts, the bias), then the arithmetic,
+  // then the stores: interleaved, each store would order the next load behind it
+  float zv[P], bv[P];
+#pragma unroll
+  for (int j = 0; j < P; ++j) {
+    const int e = e0 + j;
+    zv[j] = e < E ? zrow[e] : 0.f;
+    bv[j] = (bias && e < E) ? bias[e] : 0.f;
+  }
+  for (int p = 1; p < nparts; ++p) {
+#pragma unroll
+    for (int j = 0; j < P; ++j)
+      if (e0 + j < E) zv[j] += zrow[p * part_stride + e0 + j];   // K parts added in part order
+  }
 #pragma unroll
   for (int j = 0; j < P; ++j) {
     const int e = e0 + j;
     if (e < E) {
-      // logits split over K parts are added here, in part order
-      float z = zrow[e];
-      for (int p = 1; p < nparts; ++p) z += zrow[p * part_stride + e];
-      if (logits_out) logits_out[(int64_t)t * E + e] = z;
-      const float sv = 1.0f / (1.0f + expf(-z));
+      const float sv = 1.0f / (1.0f + expf(-zv[j]));
       s[j] = sv;
-      srow[e] = sv;
-      const float cv = bias ? sv + bias[e] : sv;
+      const float cv = bias ? sv + bv[j] : sv;
       c[j] = cv;
       key[j] = order_key(cv);
       any_nan |= isnan(cv);
@@ -94,6 +103,14 @@ __device__ __forceinline__ void select_token(const float* __restrict__ logits, i
       s[j] = 0.f;
       c[j] = 0.f;
       key[j] = INT_MIN;  // not an expert: never chosen
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < P; ++j) {
+    const int e = e0 + j;
+    if (e < E) {
+      srow[e] = s[j];
+      if (logits_out) logits_out[(int64_t)t * E + e] = zv[j];
     }
   }
   if (__any_sync(0xffffffffu, any_nan) && lane == 0) set_error(err, MOE_DEVERR_NONFINITE);
