@@ -121,7 +121,9 @@ moe_status_t moe_check_config(const moe_config_t* cfg);
 /* Bytes of device workspace moe_layer_forward needs for T tokens (0 on an
  * invalid configuration).  The same workspace serves every step entry point;
  * its first 256 bytes hold the device error word and the expert schedule that
- * moe_dispatch leaves for moe_experts_up / moe_experts_down_combine. */
+ * moe_dispatch leaves for moe_experts_up / moe_experts_down_combine.  The
+ * error word is sticky: clear it once on a new workspace (zero the first 256
+ * bytes, or moe_clear_device_error) before reading it. */
 size_t moe_workspace_bytes(const moe_config_t* cfg, int32_t T);
 
 /* Step 1: router (page "Nemotron Is Not One Circuit", sections "The Router Is

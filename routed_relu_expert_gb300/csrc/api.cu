@@ -190,8 +190,25 @@ moe_status_t run_dispatch(const moe_config_t* c, int T, const int32_t* ids, cons
   return MOE_OK;
 }
 
+// The NVFP4 decode products take FP16 activations: the expert up and down
+// GEMVs both run the streaming kernel, so the layer hands them FP16 copies
+// (x_e converted once, h written as FP16) instead of converting per use.
+bool up_down_f16(const moe_config_t* c, int T, const moe_weights_t* w) {
+  if (use_tc(c, T) || c->expert_dtype != MOE_DT_NVFP4 || c->act_dtype != MOE_DT_BF16) return false;
+  const int de = de_of(c), I = c->d_expert;
+  GemvArgs up{}, dn{};
+  int32_t dummy = 0;
+  up.offsets = dn.offsets = &dummy;
+  up.W = w->w_up; up.W_sf = w->w_up_sf; up.N = I; up.K = de;
+  dn.W = w->w_down; dn.W_sf = w->w_down_sf; dn.N = de; dn.K = I;
+  return gemv_nvfp4_streams(up) && gemv_nvfp4_streams(dn);
+}
+
+// f16: x_e holds FP16 activations and h receives FP16 (the layer's NVFP4
+// decode path, where up_down_f16() holds)
 moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x_packed, const int32_t* rt,
-                    const int32_t* offsets, const moe_weights_t* w, void* h, const Ptrs& P, cudaStream_t s) {
+                    const int32_t* offsets, const moe_weights_t* w, void* h, const Ptrs& P, cudaStream_t s,
+                    bool f16 = false) {
   const int de = de_of(c), I = c->d_expert;
   const bool fp4 = c->expert_dtype == MOE_DT_NVFP4;
   GemvArgs a{};
@@ -200,6 +217,7 @@ moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x
   a.X = x_packed ? x_packed : x_e; a.x_ld = de; a.gather = x_packed ? nullptr : rt;
   a.offsets = offsets; a.active = P.at<int32_t>(P.L.active); a.hdr = P.hdr();
   a.out = h; a.out_ld = I; a.err = &P.hdr()->err;
+  a.x_f16 = a.out_f16 = f16;
   const int segs = (int)std::min<int64_t>(c->n_experts, (int64_t)T * c->top_k);
   if (use_tc(c, T) && x_packed) {
     const int64_t R = (int64_t)T * c->top_k;
@@ -214,7 +232,7 @@ moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x
 
 moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t* offsets, const int32_t* rt,
                       const int32_t* rs, const float* topw, const moe_weights_t* w, float* u, const Ptrs& P,
-                      cudaStream_t s) {
+                      cudaStream_t s, bool f16 = false) {
   const int de = de_of(c), I = c->d_expert;
   const bool fp4 = c->expert_dtype == MOE_DT_NVFP4;
   GemvArgs a{};
@@ -224,6 +242,7 @@ moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t
   a.offsets = offsets; a.active = P.at<int32_t>(P.L.active); a.hdr = P.hdr();
   a.out = u; a.out_ld = de;
   a.topw = topw; a.route_token = rt; a.route_slot = rs; a.top_k = c->top_k; a.err = &P.hdr()->err;
+  a.x_f16 = f16;
   const int segs = (int)std::min<int64_t>(c->n_experts, (int64_t)T * c->top_k);
   if (use_tc(c, T)) {
     const int64_t R = (int64_t)T * c->top_k;
@@ -459,16 +478,19 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
   const bool latent = cfg->d_latent > 0;
   float* ys = P.at<float>(P.L.ys);
   const void* x_e = latent ? P.at<void>(P.L.x_l) : x;
+  // NVFP4 decode: FP16 copy of x_e in the (then unused) packed-row buffer
+  const bool f16 = up_down_f16(cfg, T, w);
+  void* x16 = f16 ? P.at<void>(P.L.x_packed) : nullptr;
+  const bool pre = latent || f16;          // work before the expert up projection
   std::unique_lock<std::mutex> aux_lock(g_aux_mutex);
   AuxStream* aux = nullptr;
-  if (shared || latent) {
+  if (shared || pre) {
     if (!aux_stream(&aux)) return MOE_ERR_CUDA;
     CU(cudaEventRecord(aux->fork, s));
     CU(cudaStreamWaitEvent(aux->s, aux->fork, 0));
-    if (latent) {
-      if ((st = run_latent_down(cfg, T, x, w, const_cast<void*>(x_e), aux->s)) != MOE_OK) return st;
-      CU(cudaEventRecord(aux->latent, aux->s));
-    }
+    if (latent && (st = run_latent_down(cfg, T, x, w, const_cast<void*>(x_e), aux->s)) != MOE_OK) return st;
+    if (f16) CU(launch_bf16_to_f16(x_e, (int64_t)T * de_of(cfg), x16, aux->s));
+    if (pre) CU(cudaEventRecord(aux->latent, aux->s));
     if (shared && (st = run_shared_to_f32(cfg, T, x, w, ys, P, aux->s)) != MOE_OK) return st;
     CU(cudaEventRecord(aux->join, aux->s));
   }
@@ -494,11 +516,11 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
     if (latent && x_packed) CU(cudaStreamWaitEvent(s, aux->latent, 0));   // the pack reads the latent rows
     CU(launch_dispatch(da, s));
   }
-  if (latent && !x_packed) CU(cudaStreamWaitEvent(s, aux->latent, 0));    // the up GEMV reads them
+  if (pre && !x_packed) CU(cudaStreamWaitEvent(s, aux->latent, 0));    // the up GEMV reads them
   void* h = P.at<void>(P.L.h);
-  if ((st = run_up(cfg, T, x_e, x_packed, rt, offsets, w, h, P, s)) != MOE_OK) return st;
+  if ((st = run_up(cfg, T, f16 ? x16 : x_e, x_packed, rt, offsets, w, h, P, s, f16)) != MOE_OK) return st;
   float* u = P.at<float>(P.L.u);
-  if ((st = run_down(cfg, T, h, offsets, rt, rs, topw, w, u, P, s)) != MOE_OK) return st;
+  if ((st = run_down(cfg, T, h, offsets, rt, rs, topw, w, u, P, s, f16)) != MOE_OK) return st;
   if (cfg->d_latent == 0) {
     // join, then y = act(sum of routed rows + y_s): the same two FP32 terms, one rounding
     if (aux) CU(cudaStreamWaitEvent(s, aux->join, 0));

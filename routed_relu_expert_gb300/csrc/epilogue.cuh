@@ -4,6 +4,8 @@
 
 #include "internal.h"
 
+#include <cuda_fp16.h>
+
 namespace moe {
 
 template <int EPI, bool OUT_F32, bool ACT_F32>
@@ -34,29 +36,41 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, int seg, int row, in
   }
 }
 
+// The output value before storage, from the per-tensor-scaled accumulation v
+// and, for EPI_SCALE, the row's routing weight wr.
+template <int EPI, bool ACT_F32>
+__device__ __forceinline__ float epi_value(const GemvArgs& a, int row, int f, float v, float wr) {
+  if (EPI == EPI_RELU2) {
+    const float u = ACT_F32 ? fmaxf(v, 0.f) : fmaxf(round_bf16(v), 0.f);
+    return u * u;
+  } else if (EPI == EPI_SCALE) {
+    return wr * v;
+  } else if (EPI == EPI_ADD) {
+    return v + (a.add_src ? a.add_src[(int64_t)row * a.add_ld + f] : 0.f);
+  }
+  return v;
+}
+
 // The same with the segment's per-tensor scale (1 if none) and, for
 // EPI_SCALE, the row's routing weight, both fetched earlier by the caller so
 // that their load latency overlaps the weight stream.
 template <int EPI, bool OUT_F32, bool ACT_F32>
 __device__ __forceinline__ void epilogue_pre(const GemvArgs& a, int row, int f, float v, float gs, float wr) {
-  v *= gs;
+  const float r = epi_value<EPI, ACT_F32>(a, row, f, v * gs, wr);
   const int64_t o = (int64_t)row * a.out_ld + f;
-  float r;
-  if (EPI == EPI_RELU2) {
-    const float u = ACT_F32 ? fmaxf(v, 0.f) : fmaxf(round_bf16(v), 0.f);
-    r = u * u;
-  } else if (EPI == EPI_SCALE) {
-    r = wr * v;
-  } else if (EPI == EPI_ADD) {
-    r = v + (a.add_src ? a.add_src[(int64_t)row * a.add_ld + f] : 0.f);
-  } else {
-    r = v;
-  }
   if (OUT_F32 || ACT_F32) {
     reinterpret_cast<float*>(a.out)[o] = r;
   } else {
     reinterpret_cast<bf16*>(a.out)[o] = __float2bfloat16_rn(r);
   }
+}
+
+// BF16-activation output stored as FP16: the BF16 value itself (exact while
+// inside FP16's range), for a consumer that multiplies in FP16.
+template <int EPI>
+__device__ __forceinline__ void epilogue_pre_f16(const GemvArgs& a, int row, int f, float v, float gs, float wr) {
+  const float r = epi_value<EPI, false>(a, row, f, v * gs, wr);
+  reinterpret_cast<__half*>(a.out)[(int64_t)row * a.out_ld + f] = __float2half_rn(round_bf16(r));
 }
 
 // routing weight of packed row `row` (EPI_SCALE)

@@ -316,7 +316,10 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_nvfp4_kernel(const GemvArgs 
 // as above (hardware E2M1 / E4M3 conversion, exact FP16 scale multiply, same
 // MMA k permutation) while the next chunk's activations load; a group's two
 // partial sums are added in a fixed order.  Row passes of 16 re-read the tile
-// from shared memory.
+// from shared memory.  The activations may come as FP16 (the exact FP16 copy
+// of BF16 values, made once per layer call) so that no CTA converts them
+// again, and the up projection may store its ReLU^2 rows as FP16 copies of
+// their BF16 values for the down projection to read the same way.
 // ---------------------------------------------------------------------------
 constexpr int kBulkWarps = 4;
 constexpr int kBulkThreads = kBulkWarps * 32;
@@ -336,7 +339,12 @@ size_t nvfp4_bulk_smem(int K, int wpg) {
   return (size_t)rows * (K / 2) + (size_t)rows * (K / 16) + (size_t)kBulkWarps * 2 * 128 * sizeof(float) + 16;
 }
 
-template <int EPI, bool OUT_F32, int WPG>
+// an activation pair as the FP16 pair the MMA takes
+template <bool XF16>
+__device__ __forceinline__ uint32_t as_f16x2(uint32_t v) { return XF16 ? v : bf16x2_to_f16x2(v); }
+
+// OUT: 0 = BF16, 1 = FP32, 2 = FP16 copy of the BF16 value; XF16: X is FP16
+template <int EPI, int OUT, bool XF16, int WPG>
 __global__ void __launch_bounds__(kBulkThreads) gemv_nvfp4_bulk_kernel(const GemvArgs a) {
   extern __shared__ __align__(16) uint8_t bsm[];
   pdl_wait();
@@ -404,15 +412,14 @@ __global__ void __launch_bounds__(kBulkThreads) gemv_nvfp4_bulk_kernel(const Gem
       if (EPI == EPI_SCALE && threadIdx.x < prow) wrs[0][threadIdx.x] = route_weight(a, sg.row0 + p0 + threadIdx.x);
       __syncthreads();
     }
-    const bf16* xr[NT];
+    // activation rows of the pass (a lane past the last row loads nothing)
+    const uint16_t* xr[NT];
     bool xv[NT];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      const int r = j * 8 + g;
-      xv[j] = r < prow;
-      int64_t row = 0;
-      if (xv[j]) row = a.gather ? a.gather[sg.row0 + p0 + r] : (sg.row0 + p0 + r);
-      xr[j] = reinterpret_cast<const bf16*>(a.X) + row * a.x_ld + 32 * t4;
+      xv[j] = j * 8 + g < prow;
+      const int64_t row = !xv[j] ? 0 : a.gather ? a.gather[sg.row0 + p0 + j * 8 + g] : (sg.row0 + p0 + j * 8 + g);
+      xr[j] = reinterpret_cast<const uint16_t*>(a.X) + row * a.x_ld + 32 * t4;
     }
     const bool two = prow > 8;
     float acc[NT][4];
@@ -424,20 +431,23 @@ __global__ void __launch_bounds__(kBulkThreads) gemv_nvfp4_bulk_kernel(const Gem
     for (int q = 0; q < 4; ++q) B0[q] = B1[q] = make_uint4(0, 0, 0, 0);
     if (sub < nchunks) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (xv[0]) B0[q] = ldg_keep(xr[0] + sub * 128 + 8 * q);
-        if (two && xv[1]) B1[q] = ldg_keep(xr[1] + sub * 128 + 8 * q);
+      for (int q = 0; q < 4; ++q) B0[q] = xv[0] ? ldg_keep(xr[0] + sub * 128 + 8 * q) : make_uint4(0, 0, 0, 0);
+      if (two) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) B1[q] = xv[1] ? ldg_keep(xr[1] + sub * 128 + 8 * q) : make_uint4(0, 0, 0, 0);
       }
     }
     for (int cc = sub; cc < nchunks; cc += WPG) {
       const int cn = cc + WPG;
       uint4 N0[4], N1[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        N0[q] = N1[q] = make_uint4(0, 0, 0, 0);
-        if (cn < nchunks) {
-          if (xv[0]) N0[q] = ldg_keep(xr[0] + cn * 128 + 8 * q);
-          if (two && xv[1]) N1[q] = ldg_keep(xr[1] + cn * 128 + 8 * q);
+      for (int q = 0; q < 4; ++q) N0[q] = N1[q] = make_uint4(0, 0, 0, 0);
+      if (cn < nchunks) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) N0[q] = xv[0] ? ldg_keep(xr[0] + cn * 128 + 8 * q) : make_uint4(0, 0, 0, 0);
+        if (two) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) N1[q] = xv[1] ? ldg_keep(xr[1] + cn * 128 + 8 * q) : make_uint4(0, 0, 0, 0);
         }
       }
       const uint4 A0 = *reinterpret_cast<const uint4*>(wrow + g * rowb + cc * 64 + 16 * t4);
@@ -460,11 +470,11 @@ __global__ void __launch_bounds__(kBulkThreads) gemv_nvfp4_bulk_kernel(const Gem
                                  hmul2_f16(p1v[1], sc1[h])};
         const uint32_t fa1[4] = {hmul2_f16(p0v[2], sc0[h]), hmul2_f16(p1v[2], sc1[h]), hmul2_f16(p0v[3], sc0[h]),
                                  hmul2_f16(p1v[3], sc1[h])};
-        mma_f16_16816(acc[0], fa0[0], fa0[1], fa0[2], fa0[3], bf16x2_to_f16x2(B0[q].x), bf16x2_to_f16x2(B0[q].y));
-        mma_f16_16816(acc[0], fa1[0], fa1[1], fa1[2], fa1[3], bf16x2_to_f16x2(B0[q].z), bf16x2_to_f16x2(B0[q].w));
+        mma_f16_16816(acc[0], fa0[0], fa0[1], fa0[2], fa0[3], as_f16x2<XF16>(B0[q].x), as_f16x2<XF16>(B0[q].y));
+        mma_f16_16816(acc[0], fa1[0], fa1[1], fa1[2], fa1[3], as_f16x2<XF16>(B0[q].z), as_f16x2<XF16>(B0[q].w));
         if (two) {
-          mma_f16_16816(acc[1], fa0[0], fa0[1], fa0[2], fa0[3], bf16x2_to_f16x2(B1[q].x), bf16x2_to_f16x2(B1[q].y));
-          mma_f16_16816(acc[1], fa1[0], fa1[1], fa1[2], fa1[3], bf16x2_to_f16x2(B1[q].z), bf16x2_to_f16x2(B1[q].w));
+          mma_f16_16816(acc[1], fa0[0], fa0[1], fa0[2], fa0[3], as_f16x2<XF16>(B1[q].x), as_f16x2<XF16>(B1[q].y));
+          mma_f16_16816(acc[1], fa1[0], fa1[1], fa1[2], fa1[3], as_f16x2<XF16>(B1[q].z), as_f16x2<XF16>(B1[q].w));
         }
       }
 #pragma unroll
@@ -496,8 +506,11 @@ __global__ void __launch_bounds__(kBulkThreads) gemv_nvfp4_bulk_kernel(const Gem
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = r0 + (i & 1), f = f0 + g + (i >> 1) * 8;
-          if (r < prow)
-            epilogue_pre<EPI, OUT_F32, false>(a, sg.row0 + p0 + r, f, v[i], gs, EPI == EPI_SCALE ? wrs[0][r] : 0.f);
+          if (r < prow) {
+            const float wr = EPI == EPI_SCALE ? wrs[0][r] : 0.f;
+            if (OUT == 2) epilogue_pre_f16<EPI>(a, sg.row0 + p0 + r, f, v[i], gs, wr);
+            else epilogue_pre<EPI, OUT == 1, false>(a, sg.row0 + p0 + r, f, v[i], gs, wr);
+          }
         }
       }
     }
@@ -534,6 +547,16 @@ __global__ void __launch_bounds__(kThreads) gemv_f32_kernel(const GemvArgs a) {
   }
 }
 
+// FP16 copy of BF16 activations, 8 values per thread
+__global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* x, int64_t n8, uint4* out) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const uint4 v = x[i];
+  out[i] = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+}
+
 template <int EPI, bool OUT_F32>
 cudaError_t pick_nt(const GemvArgs& a, int max_rows, int segs, cudaStream_t s) {
   dim3 grid(a.N / 16, segs, a.offsets ? 1u : (unsigned)ceil_div(max_rows, 16));
@@ -542,6 +565,20 @@ cudaError_t pick_nt(const GemvArgs& a, int max_rows, int segs, cudaStream_t s) {
 }
 
 }  // namespace
+
+bool gemv_nvfp4_streams(const GemvArgs& a) {
+  const int wpg = nvfp4_wpg(a.K);
+  return a.offsets && a.K % 128 == 0 && a.N % (64 / wpg) == 0 && nvfp4_bulk_smem(a.K, wpg) <= kBulkSmemMax &&
+         !(reinterpret_cast<uintptr_t>(a.W) & 15) && !(reinterpret_cast<uintptr_t>(a.W_sf) & 15);
+}
+
+cudaError_t launch_bf16_to_f16(const void* x, int64_t n, void* out, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t v = n / 8;
+  launch_k(bf16_to_f16_kernel, dim3((unsigned)ceil_div(v, 256)), 256, 0, s, reinterpret_cast<const uint4*>(x), v,
+           reinterpret_cast<uint4*>(out));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_f32, int max_rows,
                         int segs, cudaStream_t s) {
@@ -556,38 +593,34 @@ cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_
     }
     return cudaGetLastError();
   }
-  const int wpg = nvfp4_wpg(a.K);
-  const bool bulk_ok = a.offsets && nvfp4_bulk_smem(a.K, wpg) <= kBulkSmemMax && (a.N % (64 / wpg)) == 0 &&
-                       !(reinterpret_cast<uintptr_t>(a.W) & 15) && !(reinterpret_cast<uintptr_t>(a.W_sf) & 15);
-  if (wfmt == WF_NVFP4 && act == MOE_DT_BF16 && bulk_ok) {
+  if (wfmt == WF_NVFP4 && act == MOE_DT_BF16 && gemv_nvfp4_streams(a)) {
     // one CTA per 64 / WPG features of each active segment, weight tile bulk-copied
+    const int wpg = nvfp4_wpg(a.K);
     const size_t smem = nvfp4_bulk_smem(a.K, wpg);
-    static bool attr_set = false;
-    if (!attr_set) {
-      const void* ks[4] = {(const void*)gemv_nvfp4_bulk_kernel<EPI_RELU2, false, 1>,
-                           (const void*)gemv_nvfp4_bulk_kernel<EPI_RELU2, false, 2>,
-                           (const void*)gemv_nvfp4_bulk_kernel<EPI_SCALE, true, 1>,
-                           (const void*)gemv_nvfp4_bulk_kernel<EPI_SCALE, true, 2>};
-      for (const void* k : ks) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmemMax);
-        if (e != cudaSuccess) return e;
-      }
-      attr_set = true;
-    }
-    dim3 grid((unsigned)(a.N / (64 / wpg)), segs, 1);
-#define MOE_NVB(E_, F_, W_) launch_k(gemv_nvfp4_bulk_kernel<E_, F_, W_>, grid, kBulkThreads, smem, s, a)
-    if (epi == EPI_RELU2) {
-      if (wpg == 1) MOE_NVB(EPI_RELU2, false, 1);
-      else MOE_NVB(EPI_RELU2, false, 2);
-    } else if (epi == EPI_SCALE) {
-      if (wpg == 1) MOE_NVB(EPI_SCALE, true, 1);
-      else MOE_NVB(EPI_SCALE, true, 2);
+    void (*k)(GemvArgs) = nullptr;
+#define MOE_NVK(E_, O_, X_) (wpg == 1 ? gemv_nvfp4_bulk_kernel<E_, O_, X_, 1> : gemv_nvfp4_bulk_kernel<E_, O_, X_, 2>)
+    if (epi == EPI_RELU2 && !out_f32) {
+      k = a.out_f16 ? (a.x_f16 ? MOE_NVK(EPI_RELU2, 2, true) : MOE_NVK(EPI_RELU2, 2, false))
+                    : (a.x_f16 ? MOE_NVK(EPI_RELU2, 0, true) : MOE_NVK(EPI_RELU2, 0, false));
+    } else if (epi == EPI_SCALE && out_f32 && !a.out_f16) {
+      k = a.x_f16 ? MOE_NVK(EPI_SCALE, 1, true) : MOE_NVK(EPI_SCALE, 1, false);
     } else {
       return cudaErrorNotSupported;
     }
-#undef MOE_NVB
-    return cudaGetLastError();
+#undef MOE_NVK
+    // (the attribute is set once per kernel; the cache holds the few instantiations)
+    static void (*attr_set[16])(GemvArgs) = {};
+    bool seen = false;
+    for (auto p : attr_set) seen = seen || p == k;
+    if (!seen) {
+      cudaError_t e = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmemMax);
+      if (e != cudaSuccess) return e;
+      for (auto& p : attr_set)
+        if (!p) { p = k; break; }
+    }
+    return launch_k(k, dim3((unsigned)(a.N / (64 / wpg)), segs, 1), kBulkThreads, smem, s, a);
   }
+  if (a.x_f16 || a.out_f16) return cudaErrorNotSupported;
   if (wfmt == WF_NVFP4 && act == MOE_DT_BF16) {
     // one warp per 16 features: a CTA's 8 warps cover 128 features
     dim3 grid((unsigned)ceil_div(a.N / 16, kWarps), segs, 1);

@@ -61,12 +61,23 @@ struct GemvArgs {
   const int32_t* route_slot;
   int top_k;
   int32_t* err;
+  // NVFP4 streaming GEMV only (gemv_nvfp4_streams): X holds FP16 activations
+  // (the exact FP16 copy of BF16 ones); out receives FP16 copies of the
+  // BF16-rounded outputs
+  bool x_f16, out_f16;
 };
 
 // act: MOE_DT_BF16 / MOE_DT_F32 activation type of X and of non-f32 outputs.
 // out_f32: output element type is f32 (else act type).
 cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_f32,
                         int max_rows, int grid_segments, cudaStream_t s);
+
+// true when launch_gemv runs a grouped NVFP4 product (BF16 activations) with
+// the streaming kernel, the one that accepts x_f16 / out_f16
+bool gemv_nvfp4_streams(const GemvArgs& a);
+
+// out[i] = FP16(x[i]) for n BF16 values (n a multiple of 8, 16-byte aligned)
+cudaError_t launch_bf16_to_f16(const void* x, int64_t n, void* out, cudaStream_t s);
 
 // Tensor-core grouped GEMM (tcgen05): same arguments as launch_gemv; X rows must
 // be contiguous (no gather).  w_rows/x_rows: rows of the W and X matrices (TMA

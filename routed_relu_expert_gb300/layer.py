@@ -89,7 +89,9 @@ def new_workspace(cfg: N.MoeConfig, T: int, device="cuda") -> torch.Tensor:
     n = workspace_bytes(cfg, T)
     if n == 0 and T > 0:
         N.check(N.load().moe_check_config(ctypes.byref(cfg)), "moe_workspace_bytes")
-    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+    ws[:256].zero_()    # the header: error word clear, no schedule yet
+    return ws
 
 
 def _ws(ws: torch.Tensor):

@@ -147,7 +147,9 @@ def test_dispatch_is_bit_exact(T, E, K):
 
 
 def test_step_entry_points_reproduce_layer_forward_bit_for_bit():
-    for shape, T in ((SMALL_NANO, 37), (SMALL_SUPER, 13)):
+    # (the NVFP4 layer runs its decode GEMVs on FP16 copies of the activations,
+    # the step entry points on the BF16 tensors: the same values either way)
+    for shape, T in ((SMALL_NANO, 37), (SMALL_SUPER, 13), (SMALL_NVFP4, 9)):
         w = device_weights(shape)
         x = make_x(shape, T, "cuda", 3)
         cfg = M.config_from(shape)
