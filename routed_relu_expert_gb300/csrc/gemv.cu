@@ -326,6 +326,10 @@ constexpr int kBulkThreads = kBulkWarps * 32;
 constexpr uint64_t kBulkWaitNs = 4000000000ull;
 constexpr size_t kBulkSmemMax = 200 * 1024;
 
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
@@ -382,6 +386,18 @@ __global__ void __launch_bounds__(kBulkThreads) gemv_nvfp4_bulk_kernel(const Gem
   const float gs = a.W_gs ? a.W_gs[sg.id] : 1.f;
   __shared__ float wrs[1][16];
   if (EPI == EPI_SCALE && threadIdx.x < min(sg.nrows, 16)) wrs[0][threadIdx.x] = route_weight(a, sg.row0 + threadIdx.x);
+  {
+    // the first pass's activation rows are pulled into L1 while the weight
+    // tile is in flight: every warp reads all of them, chunk by chunk, and a
+    // load that went to L2 each chunk would stall the chunk loop
+    const int lines = K / 64;                          // 128-byte lines of a row (2-byte values)
+    const int n = min(sg.nrows, 16) * lines;
+    for (int i = threadIdx.x; i < n; i += kBulkThreads) {
+      const int r = i / lines;
+      const int64_t row = a.gather ? a.gather[sg.row0 + r] : (sg.row0 + r);
+      prefetch_l1(reinterpret_cast<const uint16_t*>(a.X) + row * a.x_ld + (i - r * lines) * 64);
+    }
+  }
   __syncthreads();
   bool ok = mbar_try(b, 0);
   if (!ok) {
