@@ -190,11 +190,14 @@ moe_status_t run_dispatch(const moe_config_t* c, int T, const int32_t* ids, cons
   return MOE_OK;
 }
 
-// The NVFP4 decode products take FP16 activations: the expert up and down
-// GEMVs both run the streaming kernel, so the layer hands them FP16 copies
-// (x_e converted once, h written as FP16) instead of converting per use.
+// NVFP4 expert products multiply in FP16: the layer hands them FP16 copies of
+// their BF16 input rows (exact inside FP16's range) and has the up projection
+// store h as FP16 copies of its BF16 values, so no CTA converts activations
+// and the tensor-core kernel's two operands share a type.  Decode needs both
+// products on the streaming GEMV kernel; the tensor-core kernels always qualify.
 bool up_down_f16(const moe_config_t* c, int T, const moe_weights_t* w) {
-  if (use_tc(c, T) || c->expert_dtype != MOE_DT_NVFP4 || c->act_dtype != MOE_DT_BF16) return false;
+  if (c->expert_dtype != MOE_DT_NVFP4 || c->act_dtype != MOE_DT_BF16) return false;
+  if (use_tc(c, T)) return true;
   const int de = de_of(c), I = c->d_expert;
   GemvArgs up{}, dn{};
   int32_t dummy = 0;
@@ -221,7 +224,7 @@ moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x
   const int segs = (int)std::min<int64_t>(c->n_experts, (int64_t)T * c->top_k);
   if (use_tc(c, T) && x_packed) {
     const int64_t R = (int64_t)T * c->top_k;
-    // (NVFP4 weights are converted to BF16 inside the tensor-core kernel)
+    // (NVFP4 weights are converted to BF16, or with f16 to FP16, inside the tensor-core kernel)
     CU(launch_gemm_tc(a, EPI_RELU2, false, (int64_t)c->n_experts * I, R, c->n_experts,
                       tc_tile_rows(R / segs, segs, I), s));
     return MOE_OK;
@@ -478,10 +481,12 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
   const bool latent = cfg->d_latent > 0;
   float* ys = P.at<float>(P.L.ys);
   const void* x_e = latent ? P.at<void>(P.L.x_l) : x;
-  // NVFP4 decode: FP16 copy of x_e in the (then unused) packed-row buffer
+  // NVFP4: FP16 expert rows; decode makes an FP16 copy of x_e in the (then
+  // unused) packed-row buffer, prefill packs the rows as FP16
   const bool f16 = up_down_f16(cfg, T, w);
-  void* x16 = f16 ? P.at<void>(P.L.x_packed) : nullptr;
-  const bool pre = latent || f16;          // work before the expert up projection
+  const bool conv = f16 && !use_tc(cfg, T);
+  void* x16 = conv ? P.at<void>(P.L.x_packed) : nullptr;
+  const bool pre = latent || conv;         // work before the expert up projection
   std::unique_lock<std::mutex> aux_lock(g_aux_mutex);
   AuxStream* aux = nullptr;
   if (shared || pre) {
@@ -489,7 +494,7 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
     CU(cudaEventRecord(aux->fork, s));
     CU(cudaStreamWaitEvent(aux->s, aux->fork, 0));
     if (latent && (st = run_latent_down(cfg, T, x, w, const_cast<void*>(x_e), aux->s)) != MOE_OK) return st;
-    if (f16) CU(launch_bf16_to_f16(x_e, (int64_t)T * de_of(cfg), x16, aux->s));
+    if (conv) CU(launch_bf16_to_f16(x_e, (int64_t)T * de_of(cfg), x16, aux->s));
     if (pre) CU(cudaEventRecord(aux->latent, aux->s));
     if (shared && (st = run_shared_to_f32(cfg, T, x, w, ys, P, aux->s)) != MOE_OK) return st;
     CU(cudaEventRecord(aux->join, aux->s));
@@ -507,8 +512,8 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
   int32_t* rs = P.at<int32_t>(P.L.route_slot);
   int32_t* tsr = P.at<int32_t>(P.L.tsr);
   void* x_packed = use_tc(cfg, T) ? P.at<void>(P.L.x_packed) : nullptr;
-  const DispatchArgs da =
-      dispatch_args(cfg, T, ids, x_e, P.at<int32_t>(P.L.counts), offsets, rt, rs, tsr, x_packed, P);
+  DispatchArgs da = dispatch_args(cfg, T, ids, x_e, P.at<int32_t>(P.L.counts), offsets, rt, rs, tsr, x_packed, P);
+  da.pack_f16 = f16 && x_packed;
   if (select_dispatch_fits(T, cfg->top_k, da)) {
     CU(launch_select_dispatch(sa, da, s));       // a few tokens: one kernel
   } else {
@@ -518,7 +523,7 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
   }
   if (pre && !x_packed) CU(cudaStreamWaitEvent(s, aux->latent, 0));    // the up GEMV reads them
   void* h = P.at<void>(P.L.h);
-  if ((st = run_up(cfg, T, f16 ? x16 : x_e, x_packed, rt, offsets, w, h, P, s, f16)) != MOE_OK) return st;
+  if ((st = run_up(cfg, T, conv ? x16 : x_e, x_packed, rt, offsets, w, h, P, s, f16)) != MOE_OK) return st;
   float* u = P.at<float>(P.L.u);
   if ((st = run_down(cfg, T, h, offsets, rt, rs, topw, w, u, P, s, f16)) != MOE_OK) return st;
   if (cfg->d_latent == 0) {

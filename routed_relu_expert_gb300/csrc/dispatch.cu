@@ -11,6 +11,7 @@
 // bases are exclusive scans over (tile, warp) in index order, so route r lands
 // after every earlier route of the same expert: the order is (expert, r) =
 // (expert, token, slot) because a token names an expert at most once.
+#include "nvfp4.cuh"
 #include "select.cuh"
 
 #include <algorithm>
@@ -101,7 +102,9 @@ __device__ void warp_scatter(const int32_t* __restrict__ ids, int r0, int r1, in
 }
 
 // x_packed[j] = x_e[route_token[j]]: one warp per packed row, every 16-byte
-// piece of the row loaded before any is stored.
+// piece of the row loaded before any is stored.  TO_F16: BF16 rows are stored
+// as their FP16 copies (exact inside FP16's range).
+template <bool TO_F16>
 __global__ void __launch_bounds__(256) pack_rows_kernel(const uint4* __restrict__ x_e,
                                                         const int32_t* __restrict__ route_token,
                                                         const int32_t* __restrict__ offsets, int E, int row_vecs,
@@ -120,8 +123,13 @@ __global__ void __launch_bounds__(256) pack_rows_kernel(const uint4* __restrict_
       for (int u = 0; u < U; ++u)
         if (v0 + 32 * u < row_vecs) q[u] = __ldg(src + v0 + 32 * u);
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (v0 + 32 * u < row_vecs) dst[v0 + 32 * u] = q[u];
+      for (int u = 0; u < U; ++u) {
+        if (v0 + 32 * u >= row_vecs) continue;
+        if (TO_F16)
+          q[u] = make_uint4(bf16x2_to_f16x2(q[u].x), bf16x2_to_f16x2(q[u].y), bf16x2_to_f16x2(q[u].z),
+                            bf16x2_to_f16x2(q[u].w));
+        dst[v0 + 32 * u] = q[u];
+      }
     }
   }
 }
@@ -351,8 +359,10 @@ cudaError_t launch_pack(const DispatchArgs& a, cudaStream_t s) {
   if (!a.x_packed || !a.x_e) return cudaSuccess;
   const int R = a.T * a.K;
   const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(R, 8), 16384);
-  launch_k(pack_rows_kernel, grid, 256, 0, s, reinterpret_cast<const uint4*>(a.x_e), a.route_token, a.offsets, a.E,
-                                        a.de * a.elem_bytes / 16, reinterpret_cast<uint4*>(a.x_packed));
+  if (a.pack_f16 && a.elem_bytes != 2) return cudaErrorNotSupported;
+  launch_k(a.pack_f16 ? pack_rows_kernel<true> : pack_rows_kernel<false>, grid, 256, 0, s,
+           reinterpret_cast<const uint4*>(a.x_e), a.route_token, a.offsets, a.E, a.de * a.elem_bytes / 16,
+           reinterpret_cast<uint4*>(a.x_packed));
   return cudaGetLastError();
 }
 

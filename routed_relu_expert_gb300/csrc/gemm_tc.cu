@@ -231,9 +231,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: BF16 A and B (K-major), FP32 D, M x N.
-__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor, kind::f16: BF16 (or, F16, FP16) A and B (K-major),
+// FP32 D, M x N.
+__device__ __forceinline__ uint32_t idesc_f16kind(int M, int N, bool F16) {
+  const uint32_t fmt = F16 ? 0u : 1u;          // operand format: 0 FP16, 1 BF16
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // ---------------------------------------------------------------------------
@@ -278,7 +280,8 @@ __device__ __forceinline__ void decode_tile(int t, const int* prefix, int E, int
 // [row][32 features] and written by one TMA store (a few wide writes instead of
 // 32 two- or four-byte stores per thread); a partial chunk, or an output
 // without a tensor map, is stored element by element.
-template <int EPI, bool OUT_F32>
+// OUT16: BF16-activation output stored as FP16 copies of the BF16 values.
+template <int EPI, bool OUT_F32, bool OUT16>
 __device__ __forceinline__ void tile_epilogue(const GemvArgs& a, const CUtensorMap* out_map, const Tile& ti, int c0,
                                               int f0, int lane, const float* wrow, uint8_t* stg, float (&v)[32]) {
   constexpr bool F32 = OUT_F32 || EPI == EPI_SCALE;
@@ -316,6 +319,8 @@ __device__ __forceinline__ void tile_epilogue(const GemvArgs& a, const CUtensorM
     for (int c = 0; c < 32; ++c) {
       if (F32)
         reinterpret_cast<float*>(stg)[c * 32 + lane] = v[c];
+      else if (OUT16)
+        reinterpret_cast<__half*>(stg)[c * 32 + lane] = __float2half_rn(round_bf16(v[c]));
       else
         reinterpret_cast<bf16*>(stg)[c * 32 + lane] = __float2bfloat16_rn(v[c]);
     }
@@ -330,21 +335,25 @@ __device__ __forceinline__ void tile_epilogue(const GemvArgs& a, const CUtensorM
     const int64_t o = (int64_t)(ti.orow0 + c0 + c) * a.out_ld + f;
     if (F32)
       reinterpret_cast<float*>(a.out)[o] = v[c];
+    else if (OUT16)
+      reinterpret_cast<__half*>(a.out)[o] = __float2half_rn(round_bf16(v[c]));
     else
       reinterpret_cast<bf16*>(a.out)[o] = __float2bfloat16_rn(v[c]);
   }
 }
 
 // FP4A: the A operand (weights) is NVFP4 (a.W packed bytes, a.W_sf E4M3 block
-// scales) and warps 7..10 turn each 128 x 64 stage into BF16 in shared memory
-// (value * block scale, exact), in the 128-byte-swizzled layout TMA would have
+// scales) and the converter warps turn each 128 x 64 stage into BF16 (FP4A 1)
+// or FP16 (FP4A 2: the B rows are FP16 too, and a BF16-activation output is
+// stored as FP16 copies of its BF16 values) in shared memory (value * block
+// scale, exact in either), in the 128-byte-swizzled layout TMA would have
 // written; the per-tensor scale is applied by the epilogue.
-template <int EPI, bool OUT_F32, bool FP4A, int CG>
+template <int EPI, bool OUT_F32, int FP4A, int CG>
 __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, int E, int m_tiles, int bn, int b_period,
                    int tma_out, int ksplit) {
   static_assert(!(FP4A && CG == 2), "NVFP4 weights run on single CTAs");
-  using G = Ring<CG, FP4A>;
+  using G = Ring<CG, (FP4A != 0)>;
   constexpr int NTHR = FP4A ? kThreadsFp4 : kThreads;
   constexpr int STAGES = G::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -530,7 +539,7 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
       for (int t = unit; t < total && ok; t += n_units) {
         Tile ti;
         decode_tile(t, prefix, E, m_tiles, G::TILE_M, bn, a, per_part, ksplit, nkb, ti);
-        const uint32_t idesc = idesc_bf16(G::TILE_M, (ti.rows + 15) & ~15);
+        const uint32_t idesc = idesc_f16kind(G::TILE_M, (ti.rows + 15) & ~15, FP4A == 2);
         if (!mbar_wait<CG == 2>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, a.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN_MAX);
@@ -601,8 +610,9 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
         if (!mbar_wait(rfull_bar(rs), rphase, abort_flag, a.err)) { ok = false; break; }
         const uint4 q = reinterpret_cast<const uint4*>(raw_smem + rs * (BM * (BK / 2)) + r * (BK / 2))[hf];
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.err)) { ok = false; break; }
-        // this half's two block scales as BF16 pairs (exact), one per 16 values
-        const uint32_t s2 = f16x2_to_bf16x2(e4m3x2_to_f16x2((sc_word >> (16 * hf)) & 0xFFFFu));
+        // this half's two block scales as BF16 (FP16) pairs, exact, one per 16 values
+        const uint32_t s16 = e4m3x2_to_f16x2((sc_word >> (16 * hf)) & 0xFFFFu);
+        const uint32_t s2 = FP4A == 2 ? s16 : f16x2_to_bf16x2(s16);
         const uint32_t sc[2] = {__byte_perm(s2, 0, 0x1010), __byte_perm(s2, 0, 0x3232)};
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
         uint8_t* dst = gbase + stage * G::STAGE_BYTES + r * 128;
@@ -610,12 +620,20 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
         for (int c = 0; c < kConvChunks; ++c) {  // 16-byte chunk cc = values 8cc .. 8cc+7
           const int cc = hf * kConvChunks + c;
           uint32_t p[4];
-          e2m1x8_to_bf16x2(w[c], p);
           uint4 o;                               // value x scale: at most 6 significant bits, exact
-          o.x = hmul2_bf16(p[0], sc[c >> 1]);
-          o.y = hmul2_bf16(p[1], sc[c >> 1]);
-          o.z = hmul2_bf16(p[2], sc[c >> 1]);
-          o.w = hmul2_bf16(p[3], sc[c >> 1]);
+          if (FP4A == 2) {
+            e2m1x8_to_f16x2(w[c], p);
+            o.x = hmul2_f16(p[0], sc[c >> 1]);
+            o.y = hmul2_f16(p[1], sc[c >> 1]);
+            o.z = hmul2_f16(p[2], sc[c >> 1]);
+            o.w = hmul2_f16(p[3], sc[c >> 1]);
+          } else {
+            e2m1x8_to_bf16x2(w[c], p);
+            o.x = hmul2_bf16(p[0], sc[c >> 1]);
+            o.y = hmul2_bf16(p[1], sc[c >> 1]);
+            o.z = hmul2_bf16(p[2], sc[c >> 1]);
+            o.w = hmul2_bf16(p[3], sc[c >> 1]);
+          }
           *reinterpret_cast<uint4*>(dst + ((cc ^ (r & 7)) << 4)) = o;
         }
         // order this thread's shared-memory accesses (the raw bytes read, the
@@ -657,7 +675,7 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
       for (int c0 = 0; c0 < ti.rows; c0 += 32) {
         float v[32];
         tmem_ld32(tb + (uint32_t)c0, v);
-        tile_epilogue<EPI, OUT_F32>(a, out_map, ti, c0, f0, lane, wrow, stg, v);
+        tile_epilogue<EPI, OUT_F32, FP4A == 2>(a, out_map, ti, c0, f0, lane, wrow, stg, v);
       }
       // TMEM reads are complete (tcgen05.wait::ld); the stores need no ordering
       // with the next MMAs, so the peer's arrive is relaxed
@@ -836,11 +854,11 @@ int max_pairs(K kernel, size_t smem, int threads) {
   return n;
 }
 
-template <int EPI, bool OUT_F32, bool FP4A, int CG>
+template <int EPI, bool OUT_F32, int FP4A, int CG>
 cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, int bn, int b_period, int units,
                      int tma_out, int ksplit, cudaStream_t s) {
   auto kernel = tc_gemm_kernel<EPI, OUT_F32, FP4A, CG>;
-  const size_t smem = smem_bytes<CG, FP4A>(kMaxSegments);
+  const size_t smem = smem_bytes<CG, (FP4A != 0)>(kMaxSegments);
   const int threads = FP4A ? kThreadsFp4 : kThreads;
   static int unit_cap = -1;           // CTAs (CG 1) or CTA pairs (CG 2) resident at once
   if (unit_cap < 0) {
@@ -873,28 +891,37 @@ cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, 
   return cudaLaunchKernelEx(&cfg, kernel, maps, a, E, m_tiles, bn, b_period, tma_out, ksplit);
 }
 
+// fp4: 0 BF16 weights, 1 NVFP4 weights with BF16 operands, 2 NVFP4 weights
+// with FP16 operands (FP16 B rows; a ReLU^2 output stored as FP16)
 template <int CG>
-cudaError_t launch_cg(const TcMaps& maps, const GemvArgs& a, int epi, bool out_f32, bool fp4, int E, int m_tiles,
+cudaError_t launch_cg(const TcMaps& maps, const GemvArgs& a, int epi, bool out_f32, int fp4, int E, int m_tiles,
                       int bn, int b_period, int units, int to, int ks, cudaStream_t s) {
   if (fp4) {
     if constexpr (CG == 1) {
+      if (fp4 == 2) {
+        switch (epi) {
+          case EPI_RELU2: return launch_t<EPI_RELU2, false, 2, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
+          case EPI_SCALE: return launch_t<EPI_SCALE, true, 2, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
+          default: return cudaErrorNotSupported;
+        }
+      }
       switch (epi) {
-        case EPI_RELU2: return launch_t<EPI_RELU2, false, true, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
-        case EPI_SCALE: return launch_t<EPI_SCALE, true, true, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
+        case EPI_RELU2: return launch_t<EPI_RELU2, false, 1, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
+        case EPI_SCALE: return launch_t<EPI_SCALE, true, 1, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
         default: return cudaErrorNotSupported;
       }
     }
     return cudaErrorNotSupported;
   }
   switch (epi) {
-    case EPI_RELU2: return launch_t<EPI_RELU2, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
-    case EPI_SCALE: return launch_t<EPI_SCALE, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
+    case EPI_RELU2: return launch_t<EPI_RELU2, false, 0, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
+    case EPI_SCALE: return launch_t<EPI_SCALE, true, 0, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
     case EPI_STORE:
-      return out_f32 ? launch_t<EPI_STORE, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s)
-                     : launch_t<EPI_STORE, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
+      return out_f32 ? launch_t<EPI_STORE, true, 0, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s)
+                     : launch_t<EPI_STORE, false, 0, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
     default:
-      return out_f32 ? launch_t<EPI_ADD, true, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s)
-                     : launch_t<EPI_ADD, false, false, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
+      return out_f32 ? launch_t<EPI_ADD, true, 0, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s)
+                     : launch_t<EPI_ADD, false, 0, CG>(maps, a, E, m_tiles, bn, b_period, units, to, ks, s);
   }
 }
 
@@ -925,6 +952,12 @@ cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_r
   if (x_cols <= 0) x_cols = a.K;
   if (x_cols % BK != 0 || a.K % x_cols != 0) return cudaErrorNotSupported;
   const bool fp4 = a.W_sf != nullptr;       // NVFP4 weights: converted in the kernel
+  // FP16 operands: NVFP4 products only, FP16 rows in and, for ReLU^2, out
+  // (the tensor maps move 2-byte elements either way)
+  if (a.x_f16 || a.out_f16) {
+    const bool ok = fp4 && a.x_f16 && (epi == EPI_RELU2 ? a.out_f16 : epi == EPI_SCALE && !a.out_f16);
+    if (!ok) return cudaErrorNotSupported;
+  }
   const int cg = pick_cg(a.N, fp4);
   TcMaps maps;
   int to = 0;
@@ -938,8 +971,9 @@ cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_r
   int units = num_sms() / cg;
   if (!a.offsets) units = (int)std::min<int64_t>(units, ceil_div(a.dense_rows, bn) * m_tiles * ksplit);
   if (units <= 0) return cudaSuccess;
-  if (cg == 2) return launch_cg<2>(maps, a, epi, out_f32, fp4, E, m_tiles, bn, b_period, units, to, ksplit, s);
-  return launch_cg<1>(maps, a, epi, out_f32, fp4, E, m_tiles, bn, b_period, units, to, ksplit, s);
+  const int fmt = fp4 ? (a.x_f16 ? 2 : 1) : 0;
+  if (cg == 2) return launch_cg<2>(maps, a, epi, out_f32, fmt, E, m_tiles, bn, b_period, units, to, ksplit, s);
+  return launch_cg<1>(maps, a, epi, out_f32, fmt, E, m_tiles, bn, b_period, units, to, ksplit, s);
 }
 
 }  // namespace moe

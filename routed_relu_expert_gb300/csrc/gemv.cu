@@ -198,11 +198,6 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
-  __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
 template <int EPI, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 3) gemv_nvfp4_kernel(const GemvArgs a) {
   pdl_wait();

@@ -128,6 +128,7 @@ struct DispatchArgs {
   void* x_packed;           // pack destination [R, de] (nullable)
   int de;
   int elem_bytes;
+  bool pack_f16;            // BF16 rows packed as their FP16 copies
 };
 size_t dispatch_tile_count_elems(int T, int K, int E);
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);

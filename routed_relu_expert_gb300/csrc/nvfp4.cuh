@@ -25,6 +25,12 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t s16) {
   return r;
 }
 
+// BF16 pair -> FP16 pair (exact inside FP16's range)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
 __device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
   __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
