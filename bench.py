@@ -405,9 +405,10 @@ def run_reference(args, rank, world):
     value = 1.0 / s_per_tok
     line = {
         "impl": "reference", "metric": "MoE-layer tokens/s", "value": round(value, 3), "unit": "tokens/s",
-        "n_gpus": 0, "steps": steps_done, "warmup": args.warmup, "ms_per_step": round(s_per_tok * 1e3, 3),
+        "n_gpus": world, "steps": steps_done, "warmup": args.warmup, "ms_per_step": round(s_per_tok * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{shape.name} T={T}", "sample": "one token of the batch per step"},
+        "config": {"workload": f"{shape.name} T={T}", "sample": "one token of the batch per step",
+                   "runs_on": "host cores of rank 0 (the oracle uses no GPU)"},
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                          "sample": f"{steps_done} steps of 1 token ({shape.name}, T={T} batch rows)"},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
