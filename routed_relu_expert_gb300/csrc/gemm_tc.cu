@@ -933,13 +933,33 @@ inline int pick_cg(int N, bool fp4) { return !fp4 && N > BM ? 2 : 1; }
 
 }  // namespace
 
+// Rows per tile: the largest power of two that still gives every unit two
+// tiles (the slack balances ragged segments).  Dense products (one segment,
+// uniform tiles) take instead the height with the least estimated time when it
+// is clearly (15 %) better: waves x per-tile time, a tile's time per 64-deep
+// k-block being the larger of its MMA cycles (128 x bn x 64 x 2 FLOP per SM at
+// ~6,100 FLOP/cycle) and its shared-memory fill cycles ((128 + bn / cg) x
+// 128 B per SM at ~65 B/cycle from L2, the TMA rate measured on this part).
+// Short tiles re-read the weight tile once per row tile; tall ones leave SMs
+// idle when there are few feature tiles (a 1024-feature projection of 4096
+// rows: 64-row tiles read its weights 64 times, 256-row tiles 16 times).
 int tc_tile_rows(int64_t rows_per_seg, int64_t segs, int N) {
   const int cg = pick_cg(N, false);
   const int64_t m_tiles = ceil_div(N, (int64_t)BM * cg);
   const int64_t units = num_sms() / cg;
+  const int64_t rows = std::max<int64_t>(rows_per_seg, 1);
   int bn = BN_MAX;
-  while (bn > 16 && ceil_div(std::max<int64_t>(rows_per_seg, 1), bn) * segs * m_tiles < 2 * units) bn >>= 1;
-  return bn;
+  while (bn > 16 && ceil_div(rows, bn) * segs * m_tiles < 2 * units) bn >>= 1;
+  if (segs > 1) return bn;
+  auto est = [&](int b) {
+    const double mma = 128.0 * b * 128.0 / 6100.0;
+    const double fill = (128.0 + (double)b / cg) * 128.0 / 65.0;
+    return (double)ceil_div(ceil_div(rows, b) * m_tiles, units) * std::max(mma, fill);
+  };
+  int best = bn;
+  for (int b = BN_MAX; b >= 16; b >>= 1)
+    if (est(b) < est(best)) best = b;
+  return est(best) < 0.85 * est(bn) ? best : bn;
 }
 
 cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_rows, int64_t x_rows, int E, int bn,
