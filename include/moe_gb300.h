@@ -206,7 +206,10 @@ moe_status_t moe_shared(const moe_config_t* cfg, int32_t T, const void* x,
  *   x [T, d] in; y [T, d] out (act_dtype).
  *   topk_ids_out [T,K] / topk_w_out [T,K] / logits_out [T,E] / scores_out [T,E]:
  *   optional copies of the router's results (NULL = not written).
- * Clears the device error word first.                                        */
+ * Clears the device error word first.  With NVFP4 experts the expert products
+ * multiply in FP16 (page "NemotronH ...", section "Arithmetic"): their input
+ * rows and h are FP16 copies of the BF16 values, exact for magnitudes up to
+ * 65504; a larger activation there overflows.                               */
 moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x,
                                const moe_weights_t* w, void* y,
                                int32_t* topk_ids_out, float* topk_w_out,
