@@ -68,16 +68,21 @@ __device__ __forceinline__ bool resolve_segment(const GemvArgs& a, int rows_per_
 }
 
 // ---------------------------------------------------------------------------
-// BF16 weights, BF16 activations.  A CTA handles its segment's rows in passes
-// of 16 (two 8-row MMA column blocks); a second pass finds the CTA's weight
-// tile still in L2, so HBM streams each weight once while registers stay low.
+// BF16 weights, BF16 activations.  A CTA owns FPC features (16 or 32): its 8
+// warps form FPC / 16 groups, a group owns 16 features and its warps split K
+// in 32-wide chunks (rows short enough to leave a 16-feature CTA little work
+// take 32 features, halving the CTA count and its fixed costs).  A CTA
+// handles its segment's rows in passes of 16 (two 8-row MMA column blocks); a
+// second pass finds the CTA's weight tile still in L2, so HBM streams each
+// weight once while registers stay low.
 // ---------------------------------------------------------------------------
-template <int EPI, bool OUT_F32>
+template <int EPI, bool OUT_F32, int FPC>
 __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a) {
   pdl_wait();
   pdl_trigger();
   constexpr int NT = 2;                 // 8-row column blocks per pass
   constexpr int U = 4;                  // 32-wide K chunks in flight per warp
+  constexpr int WG = kWarps * 16 / FPC; // warps per 16-feature group (K split)
   __shared__ float red[kWarps][NT][128];
   __shared__ float wrs[2][NT * 8];      // routing weights of a pass's rows (EPI_SCALE)
 
@@ -85,7 +90,8 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a
   if (!resolve_id(a, sg)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
-  const int f0 = blockIdx.x * 16;
+  const int kw = warp % WG;             // this warp's K share within its group
+  const int f0 = blockIdx.x * FPC + 16 * (warp / WG);
   const int K = a.K;
 
   const bf16* W = reinterpret_cast<const bf16*>(a.W) + sg.id * a.w_seg_stride + (int64_t)f0 * K;
@@ -96,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a
   auto load_round = [&](int c) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int cc = c + kWarps * u;
+      const int cc = c + WG * u;
       if (cc < nchunks) {
         A0[u] = ldg_stream(wg + cc * 32);
         A1[u] = ldg_stream(wg8 + cc * 32);
@@ -105,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a
   };
   // the first round of weight loads goes out before the row lookups and
   // gathers below, whose dependent loads would otherwise delay it
-  load_round(warp);
+  load_round(kw);
   // dense products split their 16-row passes over grid.z (CTAs of one feature
   // tile run together, so the tile is read from HBM once; z < ceil(rows/16),
   // so no CTA returns here after loading); grouped ones loop
@@ -130,11 +136,11 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a
 #pragma unroll
     for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
-    for (int c = warp; c < nchunks; c += kWarps * U) {
-      if (p0 > 0 || c != warp) load_round(c);
+    for (int c = kw; c < nchunks; c += WG * U) {
+      if (p0 > 0 || c != kw) load_round(c);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int cc = c + kWarps * u;
+        const int cc = c + WG * u;
         if (cc < nchunks) {
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
@@ -159,14 +165,15 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a
       red[warp][j][(g + 8) * 8 + 2 * t4 + 1] = acc[j][3];
     }
     __syncthreads();
-    for (int o = threadIdx.x; o < NT * 128; o += kThreads) {
-      const int j = o >> 7, idx = o & 127;
+    for (int o = threadIdx.x; o < (FPC / 16) * NT * 128; o += kThreads) {
+      const int gi = o / (NT * 128), j = (o >> 7) % NT, idx = o & 127;
       const int f = idx >> 3, r = j * 8 + (idx & 7);
       if (r < prow) {
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) v += red[w][j][idx];
-        epilogue_pre<EPI, OUT_F32, false>(a, sg.row0 + p0 + r, f0 + f, v, 1.f, EPI == EPI_SCALE ? wrs[pi & 1][r] : 0.f);
+        for (int w = 0; w < WG; ++w) v += red[gi * WG + w][j][idx];
+        epilogue_pre<EPI, OUT_F32, false>(a, sg.row0 + p0 + r, blockIdx.x * FPC + 16 * gi + f, v, 1.f,
+                                          EPI == EPI_SCALE ? wrs[pi & 1][r] : 0.f);
       }
     }
   }
@@ -568,10 +575,16 @@ __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* x, int64_
   out[i] = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
 }
 
+// 32 features per CTA for rows of at most 2048 values (a 16-feature CTA would
+// stream under 64 KB of weights), 16 otherwise
 template <int EPI, bool OUT_F32>
 cudaError_t pick_nt(const GemvArgs& a, int max_rows, int segs, cudaStream_t s) {
-  dim3 grid(a.N / 16, segs, a.offsets ? 1u : (unsigned)ceil_div(max_rows, 16));
-  launch_k(gemv_bf16_kernel<EPI, OUT_F32>, grid, kThreads, 0, s, a);
+  const unsigned z = a.offsets ? 1u : (unsigned)ceil_div(max_rows, 16);
+  if (a.K <= 2048 && a.N % 32 == 0) {
+    launch_k(gemv_bf16_kernel<EPI, OUT_F32, 32>, dim3(a.N / 32, segs, z), kThreads, 0, s, a);
+    return cudaGetLastError();
+  }
+  launch_k(gemv_bf16_kernel<EPI, OUT_F32, 16>, dim3(a.N / 16, segs, z), kThreads, 0, s, a);
   return cudaGetLastError();
 }
 
