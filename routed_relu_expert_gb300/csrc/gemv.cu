@@ -565,6 +565,16 @@ __global__ void __launch_bounds__(kThreads) gemv_f32_kernel(const GemvArgs a) {
   }
 }
 
+// the NVFP4 bulk GEMV's shared-memory limit for both warp splits
+template <int EPI, int OUT, bool XF16>
+cudaError_t bulk_attr() {
+  cudaError_t e = cudaFuncSetAttribute((const void*)gemv_nvfp4_bulk_kernel<EPI, OUT, XF16, 1>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmemMax);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute((const void*)gemv_nvfp4_bulk_kernel<EPI, OUT, XF16, 2>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmemMax);
+}
+
 // FP16 copy of BF16 activations, 8 values per thread
 __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* x, int64_t n8, uint4* out) {
   pdl_wait();
@@ -632,16 +642,15 @@ cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_
       return cudaErrorNotSupported;
     }
 #undef MOE_NVK
-    // (the attribute is set once per kernel; the cache holds the few instantiations)
-    static void (*attr_set[16])(GemvArgs) = {};
-    bool seen = false;
-    for (auto p : attr_set) seen = seen || p == k;
-    if (!seen) {
-      cudaError_t e = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmemMax);
-      if (e != cudaSuccess) return e;
-      for (auto& p : attr_set)
-        if (!p) { p = k; break; }
-    }
+    // every instantiation's shared-memory limit, set once (thread-safe static)
+    static const cudaError_t attr = [] {
+      for (cudaError_t e : {bulk_attr<EPI_RELU2, 0, false>(), bulk_attr<EPI_RELU2, 0, true>(),
+                            bulk_attr<EPI_RELU2, 2, false>(), bulk_attr<EPI_RELU2, 2, true>(),
+                            bulk_attr<EPI_SCALE, 1, false>(), bulk_attr<EPI_SCALE, 1, true>()})
+        if (e != cudaSuccess) return e;
+      return cudaSuccess;
+    }();
+    if (attr != cudaSuccess) return attr;
     return launch_k(k, dim3((unsigned)(a.N / (64 / wpg)), segs, 1), kBulkThreads, smem, s, a);
   }
   if (a.x_f16 || a.out_f16) return cudaErrorNotSupported;
