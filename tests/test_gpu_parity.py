@@ -70,6 +70,11 @@ def test_nano_prefill_2048_sampled():
     _parity(NANO_PREFILL, 2048, sample=192)
 
 
+def test_nano_prefill_8192_sampled():
+    """The bench's prefill size: ids of every token, outputs of a sample."""
+    _parity(NANO_PREFILL, 8192, sample=48)
+
+
 @pytest.mark.parametrize("T", [1, 16])
 def test_super_latent_full_size(T):
     _parity(SUPER_LATENT, T)
@@ -77,6 +82,10 @@ def test_super_latent_full_size(T):
 
 def test_super_latent_256_sampled():
     _parity(SUPER_LATENT, 256, sample=48)
+
+
+def test_super_latent_4096_sampled():
+    _parity(SUPER_LATENT, 4096, sample=24)
 
 
 @pytest.mark.parametrize("T", [1, 9, 64, 65, 200])
