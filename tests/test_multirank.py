@@ -35,7 +35,7 @@ def _worker(rank, world, port, times, out):
 def test_two_ranks_take_the_slowest_rank_and_count_all_tokens(times):
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:   # no fork of a threaded process
         out = mgr.dict()
         mp.spawn(_worker, args=(world, port, times, out), nprocs=world, join=True)
         res = dict(out)
