@@ -23,6 +23,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -228,6 +230,7 @@ def run_ours(args, rank, world, dev):
     ids = torch.empty((T, shape.top_k), dtype=torch.int32, device=dev)
     layers[0].forward(x, y, ids_out=ids)
     n_active = int(torch.unique(ids).numel())
+    routing = routing_stats(ids.cpu().numpy(), shape.n_experts)
     lb = layer_bytes(shape, n_active, T)
     pk = peaks()
 
@@ -306,19 +309,21 @@ def run_ours(args, rank, world, dev):
             idss = torch.empty((Ts, shape.top_k), dtype=torch.int32, device=dev)
             layers[0].forward(xs, ys, ids_out=idss)
             na = int(torch.unique(idss).numel())
+            rst = routing_stats(idss.cpu().numpy(), shape.n_experts)
             bb = layer_bytes(shape, na, Ts)["total"]
             ff = layer_flops(shape, Ts)
             sweep[str(Ts)] = {"ms_per_step": round(mss, 5), "tokens_per_s": round(Ts / (mss / 1e3), 1),
                               "experts_active": na, "hbm_gb_per_s": round(bb / (mss / 1e3) / 1e9, 1),
                               "hbm_frac": round(bb / (mss / 1e3) / 1e9 / pk["hbm_gbs"], 3),
                               "tflops": round(ff / (mss / 1e3) / 1e12, 1),
-                              "tensor_frac": round(ff / (mss / 1e3) / 1e12 / pk["bf16_tflops_sustained"], 3)}
+                              "tensor_frac": round(ff / (mss / 1e3) / 1e12 / pk["bf16_tflops_sustained"], 3),
+                              "routing": rst}
 
     return {
         "value": value, "ms_per_step": ms_step, "n_active": n_active, "bytes": lb, "clocks": clk,
         "launches": launches, "err": err, "ms_eager": ms_eager, "graphs": bool(graphs), "ms_up": ms_up, "up_bytes": up_bytes, "achieved_up": achieved,
         "up_flops": up_flops, "achieved_up_tf": achieved_tf, "flops": layer_flops(shape, T),
-        "up_launches": up_launches,
+        "up_launches": up_launches, "routing": routing,
         "peaks": pk, "e2e_s": e2e_s, "n_rep": n_rep, "sweep": sweep, "shape": shape, "T": T,
         "rep_bytes": one,
     }
@@ -371,6 +376,29 @@ def time_oracle(shape, w, x, budget_s: float, min_tokens: int = 1):
             break
         n = min(2 * n, xn.shape[0] - done_t)
     return done_t / done_s, done_t, done_s
+
+
+def routing_stats(ids, n_experts, tile_rows=128):
+    """Load skew of one batch's routing, from its [T, K] expert ids (the load
+    statistics of page "M6.1 Routed Capacity", section on load balance): routes
+    per expert -> experts with routes, max/mean, CV^2 (variance / mean^2 over
+    all experts), entropy of the route shares normalised by log E, the slope of
+    log(count) against log(rank) over the experts with routes (about -s for a
+    Zipf(s) popularity), and the share of padded rows when every expert's rows
+    are cut into tiles of `tile_rows` (the grouped GEMM's tail waste)."""
+    c = np.bincount(np.asarray(ids).reshape(-1).astype(np.int64), minlength=n_experts).astype(np.float64)
+    total = c.sum()
+    mean = total / n_experts
+    p = c[c > 0] / total
+    srt = np.sort(c[c > 0])[::-1]
+    slope = None
+    if len(srt) >= 3 and srt[0] > srt[-1]:
+        slope = round(float(np.polyfit(np.log(np.arange(1, len(srt) + 1)), np.log(srt), 1)[0]), 3)
+    padded = float((np.ceil(c / tile_rows) * tile_rows).sum())
+    return {"experts_with_routes": int((c > 0).sum()), "max_over_mean": round(float(c.max() / mean), 2),
+            "cv2": round(float(c.var() / mean ** 2), 3),
+            "norm_entropy": round(float(-(p * np.log(p)).sum() / np.log(n_experts)), 3),
+            "loglog_slope": slope, f"tail_waste_{tile_rows}_row_tiles": round(float(1.0 - total / padded), 3)}
 
 
 def cpu_cores():
@@ -478,7 +506,7 @@ def main():
                        "parallelism": f"replicas x{world}",
                        "l2": f"weights rotate over {r['n_rep']} seeded replicas "
                              f"({r['rep_bytes'] / 1e9:.2f} GB each); no step reads the previous step's weights",
-                       "experts_active": r["n_active"]},
+                       "experts_active": r["n_active"], "routing": r["routing"]},
             "roofline": roof,
             "layer_roofline": {"bound": "tensor" if layer_tensor else "hbm", "bytes_per_step": int(lb["total"]),
                                "flops_per_step": int(r["flops"]),

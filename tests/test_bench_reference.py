@@ -33,3 +33,22 @@ def test_reference_line_has_the_contract_keys():
 
 def test_reference_arm_runs_on_rank_zero_only():
     assert bench.run_reference(_args(), 1, 2) is None
+
+
+def test_routing_stats_of_uniform_and_zipf_loads():
+    import json
+
+    import numpy as np
+    E = 128
+    flat = bench.routing_stats(np.repeat(np.arange(E), 6).reshape(-1, 6), E)
+    assert flat["experts_with_routes"] == E and flat["max_over_mean"] == 1.0
+    assert flat["cv2"] == 0.0 and flat["norm_entropy"] == 1.0 and flat["loglog_slope"] is None
+    # 6 rows per expert in 128-row tiles: 122 of every 128 rows are padding
+    assert flat["tail_waste_128_row_tiles"] == round(1 - 6 / 128, 3)
+    rng = np.random.default_rng(0)
+    w = 1.0 / np.arange(1, E + 1) ** 1.1
+    ids = rng.choice(E, size=(20000, 1), p=w / w.sum())
+    z = bench.routing_stats(ids, E)
+    assert -1.3 < z["loglog_slope"] < -0.9          # about -s for Zipf(s = 1.1)
+    assert z["max_over_mean"] > 10 and 0.5 < z["norm_entropy"] < 0.9
+    json.dumps(z)                                    # plain JSON types
