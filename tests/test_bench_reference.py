@@ -52,3 +52,24 @@ def test_routing_stats_of_uniform_and_zipf_loads():
     assert -1.3 < z["loglog_slope"] < -0.9          # about -s for Zipf(s = 1.1)
     assert z["max_over_mean"] > 10 and 0.5 < z["norm_entropy"] < 0.9
     json.dumps(z)                                    # plain JSON types
+
+
+def test_roofline_numerators_match_the_worked_ledgers():
+    """The bench's algorithmic bytes and FLOPs per step against the per-unit
+    figures worked out by hand for the five workloads: one Nano expert is
+    2 x 1856 x 2688 x 2 B, one Super NVFP4 expert block 3,096,576 B (page
+    "Nemotron-3.5-Super 120B on an 8 GB GPU") plus its two FP32 tensor scales."""
+    from synth import NANO_DECODE, SUPER_LATENT, SUPER_NVFP4, TINY_FP32
+    nano = bench.layer_bytes(NANO_DECODE, 6, 1)
+    assert nano["experts"] == 6 * 19_955_712
+    assert nano["shared"] == 39_911_424 and nano["router"] == 1_376_768
+    assert nano["total"] == 161_033_216
+    sup = bench.layer_bytes(SUPER_LATENT, 22, 1)
+    assert sup["experts"] == 22 * 11_010_048 and sup["shared"] == 88_080_384
+    assert sup["latent"] == 16_777_216 and sup["router"] == 8_390_656
+    assert sup["total"] == 355_485_696
+    fp4 = bench.layer_bytes(SUPER_NVFP4, 22, 1)
+    assert fp4["experts"] == 22 * (3_096_576 + 8)
+    assert fp4["total"] == 181_389_488
+    assert bench.layer_flops(SUPER_LATENT, 1) == 351_272_960
+    assert bench.layer_flops(TINY_FP32, 16) == 16 * 528_384
