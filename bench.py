@@ -1,20 +1,26 @@
 #!/usr/bin/env python
 """Benchmark of the routed ReLU^2 MoE layer on GB300: MoE-layer tokens/s and the
-fraction of the HBM roofline reached.
+fraction of the HBM roofline (decode) or of the dense tensor peak (prefill)
+reached.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload nano_decode] [--tokens 64]
+                    [--workload nano_decode] [--tokens 64] [--points all|none|<workload>]
 
 A step is one full layer forward (router, dispatch, experts up, experts down,
 combine, shared expert; latent projections for latent shapes) over one batch
 of T synthetic tokens.  Weights come in several seeded replicas that the steps
 rotate through, so no step finds the previous step's weights in L2.  Prints
-one JSON line (rank 0).  Multi-GPU (torchrun): every rank runs its own layer
-replica on its own tokens (no collective on the data path; weak scaling).
+one JSON line (rank 0): the headline workload (Nano decode, T = 64) with its
+dominant kernel's roofline, the end-to-end figure through the host-buffer
+entry point and the oracle on the host cores, plus ``per_workload``: every
+workload at every token count it is defined for.  Multi-GPU (torchrun): every
+rank runs its own layer replica on its own tokens (no collective on the data
+path; weak scaling).
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -29,9 +35,17 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 2 ** 20
+CSRC = os.path.join(ROOT, "routed_relu_expert_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.md")
+# the sources a kernel family is compiled from: a recorded DRAM traffic figure
+# holds only while their hash is unchanged
+KERNEL_SOURCES = {
+    "gemv": ("gemv.cu", "epilogue.cuh", "nvfp4.cuh", "common.cuh", "internal.h"),
+    "tc": ("gemm_tc.cu", "epilogue.cuh", "nvfp4.cuh", "common.cuh", "internal.h"),
+}
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
@@ -41,9 +55,10 @@ def parse():
     ap.add_argument("--tokens", type=int, default=64)
     ap.add_argument("--replicas", type=int, default=0, help="weight replicas (0 = enough to defeat L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--sweep", action="store_true", help="also time every token count of the workload")
+    ap.add_argument("--points", default="all",
+                    help="per_workload entries: all, none, or one workload name")
     ap.add_argument("--eager", action="store_true", help="time eager calls instead of CUDA-graph replays")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 # ---------------------------------------------------------------------------
@@ -58,7 +73,7 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    """nvidia-smi clock / throttle-reason samples while a timed region runs."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -125,17 +140,22 @@ def job_throughput(tokens_per_rank: int, world: int, seconds: float) -> float:
 
 
 # ---------------------------------------------------------------------------
+def expert_bytes(shape) -> int:
+    """HBM bytes of one routed expert (up + down; NVFP4: values, block scales
+    and the two FP32 per-tensor scales)."""
+    de, I = shape.d_e, shape.d_expert
+    if shape.expert_dtype == 2:
+        return 2 * (I * de // 2 + I * de // 16) + 8
+    return 2 * I * de * (4 if shape.expert_dtype == 0 else 2)
+
+
 def layer_bytes(shape, n_active: int, T: int) -> dict:
     """Algorithmic HBM bytes of one layer step: weights of the experts that
     received routes, shared expert, router, latent pair, and the activations in
     and out."""
     ab = 4 if shape.act_dtype == 0 else 2
-    de, I, d, S, E = shape.d_e, shape.d_expert, shape.d_model, shape.d_shared, shape.n_experts
-    if shape.expert_dtype == 2:
-        expert = 2 * (I * de // 2 + I * de // 16) + 8
-    else:
-        expert = 2 * I * de * (4 if shape.expert_dtype == 0 else 2)
-    b = {"experts": n_active * expert, "shared": 2 * d * S * ab, "router": E * d * 4 + E * 4,
+    de, d, S, E = shape.d_e, shape.d_model, shape.d_shared, shape.n_experts
+    b = {"experts": n_active * expert_bytes(shape), "shared": 2 * d * S * ab, "router": E * d * 4 + E * 4,
          "latent": 2 * d * shape.d_latent * ab, "activations": 2 * T * d * ab}
     b["total"] = sum(b.values())
     return b
@@ -147,235 +167,19 @@ def layer_flops(shape, T: int) -> int:
     return per_tok * T
 
 
-def run_ours(args, rank, world, dev):
-    import torch
-    import __graft_entry__
-    __graft_entry__.build()
-    import routed_relu_expert_gb300 as M
-    from synth import WORKLOADS, make_weights, make_x
-
-    shape = WORKLOADS[args.workload]
-    T = args.tokens
-    cfg = M.config_from(shape)
-    one = layer_bytes(shape, shape.n_experts, T)["total"]     # one replica's full weight set
-    per_step = layer_bytes(shape, min(T * shape.top_k, shape.n_experts), T)["total"]
-    n_rep = args.replicas or max(2, min(8, -(-4 * L2_BYTES // per_step) + 1))
-    reps = [make_weights(shape, dev, replica=r) for r in range(n_rep)]
-    layers = [M.MoELayer(cfg, w) for w in reps]
-    x = make_x(shape, T, dev)
-    y = torch.empty_like(x)
-    ws = M.new_workspace(cfg, T, dev)
-    for L in layers:
-        L._ws = ws
-    stream = torch.cuda.current_stream()
-
-    def eager_step(i):
-        layers[i % n_rep].forward(x, y)
-
-    for i in range(max(args.warmup, n_rep)):
-        eager_step(i)
-    torch.cuda.synchronize()
-    err = M.moe_get_device_error(ws)
-
-    def timed(fn, K):
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(K):
-            fn(i)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-        if world > 1:
-            torch.distributed.barrier()
-        return ms
-
-    # one CUDA graph per replica: the whole layer (both streams) as one launch
-    graphs, per_step_launches = [], None
-    if not args.eager:
-        for r in range(n_rep):
-            g = torch.cuda.CUDAGraph()
-            c0 = M.load().moe_launch_count()
-            with torch.cuda.graph(g):
-                layers[r].forward(x, y)
-            per_step_launches = M.load().moe_launch_count() - c0
-            graphs.append(g)
-        for i in range(args.warmup):
-            graphs[i % n_rep].replay()
-        torch.cuda.synchronize()
-
-    def step(i):
-        if graphs:
-            graphs[i % n_rep].replay()
-        else:
-            eager_step(i)
-
-    clocks = ClockSampler(torch.cuda.current_device() if not os.environ.get("CUDA_VISIBLE_DEVICES") else 0)
-    clocks.start()
-    n0 = M.load().moe_launch_count()
-    ms = timed(step, args.steps)
-    n1 = M.load().moe_launch_count()
-    clk = clocks.stop()
-    launches = int(n1 - n0) if not graphs else int(per_step_launches) * args.steps
-    ms_step = ms / args.steps
-    value = job_throughput(T, world, ms_step / 1e3)
-    ms_eager = None
-    if graphs:
-        ke = max(10, min(args.steps, 200))
-        ms_eager = timed(eager_step, ke) / ke
-
-    # experts that received routes (same routing for every replica: router and bias are shared)
-    ids = torch.empty((T, shape.top_k), dtype=torch.int32, device=dev)
-    layers[0].forward(x, y, ids_out=ids)
-    n_active = int(torch.unique(ids).numel())
-    routing = routing_stats(ids.cpu().numpy(), shape.n_experts)
-    lb = layer_bytes(shape, n_active, T)
-    pk = peaks()
-
-    # dominant kernel, timed alone on the same stream: the grouped expert up projection
-    K_ = shape.top_k
-    R = T * K_
-    topw = torch.empty((T, K_), dtype=torch.float32, device=dev)
-    x_e = x
-    if shape.d_latent:
-        x_e = torch.empty((T, shape.d_latent), dtype=x.dtype, device=dev)
-        M.moe_latent_down(cfg, x, layers[0].weights, x_e, ws)
-    M.moe_router(cfg, x, reps[0]["w_router"], reps[0]["bias"], ids, topw, ws)
-    counts = torch.empty(shape.n_experts, dtype=torch.int32, device=dev)
-    offsets = torch.empty(shape.n_experts + 1, dtype=torch.int32, device=dev)
-    rt = torch.empty(R, dtype=torch.int32, device=dev)
-    rs = torch.empty(R, dtype=torch.int32, device=dev)
-    tsr = torch.empty((T, K_), dtype=torch.int32, device=dev)
-    xp = torch.empty((R, shape.d_e), dtype=x.dtype, device=dev) if T > 64 else None
-    M.moe_dispatch(cfg, ids, counts, offsets, rt, rs, tsr, ws, x_e=x_e if xp is not None else None, x_packed=xp)
-    h = torch.empty((R, shape.d_expert), dtype=x.dtype, device=dev)
-
-    def up(i):
-        M.moe_experts_up(cfg, T, rt, offsets, layers[i % n_rep].weights, h, ws, x_e=x_e, x_packed=xp)
-
-    for i in range(3):
-        up(i)
-    k_up = max(20, min(args.steps, 200))
-    c0 = M.load().moe_launch_count()
-    ms_up = timed(up, k_up) / k_up
-    up_launches = (M.load().moe_launch_count() - c0) // k_up
-    ab = 2
-    w_up_bytes = (shape.d_expert * shape.d_e // 2 + shape.d_expert * shape.d_e // 16 + 4
-                  if shape.expert_dtype == 2 else shape.d_expert * shape.d_e * ab)
-    up_bytes = n_active * w_up_bytes + R * shape.d_e * ab + R * shape.d_expert * ab
-    up_flops = 2 * R * shape.d_expert * shape.d_e
-    achieved = up_bytes / (ms_up / 1e3) / 1e9
-    achieved_tf = up_flops / (ms_up / 1e3) / 1e12
-
-    # end to end through the C ABI with host buffers (copies inside the timed region)
-    xh = x.cpu().pin_memory()
-    yh = torch.empty_like(xh).pin_memory()
-    x_dev = torch.empty_like(x)
-    for i in range(3):
-        M.moe_layer_forward_host(cfg, xh, x_dev, layers[i % n_rep].weights, y, yh, ws)
-    k_e2e = max(10, args.steps // 4)
-    if world > 1:
-        torch.distributed.barrier()
-    t0 = time.perf_counter()
-    for i in range(k_e2e):
-        M.moe_layer_forward_host(cfg, xh, x_dev, layers[i % n_rep].weights, y, yh, ws)
-    e2e_s = max_over_ranks((time.perf_counter() - t0) / k_e2e, world, dev)
-
-    sweep = {}
-    if args.sweep:
-        for Ts in shape.tokens:
-            xs = make_x(shape, Ts, dev)
-            ys = torch.empty_like(xs)
-            wss = M.new_workspace(cfg, Ts, dev)
-            for L in layers:
-                L._ws = wss
-            f = lambda i: layers[i % n_rep].forward(xs, ys)
-            for i in range(max(5, n_rep)):
-                f(i)
-            if not args.eager:
-                gs = []
-                for r in range(n_rep):
-                    g = torch.cuda.CUDAGraph()
-                    with torch.cuda.graph(g):
-                        layers[r].forward(xs, ys)
-                    gs.append(g)
-                f = lambda i: gs[i % n_rep].replay()
-                for i in range(3):
-                    f(i)
-            kk = max(50, args.steps // 2)
-            mss = timed(f, kk) / kk
-            idss = torch.empty((Ts, shape.top_k), dtype=torch.int32, device=dev)
-            layers[0].forward(xs, ys, ids_out=idss)
-            na = int(torch.unique(idss).numel())
-            rst = routing_stats(idss.cpu().numpy(), shape.n_experts)
-            bb = layer_bytes(shape, na, Ts)["total"]
-            ff = layer_flops(shape, Ts)
-            sweep[str(Ts)] = {"ms_per_step": round(mss, 5), "tokens_per_s": round(Ts / (mss / 1e3), 1),
-                              "experts_active": na, "hbm_gb_per_s": round(bb / (mss / 1e3) / 1e9, 1),
-                              "hbm_frac": round(bb / (mss / 1e3) / 1e9 / pk["hbm_gbs"], 3),
-                              "tflops": round(ff / (mss / 1e3) / 1e12, 1),
-                              "tensor_frac": round(ff / (mss / 1e3) / 1e12 / pk["bf16_tflops_sustained"], 3),
-                              "routing": rst}
-
-    return {
-        "value": value, "ms_per_step": ms_step, "n_active": n_active, "bytes": lb, "clocks": clk,
-        "launches": launches, "err": err, "ms_eager": ms_eager, "graphs": bool(graphs), "ms_up": ms_up, "up_bytes": up_bytes, "achieved_up": achieved,
-        "up_flops": up_flops, "achieved_up_tf": achieved_tf, "flops": layer_flops(shape, T),
-        "up_launches": up_launches, "routing": routing,
-        "peaks": pk, "e2e_s": e2e_s, "n_rep": n_rep, "sweep": sweep, "shape": shape, "T": T,
-        "rep_bytes": one,
-    }
-
-
-# ---------------------------------------------------------------------------
-class _Rows:
-    """weights[name][e] as float64 numpy (CPU tensors are converted on access)."""
-
-    def __init__(self, t):
-        self.t = t
-
-    def __getitem__(self, e):
-        import numpy as np
-        v = self.t[e]
-        return v.numpy() if v.dtype == __import__("torch").uint8 else v.float().numpy().astype(np.float64)
-
-
-def oracle_inputs(w):
-    import numpy as np
-    out = {}
-    for k, v in w.items():
-        v = v.cpu()
-        if k in ("w_up", "w_down", "w_up_q", "w_down_q", "w_up_sf", "w_down_sf"):
-            out[k] = _Rows(v)
-        elif k in ("w_router", "bias"):
-            out[k] = v.numpy()
-        else:
-            out[k] = v.float().numpy().astype(np.float64)
-    return out
-
-
-def time_oracle(shape, w, x, budget_s: float, min_tokens: int = 1):
-    """Tokens/s of the oracle on the first rows of x, growing the sample until
-    it takes at least budget_s (bounded)."""
-    import numpy as np
-    from oracle import moe_oracle as O
-    ow = oracle_inputs(w)
-    xn = x.float().cpu().numpy().astype(np.float64)
-    n = min_tokens
-    done_t, done_s = 0, 0.0
-    while True:
-        rows = xn[done_t % xn.shape[0]:][:n]
-        t0 = time.perf_counter()
-        O.full_layer(rows, ow, shape.n_experts, shape.top_k, shape.n_group, shape.topk_group,
-                     shape.norm_topk_prob, shape.routed_scaling_factor, bf16_points=shape.act_dtype == 1)
-        done_s += time.perf_counter() - t0
-        done_t += rows.shape[0]
-        if done_s >= budget_s or done_t >= xn.shape[0]:
-            break
-        n = min(2 * n, xn.shape[0] - done_t)
-    return done_t / done_s, done_t, done_s
+def product_ledger(shape, n_active: int, T: int, which: str) -> dict:
+    """Algorithmic bytes and FLOPs of one grouped expert product over a batch:
+    ``up`` reads the active experts' up weights and the R = T*K routed rows and
+    writes h [R, I]; ``down`` reads the down weights and h and writes the FP32
+    routed rows u [R, de] (plus the routing weight of every row)."""
+    ab = 4 if shape.act_dtype == 0 else 2
+    de, I, R = shape.d_e, shape.d_expert, T * shape.top_k
+    w1 = expert_bytes(shape) // 2 if shape.expert_dtype != 2 else (I * de // 2 + I * de // 16 + 4)
+    if which == "up":
+        b = n_active * w1 + R * de * ab + R * I * ab
+    else:
+        b = n_active * w1 + R * I * ab + R * de * 4 + R * 4
+    return {"bytes": int(b), "flops": int(2 * R * de * I)}
 
 
 def routing_stats(ids, n_experts, tile_rows=128):
@@ -401,6 +205,49 @@ def routing_stats(ids, n_experts, tile_rows=128):
             "loglog_slope": slope, f"tail_waste_{tile_rows}_row_tiles": round(float(1.0 - total / padded), 3)}
 
 
+def roofline_fractions(shape, T: int, n_active: int, ms: float, pk: dict) -> dict:
+    """A layer step's bytes and FLOPs over its time, against the measured peaks;
+    the binding one is the larger ideal time (bytes at the copy bandwidth,
+    FLOPs at the burst bf16 peak)."""
+    lb = layer_bytes(shape, n_active, T)
+    fl = layer_flops(shape, T)
+    s = ms / 1e3
+    gbs = lb["total"] / s / 1e9
+    tf = fl / s / 1e12
+    tensor = fl / (pk["bf16_tflops"] * 1e12) > lb["total"] / (pk["hbm_gbs"] * 1e9)
+    return {"bound": "tensor" if tensor else "hbm", "bytes_per_step": int(lb["total"]), "flops_per_step": int(fl),
+            "hbm_gb_per_s": round(gbs, 1), "hbm_frac": round(gbs / pk["hbm_gbs"], 4), "tflops": round(tf, 1),
+            "tensor_frac_burst": round(tf / pk["bf16_tflops"], 4),
+            "tensor_frac_sustained": round(tf / pk["bf16_tflops_sustained"], 4)}
+
+
+# ---------------------------------------------------------------------------
+def sources_sha16(family: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[family]:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str, family: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, or None when there is none or the kernel's sources changed since
+    it was taken (rows: | kernel | workload | bytes | sources sha16 |)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None, None
+    want = sources_sha16(family)
+    for line in open(TRAFFIC_FILE):
+        cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload:
+            try:
+                b = int(cells[2].replace(",", ""))
+            except ValueError:
+                continue
+            return (b if cells[3] == want else None), cells[3]
+    return None, None
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -408,11 +255,347 @@ def cpu_cores():
         return os.cpu_count()
 
 
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+# ---------------------------------------------------------------------------
+class _Rows:
+    """weights[name][e] as float64 numpy (CPU tensors are converted on access)."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __getitem__(self, e):
+        v = self.t[e]
+        return v.numpy() if v.dtype == __import__("torch").uint8 else v.float().numpy().astype(np.float64)
+
+
+def oracle_inputs(w):
+    out = {}
+    for k, v in w.items():
+        v = v.cpu()
+        if k in ("w_up", "w_down", "w_up_q", "w_down_q", "w_up_sf", "w_down_sf"):
+            out[k] = _Rows(v)
+        elif k in ("w_router", "bias"):
+            out[k] = v.numpy()
+        else:
+            out[k] = v.float().numpy().astype(np.float64)
+    return out
+
+
+def time_oracle(shape, w, x, budget_s: float, min_tokens: int = 1):
+    """Tokens/s of the oracle on the first rows of x, growing the sample until
+    it takes at least budget_s (bounded)."""
+    from oracle import moe_oracle as O
+    ow = oracle_inputs(w)
+    xn = x.float().cpu().numpy().astype(np.float64)
+    n = min_tokens
+    done_t, done_s = 0, 0.0
+    while True:
+        rows = xn[done_t % xn.shape[0]:][:n]
+        t0 = time.perf_counter()
+        O.full_layer(rows, ow, shape.n_experts, shape.top_k, shape.n_group, shape.topk_group,
+                     shape.norm_topk_prob, shape.routed_scaling_factor, bf16_points=shape.act_dtype == 1)
+        done_s += time.perf_counter() - t0
+        done_t += rows.shape[0]
+        if done_s >= budget_s or done_t >= xn.shape[0]:
+            break
+        n = min(2 * n, xn.shape[0] - done_t)
+    return done_t / done_s, done_t, done_s
+
+
+_ONE_THREAD = r"""
+import json, sys, time
+sys.path.insert(0, sys.argv[1])
+import torch
+torch.set_num_threads(int(sys.argv[4]))          # the draws may use every core
+import bench
+from synth import WORKLOADS, make_weights, make_x
+shape = WORKLOADS[sys.argv[2]]
+w = make_weights(shape, "cpu")
+x = make_x(shape, int(sys.argv[3]), "cpu")
+torch.set_num_threads(1)
+tps, nt, secs = bench.time_oracle(shape, w, x, float(sys.argv[5]))
+print(json.dumps({"value": tps, "tokens": nt, "seconds": secs}))
+"""
+
+
+def time_oracle_one_thread(shape, T: int, budget_s: float):
+    """The oracle with its BLAS held to one thread, in a fresh interpreter
+    (started after this process has used the GPU, so spawned, not forked)."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    try:
+        r = subprocess.run([sys.executable, "-c", _ONE_THREAD, ROOT, shape.name, str(T), str(cpu_cores()),
+                            str(budget_s)], capture_output=True, text=True, env=env, timeout=300)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+def n_replicas(shape, T: int, requested: int = 0) -> int:
+    """Weight replicas that together exceed 4x L2 for the bytes a step reads."""
+    if requested:
+        return requested
+    per_step = layer_bytes(shape, min(T * shape.top_k, shape.n_experts), T)["total"]
+    return max(2, min(8, -(-4 * L2_BYTES // per_step) + 1))
+
+
+class Runner:
+    """Device-side timing of the layer through the C ABI binding."""
+
+    def __init__(self, M, dev, world, eager=False):
+        import torch
+        self.torch, self.M, self.dev, self.world, self.eager = torch, M, dev, world, eager
+        self.stream = torch.cuda.current_stream()
+
+    def timed(self, fn, K):
+        """Milliseconds of K calls of fn, CUDA events on the launching stream,
+        barrier + synchronize on both sides, max over ranks."""
+        torch = self.torch
+        if self.world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for i in range(K):
+            fn(i)
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(e0.elapsed_time(e1), self.world, self.dev)
+        if self.world > 1:
+            torch.distributed.barrier()
+        return ms
+
+    def layers(self, shape, n_rep):
+        from synth import make_weights
+        reps = [make_weights(shape, self.dev, replica=r) for r in range(n_rep)]
+        return reps, [self.M.MoELayer(self.M.config_from(shape), w) for w in reps]
+
+    def step_fn(self, layers, x, y, warmup):
+        """A step function replaying one CUDA graph of the whole layer per
+        weight replica (eager calls with --eager), and kernel launches per step."""
+        torch, M = self.torch, self.M
+        n_rep = len(layers)
+        ws = M.new_workspace(layers[0].cfg, x.shape[0], self.dev)
+        for L in layers:
+            L._ws = ws
+
+        def eager(i):
+            layers[i % n_rep].forward(x, y)
+
+        for i in range(max(warmup, n_rep)):
+            eager(i)
+        torch.cuda.synchronize()
+        if self.eager:
+            c0 = M.load().moe_launch_count()
+            eager(0)
+            return eager, M.load().moe_launch_count() - c0, ws, eager
+        graphs, per = [], 0
+        for r in range(n_rep):
+            g = torch.cuda.CUDAGraph()
+            c0 = M.load().moe_launch_count()
+            with torch.cuda.graph(g):
+                layers[r].forward(x, y)
+            per = M.load().moe_launch_count() - c0
+            graphs.append(g)
+        for i in range(max(3, warmup)):
+            graphs[i % n_rep].replay()
+        torch.cuda.synchronize()
+        return (lambda i: graphs[i % n_rep].replay()), per, ws, eager
+
+    def steps_for(self, fn, target_ms=150.0, lo=20, hi=2000):
+        est = self.timed(fn, 5) / 5
+        return int(max(lo, min(hi, target_ms / max(est, 1e-3))))
+
+    def active_and_routing(self, layer, x, y, shape):
+        T = x.shape[0]
+        ids = self.torch.empty((T, shape.top_k), dtype=self.torch.int32, device=self.dev)
+        layer.forward(x, y, ids_out=ids)
+        ids_np = ids.cpu().numpy()
+        return int(np.unique(ids_np).size), routing_stats(ids_np, shape.n_experts), ids
+
+
+def measure_products(run: Runner, shape, T, layers, x, n_active, pk):
+    """The two grouped expert products timed alone on the launching stream
+    (moe_experts_up, moe_experts_down), each over >= 20 launches rotating the
+    weight replicas; algorithmic bytes / FLOPs per launch over the mean time."""
+    torch, M = run.torch, run.M
+    cfg = layers[0].cfg
+    K_, R = shape.top_k, T * shape.top_k
+    ws = M.new_workspace(cfg, T, run.dev)
+    ids = torch.empty((T, K_), dtype=torch.int32, device=run.dev)
+    topw = torch.empty((T, K_), dtype=torch.float32, device=run.dev)
+    x_e = x
+    if shape.d_latent:
+        x_e = torch.empty((T, shape.d_latent), dtype=x.dtype, device=run.dev)
+        M.moe_latent_down(cfg, x, layers[0].weights, x_e, ws)
+    w0 = layers[0].weights.tensors
+    M.moe_router(cfg, x, w0["w_router"], w0["router_bias"], ids, topw, ws)
+    counts = torch.empty(shape.n_experts, dtype=torch.int32, device=run.dev)
+    offsets = torch.empty(shape.n_experts + 1, dtype=torch.int32, device=run.dev)
+    rt = torch.empty(R, dtype=torch.int32, device=run.dev)
+    rs = torch.empty(R, dtype=torch.int32, device=run.dev)
+    tsr = torch.empty((T, K_), dtype=torch.int32, device=run.dev)
+    xp = torch.empty((R, shape.d_e), dtype=x.dtype, device=run.dev) if T > 64 else None
+    M.moe_dispatch(cfg, ids, counts, offsets, rt, rs, tsr, ws, x_e=x_e if xp is not None else None, x_packed=xp)
+    h = torch.empty((R, shape.d_expert), dtype=x.dtype, device=run.dev)
+    u = torch.empty((R, shape.d_e), dtype=torch.float32, device=run.dev)
+    n_rep = len(layers)
+
+    def up(i):
+        M.moe_experts_up(cfg, T, rt, offsets, layers[i % n_rep].weights, h, ws, x_e=x_e, x_packed=xp)
+
+    def down(i):
+        M.moe_experts_down(cfg, T, h, offsets, rt, rs, topw, layers[i % n_rep].weights, u, ws)
+
+    out = {}
+    for name, fn in (("up", up), ("down", down)):
+        for i in range(3):
+            fn(i)
+        k = 40
+        c0 = M.load().moe_launch_count()
+        ms = run.timed(fn, k) / k
+        launches = (M.load().moe_launch_count() - c0) // k
+        led = product_ledger(shape, n_active, T, name)
+        tensor = led["flops"] / (pk["bf16_tflops"] * 1e12) > led["bytes"] / (pk["hbm_gbs"] * 1e9)
+        out[name] = {"ms": ms, "launches": int(launches), "bytes": led["bytes"], "flops": led["flops"],
+                     "gbs": led["bytes"] / (ms / 1e3) / 1e9, "tflops": led["flops"] / (ms / 1e3) / 1e12,
+                     "tensor": tensor}
+    return out
+
+
+def product_kernel_name(shape, T, which):
+    """The kernel that runs a grouped expert product at this size (names as the
+    profiler prints their template arguments)."""
+    if T > 64:
+        # (the step entry points hand NVFP4 products BF16 rows: FP4A = 1)
+        cg = 1 if shape.expert_dtype == 2 else 2
+        fp4 = 1 if shape.expert_dtype == 2 else 0
+        return f"tc_gemm_kernel<{0 if which == 'up' else 1}, {0 if which == 'up' else 1}, {fp4}, {cg}>", "tc"
+    if shape.expert_dtype == 2:
+        K = shape.d_e if which == "up" else shape.d_expert
+        wpg = 1 if K <= 1536 else 2
+        return (f"gemv_nvfp4_bulk_kernel<{0 if which == 'up' else 1}, {0 if which == 'up' else 1}, 0, {wpg}>",
+                "gemv")
+    K = shape.d_e if which == "up" else shape.d_expert
+    N = shape.d_expert if which == "up" else shape.d_e
+    fpc = 32 if K <= 2048 and N % 32 == 0 else 16
+    return f"gemv_bf16_kernel<{0 if which == 'up' else 1}, {0 if which == 'up' else 1}, {fpc}>", "gemv"
+
+
+def measure_point(run: Runner, shape, T, layers, warmup):
+    """One workload point: the whole layer step timed as graph replays."""
+    from synth import make_x
+    torch, M = run.torch, run.M
+    x = make_x(shape, T, run.dev)
+    y = torch.empty_like(x)
+    fn, per, ws, _ = run.step_fn(layers, x, y, warmup)
+    K = run.steps_for(fn)
+    ms = run.timed(fn, K) / K
+    err = M.moe_get_device_error(ws)
+    n_active, routing, _ = run.active_and_routing(layers[0], x, y, shape)
+    return {"ms": ms, "steps": K, "launches_per_step": int(per), "n_active": n_active, "routing": routing,
+            "err": err}
+
+
+def run_ours(args, rank, world, dev):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import routed_relu_expert_gb300 as M
+    from synth import WORKLOADS, make_x
+
+    pk = peaks()
+    run = Runner(M, dev, world, eager=args.eager)
+    shape = WORKLOADS[args.workload]
+    T = args.tokens
+    n_rep = n_replicas(shape, T, args.replicas)
+    reps, layers = run.layers(shape, n_rep)
+    x = make_x(shape, T, dev)
+    y = torch.empty_like(x)
+    fn, per_step_launches, ws, eager_fn = run.step_fn(layers, x, y, args.warmup)
+    err = M.moe_get_device_error(ws)
+
+    clocks = ClockSampler(torch.cuda.current_device() if not os.environ.get("CUDA_VISIBLE_DEVICES") else 0)
+    clocks.start()
+    ms = run.timed(fn, args.steps)
+    clk = clocks.stop()
+    ms_step = ms / args.steps
+    value = job_throughput(T, world, ms_step / 1e3)
+    ms_eager = None
+    if not args.eager:
+        ke = max(10, min(args.steps, 200))
+        ms_eager = run.timed(eager_fn, ke) / ke
+    n_active, routing, _ = run.active_and_routing(layers[0], x, y, shape)
+    prods = measure_products(run, shape, T, layers, x, n_active, pk)
+
+    # end to end through the C ABI with host buffers (copies inside the timed region)
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    x_dev = torch.empty_like(x)
+    for i in range(3):
+        M.moe_layer_forward_host(layers[0].cfg, xh, x_dev, layers[i % n_rep].weights, y, yh, ws)
+    k_e2e = max(10, args.steps // 4)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for i in range(k_e2e):
+        M.moe_layer_forward_host(layers[0].cfg, xh, x_dev, layers[i % n_rep].weights, y, yh, ws)
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / k_e2e, world, dev)
+
+    # every workload at every token count it is defined for
+    per_workload, pw_clocks = {}, None
+    if args.points != "none":
+        names = [n for n in ("tiny_fp32", "nano_decode", "nano_prefill", "super_latent", "super_nvfp4")
+                 if args.points in ("all", n)]
+        sampler = ClockSampler(torch.cuda.current_device() if not os.environ.get("CUDA_VISIBLE_DEVICES") else 0)
+        sampler.start()
+        for name in names:
+            sh = WORKLOADS[name]
+            need = n_replicas(sh, min(sh.tokens))
+            if sh is shape and len(layers) >= need:
+                lay = layers
+            else:
+                lay = None
+                torch.cuda.empty_cache()
+                lay = run.layers(sh, need)[1]
+            for Ts in sh.tokens:
+                p = measure_point(run, sh, Ts, lay, 3)
+                entry = {"ms_per_step": round(p["ms"], 5), "tokens_per_s": round(Ts / (p["ms"] / 1e3), 1),
+                         "timed_steps": p["steps"], "weight_replicas": len(lay), "experts_active": p["n_active"],
+                         "launches_per_step": p["launches_per_step"], "device_error_word": p["err"]}
+                entry.update(roofline_fractions(sh, Ts, p["n_active"], p["ms"], pk))
+                entry["routing"] = p["routing"]
+                per_workload[f"{name} T={Ts}"] = entry
+            if lay is not layers:
+                del lay
+        pw_clocks = sampler.stop()
+
+    return {
+        "value": value, "ms_per_step": ms_step, "n_active": n_active, "clocks": clk,
+        "launches": int(per_step_launches) * args.steps, "err": err, "ms_eager": ms_eager,
+        "prods": prods, "routing": routing, "peaks": pk, "e2e_s": e2e_s, "n_rep": n_rep, "shape": shape, "T": T,
+        "rep_bytes": layer_bytes(shape, shape.n_experts, T)["total"], "per_workload": per_workload,
+        "per_workload_clocks": pw_clocks,
+    }
+
+
+# ---------------------------------------------------------------------------
 def run_reference(args, rank, world):
     """The oracle as it stands, on the host cores, as the reference arm."""
     if rank != 0:
         return None
-    import torch
     from synth import WORKLOADS, make_weights, make_x
     shape = WORKLOADS[args.workload]
     T = args.tokens
@@ -438,10 +621,42 @@ def run_reference(args, rank, world):
         "config": {"workload": f"{shape.name} T={T}", "sample": "one token of the batch per step",
                    "runs_on": "host cores of rank 0 (the oracle uses no GPU)"},
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": f"{steps_done} steps of 1 token ({shape.name}, T={T} batch rows)"},
+                         "sample": f"{steps_done} steps of 1 token ({shape.name}, T={T} batch rows)",
+                         "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     return line
+
+
+def roofline_entry(r, shape, T, pk):
+    """The dominant kernel: the longer of the two grouped expert products."""
+    prods = r["prods"]
+    which = max(prods, key=lambda k: prods[k]["ms"])
+    p = prods[which]
+    kname, family = product_kernel_name(shape, T, which)
+    workload = f"{shape.name} T={T}"
+    traffic, sha = recorded_traffic(kname, workload, family)
+    if p["tensor"]:
+        roof = {"bound": "tensor", "achieved": round(p["tflops"], 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(p["tflops"] / pk["bf16_tflops"], 4), "algorithmic_flops_per_launch": p["flops"]}
+    else:
+        roof = {"bound": "hbm", "achieved": round(p["gbs"], 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(p["gbs"] / pk["hbm_gbs"], 4)}
+    roof.update({
+        "kernel": f"grouped expert {which} projection ({kname}, through moe_experts_{which})",
+        "traffic": traffic,
+        "traffic_source": (f"ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, profiles/"
+                           f"roofline_traffic.md (kernel sources {sha})" if traffic else
+                           "no ncu capture of the current kernel sources"),
+        "algorithmic_bytes_per_launch": p["bytes"], "avg_launch_ms": round(p["ms"], 5),
+        "launches_per_call": p["launches"],
+        "peak_source": pk["source"] + (" (cuBLAS bf16 burst)" if p["tensor"] else " (burst copy)"),
+        "other_product": {k: {"avg_launch_ms": round(v["ms"], 5), "gb_per_s": round(v["gbs"], 1),
+                              "hbm_frac": round(v["gbs"] / pk["hbm_gbs"], 4), "tflops": round(v["tflops"], 1),
+                              "algorithmic_bytes_per_launch": v["bytes"]}
+                          for k, v in prods.items() if k != which},
+    })
+    return roof
 
 
 # ---------------------------------------------------------------------------
@@ -472,29 +687,18 @@ def main():
         wc = make_weights(shape, "cpu")
         xc = make_x(shape, T, "cpu")
         tps, nt, secs = time_oracle(shape, wc, xc, 12.0)
+        del wc
+        one = time_oracle_one_thread(shape, T, 6.0)
         cpu = {"value": round(tps, 3), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"{nt} of the {T} tokens of one {shape.name} batch, {secs:.1f} s"}
-    lb = r["bytes"]
+               "sample": f"{nt} of the {T} tokens of one {shape.name} batch, {secs:.1f} s",
+               "cpu_model": cpu_model(),
+               "one_thread": ({"value": round(one["value"], 3), "unit": "tokens/s", "cores": 1,
+                               "sample": f"{one['tokens']} tokens, {one['seconds']:.1f} s, BLAS held to one thread"}
+                              if one else None)}
     ab = 2 if shape.act_dtype != 0 else 4
     if rank == 0:
-        layer_gbs = lb["total"] / (r["ms_per_step"] / 1e3) / 1e9
-        layer_tf = r["flops"] / (r["ms_per_step"] / 1e3) / 1e12
-        # the dominant kernel's bound: whichever ideal time (bytes / bandwidth, FLOPs / peak) is larger
-        up_tensor = r["up_flops"] / (pk["bf16_tflops"] * 1e12) > r["up_bytes"] / (pk["hbm_gbs"] * 1e9)
-        if up_tensor:
-            roof = {"bound": "tensor", "achieved": round(r["achieved_up_tf"], 1), "peak": pk["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": round(r["achieved_up_tf"] / pk["bf16_tflops"], 4),
-                    "algorithmic_flops_per_launch": int(r["up_flops"])}
-        else:
-            roof = {"bound": "hbm", "achieved": round(r["achieved_up"], 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(r["achieved_up"] / pk["hbm_gbs"], 4)}
-        up_name = "grouped expert up projection (moe_experts_up)"
-        if r["up_launches"] > 1:
-            up_name += f", {r['up_launches']} launches per call (NVFP4 dequantise + GEMM)"
-        roof.update({"kernel": up_name, "traffic": None,
-                     "algorithmic_bytes_per_launch": int(r["up_bytes"]), "avg_launch_ms": round(r["ms_up"], 5),
-                     "peak_source": pk["source"] + (" (cuBLAS bf16 burst)" if up_tensor else " (burst copy)")})
-        layer_tensor = r["flops"] / (pk["bf16_tflops_sustained"] * 1e12) > lb["total"] / (pk["hbm_gbs"] * 1e9)
+        layer = roofline_fractions(shape, T, r["n_active"], r["ms_per_step"], pk)
+        layer["bytes_breakdown"] = layer_bytes(shape, r["n_active"], T)
         line = {
             "metric": "MoE-layer tokens/s", "value": round(r["value"], 1), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -507,17 +711,12 @@ def main():
                        "l2": f"weights rotate over {r['n_rep']} seeded replicas "
                              f"({r['rep_bytes'] / 1e9:.2f} GB each); no step reads the previous step's weights",
                        "experts_active": r["n_active"], "routing": r["routing"]},
-            "roofline": roof,
-            "layer_roofline": {"bound": "tensor" if layer_tensor else "hbm", "bytes_per_step": int(lb["total"]),
-                               "flops_per_step": int(r["flops"]),
-                               "hbm_gb_per_s": round(layer_gbs, 1), "hbm_frac": round(layer_gbs / pk["hbm_gbs"], 4),
-                               "tflops": round(layer_tf, 1),
-                               "tensor_frac": round(layer_tf / pk["bf16_tflops_sustained"], 4),
-                               "tensor_peak": "sustained", "bytes_breakdown": lb},
+            "roofline": roofline_entry(r, shape, T, pk),
+            "layer_roofline": layer,
             "clocks": r["clocks"],
             "gpu_launches": r["launches"],
             "execution": ("CUDA graph of the layer per weight replica, replayed each step"
-                          if r["graphs"] else "eager C-ABI calls"),
+                          if not args.eager else "eager C-ABI calls"),
             "eager_ms_per_step": round(r["ms_eager"], 5) if r["ms_eager"] else None,
             "device_error_word": r["err"],
             "e2e": {"value": round(world * T / r["e2e_s"], 1), "unit": "tokens/s",
@@ -525,8 +724,12 @@ def main():
                     "api": "moe_layer_forward_host (pinned host x and y)"},
             "cpu_baseline": cpu,
         }
-        if r["sweep"]:
-            line["per_T"] = r["sweep"]
+        if r["per_workload"]:
+            line["per_workload"] = r["per_workload"]
+            line["per_workload_clocks"] = r["per_workload_clocks"]
+            line["per_workload_note"] = ("graph replays; bound = the larger ideal time (bytes at the measured copy "
+                                         "bandwidth, FLOPs at the burst bf16 peak); tensor fractions against both "
+                                         "the burst and the sustained measured bf16 peaks")
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -162,7 +162,9 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, int32_t T, const int32_t* top
  * ...", section "Arithmetic": bf16(relu(bf16(up x))^2)).
  *   x_e         [T, de] rows the experts read (gathered through route_token),
  *               ignored when x_packed is given
- *   x_packed    [T*K, de] packed rows from moe_dispatch, or NULL
+ *   x_packed    [T*K, de] packed rows from moe_dispatch, or NULL (above 64
+ *               BF16 tokens, where the tensor-core kernel reads contiguous
+ *               rows, x_e is then first gathered into the workspace)
  *   route_token, offsets: from moe_dispatch (same workspace)
  *   h           [T*K, I] out, packed order; BF16 (F32 for F32 layers)        */
 moe_status_t moe_experts_up(const moe_config_t* cfg, int32_t T, const void* x_e,
@@ -183,6 +185,17 @@ moe_status_t moe_experts_down_combine(const moe_config_t* cfg, int32_t T, const 
                                       const int32_t* route_slot, const int32_t* token_slot_row,
                                       const float* topk_w, const moe_weights_t* w,
                                       float* y_routed, void* ws, size_t ws_bytes, void* stream);
+
+/* Step 4 alone: the expert down projections times the routing weights, one
+ * FP32 row per route in packed order, without the combine (page "NemotronH
+ * ...", section "Arithmetic": the down projection accumulates in FP32; page
+ * "M6.1 ...", section 0x05B, the gate-weighted routed rows).
+ *   h, offsets, route_token, route_slot, topk_w: as for moe_experts_down_combine
+ *   u   [T*K, de] FP32 out: u[r] = topk_w[t, k] * (h_r W_down,e^T) for packed
+ *       row r of route (t, k) to expert e                                    */
+moe_status_t moe_experts_down(const moe_config_t* cfg, int32_t T, const void* h, const int32_t* offsets,
+                              const int32_t* route_token, const int32_t* route_slot, const float* topk_w,
+                              const moe_weights_t* w, float* u, void* ws, size_t ws_bytes, void* stream);
 
 /* Latent down projection of latent shapes: x_l = bf16(x W_ld^T), FP32
  * accumulation (page "Nemotron-3.5-Super 120B on an 8 GB GPU", section "The
@@ -222,6 +235,33 @@ moe_status_t moe_get_device_error(const void* ws, void* stream, int32_t* code);
 
 /* Enqueues a clear of the device error word. */
 moe_status_t moe_clear_device_error(void* ws, void* stream);
+
+/* Where a workspace for T tokens keeps the layer's route tables, so a caller
+ * can read what moe_layer_forward decided (host arithmetic only; no CUDA call).
+ * After moe_layer_forward (same cfg, T and workspace) the regions hold:
+ *   MOE_WS_COUNTS          [E]     int32  routes per expert
+ *   MOE_WS_OFFSETS         [E+1]   int32  exclusive prefix sum of the counts
+ *   MOE_WS_ROUTE_TOKEN     [T*K]   int32  token of each packed row
+ *   MOE_WS_ROUTE_SLOT      [T*K]   int32  slot of each packed row
+ *   MOE_WS_TOKEN_SLOT_ROW  [T, K]  int32  packed row of route (t, k)
+ *   MOE_WS_TOPK_IDS        [T, K]  int32  chosen experts   } only when the
+ *   MOE_WS_TOPK_W          [T, K]  FP32   routing weights  } matching optional
+ *   MOE_WS_LOGITS          [T, E]  FP32   router logits    } output of
+ *   MOE_WS_SCORES          [T, E]  FP32   sigmoid scores   } moe_layer_forward is NULL
+ *   MOE_WS_X_LATENT        [T, L]  act    latent rows (latent shapes)
+ *   MOE_WS_X_PACKED        [T*K, de]      rows packed for the tensor-core path
+ *                                         (above 64 BF16 tokens: act_dtype, or
+ *                                         FP16 copies of the BF16 values with
+ *                                         NVFP4 experts)
+ * *offset receives the region's byte offset from the workspace start, *bytes
+ * its size.  MOE_ERR_INVALID_ARG for an unknown region or T < 0.           */
+enum {
+  MOE_WS_COUNTS = 0, MOE_WS_OFFSETS = 1, MOE_WS_ROUTE_TOKEN = 2, MOE_WS_ROUTE_SLOT = 3,
+  MOE_WS_TOKEN_SLOT_ROW = 4, MOE_WS_TOPK_IDS = 5, MOE_WS_TOPK_W = 6, MOE_WS_LOGITS = 7,
+  MOE_WS_SCORES = 8, MOE_WS_X_LATENT = 9, MOE_WS_X_PACKED = 10
+};
+moe_status_t moe_workspace_region(const moe_config_t* cfg, int32_t T, int32_t region, size_t* offset,
+                                  size_t* bytes);
 
 /* Number of kernel launches this library has enqueued in this process (a host
  * counter, incremented once per kernel launch; memset and copy operations are

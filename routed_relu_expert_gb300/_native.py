@@ -16,6 +16,9 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUD
 MOE_DEVERR_EXPERT_ID, MOE_DEVERR_NONFINITE, MOE_DEVERR_SCHEDULE, MOE_DEVERR_TIMEOUT = 1, 2, 4, 8
 MOE_DT_F32, MOE_DT_BF16, MOE_DT_NVFP4 = 0, 1, 2
 MOE_NOALLOC_MAX_ROUTER_ELEMS = 131072
+MOE_NOALLOC_MAX_SPLIT_ELEMS = 7340032
+(MOE_WS_COUNTS, MOE_WS_OFFSETS, MOE_WS_ROUTE_TOKEN, MOE_WS_ROUTE_SLOT, MOE_WS_TOKEN_SLOT_ROW, MOE_WS_TOPK_IDS,
+ MOE_WS_TOPK_W, MOE_WS_LOGITS, MOE_WS_SCORES, MOE_WS_X_LATENT, MOE_WS_X_PACKED) = range(11)
 
 
 class MoeConfig(ctypes.Structure):
@@ -43,9 +46,9 @@ class MoeWeights(ctypes.Structure):
 
 EXPORTS = (
     "moe_version", "moe_status_string", "moe_check_config", "moe_workspace_bytes", "moe_router",
-    "moe_dispatch", "moe_experts_up", "moe_experts_down_combine", "moe_latent_down", "moe_shared",
+    "moe_dispatch", "moe_experts_up", "moe_experts_down", "moe_experts_down_combine", "moe_latent_down", "moe_shared",
     "moe_layer_forward", "moe_get_device_error", "moe_clear_device_error", "moe_layer_forward_host",
-    "moe_launch_count", "moe_router_noalloc",
+    "moe_launch_count", "moe_router_noalloc", "moe_workspace_region",
 )
 
 _lib = None
@@ -73,6 +76,7 @@ def load() -> ctypes.CDLL:
         "moe_router": (I32, [CFG, I32, P, P, P, P, P, P, P, P, S, P]),
         "moe_dispatch": (I32, [CFG, I32, P, P, P, P, P, P, P, P, P, S, P]),
         "moe_experts_up": (I32, [CFG, I32, P, P, P, P, W, P, P, S, P]),
+        "moe_experts_down": (I32, [CFG, I32, P, P, P, P, P, W, P, P, S, P]),
         "moe_experts_down_combine": (I32, [CFG, I32, P, P, P, P, P, P, W, P, P, S, P]),
         "moe_latent_down": (I32, [CFG, I32, P, W, P, P, S, P]),
         "moe_shared": (I32, [CFG, I32, P, W, P, P, P, S, P]),
@@ -82,6 +86,7 @@ def load() -> ctypes.CDLL:
         "moe_layer_forward_host": (I32, [CFG, I32, P, P, W, P, P, P, S, P]),
         "moe_launch_count": (ctypes.c_int64, []),
         "moe_router_noalloc": (I32, [CFG, I32, P, P, P, P, P, P]),
+        "moe_workspace_region": (I32, [CFG, I32, I32, ctypes.POINTER(S), ctypes.POINTER(S)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -222,8 +222,16 @@ moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x
   a.out = h; a.out_ld = I; a.err = &P.hdr()->err;
   a.x_f16 = a.out_f16 = f16;
   const int segs = (int)std::min<int64_t>(c->n_experts, (int64_t)T * c->top_k);
-  if (use_tc(c, T) && x_packed) {
+  if (use_tc(c, T)) {
     const int64_t R = (int64_t)T * c->top_k;
+    if (!x_packed) {
+      // the tensor-core kernel reads contiguous rows: gather them into the
+      // workspace's packed-row region first
+      void* xp = P.at<void>(P.L.x_packed);
+      CU(launch_pack_rows(x_e, rt, offsets, c->n_experts, (int)R, de, act_bytes(c), f16, xp, s));
+      a.X = xp;
+      a.gather = nullptr;
+    }
     // (NVFP4 weights are converted to BF16, or with f16 to FP16, inside the tensor-core kernel)
     CU(launch_gemm_tc(a, EPI_RELU2, false, (int64_t)c->n_experts * I, R, c->n_experts,
                       tc_tile_rows(R / segs, segs, I), s));
@@ -308,7 +316,6 @@ struct AuxStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr, latent = nullptr;
 };
-constexpr int kMaxDevices = 64;
 std::mutex g_aux_mutex;
 AuxStream g_aux[kMaxDevices];
 
@@ -380,6 +387,34 @@ const char* moe_status_string(moe_status_t s) {
 
 moe_status_t moe_check_config(const moe_config_t* cfg) { return check_config(cfg); }
 
+moe_status_t moe_workspace_region(const moe_config_t* cfg, int32_t T, int32_t region, size_t* offset,
+                                  size_t* bytes) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (T < 0 || !offset || !bytes) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(cfg, T);
+  const size_t t = (size_t)T, E = cfg->n_experts, R = t * cfg->top_k;
+  const size_t ab = act_bytes(cfg);
+  size_t o = 0, n = 0;
+  switch (region) {
+    case MOE_WS_COUNTS: o = L.counts; n = E * 4; break;
+    case MOE_WS_OFFSETS: o = L.offsets; n = (E + 1) * 4; break;
+    case MOE_WS_ROUTE_TOKEN: o = L.route_token; n = R * 4; break;
+    case MOE_WS_ROUTE_SLOT: o = L.route_slot; n = R * 4; break;
+    case MOE_WS_TOKEN_SLOT_ROW: o = L.tsr; n = R * 4; break;
+    case MOE_WS_TOPK_IDS: o = L.ids; n = R * 4; break;
+    case MOE_WS_TOPK_W: o = L.topw; n = R * 4; break;
+    case MOE_WS_LOGITS: o = L.logits; n = t * E * 4; break;
+    case MOE_WS_SCORES: o = L.scores; n = t * E * 4; break;
+    case MOE_WS_X_LATENT: o = L.x_l; n = t * (size_t)cfg->d_latent * ab; break;
+    case MOE_WS_X_PACKED: o = L.x_packed; n = R * (size_t)de_of(cfg) * ab; break;
+    default: return MOE_ERR_INVALID_ARG;
+  }
+  *offset = o;
+  *bytes = n;
+  return MOE_OK;
+}
+
 size_t moe_workspace_bytes(const moe_config_t* cfg, int32_t T) {
   if (check_config(cfg) != MOE_OK || T < 0) return 0;
   return make_layout(cfg, T).total;
@@ -435,6 +470,17 @@ moe_status_t moe_experts_down_combine(const moe_config_t* cfg, int32_t T, const 
   if ((st = run_down(cfg, T, h, offsets, route_token, route_slot, topk_w, w, u, P, s)) != MOE_OK) return st;
   CU(launch_combine(u, token_slot_row, T, cfg->top_k, de_of(cfg), y_routed, nullptr, cfg->act_dtype, s));
   return MOE_OK;
+}
+
+moe_status_t moe_experts_down(const moe_config_t* cfg, int32_t T, const void* h, const int32_t* offsets,
+                              const int32_t* route_token, const int32_t* route_slot, const float* topk_w,
+                              const moe_weights_t* w, float* u, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_common(cfg, T, ws, ws_bytes);
+  if (st != MOE_OK || T == 0) return st;
+  if ((st = check_weights(cfg, w, true, false, false)) != MOE_OK) return st;
+  REQ(h); REQ(offsets); REQ(route_token); REQ(route_slot); REQ(topk_w); REQ(u);
+  Ptrs P{(char*)ws, make_layout(cfg, T)};
+  return run_down(cfg, T, h, offsets, route_token, route_slot, topk_w, w, u, P, (cudaStream_t)stream);
 }
 
 moe_status_t moe_latent_down(const moe_config_t* cfg, int32_t T, const void* x, const moe_weights_t* w, void* x_l,

@@ -352,21 +352,27 @@ __global__ void __launch_bounds__(kTinyThreads) select_dispatch_tiny(const Selec
 
 constexpr int kSingleMaxRoutes = 4096;
 
-// the dynamic shared-memory limits are raised once, to the largest expert count
-bool g_attr_single = false, g_attr_multi = false;
+// the dynamic shared-memory limits are raised once per device, to the largest expert count
+PerDeviceOnce g_attr_single, g_attr_multi;
 
 cudaError_t launch_pack(const DispatchArgs& a, cudaStream_t s) {
   if (!a.x_packed || !a.x_e) return cudaSuccess;
-  const int R = a.T * a.K;
-  const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(R, 8), 16384);
-  if (a.pack_f16 && a.elem_bytes != 2) return cudaErrorNotSupported;
-  launch_k(a.pack_f16 ? pack_rows_kernel<true> : pack_rows_kernel<false>, grid, 256, 0, s,
-           reinterpret_cast<const uint4*>(a.x_e), a.route_token, a.offsets, a.E, a.de * a.elem_bytes / 16,
-           reinterpret_cast<uint4*>(a.x_packed));
-  return cudaGetLastError();
+  return launch_pack_rows(a.x_e, a.route_token, a.offsets, a.E, a.T * a.K, a.de, a.elem_bytes, a.pack_f16,
+                          a.x_packed, s);
 }
 
 }  // namespace
+
+cudaError_t launch_pack_rows(const void* x_e, const int32_t* route_token, const int32_t* offsets, int E, int R,
+                             int de, int elem_bytes, bool to_f16, void* x_packed, cudaStream_t s) {
+  if (R <= 0) return cudaSuccess;
+  if ((to_f16 && elem_bytes != 2) || (de * elem_bytes) % 16) return cudaErrorNotSupported;
+  const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(R, 8), 16384);
+  launch_k(to_f16 ? pack_rows_kernel<true> : pack_rows_kernel<false>, grid, 256, 0, s,
+           reinterpret_cast<const uint4*>(x_e), route_token, offsets, E, de * elem_bytes / 16,
+           reinterpret_cast<uint4*>(x_packed));
+  return cudaGetLastError();
+}
 
 bool select_dispatch_fits(int T, int K, const DispatchArgs& a) {
   return T >= 1 && T <= kTinyMaxTokens && T * K <= kTinyMaxRoutes && a.tile_rows == 0 && !a.x_packed;
@@ -397,13 +403,11 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
   if (R <= kSingleMaxRoutes) {
     const size_t smem = (size_t)(kWarps * a.E + 32) * sizeof(int);
-    cudaError_t e = cudaSuccess;
-    if (!g_attr_single) {
-      e = cudaFuncSetAttribute(dispatch_single, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)((kWarps * 1024 + 32) * sizeof(int)));
-      if (e != cudaSuccess) return e;
-      g_attr_single = true;
-    }
+    cudaError_t e = g_attr_single.run([](int&) {
+      return cudaFuncSetAttribute(dispatch_single, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)((kWarps * 1024 + 32) * sizeof(int)));
+    });
+    if (e != cudaSuccess) return e;
     launch_k(dispatch_single, 1, kThreads, smem, s, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -411,15 +415,13 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
   }
   const int n_tiles = (int)ceil_div(a.T, kTileTokens);
   const size_t smem = (size_t)(kWarps * a.E) * sizeof(int);
-  cudaError_t e = cudaSuccess;
-  if (!g_attr_multi) {
+  cudaError_t e = g_attr_multi.run([](int&) {
     const int most = (int)(kWarps * 1024 * sizeof(int));
-    e = cudaFuncSetAttribute(dispatch_count, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(dispatch_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-    if (e != cudaSuccess) return e;
-    g_attr_multi = true;
-  }
+    const cudaError_t r = cudaFuncSetAttribute(dispatch_count, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (r != cudaSuccess) return r;
+    return cudaFuncSetAttribute(dispatch_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+  });
+  if (e != cudaSuccess) return e;
   launch_k(dispatch_count, n_tiles, kThreads, smem, s, a);
   launch_k(dispatch_scan, 1, kThreads, 0, s, a, n_tiles);
   launch_k(dispatch_scatter, n_tiles, kThreads, smem, s, a);

@@ -860,20 +860,25 @@ cudaError_t launch_t(const TcMaps& maps, const GemvArgs& a, int E, int m_tiles, 
   auto kernel = tc_gemm_kernel<EPI, OUT_F32, FP4A, CG>;
   const size_t smem = smem_bytes<CG, (FP4A != 0)>(kMaxSegments);
   const int threads = FP4A ? kThreadsFp4 : kThreads;
-  // shared-memory limit set once, and the CTAs (CG 1) or CTA pairs (CG 2)
-  // resident at once (thread-safe static initialisation)
-  struct Cap { cudaError_t e; int units; };
-  static const Cap cap = [&]() -> Cap {
-    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return {e, 0};
-    if (CG == 2) {
-      const int p = max_pairs(kernel, smem, threads);
-      return {cudaSuccess, p > 0 ? p : num_sms() / 2};
-    }
-    return {cudaSuccess, num_sms()};
-  }();
-  if (cap.e != cudaSuccess) return cap.e;
-  units = std::max(1, std::min(units, cap.units));
+  // shared-memory limit set once per device, and the CTAs (CG 1) or CTA pairs
+  // (CG 2) resident at once on it
+  static PerDeviceOnce cap;
+  int cap_units = 0;
+  const cudaError_t ce = cap.run(
+      [&](int& v) -> cudaError_t {
+        const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (CG == 2) {
+          const int p = max_pairs(kernel, smem, threads);
+          v = p > 0 ? p : num_sms() / 2;
+        } else {
+          v = num_sms();
+        }
+        return cudaSuccess;
+      },
+      &cap_units);
+  if (ce != cudaSuccess) return ce;
+  units = std::max(1, std::min(units, cap_units));
   if (CG == 1) return launch_k(kernel, units, threads, smem, s, maps, a, E, m_tiles, bn, b_period, tma_out, ksplit);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * units);

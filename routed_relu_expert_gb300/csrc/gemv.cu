@@ -642,14 +642,15 @@ cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_
       return cudaErrorNotSupported;
     }
 #undef MOE_NVK
-    // every instantiation's shared-memory limit, set once (thread-safe static)
-    static const cudaError_t attr = [] {
+    // every instantiation's shared-memory limit, set once per device
+    static PerDeviceOnce attr_once;
+    const cudaError_t attr = attr_once.run([](int&) {
       for (cudaError_t e : {bulk_attr<EPI_RELU2, 0, false>(), bulk_attr<EPI_RELU2, 0, true>(),
                             bulk_attr<EPI_RELU2, 2, false>(), bulk_attr<EPI_RELU2, 2, true>(),
                             bulk_attr<EPI_SCALE, 1, false>(), bulk_attr<EPI_SCALE, 1, true>()})
         if (e != cudaSuccess) return e;
       return cudaSuccess;
-    }();
+    });
     if (attr != cudaSuccess) return attr;
     return launch_k(k, dim3((unsigned)(a.N / (64 / wpg)), segs, 1), kBulkThreads, smem, s, a);
   }

@@ -3,10 +3,33 @@
 
 #include "common.cuh"
 
+#include <mutex>
+
 namespace moe {
 
 // host-side count of kernel launches (moe_launch_count)
 void count_launches(int n);
+
+// One-time set-up that belongs to a device (a kernel's shared-memory limit set
+// by cudaFuncSetAttribute, a resident-CTA count): run once per device index,
+// with that device current, and the result kept per device, so a process that
+// drives several GPUs sets each one up.  Thread-safe.
+constexpr int kMaxDevices = 64;
+struct PerDeviceOnce {
+  std::once_flag flag[kMaxDevices];
+  cudaError_t err[kMaxDevices] = {};
+  int val[kMaxDevices] = {};
+  // fn(int& value) -> cudaError_t runs on the first call for the current
+  // device; *value receives the value it stored
+  template <class F>
+  cudaError_t run(F&& fn, int* value = nullptr) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(flag[dev], [&] { err[dev] = fn(val[dev]); });
+    if (value) *value = val[dev];
+    return err[dev];
+  }
+};
 
 // Launch with programmatic stream serialisation (see pdl_wait / pdl_trigger).
 template <typename... KArgs, typename... Args>
@@ -132,6 +155,10 @@ struct DispatchArgs {
 };
 size_t dispatch_tile_count_elems(int T, int K, int E);
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
+// x_packed[j] = x_e[route_token[j]] for the offsets[E] <= R packed rows (rows
+// of de elements of elem_bytes; to_f16: BF16 rows stored as FP16 copies)
+cudaError_t launch_pack_rows(const void* x_e, const int32_t* route_token, const int32_t* offsets, int E, int R,
+                             int de, int elem_bytes, bool to_f16, void* x_packed, cudaStream_t s);
 
 // selection arguments (see launch_router_select)
 struct SelectArgs {

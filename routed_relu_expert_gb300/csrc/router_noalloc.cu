@@ -16,7 +16,9 @@
 //    (four logit-sized slabs), both held in the array.
 //  - The first call on a device looks up the array's device address with
 //    cudaGetSymbolAddress (once per device, with that device current); make
-//    that first call before any stream capture.
+//    that first call before any stream capture.  The address is kept for the
+//    life of the process: it assumes the device's primary context is never
+//    reset (after cudaDeviceReset the array would have to be looked up again).
 //  - Every call shares the one array: two calls whose work overlaps on the GPU
 //    (different streams, no ordering between them) race on it.  The error
 //    word is cleared at the start of every call; logits and scores are fully
@@ -71,7 +73,9 @@ extern "C" moe_status_t moe_router_noalloc(const moe_config_t* cfg, int32_t T, c
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if ((int64_t)T * cfg->n_experts > kMaxElems) return MOE_ERR_WORKSPACE;   // beyond the static scratch
-  const bool needs_split = cfg->act_dtype == MOE_DT_BF16 && T > 64;
+  // the same condition as the router's tensor-core path (d_model % 64 == 0
+  // holds for every valid configuration)
+  const bool needs_split = cfg->act_dtype == MOE_DT_BF16 && T > 64 && cfg->n_experts % 32 == 0;
   if (needs_split && (int64_t)3 * cfg->n_experts * cfg->d_model > kMaxSplit) return MOE_ERR_WORKSPACE;
   if (!x || !w_router || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(topk_ids) || !aligned16(topk_w) ||

@@ -94,6 +94,14 @@ def new_workspace(cfg: N.MoeConfig, T: int, device="cuda") -> torch.Tensor:
     return ws
 
 
+def workspace_region(cfg: N.MoeConfig, T: int, region: int):
+    """(byte offset, bytes) of one of the route tables in a workspace for T tokens."""
+    off, n = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    N.check(N.load().moe_workspace_region(ctypes.byref(cfg), int(T), int(region), ctypes.byref(off),
+                                          ctypes.byref(n)), "moe_workspace_region")
+    return int(off.value), int(n.value)
+
+
 def _ws(ws: torch.Tensor):
     return _p(ws), ctypes.c_size_t(ws.numel())
 
@@ -133,6 +141,12 @@ def moe_experts_down_combine(cfg, T, h, offsets, route_token, route_slot, token_
     N.check(N.load().moe_experts_down_combine(ctypes.byref(cfg), T, _p(h), _p(offsets), _p(route_token),
                                               _p(route_slot), _p(token_slot_row), _p(topw), weights.ref,
                                               _p(y_routed), w, n, _s(stream)), "moe_experts_down_combine")
+
+
+def moe_experts_down(cfg, T, h, offsets, route_token, route_slot, topw, weights: Weights, u, ws, stream=None):
+    w, n = _ws(ws)
+    N.check(N.load().moe_experts_down(ctypes.byref(cfg), T, _p(h), _p(offsets), _p(route_token), _p(route_slot),
+                                      _p(topw), weights.ref, _p(u), w, n, _s(stream)), "moe_experts_down")
 
 
 def moe_latent_down(cfg, x, weights: Weights, x_l, ws, stream=None):

@@ -70,9 +70,33 @@ def run_gpu(shape: MoEShape, w: Dict[str, torch.Tensor], x: torch.Tensor):
     logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
     scores = torch.empty((T, E), dtype=torch.float32, device="cuda")
     layer.forward(x, y, ids_out=ids, topw_out=topw, logits_out=logits, scores_out=scores)
-    err = M.moe_get_device_error(layer.workspace(T, x.device))
+    ws = layer.workspace(T, x.device)
+    err = M.moe_get_device_error(ws)
     torch.cuda.synchronize()
-    return {"y": y, "ids": ids, "topw": topw, "logits": logits, "scores": scores, "err": err, "layer": layer}
+    return {"y": y, "ids": ids, "topw": topw, "logits": logits, "scores": scores, "err": err, "layer": layer,
+            "ws": ws}
+
+
+def ws_table(ws: torch.Tensor, cfg, T: int, region: int, dtype: torch.dtype) -> torch.Tensor:
+    """A route table (or row region) the layer left in its workspace, as a flat
+    device tensor view."""
+    off, nbytes = M.workspace_region(cfg, T, region)
+    return ws[off:off + nbytes].view(dtype)
+
+
+def check_route_tables(shape: MoEShape, ws: torch.Tensor, ids_gpu: np.ndarray, T: int) -> Dict[str, np.ndarray]:
+    """The dispatch tables moe_layer_forward left in its workspace (counts,
+    offsets, per-expert token lists, slots, inverse map) bit-exact against the
+    oracle's dispatch of the same expert ids.  Returns the oracle's tables."""
+    from routed_relu_expert_gb300 import _native as N
+    cfg = M.config_from(shape)
+    ref = O.dispatch(ids_gpu, shape.n_experts)
+    for region, key in ((N.MOE_WS_COUNTS, "counts"), (N.MOE_WS_OFFSETS, "offsets"),
+                        (N.MOE_WS_ROUTE_TOKEN, "route_token"), (N.MOE_WS_ROUTE_SLOT, "route_slot"),
+                        (N.MOE_WS_TOKEN_SLOT_ROW, "token_slot_row")):
+        got = ws_table(ws, cfg, T, region, torch.int32).cpu().numpy().astype(np.int64)
+        assert np.array_equal(got, ref[key].reshape(-1)), f"{key} differs from the oracle's dispatch"
+    return ref
 
 
 def check_router(shape: MoEShape, x_np: np.ndarray, ow: Dict, g: Dict, rows: Optional[np.ndarray] = None):
@@ -97,11 +121,24 @@ def check_router(shape: MoEShape, x_np: np.ndarray, ow: Dict, g: Dict, rows: Opt
 
 
 def check_output(shape: MoEShape, x_np: np.ndarray, ow: Dict, ids_o, w_o, y_gpu: np.ndarray, tol: float,
-                 rows: Optional[np.ndarray] = None) -> float:
+                 rows: Optional[np.ndarray] = None, chunk: int = 0) -> float:
+    """max |y - y_ref| / RMS(y_ref) over the given rows (all by default), the
+    oracle evaluated on the GPU's routing; ``chunk`` > 0 evaluates the oracle
+    that many rows at a time (the layer is per token, so the result is the
+    same; only host memory is bounded)."""
     rows = np.arange(x_np.shape[0]) if rows is None else rows
-    ref = O.layer_forward(x_np[rows], ow, ids_o, w_o, shape.n_experts, bf16_points=shape.act_dtype == BF16)["y"]
-    rms = float(np.sqrt(np.mean(ref ** 2)))
-    err = float(np.max(np.abs(y_gpu[rows].astype(np.float64) - ref))) / rms
+    ids_o, w_o = np.asarray(ids_o), np.asarray(w_o)
+    step = chunk if chunk > 0 else len(rows)
+    worst, sq, n = 0.0, 0.0, 0
+    for i in range(0, len(rows), step):
+        sel = rows[i:i + step]
+        ref = O.layer_forward(x_np[sel], ow, ids_o[i:i + step], w_o[i:i + step], shape.n_experts,
+                              bf16_points=shape.act_dtype == BF16)["y"]
+        worst = max(worst, float(np.max(np.abs(y_gpu[sel].astype(np.float64) - ref))))
+        sq += float(np.sum(ref ** 2))
+        n += ref.size
+    rms = (sq / n) ** 0.5
+    err = worst / rms
     assert err <= tol, f"max |y - y_ref| = {err:.3e} RMS > {tol}"
     return err
 

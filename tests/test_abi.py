@@ -113,3 +113,40 @@ def test_status_strings(lib):
     for s in range(6):
         assert lib.moe_status_string(s)
     assert lib.moe_version() >= 100
+
+
+def test_noalloc_limits_match_header():
+    """The binding's copies of the static-scratch limits equal the header's."""
+    from routed_relu_expert_gb300 import _native as N
+    text = open(HEADER).read()
+    for name in ("MOE_NOALLOC_MAX_ROUTER_ELEMS", "MOE_NOALLOC_MAX_SPLIT_ELEMS"):
+        m = re.search(r"#define\s+" + name + r"\s+(\d+)", text)
+        assert m, name
+        assert int(m.group(1)) == getattr(N, name)
+
+
+def test_workspace_regions_lie_inside_the_workspace(lib):
+    """Every route table moe_workspace_region names fits in moe_workspace_bytes,
+    with the sizes the header states, and no two overlap."""
+    from routed_relu_expert_gb300 import _native as N
+    import routed_relu_expert_gb300 as M
+    from synth import NANO_DECODE, SUPER_NVFP4
+    for shape, T in ((NANO_DECODE, 1), (NANO_DECODE, 300), (SUPER_NVFP4, 65)):
+        cfg = M.config_from(shape)
+        total = M.workspace_bytes(cfg, T)
+        E, K, R = shape.n_experts, shape.top_k, T * shape.top_k
+        sizes = {N.MOE_WS_COUNTS: E * 4, N.MOE_WS_OFFSETS: (E + 1) * 4, N.MOE_WS_ROUTE_TOKEN: R * 4,
+                 N.MOE_WS_ROUTE_SLOT: R * 4, N.MOE_WS_TOKEN_SLOT_ROW: R * 4, N.MOE_WS_TOPK_IDS: R * 4,
+                 N.MOE_WS_TOPK_W: R * 4, N.MOE_WS_LOGITS: T * E * 4, N.MOE_WS_SCORES: T * E * 4,
+                 N.MOE_WS_X_LATENT: T * shape.d_latent * 2, N.MOE_WS_X_PACKED: R * shape.d_e * 2}
+        spans = []
+        for region, nbytes in sizes.items():
+            off, n = M.workspace_region(cfg, T, region)
+            assert n == nbytes and off % 256 == 0 and off + n <= total
+            if n:
+                spans.append((off, off + n))
+        spans.sort()
+        assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:]))
+        off = ctypes.c_size_t(0)
+        assert lib.moe_workspace_region(ctypes.byref(cfg), T, 99, ctypes.byref(off), ctypes.byref(off)) == \
+            N.MOE_ERR_INVALID_ARG

@@ -9,15 +9,15 @@ import pytest
 import torch
 
 from oracle import moe_oracle as O
-from synth import (NANO_DECODE, NANO_PREFILL, ROUTER_ONLY_GROUPED, SUPER_LATENT, SUPER_NVFP4, TINY_FP32,
+from synth import (BF16, NANO_DECODE, NANO_PREFILL, ROUTER_ONLY_GROUPED, SUPER_LATENT, SUPER_NVFP4, TINY_FP32,
                    make_weights, make_x, scaled)
 
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     import routed_relu_expert_gb300 as M
-    from gpu_helpers import (check_output, check_router, device_weights, oracle_weights, run_gpu, to_np,
-                             tol_of)
+    from gpu_helpers import (check_output, check_route_tables, check_router, device_weights, oracle_weights,
+                             run_gpu, to_np, tol_of, ws_table)
 
 SMALL_NANO = scaled(NANO_DECODE, name="nano_scaled", d_model=512, n_experts=32, top_k=4, d_expert=320,
                     d_shared=384, weight_seed=11, tokens=())
@@ -28,21 +28,48 @@ SMALL_NVFP4 = scaled(SUPER_LATENT, name="nvfp4_scaled", d_model=512, d_latent=25
                      tokens=())
 
 
-def _parity(shape, T, sample=None, seed_stream=0):
+def _check_packed_rows(shape, g, x, T):
+    """Above 64 BF16 tokens the layer packs its expert input rows for the
+    tensor-core kernels: x_packed[j] must be x_e[route_token[j]] bit for bit
+    (with NVFP4 experts, the FP16 copy of that BF16 row)."""
+    from routed_relu_expert_gb300 import _native as N
+    cfg = M.config_from(shape)
+    ws = g["ws"]
+    de = shape.d_e
+    rt = ws_table(ws, cfg, T, N.MOE_WS_ROUTE_TOKEN, torch.int32).long()
+    x_e = x if not shape.d_latent else ws_table(ws, cfg, T, N.MOE_WS_X_LATENT, torch.bfloat16).view(T, de)
+    want = x_e[rt]
+    if shape.expert_dtype == 2:
+        want = want.to(torch.float16)
+    got = ws_table(ws, cfg, T, N.MOE_WS_X_PACKED, want.dtype).view(-1, de)
+    assert torch.equal(got.view(torch.int16), want.contiguous().view(torch.int16))
+
+
+def _parity(shape, T, sample=None, seed_stream=0, chunk=0):
+    """Routing of every token (ids bit-exact, weights 1e-6, logits 1e-5), the
+    dispatch tables the layer left in its workspace bit-exact, the packed rows
+    of the tensor-core path bit-exact, and the output against the oracle on
+    every row (or on ``sample`` rows)."""
     w = device_weights(shape)
     x = make_x(shape, T, "cuda", seed_stream)
-    g = to_np(run_gpu(shape, w, x))
+    g = run_gpu(shape, w, x)
     assert g["err"] == 0
+    if T > 64 and shape.act_dtype == BF16:
+        _check_packed_rows(shape, g, x, T)
+    ws = g.pop("ws")
+    g = to_np(g)
+    check_route_tables(shape, ws, g["ids"], T)
+    del ws
     ow = oracle_weights(w)
     x_np = x.float().cpu().numpy().astype(np.float64)
     # routing on every token
-    ids_all, _ = check_router(shape, x_np, ow, g)
+    ids_o, w_o = check_router(shape, x_np, ow, g)
     rows = None
     if sample is not None and sample < T:
-        rng = np.random.default_rng(T)
-        rows = np.sort(rng.choice(T, sample, replace=False))
-    ids_o, w_o = check_router(shape, x_np, ow, g, rows)
-    err = check_output(shape, x_np, ow, ids_o, w_o, g["y"], tol_of(shape), rows)
+        rows = sample if isinstance(sample, np.ndarray) else np.sort(
+            np.random.default_rng(T).choice(T, sample, replace=False))
+        ids_o, w_o = ids_o[rows], w_o[rows]
+    err = check_output(shape, x_np, ow, ids_o, w_o, g["y"], tol_of(shape), rows, chunk=chunk)
     return err, g
 
 
@@ -66,13 +93,20 @@ def test_nano_decode_full_size(T):
     _parity(NANO_DECODE, T)
 
 
-def test_nano_prefill_2048_sampled():
-    _parity(NANO_PREFILL, 2048, sample=192)
+def test_nano_prefill_2048_full():
+    _parity(NANO_PREFILL, 2048)
 
 
-def test_nano_prefill_8192_sampled():
-    """The bench's prefill size: ids of every token, outputs of a sample."""
-    _parity(NANO_PREFILL, 8192, sample=48)
+def test_nano_prefill_8192_full():
+    """Every token's routing and every output row at T=8192."""
+    _parity(NANO_PREFILL, 8192, chunk=4096)
+
+
+def test_nano_prefill_32768_full():
+    """The largest routed workload (196,608 routes, one expert holding most of
+    the tokens under the Zipf popularity): routing, dispatch tables and packed
+    rows of every token, and every output row."""
+    _parity(NANO_PREFILL, 32768, chunk=4096)
 
 
 @pytest.mark.parametrize("T", [1, 16])
@@ -80,12 +114,12 @@ def test_super_latent_full_size(T):
     _parity(SUPER_LATENT, T)
 
 
-def test_super_latent_256_sampled():
-    _parity(SUPER_LATENT, 256, sample=48)
+def test_super_latent_256_full():
+    _parity(SUPER_LATENT, 256)
 
 
-def test_super_latent_4096_sampled():
-    _parity(SUPER_LATENT, 4096, sample=24)
+def test_super_latent_4096_full():
+    _parity(SUPER_LATENT, 4096, chunk=2048)
 
 
 @pytest.mark.parametrize("T", [1, 9, 64, 65, 200])
@@ -98,8 +132,8 @@ def test_super_nvfp4_full_size(T):
     _parity(SUPER_NVFP4, T)
 
 
-def test_super_nvfp4_8192_sampled():
-    _parity(SUPER_NVFP4, 8192, sample=24)
+def test_super_nvfp4_8192_full():
+    _parity(SUPER_NVFP4, 8192, chunk=8192)
 
 
 def test_router_grouped_case_from_the_router_parity_test():
@@ -155,10 +189,15 @@ def test_dispatch_is_bit_exact(T, E, K):
     assert M.moe_get_device_error(ws) == 0
 
 
-def test_step_entry_points_reproduce_layer_forward_bit_for_bit():
+@pytest.mark.parametrize("case", ["decode", "prefill"])
+def test_step_entry_points_reproduce_layer_forward_bit_for_bit(case):
     # (the NVFP4 layer runs its decode GEMVs on FP16 copies of the activations,
-    # the step entry points on the BF16 tensors: the same values either way)
-    for shape, T in ((SMALL_NANO, 37), (SMALL_SUPER, 13), (SMALL_NVFP4, 9)):
+    # the step entry points on the BF16 tensors: the same values either way.
+    # At prefill sizes moe_experts_up is given x_e only and gathers the rows
+    # itself for the tensor-core kernel.)
+    cases = (((SMALL_NANO, 37), (SMALL_SUPER, 13), (SMALL_NVFP4, 9)) if case == "decode"
+             else ((SMALL_NANO, 300), (SMALL_SUPER, 200)))
+    for shape, T in cases:
         w = device_weights(shape)
         x = make_x(shape, T, "cuda", 3)
         cfg = M.config_from(shape)
