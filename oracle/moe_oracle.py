@@ -116,6 +116,83 @@ def dequant_nvfp4(q: np.ndarray, sf: np.ndarray, gs) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
+# NVFP4 activation terms (the FP4 tensor-core path).  The NVFP4 block format
+# -- E2M1 values, one E4M3 scale per 16 consecutive values, one FP32 scale
+# per tensor -- is the one of page "Nemotron-3.5-Super 120B on an 8 GB GPU",
+# section "The engine, step by step", item 4.  A row of activations is split
+# into n terms of that format, each quantising what the previous terms left
+# (residual quantisation), so the products can run with both operands in
+# NVFP4; n = 1 is plain W4A4.  Every decision is taken in FP32, as the device
+# takes it: g = amax(row) / (6 * 448); per term and 16-value block,
+# scale = E4M3_rn(amax(block) / (6 g)) (saturating), s = scale * g,
+# code = E2M1_rn(r / s) (saturating; 0 where s = 0), r -= code * s.
+# ----------------------------------------------------------------------------
+_E2M1_GRID = np.array([e2m1_value(c) for c in range(8)], dtype=np.float64)          # codes 0..7
+_E4M3_GRID = np.array([e4m3_value(b) for b in range(127)], dtype=np.float64)        # codes 0..126 (127 = NaN)
+
+
+def _rne_code(a: np.ndarray, grid: np.ndarray) -> np.ndarray:
+    """Code of the nearest value of an increasing grid to a >= 0, ties to the
+    even code, values beyond the last one saturating to it."""
+    a = np.minimum(np.asarray(a, dtype=np.float64), grid[-1])
+    hi = np.clip(np.searchsorted(grid, a, side="left"), 0, len(grid) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - grid[lo], grid[hi] - a
+    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    return np.where(a == grid[hi], hi, np.where(take_hi, hi, lo)).astype(np.uint8)
+
+
+def e4m3_rn_code(v) -> np.ndarray:
+    """E4M3 code of the nearest E4M3 value to v >= 0 (ties to even, saturating at 448)."""
+    return _rne_code(v, _E4M3_GRID)
+
+
+def e2m1_rn_code(v) -> np.ndarray:
+    """Signed 4-bit E2M1 code of the nearest E2M1 value to v (ties to even,
+    saturating at +-6); a value that rounds to zero gets the code 0."""
+    v = np.asarray(v, dtype=np.float64)
+    c = _rne_code(np.abs(v), _E2M1_GRID)
+    return np.where((v < 0) & (c > 0), c | 8, c).astype(np.uint8)
+
+
+def nvfp4_terms(x: np.ndarray, n_terms: int):
+    """Rows x [T, K] (FP32 values; K a multiple of 16) -> (codes [n, T, K] u8
+    signed E2M1 codes, scales [n, T, K/16] u8 E4M3 codes, g [T] FP32)."""
+    x = np.asarray(x, dtype=np.float32)
+    T, K = x.shape
+    g = (np.max(np.abs(x), axis=1) / np.float32(6.0 * 448.0)).astype(np.float32) if K else np.zeros(T, np.float32)
+    g = np.where(g > 0, g, np.float32(1.0)).astype(np.float32)
+    six_g = (np.float32(6.0) * g).astype(np.float32)
+    r = x.reshape(T, K // 16, 16).copy()
+    codes = np.zeros((n_terms, T, K // 16, 16), dtype=np.uint8)
+    scales = np.zeros((n_terms, T, K // 16), dtype=np.uint8)
+    for j in range(n_terms):
+        amax_b = np.max(np.abs(r), axis=2).astype(np.float32)
+        sf = e4m3_rn_code((amax_b / six_g[:, None]).astype(np.float32))
+        s = (_E4M3_GRID[sf].astype(np.float32) * g[:, None]).astype(np.float32)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            ratio = np.where(s[..., None] > 0, r / np.where(s > 0, s, np.float32(1))[..., None], np.float32(0))
+        c = e2m1_rn_code(ratio.astype(np.float32))
+        q = (np.where(c & 8, -1.0, 1.0) * _E2M1_GRID[c & 7]).astype(np.float32)
+        r = (r - (q * s[..., None]).astype(np.float32)).astype(np.float32)
+        codes[j], scales[j] = c, sf
+    return codes.reshape(n_terms, T, K), scales, g
+
+
+def dequant_terms(codes: np.ndarray, scales: np.ndarray, g: np.ndarray) -> np.ndarray:
+    """Sum over terms of E2M1(code) * E4M3(scale) * g, float64 [T, K]."""
+    n, T, K = codes.shape
+    v = np.where(codes & 8, -1.0, 1.0) * _E2M1_GRID[codes & 7]
+    v = v.reshape(n, T, K // 16, 16) * _E4M3_TABLE[scales][..., None]
+    return v.sum(axis=0).reshape(T, K) * np.asarray(g, dtype=np.float64)[:, None]
+
+
+def nvfp4_activations(x: np.ndarray, n_terms: int) -> np.ndarray:
+    """x replaced by the sum of its n_terms NVFP4 terms (float64)."""
+    return dequant_terms(*nvfp4_terms(x, n_terms))
+
+
+# ----------------------------------------------------------------------------
 # router (page "Nemotron Is Not One Circuit", "The Router Is A Deterministic
 # Algorithm" and "The C Kernel Contract")
 # ----------------------------------------------------------------------------
@@ -303,16 +380,24 @@ def moe_apply(h: np.ndarray, ids: np.ndarray, gates: np.ndarray,
 # ----------------------------------------------------------------------------
 
 
-def relu2_mlp(x: np.ndarray, w_up: np.ndarray, w_down: np.ndarray, bf16_points: bool) -> np.ndarray:
+def relu2_mlp(x: np.ndarray, w_up: np.ndarray, w_down: np.ndarray, bf16_points: bool,
+              act_terms: Optional[int] = None) -> np.ndarray:
     """ReLU^2 MLP without gate: W_down relu(W_up x)^2 with stored [out, in]
     matrices; with ``bf16_points`` the up output and the squared ReLU are each
-    rounded to BF16 (page "NemotronH ...", section "Arithmetic")."""
-    a = np.asarray(x, dtype=np.float64) @ np.asarray(w_up, dtype=np.float64).T
+    rounded to BF16 (page "NemotronH ...", section "Arithmetic").  With
+    ``act_terms`` the inputs of both products (x and h) are replaced by their
+    NVFP4 terms (``nvfp4_activations``)."""
+    x = np.asarray(x, dtype=np.float64)
+    if act_terms:
+        x = nvfp4_activations(x, act_terms)
+    a = x @ np.asarray(w_up, dtype=np.float64).T
     if bf16_points:
         a = bf16_round(a)
     h = np.maximum(a, 0.0) ** 2
     if bf16_points:
         h = bf16_round(h)
+    if act_terms:
+        h = nvfp4_activations(h, act_terms)
     return h @ np.asarray(w_down, dtype=np.float64).T
 
 
@@ -327,14 +412,16 @@ def expert_matrices(weights: Dict[str, np.ndarray], e: int) -> Tuple[np.ndarray,
 
 
 def layer_forward(x: np.ndarray, weights: Dict[str, np.ndarray], ids: np.ndarray, w: np.ndarray,
-                  n_experts: int, bf16_points: bool) -> Dict[str, np.ndarray]:
+                  n_experts: int, bf16_points: bool, act_terms: Optional[int] = None) -> Dict[str, np.ndarray]:
     """MoE layer output for given routing (ids [T,K], weights w [T,K]).
 
     Steps: latent down (if any) -> packed dispatch -> per expert ReLU^2 MLP ->
     weighted scatter-add in ascending expert id -> shared expert -> latent up
     (if any) -> sum.  No residual and no norm (page "M6.1 Routed Capacity",
     section 0x05F: the residual is not part of the MoE output).  Returns the
-    float64 output before storage rounding plus the intermediates."""
+    float64 output before storage rounding plus the intermediates.
+    ``act_terms``: the routed experts' input rows and h enter their products
+    as NVFP4 terms (``relu2_mlp``); the shared expert is unchanged."""
     x = np.asarray(x, dtype=np.float64)
     latent = "w_lat_down" in weights
     if latent:
@@ -345,7 +432,7 @@ def layer_forward(x: np.ndarray, weights: Dict[str, np.ndarray], ids: np.ndarray
         x_e = x
     experts = []
     for e in range(n_experts):
-        experts.append(_LazyExpert(weights, e, bf16_points))
+        experts.append(_LazyExpert(weights, e, bf16_points, act_terms))
     y_r = moe_apply(x_e, ids, w, experts)
     out = {"y_routed": y_r, "x_e": x_e}
     if "w_sh_up" in weights:
@@ -365,12 +452,12 @@ def layer_forward(x: np.ndarray, weights: Dict[str, np.ndarray], ids: np.ndarray
 class _LazyExpert:
     """Expert e as a callable (matrices fetched, and dequantised, on first use)."""
 
-    def __init__(self, weights, e, bf16_points):
-        self.weights, self.e, self.bf16_points = weights, e, bf16_points
+    def __init__(self, weights, e, bf16_points, act_terms=None):
+        self.weights, self.e, self.bf16_points, self.act_terms = weights, e, bf16_points, act_terms
 
     def __call__(self, xs: np.ndarray) -> np.ndarray:
         up, down = expert_matrices(self.weights, self.e)
-        return relu2_mlp(xs, up, down, self.bf16_points)
+        return relu2_mlp(xs, up, down, self.bf16_points, self.act_terms)
 
 
 def full_layer(x: np.ndarray, weights: Dict[str, np.ndarray], n_experts: int, top_k: int,

@@ -145,3 +145,95 @@ def test_super_latent_pair_and_shared_bytes_match_the_super_ledger():
     assert round(layers * latent_pair / 1e9, 2) == g["super_latent_pair_gb"]
     shared_nvfp4 = 2 * s.d_model * s.d_shared * (0.5 + 1 / 16)
     assert round(layers * shared_nvfp4 / 1e9, 2) == g["super_shared_nvfp4_gb"]
+
+
+# ------------------------------------------------ NVFP4 activation terms ----
+def test_e4m3_rn_code_matches_torch_cast():
+    """Round-to-nearest-even onto E4M3 (saturating at 448) equals torch's
+    float8_e4m3fn cast on random values, subnormals and exact midpoints."""
+    rng = np.random.default_rng(3)
+    grid = np.array([O.e4m3_value(b) for b in range(127)])
+    mids = ((grid[1:] + grid[:-1]) / 2).astype(np.float32)
+    v = np.concatenate([rng.uniform(0, 448, 5000), 2.0 ** rng.uniform(-12, 8.8, 5000), mids, grid,
+                        [0.0, 448.0, 2.0 ** -10, 3 * 2.0 ** -11]]).astype(np.float32)
+    v = v[v <= 448]
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_rn_code(v), ref)
+    assert O.e4m3_rn_code(np.float32(1e6)) == 126            # saturates to 448
+
+
+def test_e2m1_rn_code_matches_the_weight_quantiser():
+    """Signed E2M1 rounding equals the synthetic weights' encoder (ties to the
+    even code, saturating at 6) on random values and every midpoint."""
+    from synth.generate import _e2m1_codes
+    rng = np.random.default_rng(4)
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    v = np.concatenate([rng.uniform(-8, 8, 20000), mids, [-m for m in mids], [0, 6, -6, 7.5, -100]]).astype(np.float32)
+    ref = _e2m1_codes(torch.from_numpy(v)).numpy()
+    assert np.array_equal(O.e2m1_rn_code(v), ref)
+
+
+def test_first_activation_term_is_the_weight_quantiser():
+    """One term of a row is exactly the NVFP4 encoding the synthetic weights
+    use (per-row scale amax/(6*448), E4M3 block scales, E2M1 codes)."""
+    rng = np.random.default_rng(5)
+    x = torch.from_numpy(rng.standard_normal((6, 256)).astype(np.float32) * 3).to(torch.bfloat16).float()
+    codes, sf, g = O.nvfp4_terms(x.numpy(), 1)
+    for t in range(6):
+        q, s, gs = quantize_nvfp4(x[t:t + 1])
+        ref_codes = np.empty(256, dtype=np.uint8)
+        ref_codes[0::2] = q.numpy()[0] & 0xF
+        ref_codes[1::2] = q.numpy()[0] >> 4
+        val = lambda c: np.where(c & 8, -1.0, 1.0) * np.array([O.e2m1_value(i) for i in range(8)])[c & 7]
+        assert np.array_equal(val(codes[0, t]), val(ref_codes))
+        assert np.array_equal(sf[0, t], s.numpy()[0])
+        assert g[t] == np.float32(gs.item())
+
+
+def test_activation_terms_of_representable_values():
+    """Blocks that are powers of two times E2M1 values come back from the
+    first term exactly (codes) and the remaining residual is FP32 noise."""
+    rng = np.random.default_rng(6)
+    vals = np.array([O.e2m1_value(c) for c in range(16)])
+    x = np.empty((2, 128), dtype=np.float32)
+    for t in range(2):
+        for b in range(8):
+            blk = rng.choice(vals, 16)
+            blk[0] = 6.0                                   # every block reaches the top code
+            x[t, 16 * b:16 * b + 16] = blk * 2.0 ** (b - 4)
+    codes, sf, g = O.nvfp4_terms(x, 3)
+    c0 = np.where(codes[0] & 8, -1.0, 1.0) * np.abs(vals[codes[0] & 7])
+    expect = x.reshape(2, 8, 16) / (2.0 ** (np.arange(8) - 4))[None, :, None]
+    assert np.array_equal(c0.reshape(2, 8, 16), expect)
+    rec = O.dequant_terms(codes, sf, g)
+    assert np.max(np.abs(rec - x)) <= 1e-6 * np.max(np.abs(x))
+
+
+def test_activation_terms_shrink_the_error_per_term():
+    """Each term leaves at most ~0.18 of the previous residual of a block (the
+    E2M1 grid's widest half-gap relative to its top value, plus the E4M3 scale
+    rounding), so n terms reach 0.18^n of the block's largest magnitude."""
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal((8, 1024)) * np.exp(rng.standard_normal((8, 1)))).astype(np.float32)
+    bmax = np.abs(x.reshape(8, 64, 16)).max(-1)
+    prev = None
+    for n in (1, 2, 3, 4):
+        err = np.abs(O.nvfp4_activations(x, n) - x).reshape(8, 64, 16).max(-1)
+        assert np.all(err <= 0.18 ** n * bmax + 1e-30)
+        if prev is not None:
+            assert err.max() < prev
+        prev = err.max()
+
+
+def test_many_activation_terms_converge_to_the_exact_mlp():
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((5, 256))
+    up = rng.standard_normal((128, 256)) / 16
+    down = rng.standard_normal((256, 128)) / 11
+    exact = O.relu2_mlp(x, up, down, bf16_points=False)
+    approx = O.relu2_mlp(x, up, down, bf16_points=False, act_terms=6)
+    assert np.max(np.abs(approx - exact)) <= 1e-4 * np.sqrt(np.mean(exact ** 2))
+    # one term (plain W4A4) quantises both product inputs: x and h
+    xq = O.nvfp4_activations(x, 1)
+    h = O.nvfp4_activations(np.maximum(xq @ up.T, 0) ** 2, 1)
+    assert np.allclose(O.relu2_mlp(x, up, down, bf16_points=False, act_terms=1), h @ down.T, rtol=0, atol=1e-12)
