@@ -41,8 +41,10 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.md")
 # holds only while their hash is unchanged
 KERNEL_SOURCES = {
     "gemv": ("gemv.cu", "epilogue.cuh", "nvfp4.cuh", "common.cuh", "internal.h"),
-    "tc": ("gemm_tc.cu", "epilogue.cuh", "nvfp4.cuh", "common.cuh", "internal.h"),
+    "tc": ("gemm_tc.cu", "tc_common.cuh", "epilogue.cuh", "nvfp4.cuh", "common.cuh", "internal.h"),
+    "fp4": ("gemm_fp4.cu", "tc_common.cuh", "epilogue.cuh", "nvfp4.cuh", "common.cuh", "internal.h"),
 }
+ACT_TERMS = 3            # the library's default NVFP4 activation terms
 
 
 def parse(argv=None):
@@ -475,9 +477,24 @@ def measure_products(run: Runner, shape, T, layers, x, n_active, pk):
     return out
 
 
+def fp4_tile_rows(rows_per_seg, segs, N, sms=152):
+    """Rows per tile of the FP4 grouped GEMM (the library's rule)."""
+    bn = 16 if rows_per_seg <= 16 else 32 if rows_per_seg <= 32 else 64 if rows_per_seg <= 64 else 128
+    while bn > 16 and -(-rows_per_seg // bn) * segs * -(-N // 128) < 2 * sms:
+        bn -= 16
+    return bn
+
+
 def product_kernel_name(shape, T, which):
     """The kernel that runs a grouped expert product at this size (names as the
     profiler prints their template arguments)."""
+    if shape.expert_dtype == 2:
+        R = T * shape.top_k
+        segs = min(shape.n_experts, R)
+        N = shape.d_expert if which == "up" else shape.d_e
+        bn = fp4_tile_rows(-(-R // segs), segs, N)
+        bnmax = 16 if bn <= 16 else 32 if bn <= 32 else 64 if bn <= 64 else 128
+        return f"fp4_gemm_kernel<{0 if which == 'up' else 1}, {0 if which == 'up' else 1}, {bnmax}, {ACT_TERMS}>", "fp4"
     if T > 64:
         # (the step entry points hand NVFP4 products BF16 rows: FP4A = 1)
         cg = 1 if shape.expert_dtype == 2 else 2

@@ -219,10 +219,8 @@ moe_status_t moe_shared(const moe_config_t* cfg, int32_t T, const void* x,
  *   x [T, d] in; y [T, d] out (act_dtype).
  *   topk_ids_out [T,K] / topk_w_out [T,K] / logits_out [T,E] / scores_out [T,E]:
  *   optional copies of the router's results (NULL = not written).
- * Clears the device error word first.  With NVFP4 experts the expert products
- * multiply in FP16 (page "NemotronH ...", section "Arithmetic"): their input
- * rows and h are FP16 copies of the BF16 values, exact for magnitudes up to
- * 65504; a larger activation there overflows.                               */
+ * Clears the device error word first.  NVFP4 experts: see
+ * moe_set_nvfp4_act_terms for how the activations enter their products.     */
 moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x,
                                const moe_weights_t* w, void* y,
                                int32_t* topk_ids_out, float* topk_w_out,
@@ -235,6 +233,24 @@ moe_status_t moe_get_device_error(const void* ws, void* stream, int32_t* code);
 
 /* Enqueues a clear of the device error word. */
 moe_status_t moe_clear_device_error(void* ws, void* stream);
+
+/* How the activations of NVFP4 experts enter their products (process-wide;
+ * applies to the calls made after it):
+ *   n = 1..4  the FP4 tensor path: every expert input row and every row of h
+ *             is split into n NVFP4 terms, each encoding what the earlier ones
+ *             left (E2M1 values, one E4M3 scale per 16 values, one FP32 scale
+ *             per row), and the block-scaled FP4 MMA multiplies them with the
+ *             NVFP4 weights; n = 1 is plain W4A4.  Each term leaves at most
+ *             ~0.18 of the previous residual of a 16-value block, so the
+ *             default n = 3 represents every activation to within ~0.006 of its
+ *             block's largest magnitude.  h is stored as BF16.
+ *   n = 0     the FP16 path: the weights are decoded to FP16 inside the kernels
+ *             and multiplied with FP16 copies of the BF16 activations (exact
+ *             for magnitudes up to 65504; a larger activation overflows).
+ * Returns the previous setting, or -1 (nothing changed) for n outside 0..4.
+ * The block format is the one of page "Nemotron-3.5-Super 120B on an 8 GB
+ * GPU", section "The engine, step by step", item 4.                        */
+int32_t moe_set_nvfp4_act_terms(int32_t n);
 
 /* Where a workspace for T tokens keeps the layer's route tables, so a caller
  * can read what moe_layer_forward decided (host arithmetic only; no CUDA call).
@@ -252,13 +268,23 @@ moe_status_t moe_clear_device_error(void* ws, void* stream);
  *   MOE_WS_X_PACKED        [T*K, de]      rows packed for the tensor-core path
  *                                         (above 64 BF16 tokens: act_dtype, or
  *                                         FP16 copies of the BF16 values with
- *                                         NVFP4 experts)
+ *                                         NVFP4 experts on the FP16 path)
+ *   MOE_WS_H               [T*K, I]  act  the experts' ReLU^2 rows h, packed order
+ * NVFP4 experts on the FP4 tensor path (moe_set_nvfp4_act_terms n > 0), term
+ * j of packed row r of the expert input rows (X) and of h (H):
+ *   MOE_WS_X_TERMS / MOE_WS_H_TERMS        [4][T*K][de/2 | I/2] u8  E2M1 codes, even
+ *                                           element in the low nibble (terms >= n unused)
+ *   MOE_WS_X_TERM_SCALES / _H_TERM_SCALES  [4][T*K][ld] u8  E4M3 scale per 16 values,
+ *                                           ld = (K/16 rounded up to 16) for K = de | I
+ *   MOE_WS_X_ROW_SCALES / _H_ROW_SCALES    [T*K] FP32  the rows' scale g
  * *offset receives the region's byte offset from the workspace start, *bytes
  * its size.  MOE_ERR_INVALID_ARG for an unknown region or T < 0.           */
 enum {
   MOE_WS_COUNTS = 0, MOE_WS_OFFSETS = 1, MOE_WS_ROUTE_TOKEN = 2, MOE_WS_ROUTE_SLOT = 3,
   MOE_WS_TOKEN_SLOT_ROW = 4, MOE_WS_TOPK_IDS = 5, MOE_WS_TOPK_W = 6, MOE_WS_LOGITS = 7,
-  MOE_WS_SCORES = 8, MOE_WS_X_LATENT = 9, MOE_WS_X_PACKED = 10
+  MOE_WS_SCORES = 8, MOE_WS_X_LATENT = 9, MOE_WS_X_PACKED = 10, MOE_WS_H = 11, MOE_WS_X_TERMS = 12,
+  MOE_WS_X_TERM_SCALES = 13, MOE_WS_X_ROW_SCALES = 14, MOE_WS_H_TERMS = 15, MOE_WS_H_TERM_SCALES = 16,
+  MOE_WS_H_ROW_SCALES = 17
 };
 moe_status_t moe_workspace_region(const moe_config_t* cfg, int32_t T, int32_t region, size_t* offset,
                                   size_t* bytes);

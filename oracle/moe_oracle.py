@@ -125,7 +125,7 @@ def dequant_nvfp4(q: np.ndarray, sf: np.ndarray, gs) -> np.ndarray:
 # NVFP4; n = 1 is plain W4A4.  Every decision is taken in FP32, as the device
 # takes it: g = amax(row) / (6 * 448); per term and 16-value block,
 # scale = E4M3_rn(amax(block) / (6 g)) (saturating), s = scale * g,
-# code = E2M1_rn(r / s) (saturating; 0 where s = 0), r -= code * s.
+# code = E2M1_rn(r * (1 / s)) (saturating; 0 where s = 0), r -= code * s.
 # ----------------------------------------------------------------------------
 _E2M1_GRID = np.array([e2m1_value(c) for c in range(8)], dtype=np.float64)          # codes 0..7
 _E4M3_GRID = np.array([e4m3_value(b) for b in range(127)], dtype=np.float64)        # codes 0..126 (127 = NaN)
@@ -170,8 +170,8 @@ def nvfp4_terms(x: np.ndarray, n_terms: int):
         amax_b = np.max(np.abs(r), axis=2).astype(np.float32)
         sf = e4m3_rn_code((amax_b / six_g[:, None]).astype(np.float32))
         s = (_E4M3_GRID[sf].astype(np.float32) * g[:, None]).astype(np.float32)
-        with np.errstate(divide="ignore", invalid="ignore"):
-            ratio = np.where(s[..., None] > 0, r / np.where(s > 0, s, np.float32(1))[..., None], np.float32(0))
+        inv = np.where(s > 0, np.float32(1) / np.where(s > 0, s, np.float32(1)), np.float32(0)).astype(np.float32)
+        ratio = (r * inv[..., None]).astype(np.float32)
         c = e2m1_rn_code(ratio.astype(np.float32))
         q = (np.where(c & 8, -1.0, 1.0) * _E2M1_GRID[c & 7]).astype(np.float32)
         r = (r - (q * s[..., None]).astype(np.float32)).astype(np.float32)

@@ -9,7 +9,8 @@ from ._native import (EXPORTS, LIB_PATH, MOE_DEVERR_EXPERT_ID, MOE_DEVERR_NONFIN
 from .layer import (MoELayer, Weights, config_from, make_config, moe_clear_device_error,
                     moe_dispatch, moe_experts_down, moe_experts_down_combine, moe_experts_up, moe_get_device_error,
                     moe_latent_down, moe_layer_forward, moe_layer_forward_host, moe_router,
-                    moe_router_noalloc, moe_shared, new_workspace, workspace_bytes, workspace_region)
+                    moe_router_noalloc, moe_shared, new_workspace, set_nvfp4_act_terms, workspace_bytes,
+                    workspace_region)
 
 __all__ = [
     "EXPORTS", "LIB_PATH", "MOE_DEVERR_EXPERT_ID", "MOE_DEVERR_NONFINITE", "MOE_DEVERR_SCHEDULE",
@@ -17,5 +18,5 @@ __all__ = [
     "MoELayer", "Weights", "config_from", "make_config", "moe_clear_device_error", "moe_dispatch",
     "moe_experts_down", "moe_experts_down_combine", "moe_experts_up", "moe_get_device_error", "moe_latent_down",
     "moe_layer_forward", "moe_layer_forward_host", "moe_router", "moe_router_noalloc", "moe_shared", "new_workspace",
-    "workspace_bytes", "workspace_region",
+    "set_nvfp4_act_terms", "workspace_bytes", "workspace_region",
 ]

@@ -18,7 +18,9 @@ MOE_DT_F32, MOE_DT_BF16, MOE_DT_NVFP4 = 0, 1, 2
 MOE_NOALLOC_MAX_ROUTER_ELEMS = 131072
 MOE_NOALLOC_MAX_SPLIT_ELEMS = 7340032
 (MOE_WS_COUNTS, MOE_WS_OFFSETS, MOE_WS_ROUTE_TOKEN, MOE_WS_ROUTE_SLOT, MOE_WS_TOKEN_SLOT_ROW, MOE_WS_TOPK_IDS,
- MOE_WS_TOPK_W, MOE_WS_LOGITS, MOE_WS_SCORES, MOE_WS_X_LATENT, MOE_WS_X_PACKED) = range(11)
+ MOE_WS_TOPK_W, MOE_WS_LOGITS, MOE_WS_SCORES, MOE_WS_X_LATENT, MOE_WS_X_PACKED, MOE_WS_H, MOE_WS_X_TERMS,
+ MOE_WS_X_TERM_SCALES, MOE_WS_X_ROW_SCALES, MOE_WS_H_TERMS, MOE_WS_H_TERM_SCALES, MOE_WS_H_ROW_SCALES) = range(18)
+ACT_TERMS_MAX = 4
 
 
 class MoeConfig(ctypes.Structure):
@@ -48,7 +50,7 @@ EXPORTS = (
     "moe_version", "moe_status_string", "moe_check_config", "moe_workspace_bytes", "moe_router",
     "moe_dispatch", "moe_experts_up", "moe_experts_down", "moe_experts_down_combine", "moe_latent_down", "moe_shared",
     "moe_layer_forward", "moe_get_device_error", "moe_clear_device_error", "moe_layer_forward_host",
-    "moe_launch_count", "moe_router_noalloc", "moe_workspace_region",
+    "moe_launch_count", "moe_router_noalloc", "moe_workspace_region", "moe_set_nvfp4_act_terms",
 )
 
 _lib = None
@@ -87,6 +89,7 @@ def load() -> ctypes.CDLL:
         "moe_launch_count": (ctypes.c_int64, []),
         "moe_router_noalloc": (I32, [CFG, I32, P, P, P, P, P, P]),
         "moe_workspace_region": (I32, [CFG, I32, I32, ctypes.POINTER(S), ctypes.POINTER(S)]),
+        "moe_set_nvfp4_act_terms": (I32, [I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -25,12 +25,19 @@ constexpr int64_t kMaxRoutes = (int64_t)1 << 28;
 constexpr int kDecodeMaxT = 64;   // up to this many tokens: weight-streaming GEMV; above: tensor cores
 
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// NVFP4 expert products: activation terms on the FP4 tensor path (1..4), or 0
+// for the FP16 path (weights decoded to FP16 inside the kernels)
+std::atomic<int> g_act_terms{kActTerms};
 inline int act_bytes(const moe_config_t* c) { return c->act_dtype == MOE_DT_F32 ? 4 : 2; }
 inline int de_of(const moe_config_t* c) { return c->d_latent > 0 ? c->d_latent : c->d_model; }
 
 struct Layout {
   size_t hdr, logits, logit_parts, scores, ids, topw, counts, offsets, active, tile_prefix, w_split;
-  size_t route_token, route_slot, tsr, x_l, x_packed, h, u, y_r, y_rl, hs, ys, tile_counts, total;
+  size_t route_token, route_slot, tsr, x_l, x_packed, h, u, y_r, y_rl, hs, ys, tile_counts;
+  // NVFP4 experts: activation terms of the expert input rows and of h, their
+  // block scales and row scales (sized for kActTermsMax terms)
+  size_t xq, xq_sf, xq_g, hq, hq_sf, hq_g, total;
 };
 
 inline size_t take(size_t& off, size_t bytes) {
@@ -68,6 +75,14 @@ Layout make_layout(const moe_config_t* c, int32_t T) {
   L.hs = take(off, t * (size_t)c->d_shared * ab);
   L.ys = take(off, t * (size_t)c->d_model * 4);
   L.tile_counts = take(off, dispatch_tile_count_elems(T, c->top_k, c->n_experts) * 4);
+  const bool fp4 = c->expert_dtype == MOE_DT_NVFP4;
+  const size_t nt = fp4 ? kActTermsMax : 0, I = c->d_expert;
+  L.xq = take(off, nt * R * de / 2);
+  L.xq_sf = take(off, nt * R * (size_t)act_sf_ld((int)de));
+  L.xq_g = take(off, fp4 ? R * 4 : 0);
+  L.hq = take(off, nt * R * I / 2);
+  L.hq_sf = take(off, nt * R * (size_t)act_sf_ld((int)I));
+  L.hq_g = take(off, fp4 ? R * 4 : 0);
   L.total = (off + 255) & ~(size_t)255;
   return L;
 }
@@ -196,7 +211,7 @@ moe_status_t run_dispatch(const moe_config_t* c, int T, const int32_t* ids, cons
 // and the tensor-core kernel's two operands share a type.  Decode needs both
 // products on the streaming GEMV kernel; the tensor-core kernels always qualify.
 bool up_down_f16(const moe_config_t* c, int T, const moe_weights_t* w) {
-  if (c->expert_dtype != MOE_DT_NVFP4 || c->act_dtype != MOE_DT_BF16) return false;
+  if (c->expert_dtype != MOE_DT_NVFP4 || c->act_dtype != MOE_DT_BF16 || g_act_terms.load() > 0) return false;
   if (use_tc(c, T)) return true;
   const int de = de_of(c), I = c->d_expert;
   GemvArgs up{}, dn{};
@@ -209,9 +224,17 @@ bool up_down_f16(const moe_config_t* c, int T, const moe_weights_t* w) {
 
 // f16: x_e holds FP16 activations and h receives FP16 (the layer's NVFP4
 // decode path, where up_down_f16() holds)
+moe_status_t run_up_fp4(const moe_config_t* c, int T, const void* x_e, const void* x_packed, const int32_t* rt,
+                        const int32_t* offsets, const moe_weights_t* w, void* h, const Ptrs& P, cudaStream_t s);
+moe_status_t run_down_fp4(const moe_config_t* c, int T, const void* h, const int32_t* offsets, const int32_t* rt,
+                          const int32_t* rs, const float* topw, const moe_weights_t* w, float* u, const Ptrs& P,
+                          cudaStream_t s);
+inline bool fp4_path(const moe_config_t* c);
+
 moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x_packed, const int32_t* rt,
                     const int32_t* offsets, const moe_weights_t* w, void* h, const Ptrs& P, cudaStream_t s,
                     bool f16 = false) {
+  if (fp4_path(c)) return run_up_fp4(c, T, x_e, x_packed, rt, offsets, w, h, P, s);
   const int de = de_of(c), I = c->d_expert;
   const bool fp4 = c->expert_dtype == MOE_DT_NVFP4;
   GemvArgs a{};
@@ -244,6 +267,7 @@ moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x
 moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t* offsets, const int32_t* rt,
                       const int32_t* rs, const float* topw, const moe_weights_t* w, float* u, const Ptrs& P,
                       cudaStream_t s, bool f16 = false) {
+  if (fp4_path(c)) return run_down_fp4(c, T, h, offsets, rt, rs, topw, w, u, P, s);
   const int de = de_of(c), I = c->d_expert;
   const bool fp4 = c->expert_dtype == MOE_DT_NVFP4;
   GemvArgs a{};
@@ -262,6 +286,64 @@ moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t
     return MOE_OK;
   }
   CU(launch_gemv(a, wfmt_of(c), c->act_dtype, EPI_SCALE, true, T, segs, s));
+  return MOE_OK;
+}
+
+// ---- NVFP4 experts on the FP4 tensor path ----
+inline bool fp4_path(const moe_config_t* c) { return c->expert_dtype == MOE_DT_NVFP4 && g_act_terms.load() > 0; }
+
+// packed rows per tile of an expert product with N output features (a decode
+// tile holds an expert's rows)
+inline int fp4_bn(const moe_config_t* c, int T, int N) {
+  const int64_t R = (int64_t)T * c->top_k;
+  const int64_t segs = std::min<int64_t>(c->n_experts, R);
+  return fp4_tile_rows(ceil_div(R, std::max<int64_t>(segs, 1)), segs, N);
+}
+
+// grouped FP4 product: W (NVFP4, [E, N, K]) times the NVFP4 terms of the
+// packed rows in q / q_sf / q_g
+GemvArgs fp4_args(const moe_config_t* c, int T, const void* W, const uint8_t* W_sf, const float* W_gs, int N, int K,
+                  const uint8_t* q, const uint8_t* q_sf, const float* q_g, const int32_t* offsets, int nt,
+                  const Ptrs& P) {
+  GemvArgs a{};
+  a.W = W; a.W_sf = W_sf; a.W_gs = W_gs; a.N = N; a.K = K;
+  a.X = q; a.X_sf = q_sf; a.x_scale = q_g; a.x_sf_ld = act_sf_ld(K);
+  a.x_rows_cap = (int64_t)T * c->top_k; a.x_terms = nt;
+  a.offsets = offsets; a.active = P.at<int32_t>(P.L.active); a.hdr = P.hdr(); a.err = &P.hdr()->err;
+  return a;
+}
+
+// h = bf16(relu(bf16(x_e W_up^T))^2) for every packed row: the rows (x_packed,
+// or x_e gathered through rt) become NVFP4 terms, then the FP4 product
+moe_status_t run_up_fp4(const moe_config_t* c, int T, const void* x_e, const void* x_packed, const int32_t* rt,
+                        const int32_t* offsets, const moe_weights_t* w, void* h, const Ptrs& P, cudaStream_t s) {
+  const int de = de_of(c), I = c->d_expert, nt = g_act_terms.load();
+  const int R = T * c->top_k;
+  uint8_t* xq = P.at<uint8_t>(P.L.xq);
+  uint8_t* xq_sf = P.at<uint8_t>(P.L.xq_sf);
+  float* xq_g = P.at<float>(P.L.xq_g);
+  const void* src = x_packed ? x_packed : x_e;
+  CU(launch_quant_terms(src, de, x_packed ? nullptr : rt, offsets + c->n_experts, R, de, nt, xq, xq_sf, xq_g, R, s));
+  GemvArgs a = fp4_args(c, T, w->w_up, w->w_up_sf, w->w_up_gs, I, de, xq, xq_sf, xq_g, offsets, nt, P);
+  a.out = h; a.out_ld = I;
+  CU(launch_gemm_fp4(a, EPI_RELU2, false, (int64_t)c->n_experts * I, c->n_experts, fp4_bn(c, T, I), s));
+  return MOE_OK;
+}
+
+// u = w * (h W_down^T) for every packed row (FP32), h quantised to NVFP4 terms first
+moe_status_t run_down_fp4(const moe_config_t* c, int T, const void* h, const int32_t* offsets, const int32_t* rt,
+                          const int32_t* rs, const float* topw, const moe_weights_t* w, float* u, const Ptrs& P,
+                          cudaStream_t s) {
+  const int de = de_of(c), I = c->d_expert, nt = g_act_terms.load();
+  const int R = T * c->top_k;
+  uint8_t* hq = P.at<uint8_t>(P.L.hq);
+  uint8_t* hq_sf = P.at<uint8_t>(P.L.hq_sf);
+  float* hq_g = P.at<float>(P.L.hq_g);
+  CU(launch_quant_terms(h, I, nullptr, offsets + c->n_experts, R, I, nt, hq, hq_sf, hq_g, R, s));
+  GemvArgs a = fp4_args(c, T, w->w_down, w->w_down_sf, w->w_down_gs, de, I, hq, hq_sf, hq_g, offsets, nt, P);
+  a.out = u; a.out_ld = de;
+  a.topw = topw; a.route_token = rt; a.route_slot = rs; a.top_k = c->top_k;
+  CU(launch_gemm_fp4(a, EPI_SCALE, true, (int64_t)c->n_experts * de, c->n_experts, fp4_bn(c, T, de), s));
   return MOE_OK;
 }
 
@@ -387,6 +469,11 @@ const char* moe_status_string(moe_status_t s) {
 
 moe_status_t moe_check_config(const moe_config_t* cfg) { return check_config(cfg); }
 
+int32_t moe_set_nvfp4_act_terms(int32_t n) {
+  if (n < 0 || n > kActTermsMax) return -1;
+  return g_act_terms.exchange(n);
+}
+
 moe_status_t moe_workspace_region(const moe_config_t* cfg, int32_t T, int32_t region, size_t* offset,
                                   size_t* bytes) {
   moe_status_t st = check_config(cfg);
@@ -395,6 +482,8 @@ moe_status_t moe_workspace_region(const moe_config_t* cfg, int32_t T, int32_t re
   const Layout L = make_layout(cfg, T);
   const size_t t = (size_t)T, E = cfg->n_experts, R = t * cfg->top_k;
   const size_t ab = act_bytes(cfg);
+  const bool fp4 = cfg->expert_dtype == MOE_DT_NVFP4;
+  const size_t nt = fp4 ? kActTermsMax : 0, de = de_of(cfg), I = cfg->d_expert;
   size_t o = 0, n = 0;
   switch (region) {
     case MOE_WS_COUNTS: o = L.counts; n = E * 4; break;
@@ -408,6 +497,13 @@ moe_status_t moe_workspace_region(const moe_config_t* cfg, int32_t T, int32_t re
     case MOE_WS_SCORES: o = L.scores; n = t * E * 4; break;
     case MOE_WS_X_LATENT: o = L.x_l; n = t * (size_t)cfg->d_latent * ab; break;
     case MOE_WS_X_PACKED: o = L.x_packed; n = R * (size_t)de_of(cfg) * ab; break;
+    case MOE_WS_H: o = L.h; n = R * (size_t)cfg->d_expert * ab; break;
+    case MOE_WS_X_TERMS: o = L.xq; n = nt * R * de / 2; break;
+    case MOE_WS_X_TERM_SCALES: o = L.xq_sf; n = nt * R * (size_t)act_sf_ld((int)de); break;
+    case MOE_WS_X_ROW_SCALES: o = L.xq_g; n = fp4 ? R * 4 : 0; break;
+    case MOE_WS_H_TERMS: o = L.hq; n = nt * R * I / 2; break;
+    case MOE_WS_H_TERM_SCALES: o = L.hq_sf; n = nt * R * (size_t)act_sf_ld((int)I); break;
+    case MOE_WS_H_ROW_SCALES: o = L.hq_g; n = fp4 ? R * 4 : 0; break;
     default: return MOE_ERR_INVALID_ARG;
   }
   *offset = o;
@@ -557,7 +653,7 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
   int32_t* rt = P.at<int32_t>(P.L.route_token);
   int32_t* rs = P.at<int32_t>(P.L.route_slot);
   int32_t* tsr = P.at<int32_t>(P.L.tsr);
-  void* x_packed = use_tc(cfg, T) ? P.at<void>(P.L.x_packed) : nullptr;
+  void* x_packed = use_tc(cfg, T) && !fp4_path(cfg) ? P.at<void>(P.L.x_packed) : nullptr;
   DispatchArgs da = dispatch_args(cfg, T, ids, x_e, P.at<int32_t>(P.L.counts), offsets, rt, rs, tsr, x_packed, P);
   da.pack_f16 = f16 && x_packed;
   if (select_dispatch_fits(T, cfg->top_k, da)) {

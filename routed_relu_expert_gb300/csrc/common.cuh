@@ -113,6 +113,19 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// the same, suspending the thread for at most about `ns` nanoseconds while the
+// phase is incomplete (for waits whose wake-up latency is on a critical path:
+// the default suspension can outlast the phase by hundreds of nanoseconds)
+__device__ __forceinline__ bool mbar_try_ns(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------------------
 // small integer helpers
 // ---------------------------------------------------------------------------

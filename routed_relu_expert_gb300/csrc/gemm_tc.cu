@@ -166,37 +166,12 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
   // results (offsets, activations) are read only after this wait
   pdl_wait();
   // row-tile prefix over segments (each segment: ceil(rows / bn) row tiles)
-  int total_q;
-  if (a.offsets) {
-    const int per = (E + NTHR - 1) / NTHR;
-    const int e0 = threadIdx.x * per;
-    int local = 0;
-    for (int e = e0; e < min(E, e0 + per); ++e) local += (a.offsets[e + 1] - a.offsets[e] + bn - 1) / bn;
-    int x = local;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, off);
-      if (lane >= off) x += y;
-    }
-    if (lane == 31) scan_tmp[warp] = x;
-    __syncthreads();
-    int wbase = 0;
-    for (int w = 0; w < warp; ++w) wbase += scan_tmp[w];
-    int run = wbase + x - local;
-    for (int e = e0; e < min(E, e0 + per); ++e) {
-      prefix[e] = run;
-      run += (a.offsets[e + 1] - a.offsets[e] + bn - 1) / bn;
-    }
-    if (threadIdx.x == NTHR - 1) prefix[E] = wbase + x;
-    // (e0 >= E for the last threads: they still write prefix[E] correctly as the block total)
-  } else {
-    total_q = (a.dense_rows + bn - 1) / bn;
-  }
+  if (a.offsets) row_tile_prefix(a, E, bn, NTHR, scan_tmp, prefix);
   tc_fence_before();
   __syncthreads();
   if (CG == 2) cluster_sync();      // the peer's barriers exist before any remote arrive or copy
   tc_fence_after();
-  if (a.offsets) total_q = prefix[E];
+  const int total_q = a.offsets ? prefix[E] : (a.dense_rows + bn - 1) / bn;
   const uint32_t tmem_base = *tmem_holder;
   const int per_part = total_q * m_tiles;
   const int total = per_part * ksplit;

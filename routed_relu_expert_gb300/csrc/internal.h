@@ -88,6 +88,14 @@ struct GemvArgs {
   // (the exact FP16 copy of BF16 ones); out receives FP16 copies of the
   // BF16-rounded outputs
   bool x_f16, out_f16;
+  // FP4 tensor-core products only (launch_gemm_fp4): X holds the rows' NVFP4
+  // activation terms [x_terms][x_rows_cap][K/2] bytes, X_sf their E4M3 block
+  // scales [x_terms][x_rows_cap][x_sf_ld] bytes, x_scale the rows' FP32 scale
+  const uint8_t* X_sf;
+  int64_t x_sf_ld;
+  const float* x_scale;
+  int64_t x_rows_cap;
+  int x_terms;
 };
 
 // act: MOE_DT_BF16 / MOE_DT_F32 activation type of X and of non-f32 outputs.
@@ -117,6 +125,28 @@ cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, bool out_f32, int64_t w_r
 // still gives every SM about two tiles, for segments of rows_per_seg rows and
 // N output features.
 int tc_tile_rows(int64_t rows_per_seg, int64_t segs, int N);
+
+// NVFP4 activation terms and the FP4 tensor-core grouped GEMM (gemm_fp4.cu).
+// A row of K activations becomes kActTerms NVFP4 terms (residual
+// quantisation: each term encodes what the earlier ones left), so both
+// operands of an expert product are NVFP4 and the block-scaled FP4 MMA
+// multiplies them; the term count trades accuracy (about 0.18^n of a 16-value
+// block's largest magnitude left over) for MMA work.
+constexpr int kActTerms = 3;
+constexpr int kActTermsMax = 4;
+// row stride of a term's block scales (K/16 bytes rounded up to 16 for TMA)
+inline int64_t act_sf_ld(int K) { return ((int64_t)K / 16 + 15) / 16 * 16; }
+// rows r < (*count if count else R) of x (BF16, row stride x_ld elements;
+// row r reads x[gather[r]] when gather is given) -> terms q [nterms][rows_cap]
+// [K/2], scales sf [nterms][rows_cap][act_sf_ld(K)], row scale g [rows_cap]
+cudaError_t launch_quant_terms(const void* x, int64_t x_ld, const int32_t* gather, const int32_t* count, int R, int K,
+                               int nterms, uint8_t* q, uint8_t* sf, float* g, int64_t rows_cap, cudaStream_t s);
+// out = epilogue(W_seg x_terms) for grouped (a.offsets) or dense products;
+// a.W / a.W_sf / a.W_gs: NVFP4 weights [w_rows, K/2] u8, E4M3 scales
+// [w_rows, K/16], per-segment FP32 scales; a.X / a.X_sf / a.x_scale: the
+// activation terms above.  bn: rows per tile (16..128, a multiple of 16).
+cudaError_t launch_gemm_fp4(const GemvArgs& a, int epi, bool out_f32, int64_t w_rows, int E, int bn, cudaStream_t s);
+int fp4_tile_rows(int64_t rows_per_seg, int64_t segs, int N);
 
 // router
 // w_split: scratch of E * 3d BF16 for the tensor-core path (many BF16 tokens);

@@ -37,10 +37,14 @@ __device__ __forceinline__ bool mbar_try_cl(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase of `parity` to complete; false if this thread
-// gave up or another role raised the abort flag.
-template <bool CL = false>
+// gave up or another role raised the abort flag.  SHORT: suspend for short
+// spells only (for the roles whose wake-up latency is on the critical path of
+// every stage or tile).
+template <bool CL = false, bool SHORT = false>
 __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
-  auto probe = [&]() { return CL ? mbar_try_cl(bar, parity) : mbar_try(bar, parity); };
+  auto probe = [&]() {
+    return CL ? mbar_try_cl(bar, parity) : SHORT ? mbar_try_ns(bar, parity, 32u) : mbar_try(bar, parity);
+  };
   if (probe()) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
@@ -71,6 +75,15 @@ __device__ __forceinline__ void cluster_sync() {
 }
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
@@ -175,10 +188,43 @@ struct Tile {
   int orow0;           // first output row (row0 shifted by the unit's K-part slab)
 };
 
+// Row-tile prefix over segments: prefix[e] = row tiles of segments < e, each
+// segment holding ceil(rows / bn) tiles; prefix[E] = all of them.  Every one of
+// the block's nthr threads takes part (it contains a __syncthreads); the
+// caller synchronises before reading prefix.  scan_tmp: 32 ints.
+__device__ __forceinline__ void row_tile_prefix(const GemvArgs& a, int E, int bn, int nthr, int* scan_tmp,
+                                                int* prefix) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per = (E + nthr - 1) / nthr;
+  const int e0 = threadIdx.x * per;
+  int local = 0;
+  for (int e = e0; e < min(E, e0 + per); ++e) local += (a.offsets[e + 1] - a.offsets[e] + bn - 1) / bn;
+  int x = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) scan_tmp[warp] = x;
+  __syncthreads();
+  int wbase = 0;
+  for (int w = 0; w < warp; ++w) wbase += scan_tmp[w];
+  int run = wbase + x - local;
+  for (int e = e0; e < min(E, e0 + per); ++e) {
+    prefix[e] = run;
+    run += (a.offsets[e + 1] - a.offsets[e] + bn - 1) / bn;
+  }
+  // (e0 >= E for the last threads: they still write prefix[E] correctly as the block total)
+  if (threadIdx.x == nthr - 1) prefix[E] = wbase + x;
+}
+
 // unit t -> (K part, row tile, feature tile); parts outermost, so units that
 // run together share their K range
+// (offs: the segment offsets, a.offsets or a copy of them in shared memory)
 __device__ __forceinline__ void decode_tile(int t, const int* prefix, int E, int m_tiles, int tile_m, int bn,
-                                            const GemvArgs& a, int per_part, int ksplit, int nkb, Tile& ti) {
+                                            const GemvArgs& a, int per_part, int ksplit, int nkb, Tile& ti,
+                                            const int* offs = nullptr) {
+  if (!offs) offs = a.offsets;
   const int ks = t / per_part;
   t -= ks * per_part;
   const int q = t / m_tiles, m = t - q * m_tiles;
@@ -191,8 +237,8 @@ __device__ __forceinline__ void decode_tile(int t, const int* prefix, int E, int
     }
     seg = lo;
     nt = q - prefix[lo];
-    base = a.offsets[lo];
-    count = a.offsets[lo + 1] - base;
+    base = offs[lo];
+    count = offs[lo + 1] - base;
   }
   ti.seg = seg;
   ti.m0 = m * tile_m;

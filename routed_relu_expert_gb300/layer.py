@@ -94,6 +94,15 @@ def new_workspace(cfg: N.MoeConfig, T: int, device="cuda") -> torch.Tensor:
     return ws
 
 
+def set_nvfp4_act_terms(n: int) -> int:
+    """How NVFP4 experts take their activations (0: FP16 path; 1..4: NVFP4
+    terms on the FP4 tensor path); returns the previous setting."""
+    prev = int(N.load().moe_set_nvfp4_act_terms(int(n)))
+    if prev < 0:
+        raise ValueError(f"activation terms must be 0..4, got {n}")
+    return prev
+
+
 def workspace_region(cfg: N.MoeConfig, T: int, region: int):
     """(byte offset, bytes) of one of the route tables in a workspace for T tokens."""
     off, n = ctypes.c_size_t(0), ctypes.c_size_t(0)

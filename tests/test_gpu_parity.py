@@ -45,6 +45,41 @@ def _check_packed_rows(shape, g, x, T):
     assert torch.equal(got.view(torch.int16), want.contiguous().view(torch.int16))
 
 
+_E2M1 = np.array([O.e2m1_value(c) for c in range(8)])
+
+
+def _term_values(codes):
+    """Signed E2M1 values of 4-bit codes (a negative zero reads as zero)."""
+    return np.where(codes & 8, -1.0, 1.0) * _E2M1[codes & 7]
+
+
+def _check_fp4_terms(shape, g, x, T, n_terms):
+    """On the FP4 tensor path the layer splits the expert input rows and h into
+    NVFP4 terms: every code, block scale and row scale must equal the oracle's
+    split of the same BF16 rows (both take the decisions in FP32)."""
+    from routed_relu_expert_gb300 import _native as N
+    cfg = M.config_from(shape)
+    ws = g["ws"]
+    R, de, I = T * shape.top_k, shape.d_e, shape.d_expert
+    nmax = N.ACT_TERMS_MAX
+    rt = ws_table(ws, cfg, T, N.MOE_WS_ROUTE_TOKEN, torch.int32).long()
+    x_e = x if not shape.d_latent else ws_table(ws, cfg, T, N.MOE_WS_X_LATENT, torch.bfloat16).view(T, de)
+    h = ws_table(ws, cfg, T, N.MOE_WS_H, torch.bfloat16).view(R, I)
+    for rows, K, rq, rs, rg in ((x_e[rt], de, N.MOE_WS_X_TERMS, N.MOE_WS_X_TERM_SCALES, N.MOE_WS_X_ROW_SCALES),
+                                (h, I, N.MOE_WS_H_TERMS, N.MOE_WS_H_TERM_SCALES, N.MOE_WS_H_ROW_SCALES)):
+        codes, sf, gg = O.nvfp4_terms(rows.float().cpu().numpy(), n_terms)
+        q = ws_table(ws, cfg, T, rq, torch.uint8).view(nmax, R, K // 2)[:n_terms].cpu().numpy()
+        got = np.empty((n_terms, R, K), dtype=np.uint8)
+        got[..., 0::2], got[..., 1::2] = q & 0xF, q >> 4
+        ld = (K // 16 + 15) // 16 * 16
+        s_got = ws_table(ws, cfg, T, rs, torch.uint8).view(nmax, R, ld)[:n_terms, :, :K // 16].cpu().numpy()
+        g_got = ws_table(ws, cfg, T, rg, torch.float32).cpu().numpy()
+        assert np.array_equal(g_got, gg), "row scales differ"
+        assert np.array_equal(s_got, sf), f"block scales differ in {np.sum(s_got != sf)} places"
+        bad = np.sum(_term_values(got) != _term_values(codes))
+        assert bad == 0, f"{bad} term codes differ"
+
+
 def _parity(shape, T, sample=None, seed_stream=0, chunk=0):
     """Routing of every token (ids bit-exact, weights 1e-6, logits 1e-5), the
     dispatch tables the layer left in its workspace bit-exact, the packed rows
@@ -54,8 +89,13 @@ def _parity(shape, T, sample=None, seed_stream=0, chunk=0):
     x = make_x(shape, T, "cuda", seed_stream)
     g = run_gpu(shape, w, x)
     assert g["err"] == 0
-    if T > 64 and shape.act_dtype == BF16:
+    terms = M.set_nvfp4_act_terms(0)
+    M.set_nvfp4_act_terms(terms)
+    fp4_terms = shape.expert_dtype == 2 and terms > 0
+    if T > 64 and shape.act_dtype == BF16 and not fp4_terms:
         _check_packed_rows(shape, g, x, T)
+    if fp4_terms:
+        _check_fp4_terms(shape, g, x, T, terms)
     ws = g.pop("ws")
     g = to_np(g)
     check_route_tables(shape, ws, g["ids"], T)
@@ -130,6 +170,47 @@ def test_scaled_nvfp4_layer(T):
 @pytest.mark.parametrize("T", [1, 64])
 def test_super_nvfp4_full_size(T):
     _parity(SUPER_NVFP4, T)
+
+
+@pytest.fixture
+def act_terms():
+    """Sets how NVFP4 experts take their activations for one test."""
+    prev = M.set_nvfp4_act_terms(3)
+    yield M.set_nvfp4_act_terms
+    M.set_nvfp4_act_terms(prev)
+
+
+@pytest.mark.parametrize("n", [0, 4])
+@pytest.mark.parametrize("T", [9, 200])
+def test_scaled_nvfp4_layer_other_activation_forms(act_terms, n, T):
+    """The FP16 path (0) and four terms on the FP4 tensor path, decode and
+    prefill sizes, against the exact oracle."""
+    act_terms(n)
+    _parity(SMALL_NVFP4, T, seed_stream=n)
+
+
+@pytest.mark.parametrize("n", [1, 2])
+@pytest.mark.parametrize("T", [9, 200])
+def test_few_term_layer_against_the_oracle_with_the_same_terms(act_terms, n, T):
+    """One term (plain W4A4) and two terms miss the exact layer by more than
+    the NVFP4 tolerance; each equals the oracle evaluated with its expert
+    inputs and h replaced by their n-term NVFP4 forms."""
+    act_terms(n)
+    shape = SMALL_NVFP4
+    w = device_weights(shape)
+    x = make_x(shape, T, "cuda", 7)
+    g = run_gpu(shape, w, x)
+    assert g["err"] == 0
+    _check_fp4_terms(shape, g, x, T, n)
+    g.pop("ws")
+    g = to_np(g)
+    ow = oracle_weights(w)
+    x_np = x.float().cpu().numpy().astype(np.float64)
+    ids_o, w_o = check_router(shape, x_np, ow, g)
+    ref = O.layer_forward(x_np, ow, ids_o, w_o, shape.n_experts, bf16_points=True, act_terms=n)["y"]
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    err = float(np.max(np.abs(g["y"].astype(np.float64) - ref))) / rms
+    assert err <= 5e-2, f"max |y - y_ref| = {err:.3e} RMS"
 
 
 def test_super_nvfp4_8192_full():
