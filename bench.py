@@ -60,6 +60,9 @@ def parse(argv=None):
     ap.add_argument("--points", default="all",
                     help="per_workload entries: all, none, or one workload name")
     ap.add_argument("--eager", action="store_true", help="time eager calls instead of CUDA-graph replays")
+    ap.add_argument("--nvfp4-act-terms", type=int, default=-1,
+                    help="NVFP4 experts: activation terms on the FP4 tensor path (1-4), 0 = FP16 path; "
+                         "-1 = the library's default")
     return ap.parse_args(argv)
 
 
@@ -479,22 +482,23 @@ def measure_products(run: Runner, shape, T, layers, x, n_active, pk):
 
 def fp4_tile_rows(rows_per_seg, segs, N, sms=152):
     """Rows per tile of the FP4 grouped GEMM (the library's rule)."""
-    bn = 16 if rows_per_seg <= 16 else 32 if rows_per_seg <= 32 else 64 if rows_per_seg <= 64 else 128
+    bn = 16 if rows_per_seg <= 16 else 32 if rows_per_seg <= 32 else 64
     while bn > 16 and -(-rows_per_seg // bn) * segs * -(-N // 128) < 2 * sms:
         bn -= 16
     return bn
 
 
-def product_kernel_name(shape, T, which):
+def product_kernel_name(shape, T, which, act_terms=ACT_TERMS):
     """The kernel that runs a grouped expert product at this size (names as the
-    profiler prints their template arguments)."""
-    if shape.expert_dtype == 2:
+    profiler prints their template arguments); act_terms: the NVFP4
+    activation terms the library uses at T (0: the FP16 path)."""
+    if shape.expert_dtype == 2 and act_terms > 0:
         R = T * shape.top_k
         segs = min(shape.n_experts, R)
         N = shape.d_expert if which == "up" else shape.d_e
         bn = fp4_tile_rows(-(-R // segs), segs, N)
-        bnmax = 16 if bn <= 16 else 32 if bn <= 32 else 64 if bn <= 64 else 128
-        return f"fp4_gemm_kernel<{0 if which == 'up' else 1}, {0 if which == 'up' else 1}, {bnmax}, {ACT_TERMS}>", "fp4"
+        bnmax = 16 if bn <= 16 else 32 if bn <= 32 else 64
+        return f"fp4_gemm_kernel<{0 if which == 'up' else 1}, {0 if which == 'up' else 1}, {bnmax}, {act_terms}>", "fp4"
     if T > 64:
         # (the step entry points hand NVFP4 products BF16 rows: FP4A = 1)
         cg = 1 if shape.expert_dtype == 2 else 2
@@ -534,6 +538,8 @@ def run_ours(args, rank, world, dev):
     from synth import WORKLOADS, make_x
 
     pk = peaks()
+    if args.nvfp4_act_terms >= 0:
+        M.set_nvfp4_act_terms(args.nvfp4_act_terms)
     run = Runner(M, dev, world, eager=args.eager)
     shape = WORKLOADS[args.workload]
     T = args.tokens
@@ -604,6 +610,7 @@ def run_ours(args, rank, world, dev):
         "launches": int(per_step_launches) * args.steps, "err": err, "ms_eager": ms_eager,
         "prods": prods, "routing": routing, "peaks": pk, "e2e_s": e2e_s, "n_rep": n_rep, "shape": shape, "T": T,
         "rep_bytes": layer_bytes(shape, shape.n_experts, T)["total"], "per_workload": per_workload,
+        "act_terms": M.nvfp4_act_terms_for(T),
         "per_workload_clocks": pw_clocks,
     }
 
@@ -650,7 +657,7 @@ def roofline_entry(r, shape, T, pk):
     prods = r["prods"]
     which = max(prods, key=lambda k: prods[k]["ms"])
     p = prods[which]
-    kname, family = product_kernel_name(shape, T, which)
+    kname, family = product_kernel_name(shape, T, which, r["act_terms"])
     workload = f"{shape.name} T={T}"
     traffic, sha = recorded_traffic(kname, workload, family)
     if p["tensor"]:

@@ -236,21 +236,28 @@ moe_status_t moe_clear_device_error(void* ws, void* stream);
 
 /* How the activations of NVFP4 experts enter their products (process-wide;
  * applies to the calls made after it):
+ *   n = -1    the default: three terms on the FP4 tensor path for 2 to 64
+ *             tokens, the FP16 path otherwise (the faster one at each size
+ *             as measured on GB300)
  *   n = 1..4  the FP4 tensor path: every expert input row and every row of h
  *             is split into n NVFP4 terms, each encoding what the earlier ones
  *             left (E2M1 values, one E4M3 scale per 16 values, one FP32 scale
  *             per row), and the block-scaled FP4 MMA multiplies them with the
  *             NVFP4 weights; n = 1 is plain W4A4.  Each term leaves at most
  *             ~0.18 of the previous residual of a 16-value block, so the
- *             default n = 3 represents every activation to within ~0.006 of its
- *             block's largest magnitude.  h is stored as BF16.
+ *             default's n = 3 represents every activation to within ~0.006 of
+ *             its block's largest magnitude.  h is stored as BF16.
  *   n = 0     the FP16 path: the weights are decoded to FP16 inside the kernels
  *             and multiplied with FP16 copies of the BF16 activations (exact
  *             for magnitudes up to 65504; a larger activation overflows).
- * Returns the previous setting, or -1 (nothing changed) for n outside 0..4.
+ * Returns the previous setting, or -2 (nothing changed) for n outside -1..4.
  * The block format is the one of page "Nemotron-3.5-Super 120B on an 8 GB
  * GPU", section "The engine, step by step", item 4.                        */
 int32_t moe_set_nvfp4_act_terms(int32_t n);
+
+/* The activation terms a call with T tokens uses under the current setting
+ * (0: the FP16 path).  Never fails. */
+int32_t moe_nvfp4_act_terms_for(int32_t T);
 
 /* Where a workspace for T tokens keeps the layer's route tables, so a caller
  * can read what moe_layer_forward decided (host arithmetic only; no CUDA call).

@@ -9,7 +9,7 @@ from ._native import (EXPORTS, LIB_PATH, MOE_DEVERR_EXPERT_ID, MOE_DEVERR_NONFIN
 from .layer import (MoELayer, Weights, config_from, make_config, moe_clear_device_error,
                     moe_dispatch, moe_experts_down, moe_experts_down_combine, moe_experts_up, moe_get_device_error,
                     moe_latent_down, moe_layer_forward, moe_layer_forward_host, moe_router,
-                    moe_router_noalloc, moe_shared, new_workspace, set_nvfp4_act_terms, workspace_bytes,
+                    moe_router_noalloc, moe_shared, new_workspace, nvfp4_act_terms_for, set_nvfp4_act_terms, workspace_bytes,
                     workspace_region)
 
 __all__ = [
@@ -18,5 +18,5 @@ __all__ = [
     "MoELayer", "Weights", "config_from", "make_config", "moe_clear_device_error", "moe_dispatch",
     "moe_experts_down", "moe_experts_down_combine", "moe_experts_up", "moe_get_device_error", "moe_latent_down",
     "moe_layer_forward", "moe_layer_forward_host", "moe_router", "moe_router_noalloc", "moe_shared", "new_workspace",
-    "set_nvfp4_act_terms", "workspace_bytes", "workspace_region",
+    "nvfp4_act_terms_for", "set_nvfp4_act_terms", "workspace_bytes", "workspace_region",
 ]

@@ -51,6 +51,7 @@ EXPORTS = (
     "moe_dispatch", "moe_experts_up", "moe_experts_down", "moe_experts_down_combine", "moe_latent_down", "moe_shared",
     "moe_layer_forward", "moe_get_device_error", "moe_clear_device_error", "moe_layer_forward_host",
     "moe_launch_count", "moe_router_noalloc", "moe_workspace_region", "moe_set_nvfp4_act_terms",
+    "moe_nvfp4_act_terms_for",
 )
 
 _lib = None
@@ -90,6 +91,7 @@ def load() -> ctypes.CDLL:
         "moe_router_noalloc": (I32, [CFG, I32, P, P, P, P, P, P]),
         "moe_workspace_region": (I32, [CFG, I32, I32, ctypes.POINTER(S), ctypes.POINTER(S)]),
         "moe_set_nvfp4_act_terms": (I32, [I32]),
+        "moe_nvfp4_act_terms_for": (I32, [I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

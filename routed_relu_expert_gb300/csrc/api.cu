@@ -26,9 +26,22 @@ constexpr int kDecodeMaxT = 64;   // up to this many tokens: weight-streaming GE
 
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// NVFP4 expert products: activation terms on the FP4 tensor path (1..4), or 0
-// for the FP16 path (weights decoded to FP16 inside the kernels)
-std::atomic<int> g_act_terms{kActTerms};
+// NVFP4 expert products: activation terms on the FP4 tensor path (1..4), 0
+// for the FP16 path (weights decoded to FP16 inside the kernels), or -1 for
+// the measured choice: kActTerms terms on the FP4 path from 2 to 64 tokens
+// (a grouped decode product there streams the weights at 70-85 % of HBM
+// against 45 % for the FP16 GEMV), the FP16 path for one token (where the
+// GEMV's shorter launch chain wins) and above 64 tokens (where quantising
+// every routed row and h into terms costs more than the FP4 products save)
+std::atomic<int> g_act_terms{-1};
+constexpr int kFp4MinT = 2, kFp4MaxT = 64;
+
+// activation terms a layer of T tokens uses on the FP4 path (0: FP16 path)
+inline int act_terms_for(int T) {
+  const int n = g_act_terms.load();
+  if (n >= 0) return n;
+  return T >= kFp4MinT && T <= kFp4MaxT ? kActTerms : 0;
+}
 inline int act_bytes(const moe_config_t* c) { return c->act_dtype == MOE_DT_F32 ? 4 : 2; }
 inline int de_of(const moe_config_t* c) { return c->d_latent > 0 ? c->d_latent : c->d_model; }
 
@@ -211,7 +224,7 @@ moe_status_t run_dispatch(const moe_config_t* c, int T, const int32_t* ids, cons
 // and the tensor-core kernel's two operands share a type.  Decode needs both
 // products on the streaming GEMV kernel; the tensor-core kernels always qualify.
 bool up_down_f16(const moe_config_t* c, int T, const moe_weights_t* w) {
-  if (c->expert_dtype != MOE_DT_NVFP4 || c->act_dtype != MOE_DT_BF16 || g_act_terms.load() > 0) return false;
+  if (c->expert_dtype != MOE_DT_NVFP4 || c->act_dtype != MOE_DT_BF16 || act_terms_for(T) > 0) return false;
   if (use_tc(c, T)) return true;
   const int de = de_of(c), I = c->d_expert;
   GemvArgs up{}, dn{};
@@ -229,12 +242,12 @@ moe_status_t run_up_fp4(const moe_config_t* c, int T, const void* x_e, const voi
 moe_status_t run_down_fp4(const moe_config_t* c, int T, const void* h, const int32_t* offsets, const int32_t* rt,
                           const int32_t* rs, const float* topw, const moe_weights_t* w, float* u, const Ptrs& P,
                           cudaStream_t s);
-inline bool fp4_path(const moe_config_t* c);
+inline bool fp4_path(const moe_config_t* c, int T);
 
 moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x_packed, const int32_t* rt,
                     const int32_t* offsets, const moe_weights_t* w, void* h, const Ptrs& P, cudaStream_t s,
                     bool f16 = false) {
-  if (fp4_path(c)) return run_up_fp4(c, T, x_e, x_packed, rt, offsets, w, h, P, s);
+  if (fp4_path(c, T)) return run_up_fp4(c, T, x_e, x_packed, rt, offsets, w, h, P, s);
   const int de = de_of(c), I = c->d_expert;
   const bool fp4 = c->expert_dtype == MOE_DT_NVFP4;
   GemvArgs a{};
@@ -267,7 +280,7 @@ moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x
 moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t* offsets, const int32_t* rt,
                       const int32_t* rs, const float* topw, const moe_weights_t* w, float* u, const Ptrs& P,
                       cudaStream_t s, bool f16 = false) {
-  if (fp4_path(c)) return run_down_fp4(c, T, h, offsets, rt, rs, topw, w, u, P, s);
+  if (fp4_path(c, T)) return run_down_fp4(c, T, h, offsets, rt, rs, topw, w, u, P, s);
   const int de = de_of(c), I = c->d_expert;
   const bool fp4 = c->expert_dtype == MOE_DT_NVFP4;
   GemvArgs a{};
@@ -290,7 +303,7 @@ moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t
 }
 
 // ---- NVFP4 experts on the FP4 tensor path ----
-inline bool fp4_path(const moe_config_t* c) { return c->expert_dtype == MOE_DT_NVFP4 && g_act_terms.load() > 0; }
+inline bool fp4_path(const moe_config_t* c, int T) { return c->expert_dtype == MOE_DT_NVFP4 && act_terms_for(T) > 0; }
 
 // packed rows per tile of an expert product with N output features (a decode
 // tile holds an expert's rows)
@@ -317,7 +330,7 @@ GemvArgs fp4_args(const moe_config_t* c, int T, const void* W, const uint8_t* W_
 // or x_e gathered through rt) become NVFP4 terms, then the FP4 product
 moe_status_t run_up_fp4(const moe_config_t* c, int T, const void* x_e, const void* x_packed, const int32_t* rt,
                         const int32_t* offsets, const moe_weights_t* w, void* h, const Ptrs& P, cudaStream_t s) {
-  const int de = de_of(c), I = c->d_expert, nt = g_act_terms.load();
+  const int de = de_of(c), I = c->d_expert, nt = act_terms_for(T);
   const int R = T * c->top_k;
   uint8_t* xq = P.at<uint8_t>(P.L.xq);
   uint8_t* xq_sf = P.at<uint8_t>(P.L.xq_sf);
@@ -334,7 +347,7 @@ moe_status_t run_up_fp4(const moe_config_t* c, int T, const void* x_e, const voi
 moe_status_t run_down_fp4(const moe_config_t* c, int T, const void* h, const int32_t* offsets, const int32_t* rt,
                           const int32_t* rs, const float* topw, const moe_weights_t* w, float* u, const Ptrs& P,
                           cudaStream_t s) {
-  const int de = de_of(c), I = c->d_expert, nt = g_act_terms.load();
+  const int de = de_of(c), I = c->d_expert, nt = act_terms_for(T);
   const int R = T * c->top_k;
   uint8_t* hq = P.at<uint8_t>(P.L.hq);
   uint8_t* hq_sf = P.at<uint8_t>(P.L.hq_sf);
@@ -469,8 +482,10 @@ const char* moe_status_string(moe_status_t s) {
 
 moe_status_t moe_check_config(const moe_config_t* cfg) { return check_config(cfg); }
 
+int32_t moe_nvfp4_act_terms_for(int32_t T) { return act_terms_for(T); }
+
 int32_t moe_set_nvfp4_act_terms(int32_t n) {
-  if (n < 0 || n > kActTermsMax) return -1;
+  if (n < -1 || n > kActTermsMax) return -2;
   return g_act_terms.exchange(n);
 }
 
@@ -653,7 +668,7 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
   int32_t* rt = P.at<int32_t>(P.L.route_token);
   int32_t* rs = P.at<int32_t>(P.L.route_slot);
   int32_t* tsr = P.at<int32_t>(P.L.tsr);
-  void* x_packed = use_tc(cfg, T) && !fp4_path(cfg) ? P.at<void>(P.L.x_packed) : nullptr;
+  void* x_packed = use_tc(cfg, T) && !fp4_path(cfg, T) ? P.at<void>(P.L.x_packed) : nullptr;
   DispatchArgs da = dispatch_args(cfg, T, ids, x_e, P.at<int32_t>(P.L.counts), offsets, rt, rs, tsr, x_packed, P);
   da.pack_f16 = f16 && x_packed;
   if (select_dispatch_fits(T, cfg->top_k, da)) {

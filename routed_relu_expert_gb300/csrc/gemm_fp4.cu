@@ -49,7 +49,7 @@ constexpr int kFp4Threads = 384;                       // 12 warps
 constexpr int kBWarpF = 6;
 constexpr int kSfWarp0 = 7;                            // warps 7..10
 constexpr int kSfbWarp = 11;
-constexpr int N_HEIGHTS = 8;                           // B boxes of 16, 32, ..., 128 rows
+constexpr int N_HEIGHTS = 4;                           // B boxes of 16, 32, 48, 64 rows
 constexpr int kSfPrefetch = 6;                         // weight-scale stages fetched ahead
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr int kTileTable = 512;                        // units a CTA finds decoded in shared memory
@@ -68,18 +68,18 @@ struct Fp4Cfg {
   // 32 rows never fill one
   static constexpr int STG = BNMAX >= 32 ? 32 * 32 * 4 : 0;
   static constexpr int EPI_WARP = STG + 2 * BNMAX * 4;                   // + routing weights, row scales
-  // MERGE (short tiles): the terms' rows, stacked, are one B operand of
-  // NT * rows, so each K step is one MMA (a block-scaled MMA costs about the
-  // same for 32 columns as for 96) and the epilogue adds the terms' columns;
-  // else one MMA per term into the same accumulator
-  static constexpr bool MERGE = BNMAX <= 32;
+  // MERGE: the terms' rows, stacked, are one B operand of NT * rows, so each
+  // K step is one MMA (a block-scaled MMA costs nearly as much for 32 columns
+  // as for 192) and the epilogue adds the terms' columns; else one MMA per
+  // term into the same accumulator
+  static constexpr bool MERGE = NT * BNMAX <= 192;
   static constexpr int ACC_COLS = MERGE ? NT * BNMAX : BNMAX;            // one accumulator
-  // every scale-factor address the MMA gets is a multiple of four columns (a
-  // K step's scales always take four columns, used or not)
+  // every scale-factor address the MMA gets is a multiple of four columns
   static constexpr int SFB_ROW_CHUNKS = (NT * BNMAX + 31) / 32;          // 32-row chunks of stacked rows
-  static constexpr int SF_COLS = 16 + 16 * (MERGE ? 1 : NT);             // TMEM scale columns per stage
+  static constexpr int SFB_STEP = MERGE ? (SFB_ROW_CHUNKS <= 4 ? 4 : 8) : 4;   // B scale columns a K step
+  static constexpr int SF_COLS = 16 + (MERGE ? 4 * SFB_STEP : 16 * NT);  // TMEM scale columns per slot
   static constexpr int TMEM_SF0 = 2 * ACC_COLS;                          // after the two accumulators
-  static_assert(!MERGE || SFB_ROW_CHUNKS <= 4, "merged terms fit four scale columns");
+  static_assert(!MERGE || SFB_ROW_CHUNKS <= 8, "merged terms fit eight scale columns");
   static_assert(!MERGE || A_STAGE_BYTES + NT * B_TERM + 32 * SFB_ROW_CHUNKS * 16 <= STAGE,
                 "the scale writers' reads stay inside the stage");
   static_assert(ACC_COLS % 4 == 0 && SF_COLS % 16 == 0, "scale and accumulator columns stay aligned");
@@ -89,12 +89,17 @@ struct Fp4Cfg {
   static constexpr size_t SMEM_LIMIT = CPS == 1 ? kSmemLimit : 113 * 1024;
   static constexpr int stages_for() {
     int s = 8;
-    while (s > 2 && ((size_t)s * STAGE + fixed_smem(1024) > SMEM_LIMIT || TMEM_SF0 + s * SF_COLS > TMEM_COLS)) --s;
+    while (s > 2 && (size_t)s * STAGE + fixed_smem(1024) > SMEM_LIMIT) --s;
     return s;
   }
   static constexpr int STAGES = stages_for();
+  // TMEM scale slots: one per stage when they fit, else fewer, reused in turn
+  // (DECOUPLED: a slot is rewritten only after the MMAs that read it completed)
+  static constexpr int SF_SLOTS =
+      (TMEM_COLS - TMEM_SF0) / SF_COLS < STAGES ? (TMEM_COLS - TMEM_SF0) / SF_COLS : STAGES;
+  static constexpr bool DECOUPLED = SF_SLOTS < STAGES;
   static_assert((size_t)STAGES * STAGE + fixed_smem(1024) <= SMEM_LIMIT, "shared memory");
-  static_assert(TMEM_SF0 + STAGES * SF_COLS <= TMEM_COLS, "tensor memory");
+  static_assert(SF_SLOTS >= 2 && TMEM_SF0 + SF_SLOTS * SF_COLS <= TMEM_COLS, "tensor memory");
   static_assert(B_TERM % 1024 == 0, "term tiles start on 1024-byte boundaries");
 };
 
@@ -173,6 +178,12 @@ __device__ __forceinline__ void tmem_st_x2(uint32_t taddr, uint32_t v0, uint32_t
 __device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
                "r"(v2), "r"(v3)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3,
+                                           uint32_t v4, uint32_t v5, uint32_t v6, uint32_t v7) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(v0),
+               "r"(v1), "r"(v2), "r"(v3), "r"(v4), "r"(v5), "r"(v6), "r"(v7)
                : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -295,14 +306,16 @@ __global__ void __launch_bounds__(kFp4Threads, Fp4Cfg<BNMAX, NT>::CPS)
   // afull: a stage's weight tile landed; bfull: its activation terms and their
   // scales landed (from L2, usually well before the weights); sf: the scale
   // writers have placed the stage's scales in TMEM; empty: its MMAs completed
+  constexpr int SLOTS = C::SF_SLOTS;
   auto afull_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto sf_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
-  auto bfull_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + s); };
-  auto tfull_bar = [&](int i) { return bar0 + 8u * (4 * STAGES + i); };
-  auto tempty_bar = [&](int i) { return bar0 + 8u * (4 * STAGES + 2 + i); };
-  const uint32_t drain_bar = bar0 + 8u * (4 * STAGES + 4);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 4 * STAGES + 5);
+  auto bfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+  auto sf_bar = [&](int k) { return bar0 + 8u * (3 * STAGES + k); };               // slot k written
+  auto sffree_bar = [&](int k) { return bar0 + 8u * (3 * STAGES + SLOTS + k); };   // slot k read
+  auto tfull_bar = [&](int i) { return bar0 + 8u * (3 * STAGES + 2 * SLOTS + i); };
+  auto tempty_bar = [&](int i) { return bar0 + 8u * (3 * STAGES + 2 * SLOTS + 2 + i); };
+  const uint32_t drain_bar = bar0 + 8u * (3 * STAGES + 2 * SLOTS + 4);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 2 * SLOTS + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* scan_tmp = reinterpret_cast<int*>(tmem_holder + 4);          // [16]
   int* prefix = scan_tmp + 16;                                         // [E+1]
@@ -318,7 +331,10 @@ __global__ void __launch_bounds__(kFp4Threads, Fp4Cfg<BNMAX, NT>::CPS)
       mbar_init(afull_bar(s), 1);
       mbar_init(bfull_bar(s), 2);       // the activation terms and their scales
       mbar_init(empty_bar(s), 1);
-      mbar_init(sf_bar(s), 128);        // the four scale-writer warps
+    }
+    for (int k = 0; k < SLOTS; ++k) {
+      mbar_init(sf_bar(k), 128);        // the four scale-writer warps
+      mbar_init(sffree_bar(k), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull_bar(i), 1);
@@ -421,8 +437,8 @@ __global__ void __launch_bounds__(kFp4Threads, Fp4Cfg<BNMAX, NT>::CPS)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      int stage = 0, acc = 0, slot = 0;
+      uint32_t phase = 0, acc_phase = 0, sphase = 0;
       bool ok = true, issued = false;
       for (int t = unit; t < total && ok; t += n_units) {
         Tile ti;
@@ -435,17 +451,18 @@ __global__ void __launch_bounds__(kFp4Threads, Fp4Cfg<BNMAX, NT>::CPS)
         uint32_t accumulate = 0;
         for (int kb = 0; kb < nkb; ++kb) {
           // (the scale writers arrive only after seeing the activation copies land)
-          if (!mbar_wait<false, true>(sf_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
+          if (!mbar_wait<false, true>(sf_bar(slot), sphase, abort_flag, a.err)) { ok = false; break; }
           if (!mbar_wait<false, true>(afull_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = base + stage * C::STAGE;
-          const uint32_t sf0 = tmem_base + (uint32_t)(C::TMEM_SF0 + stage * C::SF_COLS);
+          const uint32_t sf0 = tmem_base + (uint32_t)(C::TMEM_SF0 + slot * C::SF_COLS);
           const int steps = min(4, (K - kb * FP4_K_STAGE) / 64);
           const uint64_t da = smem_desc_sw128(st);
           const uint64_t db0 = smem_desc_sw128(st + A_STAGE_BYTES);
           for (int s = 0; s < steps; ++s) {
             if constexpr (C::MERGE) {
-              mma_fp4(d, da + 2u * s, db0 + 2u * s, idesc, sf0 + 4u * s, sf0 + 16u + 4u * s, accumulate);
+              mma_fp4(d, da + 2u * s, db0 + 2u * s, idesc, sf0 + 4u * s, sf0 + 16u + (uint32_t)(C::SFB_STEP * s),
+                      accumulate);
               accumulate = 1;
             } else {
 #pragma unroll
@@ -459,7 +476,9 @@ __global__ void __launch_bounds__(kFp4Threads, Fp4Cfg<BNMAX, NT>::CPS)
           }
           issued = true;
           tc_commit<1>(empty_bar(stage));
+          if constexpr (C::DECOUPLED) tc_commit<1>(sffree_bar(slot));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++slot == SLOTS) { slot = 0; sphase ^= 1u; }
         }
         if (!ok) break;
         tc_commit<1>(tfull_bar(acc));
@@ -505,8 +524,8 @@ __global__ void __launch_bounds__(kFp4Threads, Fp4Cfg<BNMAX, NT>::CPS)
     uint4 ring[kSfPrefetch];
 #pragma unroll
     for (int i = 0; i < kSfPrefetch; ++i) ring[i] = fetch();
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, slot = 0, g = 0;
+    uint32_t phase = 0, sphase = 0;
     bool ok = true;
     for (int t = unit; t < total && ok; t += n_units) {
       Tile ti;
@@ -522,7 +541,14 @@ __global__ void __launch_bounds__(kFp4Threads, Fp4Cfg<BNMAX, NT>::CPS)
         // columns before are complete (the copies waited for them); the
         // weight tile may still be on its way from HBM
         if (!mbar_wait<false, true>(bfull_bar(stage), phase, abort_flag, a.err)) { ok = false; break; }
-        const uint32_t col = (uint32_t)(C::TMEM_SF0 + stage * C::SF_COLS);
+        // a reused slot: the MMAs of stage g - SLOTS have read it
+        if constexpr (C::DECOUPLED) {
+          if (g >= SLOTS && !mbar_wait<false, true>(sffree_bar(slot), sphase ^ 1u, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+        }
+        const uint32_t col = (uint32_t)(C::TMEM_SF0 + slot * C::SF_COLS);
         // weight row 32q + lane: K step s at column col + 4s + q
         tmem_st_x1(lane_base + col + 0u + q, wa.x);
         tmem_st_x1(lane_base + col + 4u + q, wa.y);
@@ -533,17 +559,25 @@ __global__ void __launch_bounds__(kFp4Threads, Fp4Cfg<BNMAX, NT>::CPS)
         const uint8_t* sfb = gbase + stage * C::STAGE + A_STAGE_BYTES + NT * C::B_TERM;
         if constexpr (C::MERGE) {
           // the stacked rows n = j * r16 + i (term j, tile row i): K step s at
-          // column col + 16 + 4s + n / 32 (rows past NT * r16: unused)
-          uint4 r4[4];
+          // column col + 16 + SFB_STEP * s + n / 32 (rows past NT * r16: unused)
+          constexpr int CH = C::SFB_STEP;
+          uint4 r4[CH];
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < CH; ++c)
             r4[c] = c < C::SFB_ROW_CHUNKS ? *reinterpret_cast<const uint4*>(sfb + (32 * c + lane) * 16)
                                           : make_uint4(0u, 0u, 0u, 0u);
           const uint32_t cs = col + 16u;
-          tmem_st_x4(lane_base + cs + 0u, r4[0].x, r4[1].x, r4[2].x, r4[3].x);
-          tmem_st_x4(lane_base + cs + 4u, r4[0].y, r4[1].y, r4[2].y, r4[3].y);
-          tmem_st_x4(lane_base + cs + 8u, r4[0].z, r4[1].z, r4[2].z, r4[3].z);
-          tmem_st_x4(lane_base + cs + 12u, r4[0].w, r4[1].w, r4[2].w, r4[3].w);
+          if constexpr (CH == 4) {
+            tmem_st_x4(lane_base + cs + 0u, r4[0].x, r4[1].x, r4[2].x, r4[3].x);
+            tmem_st_x4(lane_base + cs + 4u, r4[0].y, r4[1].y, r4[2].y, r4[3].y);
+            tmem_st_x4(lane_base + cs + 8u, r4[0].z, r4[1].z, r4[2].z, r4[3].z);
+            tmem_st_x4(lane_base + cs + 12u, r4[0].w, r4[1].w, r4[2].w, r4[3].w);
+          } else {
+            tmem_st_x8(lane_base + cs + 0u, r4[0].x, r4[1].x, r4[2].x, r4[3].x, r4[4].x, r4[5].x, r4[6].x, r4[7].x);
+            tmem_st_x8(lane_base + cs + 8u, r4[0].y, r4[1].y, r4[2].y, r4[3].y, r4[4].y, r4[5].y, r4[6].y, r4[7].y);
+            tmem_st_x8(lane_base + cs + 16u, r4[0].z, r4[1].z, r4[2].z, r4[3].z, r4[4].z, r4[5].z, r4[6].z, r4[7].z);
+            tmem_st_x8(lane_base + cs + 24u, r4[0].w, r4[1].w, r4[2].w, r4[3].w, r4[4].w, r4[5].w, r4[6].w, r4[7].w);
+          }
         } else {
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
@@ -572,8 +606,10 @@ __global__ void __launch_bounds__(kFp4Threads, Fp4Cfg<BNMAX, NT>::CPS)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(sf_bar(stage));
+        mbar_arrive(sf_bar(slot));
+        ++g;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (++slot == SLOTS) { slot = 0; sphase ^= 1u; }
       }
     }
   } else if (warp >= 2 && warp < 6) {
@@ -738,8 +774,7 @@ cudaError_t launch_fp4_bn(const Fp4Maps& maps, const GemvArgs& a, int E, int m_t
                           cudaStream_t s) {
   if (bn <= 16) return launch_fp4_t<EPI, OUT_F32, 16, NT>(maps, a, E, m_tiles, bn, units, to, s);
   if (bn <= 32) return launch_fp4_t<EPI, OUT_F32, 32, NT>(maps, a, E, m_tiles, bn, units, to, s);
-  if (bn <= 64) return launch_fp4_t<EPI, OUT_F32, 64, NT>(maps, a, E, m_tiles, bn, units, to, s);
-  return launch_fp4_t<EPI, OUT_F32, 128, NT>(maps, a, E, m_tiles, bn, units, to, s);
+  return launch_fp4_t<EPI, OUT_F32, 64, NT>(maps, a, E, m_tiles, bn, units, to, s);
 }
 
 }  // namespace
@@ -761,21 +796,21 @@ cudaError_t launch_quant_terms(const void* x, int64_t x_ld, const int32_t* gathe
   return cudaGetLastError();
 }
 
-// Rows per tile: 16, 32 or 64 where the segments hold few rows (decode: an
+// Rows per tile: 16 or 32 where the segments hold few rows (decode: an
 // expert's rows fit one tile, and the kernels for short tiles keep more weight
-// stages in flight), else 128 (fewer re-reads of each weight tile); fewer when
-// the product is too small to give every SM two tiles.
+// stages in flight), else 64 (with three terms stacked, 192 MMA columns);
+// fewer when the product is too small to give every SM two tiles.
 int fp4_tile_rows(int64_t rows_per_seg, int64_t segs, int N) {
   const int64_t m_tiles = ceil_div(N, BM);
   const int64_t units = num_sms();
   const int64_t rows = std::max<int64_t>(rows_per_seg, 1);
-  int bn = rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
+  int bn = rows <= 16 ? 16 : rows <= 32 ? 32 : 64;
   while (bn > 16 && ceil_div(rows, bn) * segs * m_tiles < 2 * units) bn -= 16;
   return bn;
 }
 
 cudaError_t launch_gemm_fp4(const GemvArgs& a, int epi, bool out_f32, int64_t w_rows, int E, int bn, cudaStream_t s) {
-  if (a.K % 64 || a.N % 32 || bn < 16 || bn > 128 || bn % 16 || E > 1024 || !a.W_sf || !a.X_sf || !a.x_scale)
+  if (a.K % 64 || a.N % 32 || bn < 16 || bn > 64 || bn % 16 || E > 1024 || !a.W_sf || !a.X_sf || !a.x_scale)
     return cudaErrorNotSupported;
   if (a.x_terms < 1 || a.x_terms > kActTermsMax || a.x_rows_cap <= 0 || a.x_sf_ld % 16 || a.x_sf_ld < a.K / 16)
     return cudaErrorNotSupported;

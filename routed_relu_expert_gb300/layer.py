@@ -95,12 +95,18 @@ def new_workspace(cfg: N.MoeConfig, T: int, device="cuda") -> torch.Tensor:
 
 
 def set_nvfp4_act_terms(n: int) -> int:
-    """How NVFP4 experts take their activations (0: FP16 path; 1..4: NVFP4
-    terms on the FP4 tensor path); returns the previous setting."""
+    """How NVFP4 experts take their activations (-1: the measured default;
+    0: FP16 path; 1..4: NVFP4 terms on the FP4 tensor path); returns the
+    previous setting."""
     prev = int(N.load().moe_set_nvfp4_act_terms(int(n)))
-    if prev < 0:
-        raise ValueError(f"activation terms must be 0..4, got {n}")
+    if prev < -1:
+        raise ValueError(f"activation terms must be -1..4, got {n}")
     return prev
+
+
+def nvfp4_act_terms_for(T: int) -> int:
+    """Activation terms an NVFP4 layer of T tokens uses now (0: FP16 path)."""
+    return int(N.load().moe_nvfp4_act_terms_for(int(T)))
 
 
 def workspace_region(cfg: N.MoeConfig, T: int, region: int):

@@ -89,8 +89,7 @@ def _parity(shape, T, sample=None, seed_stream=0, chunk=0):
     x = make_x(shape, T, "cuda", seed_stream)
     g = run_gpu(shape, w, x)
     assert g["err"] == 0
-    terms = M.set_nvfp4_act_terms(0)
-    M.set_nvfp4_act_terms(terms)
+    terms = M.nvfp4_act_terms_for(T)
     fp4_terms = shape.expert_dtype == 2 and terms > 0
     if T > 64 and shape.act_dtype == BF16 and not fp4_terms:
         _check_packed_rows(shape, g, x, T)
@@ -175,18 +174,31 @@ def test_super_nvfp4_full_size(T):
 @pytest.fixture
 def act_terms():
     """Sets how NVFP4 experts take their activations for one test."""
-    prev = M.set_nvfp4_act_terms(3)
+    prev = M.set_nvfp4_act_terms(-1)
     yield M.set_nvfp4_act_terms
     M.set_nvfp4_act_terms(prev)
 
 
-@pytest.mark.parametrize("n", [0, 4])
-@pytest.mark.parametrize("T", [9, 200])
-def test_scaled_nvfp4_layer_other_activation_forms(act_terms, n, T):
-    """The FP16 path (0) and four terms on the FP4 tensor path, decode and
-    prefill sizes, against the exact oracle."""
+@pytest.mark.parametrize("n", [0, 3, 4])
+@pytest.mark.parametrize("T", [1, 9, 200])
+def test_scaled_nvfp4_layer_every_activation_form(act_terms, n, T):
+    """The FP16 path (0) and three or four terms on the FP4 tensor path, at
+    one token, decode and prefill sizes, against the exact oracle."""
     act_terms(n)
     _parity(SMALL_NVFP4, T, seed_stream=n)
+
+
+@pytest.mark.parametrize("n", [0, 3])
+def test_super_nvfp4_on_the_paths_the_default_skips(act_terms, n):
+    """Full-size Super NVFP4 layers on the path the default does not take at
+    that size, every row against the oracle: the FP16 path at 64 tokens and
+    the FP4 path at 8192 (the default's paths are covered by the full-size
+    tests above)."""
+    act_terms(n)
+    if n == 0:
+        _parity(SUPER_NVFP4, 64, chunk=64)        # the FP16 path at the decode size the default gives the FP4 path
+    else:
+        _parity(SUPER_NVFP4, 8192, chunk=8192)    # the FP4 path at the prefill size the default gives the FP16 path
 
 
 @pytest.mark.parametrize("n", [1, 2])
