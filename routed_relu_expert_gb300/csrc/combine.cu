@@ -25,7 +25,6 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
                                                                   float* __restrict__ y_r, void* __restrict__ y_act,
                                                                   const float* __restrict__ add) {
   pdl_wait();
-  pdl_trigger();
   __shared__ int rows[32];
   const int t = blockIdx.x;
   if (threadIdx.x < K) {
@@ -82,7 +81,6 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
 template <bool ACT_F32>
 __global__ void cast_kernel(const float* __restrict__ src, int64_t n4, void* __restrict__ dst) {
   pdl_wait();
-  pdl_trigger();
   for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < n4; v += (int64_t)gridDim.x * blockDim.x) {
     const float4 q = reinterpret_cast<const float4*>(src)[v];
     if (ACT_F32) {

@@ -74,13 +74,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 
 // ---------------------------------------------------------------------------
 // programmatic dependent launch: every kernel of the library is launched so
-// that it may start while its predecessor on the stream finishes; it lets its
-// own successor launch early (trigger) and waits for the predecessor's results
-// to be complete and visible (wait) before reading any of them.  Both are
-// no-ops for a kernel launched without the attribute.
+// that the launch of its successor on the stream is prepared while it runs; a
+// kernel waits for its predecessor's results to be complete and visible (wait)
+// before reading any of them, a no-op for a kernel launched without the
+// attribute.  No kernel releases its successor early
+// (griddepcontrol.launch_dependents): blocks released early sit resident,
+// waiting, in SM slots that the shared expert on the concurrent stream needs,
+// and on GB300 that cost the Super layer 4-56 us a step (T = 1..4096) while
+// an early release gained at most 1 us on the single-chain steps.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
 // shared-memory addresses, the global nanosecond timer (bounded waits) and

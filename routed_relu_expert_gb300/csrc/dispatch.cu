@@ -110,7 +110,6 @@ __global__ void __launch_bounds__(256) pack_rows_kernel(const uint4* __restrict_
                                                         const int32_t* __restrict__ offsets, int E, int row_vecs,
                                                         uint4* __restrict__ x_packed) {
   pdl_wait();
-  pdl_trigger();
   const int R = offsets[E];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int j = blockIdx.x * 8 + warp; j < R; j += gridDim.x * 8) {
@@ -171,7 +170,6 @@ __device__ void write_schedule(const DispatchArgs& a, int e, int total, int off,
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) dispatch_single(const DispatchArgs a) {
   pdl_wait();
-  pdl_trigger();
   extern __shared__ int sm[];
   int* hist = sm;                      // [32][E]
   int* tmp32 = sm + kWarps * a.E;      // [32]
@@ -202,7 +200,6 @@ __global__ void __launch_bounds__(kThreads) dispatch_single(const DispatchArgs a
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) dispatch_count(const DispatchArgs a) {
   pdl_wait();
-  pdl_trigger();
   extern __shared__ int sm[];
   int* hist = sm;
   const int tile = blockIdx.x;
@@ -221,7 +218,6 @@ __global__ void __launch_bounds__(kThreads) dispatch_count(const DispatchArgs a)
 
 __global__ void __launch_bounds__(kThreads) dispatch_scan(const DispatchArgs a, int n_tiles) {
   pdl_wait();
-  pdl_trigger();
   __shared__ int tmp32[32];
   const int e = threadIdx.x;
   int total = 0;
@@ -240,7 +236,6 @@ __global__ void __launch_bounds__(kThreads) dispatch_scan(const DispatchArgs a, 
 
 __global__ void __launch_bounds__(kThreads) dispatch_scatter(const DispatchArgs a) {
   pdl_wait();
-  pdl_trigger();
   extern __shared__ int sm[];
   int* hist = sm;
   const int tile = blockIdx.x;
@@ -276,7 +271,6 @@ constexpr int kTinyMaxTokens = kTinyThreads / 32;
 template <int P>
 __global__ void __launch_bounds__(kTinyThreads) select_dispatch_tiny(const SelectArgs sa, const DispatchArgs a) {
   pdl_wait();
-  pdl_trigger();
   __shared__ int sid[kTinyMaxRoutes];     // expert of route r (-1: invalid)
   __shared__ int first[kTinyMaxRoutes];   // route r is its expert's first route
   __shared__ int cnt_max[kTinyThreads / 32];

@@ -230,7 +230,6 @@ __global__ void __launch_bounds__(256) quant_terms_kernel(const bf16* __restrict
                                                           float* __restrict__ g, int64_t rows_cap,
                                                           int64_t sf_ld) {
   pdl_wait();
-  pdl_trigger();
   const int rows = count ? min(*count, R) : R;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = K / 16;
@@ -325,7 +324,6 @@ __global__ void __launch_bounds__(kFp4Threads, Fp4Cfg<BNMAX, NT>::CPS)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.x, n_units = gridDim.x;
-  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(afull_bar(s), 1);

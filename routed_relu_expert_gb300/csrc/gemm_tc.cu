@@ -127,7 +127,6 @@ __global__ void __launch_bounds__(FP4A ? kThreadsFp4 : kThreads, 1)
   const int unit = CG == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int n_units = CG == 2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   auto at_leader = [&](uint32_t bar) { return CG == 2 ? map_to_rank0(bar) : bar; };
-  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), FP4A ? 1 : 2);      // the A and B producers of CTA 0

@@ -79,7 +79,6 @@ __device__ __forceinline__ bool resolve_segment(const GemvArgs& a, int rows_per_
 template <int EPI, bool OUT_F32, int FPC>
 __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a) {
   pdl_wait();
-  pdl_trigger();
   constexpr int NT = 2;                 // 8-row column blocks per pass
   constexpr int U = 4;                  // 32-wide K chunks in flight per warp
   constexpr int WG = kWarps * 16 / FPC; // warps per 16-feature group (K split)
@@ -208,7 +207,6 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
 template <int EPI, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 3) gemv_nvfp4_kernel(const GemvArgs a) {
   pdl_wait();
-  pdl_trigger();
   constexpr int NT = 2;
   Seg sg;
   if (!resolve_segment(a, 1 << 30, sg)) return;
@@ -354,7 +352,6 @@ template <int EPI, int OUT, bool XF16, int WPG>
 __global__ void __launch_bounds__(kBulkThreads) gemv_nvfp4_bulk_kernel(const GemvArgs a) {
   extern __shared__ __align__(16) uint8_t bsm[];
   pdl_wait();
-  pdl_trigger();
   constexpr int NT = 2;
   constexpr int ROWS = 16 * kBulkWarps / WPG;          // features of this CTA
   Seg sg;
@@ -542,7 +539,6 @@ __global__ void __launch_bounds__(kBulkThreads) gemv_nvfp4_bulk_kernel(const Gem
 template <int EPI>
 __global__ void __launch_bounds__(kThreads) gemv_f32_kernel(const GemvArgs a) {
   pdl_wait();
-  pdl_trigger();
   Seg sg;
   if (!resolve_segment(a, 64, sg)) return;
   const int fl = threadIdx.x & 63, rg = threadIdx.x >> 6;
@@ -578,7 +574,6 @@ cudaError_t bulk_attr() {
 // FP16 copy of BF16 activations, 8 values per thread
 __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* x, int64_t n8, uint4* out) {
   pdl_wait();
-  pdl_trigger();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n8) return;
   const uint4 v = x[i];

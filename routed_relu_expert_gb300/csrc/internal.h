@@ -31,7 +31,7 @@ struct PerDeviceOnce {
   }
 };
 
-// Launch with programmatic stream serialisation (see pdl_wait / pdl_trigger).
+// Launch with programmatic stream serialisation (see pdl_wait).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
   cudaLaunchConfig_t cfg = {};

@@ -25,7 +25,6 @@ __global__ void __launch_bounds__(256) router_logits_small(const void* __restric
                                                            const float* __restrict__ Wr, int E,
                                                            float* __restrict__ logits) {
   pdl_wait();
-  pdl_trigger();
   constexpr int KS = 8 / EPC;
   __shared__ float red[8][TMAX];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -94,7 +93,6 @@ __global__ void __launch_bounds__(256) router_logits_tiled(const void* __restric
                                                            const float* __restrict__ Wr, int E,
                                                            float* __restrict__ logits) {
   pdl_wait();
-  pdl_trigger();
   __shared__ float xs[16][64 + 4];
   __shared__ float ws[16][64 + 4];
   const int tid = threadIdx.x;
@@ -159,7 +157,6 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
                                                             float* __restrict__ wout,
                                                             int32_t* err) {
   pdl_wait();
-  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -173,7 +170,6 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
 // accumulation carries FP32-level precision for BF16 x (exact in BF16).
 __global__ void split_bf16x3_kernel(const float* __restrict__ w, int E, int d, bf16* __restrict__ out) {
   pdl_wait();
-  pdl_trigger();
   const int64_t n = (int64_t)E * d;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t e = i / d, j = i - e * d;
