@@ -449,6 +449,35 @@ def layer_forward(x: np.ndarray, weights: Dict[str, np.ndarray], ids: np.ndarray
     return out
 
 
+def rms_norm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm of every row, float64: gamma * x / sqrt(mean(x^2) + eps)
+    (page "Nemotron Is Not One Circuit", section "The Four Layer Kinds CKE Must
+    Preserve": an MoE layer starts with RMSNorm).  The pages name the step
+    only; this is its usual definition, a root mean square over the hidden
+    width, no mean subtraction, a learned per-column weight."""
+    x = np.asarray(x, dtype=np.float64)
+    ms = np.mean(x * x, axis=1, keepdims=True)
+    return np.asarray(gamma, dtype=np.float64)[None, :] * (x / np.sqrt(ms + eps))
+
+
+def block_forward(x: np.ndarray, gamma: np.ndarray, eps: float, weights: Dict[str, np.ndarray],
+                  ids: np.ndarray, w: np.ndarray, n_experts: int, bf16_points: bool,
+                  xn: Optional[np.ndarray] = None, act_terms: Optional[int] = None) -> Dict[str, np.ndarray]:
+    """MoE block of a decoder layer for given routing: out = x + layer(RMSNorm(x))
+    (page "Nemotron Is Not One Circuit", section "The Four Layer Kinds CKE Must
+    Preserve": RMSNorm -> router -> group-limited top-k -> routed ReLU^2 experts
+    + shared expert -> residual).  ``xn``: the normalised rows the layer reads,
+    when they are given as the device stored them (rounded to its activation
+    type); else the float64 ``rms_norm``.  Returns the float64 ``out`` before
+    storage rounding, ``xn`` and the layer's intermediates."""
+    xn_ref = rms_norm(x, gamma, eps)
+    xl = xn_ref if xn is None else np.asarray(xn, dtype=np.float64)
+    out = layer_forward(xl, weights, ids, w, n_experts, bf16_points, act_terms)
+    out["xn_ref"] = xn_ref
+    out["out"] = np.asarray(x, dtype=np.float64) + out["y"]
+    return out
+
+
 class _LazyExpert:
     """Expert e as a callable (matrices fetched, and dequantised, on first use)."""
 

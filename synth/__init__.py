@@ -2,11 +2,11 @@
 from .configs import (BF16, F32, NVFP4, MoEShape, NANO_DECODE, NANO_PREFILL,
                       ROUTER_ONLY_GROUPED, SUPER_LATENT, SUPER_NVFP4, TINY_FP32,
                       WORKLOADS, scaled)
-from .generate import (make_calibration_x, make_weights, make_x, quantize_nvfp4,
+from .generate import (make_calibration_x, make_norm_weight, make_weights, make_x, quantize_nvfp4,
                        router_params, zipf_offsets, zipf_targets)
 
 __all__ = [
     "BF16", "F32", "NVFP4", "MoEShape", "NANO_DECODE", "NANO_PREFILL", "ROUTER_ONLY_GROUPED",
-    "SUPER_LATENT", "SUPER_NVFP4", "TINY_FP32", "WORKLOADS", "scaled", "make_calibration_x",
+    "SUPER_LATENT", "SUPER_NVFP4", "TINY_FP32", "WORKLOADS", "scaled", "make_calibration_x", "make_norm_weight",
     "make_weights", "make_x", "quantize_nvfp4", "router_params", "zipf_offsets", "zipf_targets",
 ]

@@ -34,7 +34,7 @@ from .configs import BF16, F32, NVFP4, MoEShape
 
 _DATA = os.path.join(os.path.dirname(os.path.abspath(__file__)), "data")
 
-TID_ROUTER, TID_BIAS, TID_LAT_DOWN, TID_LAT_UP, TID_UP, TID_DOWN, TID_SH_UP, TID_SH_DOWN, TID_X = range(9)
+TID_ROUTER, TID_BIAS, TID_LAT_DOWN, TID_LAT_UP, TID_UP, TID_DOWN, TID_SH_UP, TID_SH_DOWN, TID_X, TID_NORM = range(10)
 
 
 def _seed(shape: MoEShape, tensor_id: int, replica: int = 0, extra: int = 0) -> int:
@@ -177,6 +177,14 @@ def make_x(shape: MoEShape, T: int, device="cpu", stream_id: int = 0) -> torch.T
         return torch.empty((0, shape.d_model), dtype=_act_torch_dtype(shape.act_dtype), device=device)
     return _normal((T, shape.d_model), 1.0, device,
                    _seed(shape, TID_X, stream_id, extra=T), _act_torch_dtype(shape.act_dtype))
+
+
+def make_norm_weight(shape: MoEShape, device="cpu", replica: int = 0) -> torch.Tensor:
+    """RMSNorm weight gamma [d] (FP32) of an MoE block: 1 + U(-0.25, 0.25) per
+    column, drawn on the CPU (a weight near one with per-column spread)."""
+    g = _gen("cpu", _seed(shape, TID_NORM, replica))
+    gamma = 1.0 + (torch.rand((shape.d_model,), generator=g, dtype=torch.float32) * 0.5 - 0.25)
+    return gamma.to(device)
 
 
 def make_calibration_x(shape: MoEShape, T: int) -> torch.Tensor:
