@@ -60,6 +60,8 @@ def parse(argv=None):
     ap.add_argument("--points", default="all",
                     help="per_workload entries: all, none, or one workload name")
     ap.add_argument("--eager", action="store_true", help="time eager calls instead of CUDA-graph replays")
+    ap.add_argument("--no-blocks", dest="blocks", action="store_false",
+                    help="skip the MoE-block chains (RMSNorm + layer + residual) at the verify shapes")
     ap.add_argument("--nvfp4-act-terms", type=int, default=-1,
                     help="NVFP4 experts: activation terms on the FP4 tensor path (1-4), 0 = FP16 path; "
                          "-1 = the library's default")
@@ -530,6 +532,51 @@ def measure_point(run: Runner, shape, T, layers, warmup):
             "err": err}
 
 
+VERIFY_ROWS = (1, 2, 4, 8, 16)   # verify-block shapes the block chain is timed at
+
+
+def measure_block_chain(run: Runner, shape, T, layers, warmup):
+    """The MoE block (RMSNorm, layer, residual) chained over the weight
+    replicas: block r reads block r-1's output, all captured in one CUDA graph;
+    ms per block = replay time / number of blocks."""
+    from synth import make_norm_weight, make_x
+    torch, M = run.torch, run.M
+    n = len(layers)
+    blocks = [M.MoEBlock(L.cfg, L.weights.tensors, make_norm_weight(shape, run.dev, r), 1e-5)
+              for r, L in enumerate(layers)]
+    ws = M.new_workspace(blocks[0].cfg, T, run.dev)
+    for b in blocks:
+        b._ws = ws
+    x = make_x(shape, T, run.dev)
+    bufs = [torch.empty_like(x) for _ in range(n)]
+
+    def chain():
+        cur = x
+        for r in range(n):
+            blocks[r].forward(cur, bufs[r])
+            cur = bufs[r]
+
+    for _ in range(max(1, warmup)):
+        chain()
+    torch.cuda.synchronize()
+    c0 = M.load().moe_launch_count()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain()
+    per = M.load().moe_launch_count() - c0
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+
+    def fn(i):
+        g.replay()
+
+    K = max(10, run.steps_for(fn) // n)
+    ms = run.timed(fn, K) / K
+    return {"ms_per_block": ms / n, "blocks_per_graph": n, "steps": K, "launches_per_block": per // n,
+            "err": M.moe_get_device_error(ws)}
+
+
 def run_ours(args, rank, world, dev):
     import torch
     import __graft_entry__
@@ -601,6 +648,22 @@ def run_ours(args, rank, world, dev):
                 entry.update(roofline_fractions(sh, Ts, p["n_active"], p["ms"], pk))
                 entry["routing"] = p["routing"]
                 per_workload[f"{name} T={Ts}"] = entry
+            if name in ("nano_decode", "super_latent", "super_nvfp4") and args.blocks:
+                # the MoE block (RMSNorm + layer + residual) at the verify shapes,
+                # a chain of blocks with independent weights in one graph
+                for Ts in VERIFY_ROWS:
+                    b = measure_block_chain(run, sh, Ts, lay, 3)
+                    ids = torch.empty((Ts, sh.top_k), dtype=torch.int32, device=dev)
+                    xb = make_x(sh, Ts, dev)
+                    lay[0].forward(xb, torch.empty_like(xb), ids_out=ids)
+                    n_act = int(np.unique(ids.cpu().numpy()).size)
+                    entry = {"ms_per_block": round(b["ms_per_block"], 5),
+                             "tokens_per_s": round(Ts / (b["ms_per_block"] / 1e3), 1),
+                             "blocks_per_graph": b["blocks_per_graph"], "timed_replays": b["steps"],
+                             "launches_per_block": b["launches_per_block"], "device_error_word": b["err"],
+                             "experts_active_first_block": n_act}
+                    entry.update(roofline_fractions(sh, Ts, n_act, b["ms_per_block"], pk))
+                    per_workload[f"{name} block-chain T={Ts}"] = entry
             if lay is not layers:
                 del lay
         pw_clocks = sampler.stop()

@@ -227,6 +227,32 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
                                float* logits_out, float* scores_out,
                                void* ws, size_t ws_bytes, void* stream);
 
+/* The MoE block of a decoder layer: RMSNorm, the layer, the residual add
+ * (page "Nemotron Is Not One Circuit: Mamba, Attention, and MoE Routing",
+ * section "The Four Layer Kinds CKE Must Preserve": an MoE layer is RMSNorm,
+ * router, group-limited top-k, routed ReLU^2 experts + shared expert,
+ * residual).  Chains of blocks need no host work between them, so several
+ * can be captured in one CUDA graph (page "NemotronH (Nemotron 3.5 Lightning,
+ * Bolt, Super VL)", section "Speculation": verify blocks of 1-16 rows).
+ *   x        [T, d] act_dtype residual stream in
+ *   norm_w   [d] FP32 RMSNorm weight gamma;  norm_eps >= 0
+ *   out      [T, d] act_dtype: out = act(x + layer(xn)), the layer's FP32
+ *            output and the residual added before the one rounding.  out may
+ *            be x itself (in place); any other overlap with x is rejected.
+ *   xn = act(gamma * (x * r)), r = 1 / sqrt(mean(x^2) + eps) per row, all in
+ *            FP32 with one rounding: the rows the router, the latent down
+ *            projection, the shared expert and (without a latent) the experts
+ *            read.  x_norm_out [T, d]: an optional copy (NULL: kept in the
+ *            workspace, MOE_WS_X_NORM); it must not overlap x or out.
+ *   topk_ids_out / topk_w_out / logits_out / scores_out: as moe_layer_forward.
+ * The RMSNorm kernel also clears the workspace header (no separate memset). */
+moe_status_t moe_block_forward(const moe_config_t* cfg, int32_t T, const void* x,
+                               const float* norm_w, float norm_eps,
+                               const moe_weights_t* w, void* out, void* x_norm_out,
+                               int32_t* topk_ids_out, float* topk_w_out,
+                               float* logits_out, float* scores_out,
+                               void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronises `stream`, copies the device error word of `ws` to *code (host
  * pointer) and returns MOE_ERR_DEVICE if any bit is set, else MOE_OK.         */
 moe_status_t moe_get_device_error(const void* ws, void* stream, int32_t* code);
@@ -284,6 +310,8 @@ int32_t moe_nvfp4_act_terms_for(int32_t T);
  *   MOE_WS_X_TERM_SCALES / _H_TERM_SCALES  [4][T*K][ld] u8  E4M3 scale per 16 values,
  *                                           ld = (K/16 rounded up to 16) for K = de | I
  *   MOE_WS_X_ROW_SCALES / _H_ROW_SCALES    [T*K] FP32  the rows' scale g
+ * After moe_block_forward without x_norm_out:
+ *   MOE_WS_X_NORM          [T, d]  act    the RMSNorm rows xn
  * *offset receives the region's byte offset from the workspace start, *bytes
  * its size.  MOE_ERR_INVALID_ARG for an unknown region or T < 0.           */
 enum {
@@ -291,7 +319,7 @@ enum {
   MOE_WS_TOKEN_SLOT_ROW = 4, MOE_WS_TOPK_IDS = 5, MOE_WS_TOPK_W = 6, MOE_WS_LOGITS = 7,
   MOE_WS_SCORES = 8, MOE_WS_X_LATENT = 9, MOE_WS_X_PACKED = 10, MOE_WS_H = 11, MOE_WS_X_TERMS = 12,
   MOE_WS_X_TERM_SCALES = 13, MOE_WS_X_ROW_SCALES = 14, MOE_WS_H_TERMS = 15, MOE_WS_H_TERM_SCALES = 16,
-  MOE_WS_H_ROW_SCALES = 17
+  MOE_WS_H_ROW_SCALES = 17, MOE_WS_X_NORM = 18
 };
 moe_status_t moe_workspace_region(const moe_config_t* cfg, int32_t T, int32_t region, size_t* offset,
                                   size_t* bytes);

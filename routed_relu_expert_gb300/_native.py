@@ -19,7 +19,8 @@ MOE_NOALLOC_MAX_ROUTER_ELEMS = 131072
 MOE_NOALLOC_MAX_SPLIT_ELEMS = 7340032
 (MOE_WS_COUNTS, MOE_WS_OFFSETS, MOE_WS_ROUTE_TOKEN, MOE_WS_ROUTE_SLOT, MOE_WS_TOKEN_SLOT_ROW, MOE_WS_TOPK_IDS,
  MOE_WS_TOPK_W, MOE_WS_LOGITS, MOE_WS_SCORES, MOE_WS_X_LATENT, MOE_WS_X_PACKED, MOE_WS_H, MOE_WS_X_TERMS,
- MOE_WS_X_TERM_SCALES, MOE_WS_X_ROW_SCALES, MOE_WS_H_TERMS, MOE_WS_H_TERM_SCALES, MOE_WS_H_ROW_SCALES) = range(18)
+ MOE_WS_X_TERM_SCALES, MOE_WS_X_ROW_SCALES, MOE_WS_H_TERMS, MOE_WS_H_TERM_SCALES, MOE_WS_H_ROW_SCALES,
+ MOE_WS_X_NORM) = range(19)
 ACT_TERMS_MAX = 4
 
 
@@ -51,7 +52,7 @@ EXPORTS = (
     "moe_dispatch", "moe_experts_up", "moe_experts_down", "moe_experts_down_combine", "moe_latent_down", "moe_shared",
     "moe_layer_forward", "moe_get_device_error", "moe_clear_device_error", "moe_layer_forward_host",
     "moe_launch_count", "moe_router_noalloc", "moe_workspace_region", "moe_set_nvfp4_act_terms",
-    "moe_nvfp4_act_terms_for",
+    "moe_nvfp4_act_terms_for", "moe_block_forward",
 )
 
 _lib = None
@@ -84,6 +85,7 @@ def load() -> ctypes.CDLL:
         "moe_latent_down": (I32, [CFG, I32, P, W, P, P, S, P]),
         "moe_shared": (I32, [CFG, I32, P, W, P, P, P, S, P]),
         "moe_layer_forward": (I32, [CFG, I32, P, W, P, P, P, P, P, P, S, P]),
+        "moe_block_forward": (I32, [CFG, I32, P, P, ctypes.c_float, W, P, P, P, P, P, P, P, S, P]),
         "moe_get_device_error": (I32, [P, P, ctypes.POINTER(I32)]),
         "moe_clear_device_error": (I32, [P, P]),
         "moe_layer_forward_host": (I32, [CFG, I32, P, P, W, P, P, P, S, P]),

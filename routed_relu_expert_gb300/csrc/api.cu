@@ -50,7 +50,9 @@ struct Layout {
   size_t route_token, route_slot, tsr, x_l, x_packed, h, u, y_r, y_rl, hs, ys, tile_counts;
   // NVFP4 experts: activation terms of the expert input rows and of h, their
   // block scales and row scales (sized for kActTermsMax terms)
-  size_t xq, xq_sf, xq_g, hq, hq_sf, hq_g, total;
+  size_t xq, xq_sf, xq_g, hq, hq_sf, hq_g;
+  size_t xn;   // the block's RMSNorm output rows [T, d] (activation type)
+  size_t total;
 };
 
 inline size_t take(size_t& off, size_t bytes) {
@@ -96,6 +98,7 @@ Layout make_layout(const moe_config_t* c, int32_t T) {
   L.hq = take(off, nt * R * I / 2);
   L.hq_sf = take(off, nt * R * (size_t)act_sf_ld((int)I));
   L.hq_g = take(off, fp4 ? R * 4 : 0);
+  L.xn = take(off, t * (size_t)c->d_model * ab);
   L.total = (off + 255) & ~(size_t)255;
   return L;
 }
@@ -459,6 +462,84 @@ moe_status_t check_weights(const moe_config_t* c, const moe_weights_t* w, bool e
   return MOE_OK;
 }
 
+// The layer on the caller's stream after the workspace header is cleared:
+// y = act(layer(x) + resid) (resid: the block's residual rows in the
+// activation type, or nullptr; y may be resid itself).
+moe_status_t run_layer(const moe_config_t* cfg, int32_t T, const void* x, const void* resid, const moe_weights_t* w,
+                       void* y, int32_t* topk_ids_out, float* topk_w_out, float* logits_out, float* scores_out,
+                       const Ptrs& P, cudaStream_t s) {
+  moe_status_t st = MOE_OK;
+  // fork: the latent down projection and the shared expert run on the
+  // auxiliary stream, the router and the selection on the caller's stream
+  const bool shared = cfg->d_shared > 0;
+  const bool latent = cfg->d_latent > 0;
+  float* ys = P.at<float>(P.L.ys);
+  const void* x_e = latent ? P.at<void>(P.L.x_l) : x;
+  // NVFP4: FP16 expert rows; decode makes an FP16 copy of x_e in the (then
+  // unused) packed-row buffer, prefill packs the rows as FP16
+  const bool f16 = up_down_f16(cfg, T, w);
+  const bool conv = f16 && !use_tc(cfg, T);
+  void* x16 = conv ? P.at<void>(P.L.x_packed) : nullptr;
+  const bool pre = latent || conv;         // work before the expert up projection
+  std::unique_lock<std::mutex> aux_lock(g_aux_mutex);
+  AuxStream* aux = nullptr;
+  if (shared || pre) {
+    if (!aux_stream(&aux)) return MOE_ERR_CUDA;
+    CU(cudaEventRecord(aux->fork, s));
+    CU(cudaStreamWaitEvent(aux->s, aux->fork, 0));
+    if (latent && (st = run_latent_down(cfg, T, x, w, const_cast<void*>(x_e), aux->s)) != MOE_OK) return st;
+    if (conv) CU(launch_bf16_to_f16(x_e, (int64_t)T * de_of(cfg), x16, aux->s));
+    if (pre) CU(cudaEventRecord(aux->latent, aux->s));
+    if (shared && (st = run_shared_to_f32(cfg, T, x, w, ys, P, aux->s)) != MOE_OK) return st;
+    CU(cudaEventRecord(aux->join, aux->s));
+  }
+  aux_lock.unlock();
+  float* logits = logits_out ? logits_out : P.at<float>(P.L.logits);
+  float* scores = scores_out ? scores_out : P.at<float>(P.L.scores);
+  int32_t* ids = topk_ids_out ? topk_ids_out : P.at<int32_t>(P.L.ids);
+  float* topw = topk_w_out ? topk_w_out : P.at<float>(P.L.topw);
+  SelectArgs sa;
+  if ((st = run_logits(cfg, T, x, w->w_router, w->router_bias, logits, scores, ids, topw, P, s, sa)) != MOE_OK)
+    return st;
+  int32_t* offsets = P.at<int32_t>(P.L.offsets);
+  int32_t* rt = P.at<int32_t>(P.L.route_token);
+  int32_t* rs = P.at<int32_t>(P.L.route_slot);
+  int32_t* tsr = P.at<int32_t>(P.L.tsr);
+  void* x_packed = use_tc(cfg, T) && !fp4_path(cfg, T) ? P.at<void>(P.L.x_packed) : nullptr;
+  DispatchArgs da = dispatch_args(cfg, T, ids, x_e, P.at<int32_t>(P.L.counts), offsets, rt, rs, tsr, x_packed, P);
+  da.pack_f16 = f16 && x_packed;
+  if (select_dispatch_fits(T, cfg->top_k, da)) {
+    CU(launch_select_dispatch(sa, da, s));       // a few tokens: one kernel
+  } else {
+    CU(launch_select(sa, s));
+    if (latent && x_packed) CU(cudaStreamWaitEvent(s, aux->latent, 0));   // the pack reads the latent rows
+    CU(launch_dispatch(da, s));
+  }
+  if (pre && !x_packed) CU(cudaStreamWaitEvent(s, aux->latent, 0));    // the up GEMV reads them
+  void* h = P.at<void>(P.L.h);
+  if ((st = run_up(cfg, T, conv ? x16 : x_e, x_packed, rt, offsets, w, h, P, s, f16)) != MOE_OK) return st;
+  float* u = P.at<float>(P.L.u);
+  if ((st = run_down(cfg, T, h, offsets, rt, rs, topw, w, u, P, s, f16)) != MOE_OK) return st;
+  if (cfg->d_latent == 0) {
+    // join, then y = act(sum of routed rows + y_s): the same two FP32 terms, one rounding
+    if (aux) CU(cudaStreamWaitEvent(s, aux->join, 0));
+    CU(launch_combine(u, tsr, T, cfg->top_k, de_of(cfg), nullptr, y, cfg->act_dtype, s, shared ? ys : nullptr,
+                      resid));
+    return MOE_OK;
+  }
+  // latent: combined latent rows rounded once, then latent up + y_s
+  void* y_rl = P.at<void>(P.L.y_rl);
+  CU(launch_combine(u, tsr, T, cfg->top_k, de_of(cfg), nullptr, y_rl, cfg->act_dtype, s));
+  if (aux) CU(cudaStreamWaitEvent(s, aux->join, 0));
+  GemvArgs lu = dense_args(w->w_lat_up, cfg->d_model, cfg->d_latent, y_rl, T, y, cfg->d_model);
+  lu.add_src = shared ? ys : nullptr;
+  lu.add_ld = cfg->d_model;
+  lu.res = resid;
+  lu.res_ld = cfg->d_model;
+  CU(run_dense(cfg, lu, EPI_ADD, cfg->act_dtype == MOE_DT_F32, T, s));
+  return MOE_OK;
+}
+
 }  // namespace
 
 // ============================================================================
@@ -519,6 +600,7 @@ moe_status_t moe_workspace_region(const moe_config_t* cfg, int32_t T, int32_t re
     case MOE_WS_H_TERMS: o = L.hq; n = nt * R * I / 2; break;
     case MOE_WS_H_TERM_SCALES: o = L.hq_sf; n = nt * R * (size_t)act_sf_ld((int)I); break;
     case MOE_WS_H_ROW_SCALES: o = L.hq_g; n = fp4 ? R * 4 : 0; break;
+    case MOE_WS_X_NORM: o = L.xn; n = t * (size_t)cfg->d_model * ab; break;
     default: return MOE_ERR_INVALID_ARG;
   }
   *offset = o;
@@ -632,72 +714,35 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
   Ptrs P{(char*)ws, make_layout(cfg, T)};
   cudaStream_t s = (cudaStream_t)stream;
   CU(cudaMemsetAsync(P.hdr(), 0, sizeof(WsHeader), s));
-  // fork: the latent down projection and the shared expert run on the
-  // auxiliary stream, the router and the selection on the caller's stream
-  const bool shared = cfg->d_shared > 0;
-  const bool latent = cfg->d_latent > 0;
-  float* ys = P.at<float>(P.L.ys);
-  const void* x_e = latent ? P.at<void>(P.L.x_l) : x;
-  // NVFP4: FP16 expert rows; decode makes an FP16 copy of x_e in the (then
-  // unused) packed-row buffer, prefill packs the rows as FP16
-  const bool f16 = up_down_f16(cfg, T, w);
-  const bool conv = f16 && !use_tc(cfg, T);
-  void* x16 = conv ? P.at<void>(P.L.x_packed) : nullptr;
-  const bool pre = latent || conv;         // work before the expert up projection
-  std::unique_lock<std::mutex> aux_lock(g_aux_mutex);
-  AuxStream* aux = nullptr;
-  if (shared || pre) {
-    if (!aux_stream(&aux)) return MOE_ERR_CUDA;
-    CU(cudaEventRecord(aux->fork, s));
-    CU(cudaStreamWaitEvent(aux->s, aux->fork, 0));
-    if (latent && (st = run_latent_down(cfg, T, x, w, const_cast<void*>(x_e), aux->s)) != MOE_OK) return st;
-    if (conv) CU(launch_bf16_to_f16(x_e, (int64_t)T * de_of(cfg), x16, aux->s));
-    if (pre) CU(cudaEventRecord(aux->latent, aux->s));
-    if (shared && (st = run_shared_to_f32(cfg, T, x, w, ys, P, aux->s)) != MOE_OK) return st;
-    CU(cudaEventRecord(aux->join, aux->s));
+  return run_layer(cfg, T, x, nullptr, w, y, topk_ids_out, topk_w_out, logits_out, scores_out, P, s);
+}
+
+moe_status_t moe_block_forward(const moe_config_t* cfg, int32_t T, const void* x, const float* norm_w,
+                               float norm_eps, const moe_weights_t* w, void* out, void* x_norm_out,
+                               int32_t* topk_ids_out, float* topk_w_out, float* logits_out, float* scores_out,
+                               void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_common(cfg, T, ws, ws_bytes);
+  if (st != MOE_OK || T == 0) return st;
+  if ((st = check_weights(cfg, w, true, true, true)) != MOE_OK) return st;
+  REQ(x); REQ(norm_w); REQ(out); OPT(x_norm_out); OPT(topk_ids_out); OPT(topk_w_out); OPT(logits_out);
+  OPT(scores_out);
+  if (!std::isfinite(norm_eps) || norm_eps < 0.f) return MOE_ERR_INVALID_ARG;
+  Ptrs P{(char*)ws, make_layout(cfg, T)};
+  const size_t row_bytes = (size_t)T * cfg->d_model * act_bytes(cfg);
+  if (x_norm_out) {
+    // the normalised rows must not overlap the residual stream
+    const char *a = (const char*)x_norm_out, *b = (const char*)x, *o = (const char*)out;
+    if ((a < b + row_bytes && b < a + row_bytes) || (a < o + row_bytes && o < a + row_bytes))
+      return MOE_ERR_INVALID_ARG;
   }
-  aux_lock.unlock();
-  float* logits = logits_out ? logits_out : P.at<float>(P.L.logits);
-  float* scores = scores_out ? scores_out : P.at<float>(P.L.scores);
-  int32_t* ids = topk_ids_out ? topk_ids_out : P.at<int32_t>(P.L.ids);
-  float* topw = topk_w_out ? topk_w_out : P.at<float>(P.L.topw);
-  SelectArgs sa;
-  if ((st = run_logits(cfg, T, x, w->w_router, w->router_bias, logits, scores, ids, topw, P, s, sa)) != MOE_OK)
-    return st;
-  int32_t* offsets = P.at<int32_t>(P.L.offsets);
-  int32_t* rt = P.at<int32_t>(P.L.route_token);
-  int32_t* rs = P.at<int32_t>(P.L.route_slot);
-  int32_t* tsr = P.at<int32_t>(P.L.tsr);
-  void* x_packed = use_tc(cfg, T) && !fp4_path(cfg, T) ? P.at<void>(P.L.x_packed) : nullptr;
-  DispatchArgs da = dispatch_args(cfg, T, ids, x_e, P.at<int32_t>(P.L.counts), offsets, rt, rs, tsr, x_packed, P);
-  da.pack_f16 = f16 && x_packed;
-  if (select_dispatch_fits(T, cfg->top_k, da)) {
-    CU(launch_select_dispatch(sa, da, s));       // a few tokens: one kernel
-  } else {
-    CU(launch_select(sa, s));
-    if (latent && x_packed) CU(cudaStreamWaitEvent(s, aux->latent, 0));   // the pack reads the latent rows
-    CU(launch_dispatch(da, s));
+  if (out != x) {
+    const char *b = (const char*)x, *o = (const char*)out;
+    if (b < o + row_bytes && o < b + row_bytes) return MOE_ERR_INVALID_ARG;   // partial overlap
   }
-  if (pre && !x_packed) CU(cudaStreamWaitEvent(s, aux->latent, 0));    // the up GEMV reads them
-  void* h = P.at<void>(P.L.h);
-  if ((st = run_up(cfg, T, conv ? x16 : x_e, x_packed, rt, offsets, w, h, P, s, f16)) != MOE_OK) return st;
-  float* u = P.at<float>(P.L.u);
-  if ((st = run_down(cfg, T, h, offsets, rt, rs, topw, w, u, P, s, f16)) != MOE_OK) return st;
-  if (cfg->d_latent == 0) {
-    // join, then y = act(sum of routed rows + y_s): the same two FP32 terms, one rounding
-    if (aux) CU(cudaStreamWaitEvent(s, aux->join, 0));
-    CU(launch_combine(u, tsr, T, cfg->top_k, de_of(cfg), nullptr, y, cfg->act_dtype, s, shared ? ys : nullptr));
-    return MOE_OK;
-  }
-  // latent: combined latent rows rounded once, then latent up + y_s
-  void* y_rl = P.at<void>(P.L.y_rl);
-  CU(launch_combine(u, tsr, T, cfg->top_k, de_of(cfg), nullptr, y_rl, cfg->act_dtype, s));
-  if (aux) CU(cudaStreamWaitEvent(s, aux->join, 0));
-  GemvArgs lu = dense_args(w->w_lat_up, cfg->d_model, cfg->d_latent, y_rl, T, y, cfg->d_model);
-  lu.add_src = shared ? ys : nullptr;
-  lu.add_ld = cfg->d_model;
-  CU(run_dense(cfg, lu, EPI_ADD, cfg->act_dtype == MOE_DT_F32, T, s));
-  return MOE_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  void* xn = x_norm_out ? x_norm_out : P.at<void>(P.L.xn);
+  CU(launch_rmsnorm(x, norm_w, norm_eps, T, cfg->d_model, cfg->act_dtype, xn, P.hdr(), (int)sizeof(WsHeader), s));
+  return run_layer(cfg, T, xn, x, w, out, topk_ids_out, topk_w_out, logits_out, scores_out, P, s);
 }
 
 moe_status_t moe_get_device_error(const void* ws, void* stream, int32_t* code) {

@@ -14,6 +14,14 @@ namespace moe {
 
 namespace {
 
+// four consecutive activation values (f32 or bf16) from element i (a multiple of 4)
+template <bool ACT_F32>
+__device__ __forceinline__ float4 load_act4(const void* p, int64_t i) {
+  if (ACT_F32) return *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p) + i);
+  const uint2 b = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(p) + i);
+  return make_float4(bf16_lo(b.x), bf16_hi(b.x), bf16_lo(b.y), bf16_hi(b.y));
+}
+
 // grid (T, column blocks of 128 float4s): each thread owns one float4 column of
 // one token and loads all of that column's routed rows before adding them in
 // row order, so a token's K loads are in flight together
@@ -22,8 +30,8 @@ constexpr int kCombineThreads = 128;
 template <bool ACT_F32>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* __restrict__ u,
                                                                   const int32_t* __restrict__ tsr, int K, int de,
-                                                                  float* __restrict__ y_r, void* __restrict__ y_act,
-                                                                  const float* __restrict__ add) {
+                                                                  float* y_r, void* y_act,
+                                                                  const float* __restrict__ add, const void* res) {
   pdl_wait();
   __shared__ int rows[32];
   const int t = blockIdx.x;
@@ -66,6 +74,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
     // output = routed sum + an FP32 term (the shared expert), then one rounding
     acc.x += extra.x; acc.y += extra.y; acc.z += extra.z; acc.w += extra.w;
   }
+  if (res) {
+    // + the residual row (read before y_act, which may be the same row, is written)
+    const float4 q = load_act4<ACT_F32>(res, (int64_t)t * de + 4 * (int64_t)v);
+    acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+  }
   if (y_act) {
     if (ACT_F32) {
       reinterpret_cast<float4*>(reinterpret_cast<float*>(y_act) + (int64_t)t * de)[v] = acc;
@@ -79,10 +92,14 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
 }
 
 template <bool ACT_F32>
-__global__ void cast_kernel(const float* __restrict__ src, int64_t n4, void* __restrict__ dst) {
+__global__ void cast_kernel(const float* __restrict__ src, int64_t n4, void* dst, const void* res) {
   pdl_wait();
   for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < n4; v += (int64_t)gridDim.x * blockDim.x) {
-    const float4 q = reinterpret_cast<const float4*>(src)[v];
+    float4 q = reinterpret_cast<const float4*>(src)[v];
+    if (res) {
+      const float4 r = load_act4<ACT_F32>(res, 4 * v);
+      q.x += r.x; q.y += r.y; q.z += r.z; q.w += r.w;
+    }
     if (ACT_F32) {
       reinterpret_cast<float4*>(dst)[v] = q;
     } else {
@@ -96,25 +113,25 @@ __global__ void cast_kernel(const float* __restrict__ src, int64_t n4, void* __r
 
 }  // namespace
 
-cudaError_t launch_cast(const float* src, int64_t n, void* dst, int act, cudaStream_t s) {
+cudaError_t launch_cast(const float* src, int64_t n, void* dst, int act, cudaStream_t s, const void* res) {
   if (n <= 0) return cudaSuccess;
   const int64_t n4 = n / 4;
   const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(n4, 256), 4096);
   if (act == MOE_DT_F32)
-    launch_k(cast_kernel<true>, grid, 256, 0, s, src, n4, dst);
+    launch_k(cast_kernel<true>, grid, 256, 0, s, src, n4, dst, res);
   else
-    launch_k(cast_kernel<false>, grid, 256, 0, s, src, n4, dst);
+    launch_k(cast_kernel<false>, grid, 256, 0, s, src, n4, dst, res);
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const float* u, const int32_t* token_slot_row, int T, int K, int de, float* y_r,
-                           void* y_act, int act, cudaStream_t s, const float* add) {
+                           void* y_act, int act, cudaStream_t s, const float* add, const void* res) {
   if (T <= 0) return cudaSuccess;
   const dim3 grid((unsigned)T, (unsigned)ceil_div(de / 4, kCombineThreads));
   if (act == MOE_DT_F32)
-    launch_k(combine_kernel<true>, grid, kCombineThreads, 0, s, u, token_slot_row, K, de, y_r, y_act, add);
+    launch_k(combine_kernel<true>, grid, kCombineThreads, 0, s, u, token_slot_row, K, de, y_r, y_act, add, res);
   else
-    launch_k(combine_kernel<false>, grid, kCombineThreads, 0, s, u, token_slot_row, K, de, y_r, y_act, add);
+    launch_k(combine_kernel<false>, grid, kCombineThreads, 0, s, u, token_slot_row, K, de, y_r, y_act, add, res);
   return cudaGetLastError();
 }
 

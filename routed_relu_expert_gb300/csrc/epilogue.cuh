@@ -8,6 +8,15 @@
 
 namespace moe {
 
+// EPI_ADD residual value at (row, f) in the activation type (0 if none)
+template <bool ACT_F32>
+__device__ __forceinline__ float residual(const GemvArgs& a, int row, int f) {
+  if (!a.res) return 0.f;
+  const int64_t i = (int64_t)row * a.res_ld + f;
+  return ACT_F32 ? reinterpret_cast<const float*>(a.res)[i]
+                 : __bfloat162float(reinterpret_cast<const bf16*>(a.res)[i]);
+}
+
 template <int EPI, bool OUT_F32, bool ACT_F32>
 __device__ __forceinline__ void epilogue(const GemvArgs& a, int seg, int row, int f, float v) {
   if (a.W_gs) v *= a.W_gs[seg];
@@ -26,6 +35,7 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, int seg, int row, in
     r = a.topw[(int64_t)t * a.top_k + k] * v;
   } else if (EPI == EPI_ADD) {
     r = v + (a.add_src ? a.add_src[(int64_t)row * a.add_ld + f] : 0.f);
+    r += residual<ACT_F32>(a, row, f);
   } else {
     r = v;
   }
@@ -46,7 +56,8 @@ __device__ __forceinline__ float epi_value(const GemvArgs& a, int row, int f, fl
   } else if (EPI == EPI_SCALE) {
     return wr * v;
   } else if (EPI == EPI_ADD) {
-    return v + (a.add_src ? a.add_src[(int64_t)row * a.add_ld + f] : 0.f);
+    const float r = v + (a.add_src ? a.add_src[(int64_t)row * a.add_ld + f] : 0.f);
+    return r + residual<ACT_F32>(a, row, f);
   }
   return v;
 }

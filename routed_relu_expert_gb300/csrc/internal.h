@@ -53,7 +53,7 @@ enum Epi : int {
   EPI_RELU2 = 0,  // out = bf16(relu(bf16(v))^2)            (F32 layers: relu(v)^2)
   EPI_SCALE = 1,  // out(f32) = topk_w[route] * v            (expert down: routed row u)
   EPI_STORE = 2,  // out = bf16(v)                           (F32 out: v)
-  EPI_ADD = 3     // out = bf16(v + add_src[row, f])         (F32 out: v + add)
+  EPI_ADD = 3     // out = bf16(v + add_src[row, f] + res[row, f])   (F32 out: no rounding)
 };
 
 // Weight formats of the streamed matrix
@@ -79,6 +79,11 @@ struct GemvArgs {
   int64_t out_ld;
   const float* add_src;     // EPI_ADD source [rows, add_ld] f32 (nullable: adds 0)
   int64_t add_ld;
+  // EPI_ADD residual [rows, res_ld] in the activation type (nullable), added
+  // after add_src, before the one rounding; an output row may be its own
+  // residual row (each element is read before it is written, by one thread)
+  const void* res;
+  int64_t res_ld;
   const float* topw;        // EPI_SCALE: [T, K] routing weights
   const int32_t* route_token;
   const int32_t* route_slot;
@@ -212,11 +217,19 @@ bool select_dispatch_fits(int T, int K, const DispatchArgs& a);
 cudaError_t launch_select_dispatch(const SelectArgs& sa, const DispatchArgs& a, cudaStream_t s);
 
 // combine: y_r[t] = sum over t's packed rows in ascending order of u[row];
-// y_r_act[t] = act(y_r[t] + add[t]) (add nullable)
+// y_r_act[t] = act(y_r[t] + add[t] + res[t]) (add: f32, res: act dtype, both
+// nullable; y_r_act may be res itself)
 cudaError_t launch_combine(const float* u, const int32_t* token_slot_row, int T, int K, int de,
-                           float* y_r, void* y_r_act, int act, cudaStream_t s, const float* add = nullptr);
+                           float* y_r, void* y_r_act, int act, cudaStream_t s, const float* add = nullptr,
+                           const void* res = nullptr);
 
-// dst (act dtype) = src (f32), n a multiple of 4
-cudaError_t launch_cast(const float* src, int64_t n, void* dst, int act, cudaStream_t s);
+// dst (act dtype) = act(src (f32) + res (act dtype, nullable)), n a multiple of 4
+cudaError_t launch_cast(const float* src, int64_t n, void* dst, int act, cudaStream_t s, const void* res = nullptr);
+
+// RMSNorm prologue of a block: xn[t] = act(gamma * (x[t] / sqrt(mean(x[t]^2) + eps)))
+// in FP32 (x, xn: act dtype [T, d]; gamma: f32 [d]); block 0 also clears the
+// workspace header `hdr` (bytes), so that it replaces the step's header memset
+cudaError_t launch_rmsnorm(const void* x, const float* gamma, float eps, int T, int d, int act, void* xn,
+                           void* hdr, int hdr_bytes, cudaStream_t s);
 
 }  // namespace moe

@@ -281,6 +281,16 @@ __device__ __forceinline__ void tile_epilogue(const GemvArgs& a, const CUtensorM
 #pragma unroll
     for (int c = 0; c < 32; ++c) v[c] += add[c];
   }
+  if (EPI == EPI_ADD && a.res) {
+    // BF16 residual rows (the tensor-core path runs BF16 activations only)
+    float res[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+      res[c] = c < nc ? __bfloat162float(reinterpret_cast<const bf16*>(a.res)[(int64_t)(ti.row0 + c0 + c) * a.res_ld + f])
+                      : 0.f;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) v[c] += res[c];
+  }
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
     if (EPI == EPI_RELU2) {

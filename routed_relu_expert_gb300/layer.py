@@ -184,6 +184,15 @@ def moe_layer_forward(cfg, x, weights: Weights, y, ws, ids_out=None, topw_out=No
             "moe_layer_forward")
 
 
+def moe_block_forward(cfg, x, norm_w, norm_eps: float, weights: Weights, out, ws, x_norm_out=None, ids_out=None,
+                      topw_out=None, logits_out=None, scores_out=None, stream=None):
+    w, n = _ws(ws)
+    N.check(N.load().moe_block_forward(ctypes.byref(cfg), x.shape[0], _p(x), _p(norm_w), ctypes.c_float(norm_eps),
+                                       weights.ref, _p(out), _p(x_norm_out), _p(ids_out), _p(topw_out),
+                                       _p(logits_out), _p(scores_out), w, n, _s(stream)),
+            "moe_block_forward")
+
+
 def moe_layer_forward_host(cfg, x_host, x_dev, weights: Weights, y_dev, y_host, ws, stream=None):
     w, n = _ws(ws)
     N.check(N.load().moe_layer_forward_host(ctypes.byref(cfg), x_host.shape[0], _hp(x_host), _p(x_dev),
@@ -223,5 +232,25 @@ class MoELayer:
             y = torch.empty(x.shape, dtype=self.act, device=x.device)
         moe_layer_forward(self.cfg, x, self.weights, y, self.workspace(x.shape[0], x.device), **outs)
         return y
+
+    __call__ = forward
+
+
+class MoEBlock(MoELayer):
+    """The MoE block of a decoder layer: out = x + layer(RMSNorm(x)), with the
+    RMSNorm weight gamma (FP32 [d]) and epsilon; out may be x (in place)."""
+
+    def __init__(self, cfg: N.MoeConfig, tensors: Dict[str, torch.Tensor], norm_w: torch.Tensor,
+                 norm_eps: float = 1e-5):
+        super().__init__(cfg, tensors)
+        self.norm_w = norm_w
+        self.norm_eps = float(norm_eps)
+
+    def forward(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, **outs) -> torch.Tensor:
+        if out is None:
+            out = torch.empty(x.shape, dtype=self.act, device=x.device)
+        moe_block_forward(self.cfg, x, self.norm_w, self.norm_eps, self.weights, out,
+                          self.workspace(x.shape[0], x.device), **outs)
+        return out
 
     __call__ = forward
