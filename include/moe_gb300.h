@@ -107,6 +107,13 @@ typedef struct moe_weights {
   const float* w_down_gs;     /* NVFP4: FP32 per-tensor scale [E]                                    */
   const void* w_sh_up;        /* [S, d] shared expert up   (S > 0)                                    */
   const void* w_sh_down;      /* [d, S] shared expert down (S > 0)                                    */
+  /* optional: the expert down weights again, in the group-major layout of
+   * moe_sparse_down_layout (NULL = not given).  When given, decode steps (the
+   * streaming GEMV path: up to 64 tokens, and for NVFP4 experts the FP16
+   * path) compute the down projection by the ReLU^2-sparse kernel, which
+   * reads only the 16-neuron groups of W_down with a live neuron.           */
+  const void* w_down_g;       /* BF16 [E, de * I] / NVFP4 values [E, de * I / 2] u8                   */
+  const uint8_t* w_down_g_sf; /* NVFP4: E4M3 scales [E, de * I / 16]                                  */
 } moe_weights_t;
 
 /* Library version, e.g. 100 for 0.1.0.  Never fails. */
@@ -226,6 +233,33 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
                                int32_t* topk_ids_out, float* topk_w_out,
                                float* logits_out, float* scores_out,
                                void* ws, size_t ws_bytes, void* stream);
+
+/* ReLU^2-sparse down projection for decode (page "Nemotron-3.5-Super 120B on
+ * an 8 GB GPU", section "The engine, step by step", item 4 "Skip the zeros",
+ * and section "What didn't work": 16-neuron groups, not single neurons).
+ * The down weights are re-laid once, a pure permutation of their values (and,
+ * NVFP4, of their bytes and scales), so that each group of 16 neurons
+ * 16g .. 16g+15 of an expert holds all de outputs' weights for those neurons
+ * contiguously.  Within a group, 16-output tile o is one 512-byte block
+ * (BF16) in which lane l = 4r + t (r = l / 4, t = l % 4) holds 16 bytes:
+ * W[16o + r][16g + 4t .. +3] then W[16o + r + 8][16g + 4t .. +3].  NVFP4:
+ * 64-output quad q of a group is one 512-byte value block, lane l holding
+ * for tiles j = 0..3 of the quad the 2 bytes of W[64q + 16j + r][16g + 4t ..
+ * +3] then the 2 bytes of row + 8 (low nibble = even neuron, as in w_down),
+ * and one 64-byte scale block, bytes 8r + 2j and 8r + 2j + 1 holding the
+ * group's E4M3 scales of rows 64q + 16j + r and 64q + 16j + r + 8.
+ * A decode step that is given w_down_g finds, per expert, the groups with a
+ * nonzero h value in any of the expert's rows and reads only those groups'
+ * weights; dead groups only contribute zeros, so the result is that of the
+ * dense product up to the order of its FP32 sum.  Needs BF16 activations,
+ * I % 16 == 0, I / 16 <= 1024 and de % 32 == 0 (BF16) or de % 64 == 0
+ * (NVFP4); else MOE_ERR_UNSUPPORTED.
+ * moe_sparse_down_bytes: sizes of w_down_g (*values) and w_down_g_sf
+ * (*scales, 0 for BF16).  moe_sparse_down_layout: writes both from w->w_down
+ * (and w->w_down_sf) on `stream` (caller-owned, 16-byte aligned buffers).  */
+moe_status_t moe_sparse_down_bytes(const moe_config_t* cfg, size_t* values, size_t* scales);
+moe_status_t moe_sparse_down_layout(const moe_config_t* cfg, const moe_weights_t* w, void* w_down_g,
+                                    uint8_t* w_down_g_sf, void* stream);
 
 /* The MoE block of a decoder layer: RMSNorm, the layer, the residual add
  * (page "Nemotron Is Not One Circuit: Mamba, Attention, and MoE Routing",

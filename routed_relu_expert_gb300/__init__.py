@@ -9,7 +9,8 @@ from ._native import (EXPORTS, LIB_PATH, MOE_DEVERR_EXPERT_ID, MOE_DEVERR_NONFIN
 from .layer import (MoEBlock, MoELayer, Weights, config_from, make_config, moe_clear_device_error,
                     moe_dispatch, moe_experts_down, moe_experts_down_combine, moe_experts_up, moe_get_device_error,
                     moe_block_forward, moe_latent_down, moe_layer_forward, moe_layer_forward_host, moe_router,
-                    moe_router_noalloc, moe_shared, new_workspace, nvfp4_act_terms_for, set_nvfp4_act_terms, workspace_bytes,
+                    moe_router_noalloc, moe_shared, new_workspace, nvfp4_act_terms_for, set_nvfp4_act_terms,
+                    sparse_down_bytes, sparse_down_layout, workspace_bytes,
                     workspace_region)
 
 __all__ = [
@@ -19,5 +20,6 @@ __all__ = [
     "moe_block_forward", "moe_experts_down", "moe_experts_down_combine", "moe_experts_up", "moe_get_device_error",
     "moe_latent_down",
     "moe_layer_forward", "moe_layer_forward_host", "moe_router", "moe_router_noalloc", "moe_shared", "new_workspace",
-    "nvfp4_act_terms_for", "set_nvfp4_act_terms", "workspace_bytes", "workspace_region",
+    "nvfp4_act_terms_for", "set_nvfp4_act_terms", "sparse_down_bytes", "sparse_down_layout", "workspace_bytes",
+    "workspace_region",
 ]

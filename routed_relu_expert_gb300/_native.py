@@ -44,7 +44,7 @@ class MoeConfig(ctypes.Structure):
 class MoeWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "w_router", "router_bias", "w_lat_down", "w_lat_up", "w_up", "w_down",
-        "w_up_sf", "w_down_sf", "w_up_gs", "w_down_gs", "w_sh_up", "w_sh_down")]
+        "w_up_sf", "w_down_sf", "w_up_gs", "w_down_gs", "w_sh_up", "w_sh_down", "w_down_g", "w_down_g_sf")]
 
 
 EXPORTS = (
@@ -52,7 +52,7 @@ EXPORTS = (
     "moe_dispatch", "moe_experts_up", "moe_experts_down", "moe_experts_down_combine", "moe_latent_down", "moe_shared",
     "moe_layer_forward", "moe_get_device_error", "moe_clear_device_error", "moe_layer_forward_host",
     "moe_launch_count", "moe_router_noalloc", "moe_workspace_region", "moe_set_nvfp4_act_terms",
-    "moe_nvfp4_act_terms_for", "moe_block_forward",
+    "moe_nvfp4_act_terms_for", "moe_block_forward", "moe_sparse_down_bytes", "moe_sparse_down_layout",
 )
 
 _lib = None
@@ -86,6 +86,8 @@ def load() -> ctypes.CDLL:
         "moe_shared": (I32, [CFG, I32, P, W, P, P, P, S, P]),
         "moe_layer_forward": (I32, [CFG, I32, P, W, P, P, P, P, P, P, S, P]),
         "moe_block_forward": (I32, [CFG, I32, P, P, ctypes.c_float, W, P, P, P, P, P, P, P, S, P]),
+        "moe_sparse_down_bytes": (I32, [CFG, ctypes.POINTER(S), ctypes.POINTER(S)]),
+        "moe_sparse_down_layout": (I32, [CFG, W, P, P, P]),
         "moe_get_device_error": (I32, [P, P, ctypes.POINTER(I32)]),
         "moe_clear_device_error": (I32, [P, P]),
         "moe_layer_forward_host": (I32, [CFG, I32, P, P, W, P, P, P, S, P]),

@@ -280,6 +280,16 @@ moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x
   return MOE_OK;
 }
 
+// the decode down projection can run ReLU^2-sparse: group-major weights given,
+// BF16 activations, BF16 experts or NVFP4 experts with FP16 h, shapes that fit
+bool sparse_down_ok(const moe_config_t* c, const moe_weights_t* w, bool f16) {
+  if (!w->w_down_g || c->act_dtype != MOE_DT_BF16) return false;
+  const bool fp4 = c->expert_dtype == MOE_DT_NVFP4;
+  if (fp4 && (!f16 || !w->w_down_g_sf)) return false;
+  if (!fp4 && c->expert_dtype != MOE_DT_BF16) return false;
+  return sparse_down_fits(de_of(c), c->d_expert, fp4);
+}
+
 moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t* offsets, const int32_t* rt,
                       const int32_t* rs, const float* topw, const moe_weights_t* w, float* u, const Ptrs& P,
                       cudaStream_t s, bool f16 = false) {
@@ -299,6 +309,13 @@ moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t
     const int64_t R = (int64_t)T * c->top_k;
     CU(launch_gemm_tc(a, EPI_SCALE, true, (int64_t)c->n_experts * de, R, c->n_experts,
                       tc_tile_rows(R / segs, segs, de), s));
+    return MOE_OK;
+  }
+  if (sparse_down_ok(c, w, f16)) {
+    // ReLU^2-sparse: only the 16-neuron groups of W_down with a live neuron
+    a.W = w->w_down_g;
+    a.W_sf = w->w_down_g_sf;
+    CU(launch_sparse_down(a, fp4, segs, s));
     return MOE_OK;
   }
   CU(launch_gemv(a, wfmt_of(c), c->act_dtype, EPI_SCALE, true, T, segs, s));
@@ -455,6 +472,7 @@ moe_status_t check_weights(const moe_config_t* c, const moe_weights_t* w, bool e
       if (((uintptr_t)w->w_up_sf & 1u) || ((uintptr_t)w->w_down_sf & 1u)) return MOE_ERR_INVALID_ARG;
     }
   }
+  if (experts) { OPT(w->w_down_g); OPT(w->w_down_g_sf); }
   if (dense) {
     if (c->d_latent > 0) { REQ(w->w_lat_down); REQ(w->w_lat_up); }
     if (c->d_shared > 0) { REQ(w->w_sh_up); REQ(w->w_sh_down); }
@@ -715,6 +733,34 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, int32_t T, const void* x
   cudaStream_t s = (cudaStream_t)stream;
   CU(cudaMemsetAsync(P.hdr(), 0, sizeof(WsHeader), s));
   return run_layer(cfg, T, x, nullptr, w, y, topk_ids_out, topk_w_out, logits_out, scores_out, P, s);
+}
+
+moe_status_t moe_sparse_down_bytes(const moe_config_t* cfg, size_t* values, size_t* scales) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (!values || !scales) return MOE_ERR_INVALID_ARG;
+  const bool fp4 = cfg->expert_dtype == MOE_DT_NVFP4;
+  if (cfg->act_dtype != MOE_DT_BF16 || !sparse_down_fits(de_of(cfg), cfg->d_expert, fp4))
+    return MOE_ERR_UNSUPPORTED;
+  const size_t n = (size_t)cfg->n_experts * de_of(cfg) * cfg->d_expert;
+  *values = fp4 ? n / 2 : n * 2;
+  *scales = fp4 ? n / 16 : 0;
+  return MOE_OK;
+}
+
+moe_status_t moe_sparse_down_layout(const moe_config_t* cfg, const moe_weights_t* w, void* w_down_g,
+                                    uint8_t* w_down_g_sf, void* stream) {
+  size_t nv = 0, ns = 0;
+  moe_status_t st = moe_sparse_down_bytes(cfg, &nv, &ns);
+  if (st != MOE_OK) return st;
+  if (!w) return MOE_ERR_INVALID_ARG;
+  const bool fp4 = cfg->expert_dtype == MOE_DT_NVFP4;
+  REQ(w->w_down); REQ(w_down_g);
+  if (fp4) { REQ(w->w_down_sf); REQ(w_down_g_sf); }
+  CU(launch_sparse_down_layout(w->w_down, fp4 ? w->w_down_sf : nullptr, cfg->n_experts, de_of(cfg),
+                               cfg->d_expert, fp4, w_down_g, fp4 ? w_down_g_sf : nullptr,
+                               (cudaStream_t)stream));
+  return MOE_OK;
 }
 
 moe_status_t moe_block_forward(const moe_config_t* cfg, int32_t T, const void* x, const float* norm_w,

@@ -195,14 +195,6 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_bf16_kernel(const GemvArgs a
 // exact for magnitudes in [2^-14, 65504] (smaller ones keep FP16's subnormal
 // precision); accumulation is FP32 and the per-tensor scale multiplies the
 // FP32 result.
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 
 template <int EPI, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 3) gemv_nvfp4_kernel(const GemvArgs a) {

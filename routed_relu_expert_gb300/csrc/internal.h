@@ -226,6 +226,15 @@ cudaError_t launch_combine(const float* u, const int32_t* token_slot_row, int T,
 // dst (act dtype) = act(src (f32) + res (act dtype, nullable)), n a multiple of 4
 cudaError_t launch_cast(const float* src, int64_t n, void* dst, int act, cudaStream_t s, const void* res = nullptr);
 
+// ReLU^2-sparse down projection (decode): W in the group-major layout of
+// moe_sparse_down_layout, X = h (BF16, or FP16 with NVFP4 weights), grouped
+// rows (offsets / active / hdr), EPI_SCALE output; only the 16-neuron groups
+// with a nonzero h value in one of an expert's rows are read
+bool sparse_down_fits(int N, int K, bool nvfp4);
+cudaError_t launch_sparse_down(const GemvArgs& a, bool nvfp4, int segs, cudaStream_t s);
+cudaError_t launch_sparse_down_layout(const void* w, const uint8_t* sf, int E, int de, int I, bool nvfp4, void* out,
+                                      void* out_sf, cudaStream_t s);
+
 // RMSNorm prologue of a block: xn[t] = act(gamma * (x[t] / sqrt(mean(x[t]^2) + eps)))
 // in FP32 (x, xn: act dtype [T, d]; gamma: f32 [d]); block 0 also clears the
 // workspace header `hdr` (bytes), so that it replaces the step's header memset

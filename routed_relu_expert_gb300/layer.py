@@ -61,7 +61,7 @@ class Weights:
     """Keeps a layer's device tensors alive and exposes them as moe_weights_t."""
 
     FIELDS = ("w_router", "router_bias", "w_lat_down", "w_lat_up", "w_up", "w_down", "w_up_sf",
-              "w_down_sf", "w_up_gs", "w_down_gs", "w_sh_up", "w_sh_down")
+              "w_down_sf", "w_up_gs", "w_down_gs", "w_sh_up", "w_sh_down", "w_down_g", "w_down_g_sf")
     ALIASES = {"router_bias": "bias", "w_up": "w_up_q", "w_down": "w_down_q"}
 
     def __init__(self, tensors: Dict[str, torch.Tensor]):
@@ -184,6 +184,27 @@ def moe_layer_forward(cfg, x, weights: Weights, y, ws, ids_out=None, topw_out=No
             "moe_layer_forward")
 
 
+def sparse_down_bytes(cfg):
+    """(values, scales) bytes of the group-major down weights of a configuration."""
+    v, sc = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    N.check(N.load().moe_sparse_down_bytes(ctypes.byref(cfg), ctypes.byref(v), ctypes.byref(sc)),
+            "moe_sparse_down_bytes")
+    return int(v.value), int(sc.value)
+
+
+def sparse_down_layout(cfg, weights: Weights, stream=None) -> Dict[str, torch.Tensor]:
+    """The expert down weights re-laid group-major (w_down_g, and w_down_g_sf for
+    NVFP4) by the library, as new device tensors."""
+    nv, ns = sparse_down_bytes(cfg)
+    dev = weights.tensors["w_down"].device
+    out = {"w_down_g": torch.empty(nv, dtype=torch.uint8, device=dev)}
+    if ns:
+        out["w_down_g_sf"] = torch.empty(ns, dtype=torch.uint8, device=dev)
+    N.check(N.load().moe_sparse_down_layout(ctypes.byref(cfg), weights.ref, _p(out["w_down_g"]),
+                                            _p(out.get("w_down_g_sf")), _s(stream)), "moe_sparse_down_layout")
+    return out
+
+
 def moe_block_forward(cfg, x, norm_w, norm_eps: float, weights: Weights, out, ws, x_norm_out=None, ids_out=None,
                       topw_out=None, logits_out=None, scores_out=None, stream=None):
     w, n = _ws(ws)
@@ -220,6 +241,12 @@ class MoELayer:
         self.weights = Weights(tensors)
         self._ws: Optional[torch.Tensor] = None
         self.act = torch.float32 if cfg.act_dtype == N.MOE_DT_F32 else torch.bfloat16
+
+    def enable_sparse_down(self) -> None:
+        """Re-lay the expert down weights group-major once, so that decode steps
+        skip the 16-neuron groups of W_down whose neurons are all zero."""
+        extra = sparse_down_layout(self.cfg, self.weights)
+        self.weights = Weights({**self.weights.tensors, **extra})
 
     def workspace(self, T: int, device) -> torch.Tensor:
         need = workspace_bytes(self.cfg, T)

@@ -48,6 +48,7 @@ class MoEShape:
     act_dtype: int = BF16
     expert_dtype: int = BF16
     zipf_s: float = 0.0    # 0 = no popularity skew
+    relu_sparsity: float = 0.0   # 0 = plain random layer; else the fraction of expert neurons ReLU^2 zeroes
     weight_seed: int = 0   # workloads that are "the same layer" share this
     tokens: Tuple[int, ...] = field(default_factory=tuple)
 
@@ -71,11 +72,19 @@ SUPER_LATENT = MoEShape("super_latent", 4096, 1024, 512, 22, 8, 4, 2688, 5376, 5
                         weight_seed=3, tokens=(1, 16, 256, 4096))
 SUPER_NVFP4 = replace(SUPER_LATENT, name="super_nvfp4", expert_dtype=NVFP4,
                       zipf_s=1.1, tokens=(1, 64, 8192))
+# decode with the ReLU^2 sparsity of a trained layer (page "Nemotron-3.5-Super
+# 120B on an 8 GB GPU", section "The engine, step by step", item 4: 92.5 % of
+# an expert's neurons are zero for a token); inputs for the ReLU^2-sparse down
+NANO_DECODE_SPARSE = replace(NANO_DECODE, name="nano_decode_relu_sparse", relu_sparsity=0.925,
+                             tokens=(1, 2, 4, 16, 64))
+SUPER_NVFP4_SPARSE = replace(SUPER_NVFP4, name="super_nvfp4_relu_sparse", relu_sparsity=0.925, zipf_s=0.0,
+                             tokens=(1, 2))
 ROUTER_ONLY_GROUPED = MoEShape("router_only_grouped", 2688, 0, 128, 6, 8, 3, 1856, 3712, 2.5,
                                weight_seed=5, tokens=(64,))
 
 WORKLOADS = {s.name: s for s in (TINY_FP32, NANO_DECODE, NANO_PREFILL,
-                                  SUPER_LATENT, SUPER_NVFP4, ROUTER_ONLY_GROUPED)}
+                                  SUPER_LATENT, SUPER_NVFP4, ROUTER_ONLY_GROUPED,
+                                  NANO_DECODE_SPARSE, SUPER_NVFP4_SPARSE)}
 
 
 def scaled(shape: MoEShape, **kw) -> MoEShape:

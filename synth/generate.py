@@ -17,10 +17,15 @@ the tensor's id and a replica index):
                                     offset read from ``synth/data``;
 * NVFP4 experts                   quantised from the BF16 draws by
                                     round-to-nearest (``quantize_nvfp4``).
-
-The router matrix and bias are always drawn on the CPU (they are small and the
-popularity offsets were fitted against exactly these values); the large
-tensors are drawn on the requested device.
+* ReLU^2-sparse workloads (``relu_sparsity`` s > 0): trained layers zero most
+  expert neurons after ReLU^2, random ones only half.  Every hidden row has
+  its component along a seeded unit direction u replaced by a constant c, and
+  every expert up row its component along the matching unit direction v of
+  the expert input space (v = u, or for latent layers a seeded latent v with
+  u = W_ld^T v normalised) replaced by -kappa / 4, with c chosen so that
+  v . x_e = 4: a neuron's pre-activation is then about N(-kappa, 1) for every
+  row, kappa = Phi^-1(s), and a 16-neuron group of one row is dead with
+  probability about s^16.  Replicas of a latent sparse workload share W_ld.
 """
 from __future__ import annotations
 
@@ -34,7 +39,9 @@ from .configs import BF16, F32, NVFP4, MoEShape
 
 _DATA = os.path.join(os.path.dirname(os.path.abspath(__file__)), "data")
 
-TID_ROUTER, TID_BIAS, TID_LAT_DOWN, TID_LAT_UP, TID_UP, TID_DOWN, TID_SH_UP, TID_SH_DOWN, TID_X, TID_NORM = range(10)
+TID_ROUTER, TID_BIAS, TID_LAT_DOWN, TID_LAT_UP, TID_UP, TID_DOWN, TID_SH_UP, TID_SH_DOWN, TID_X, TID_NORM, \
+    TID_SPARSE = range(11)
+SPARSE_OFFSET = 4.0       # c_e: size of the expert-input offset along v
 
 
 def _seed(shape: MoEShape, tensor_id: int, replica: int = 0, extra: int = 0) -> int:
@@ -143,6 +150,41 @@ def quantize_nvfp4(w: torch.Tensor):
 
 
 # ----------------------------------------------------------------------------
+def _sparse_frame(shape: MoEShape, device):
+    """(u, c, v, kappa) of a ReLU^2-sparse workload: hidden rows get the
+    component c along the unit hidden direction u, every expert up row the
+    component -kappa / SPARSE_OFFSET along the unit expert-input direction v,
+    so that v . x_e = SPARSE_OFFSET for every row.  Latent layers: v is a
+    seeded latent direction and u = W_ld^T v normalised (W_ld of replica 0,
+    which every replica of a sparse workload shares), c = SPARSE_OFFSET /
+    |W_ld^T v|; otherwise u = v, c = SPARSE_OFFSET."""
+    from statistics import NormalDist
+    g = _gen("cpu", _seed(shape, TID_SPARSE))
+    v = torch.randn((shape.d_e,), generator=g, dtype=torch.float32)
+    v = v / v.norm()
+    if shape.d_latent:
+        wld = _normal((shape.d_latent, shape.d_model), shape.d_model ** -0.5, device,
+                      _seed(shape, TID_LAT_DOWN, 0), _act_torch_dtype(shape.act_dtype))
+        u = wld.float().T @ v.to(device)
+        c = SPARSE_OFFSET / float(u.norm())
+        u = u / u.norm()
+    else:
+        u, c = v.to(device), SPARSE_OFFSET
+    kappa = NormalDist().inv_cdf(shape.relu_sparsity)
+    return u, c, v.to(device), kappa
+
+
+def _sparsify_up(w_up: torch.Tensor, v: torch.Tensor, kappa: float) -> torch.Tensor:
+    """Every up row w -> w - (w . v) v - (kappa / SPARSE_OFFSET) v, expert by expert."""
+    v = v.to(w_up.device)
+    out = torch.empty_like(w_up)
+    for e in range(w_up.shape[0]):
+        w = w_up[e].float()
+        w = w - (w @ v)[:, None] * v[None, :] - (kappa / SPARSE_OFFSET) * v[None, :]
+        out[e] = w.to(w_up.dtype)
+    return out
+
+
 def make_weights(shape: MoEShape, device="cpu", replica: int = 0) -> Dict[str, torch.Tensor]:
     """All weights of one layer.  ``replica`` > 0 draws an independent copy of the
     large tensors (the router and bias are shared by all replicas)."""
@@ -155,9 +197,14 @@ def make_weights(shape: MoEShape, device="cpu", replica: int = 0) -> Dict[str, t
     out["w_router"] = rp["w_router"].to(device)
     out["bias"] = rp["bias"].to(device)
     if L:
-        out["w_lat_down"] = _normal((L, d), d ** -0.5, device, _seed(shape, TID_LAT_DOWN, replica), sdt)
+        # (the ReLU^2-sparse workloads share replica 0's latent down matrix)
+        rld = 0 if shape.relu_sparsity > 0 else replica
+        out["w_lat_down"] = _normal((L, d), d ** -0.5, device, _seed(shape, TID_LAT_DOWN, rld), sdt)
         out["w_lat_up"] = _normal((d, L), L ** -0.5, device, _seed(shape, TID_LAT_UP, replica), sdt)
     w_up = _normal((E, I, de), de ** -0.5, device, _seed(shape, TID_UP, replica), wdt)
+    if shape.relu_sparsity > 0:
+        _, _, v, kappa = _sparse_frame(shape, device)
+        w_up = _sparsify_up(w_up, v, kappa)
     w_down = _normal((E, de, I), I ** -0.5, device, _seed(shape, TID_DOWN, replica), wdt)
     if shape.expert_dtype == NVFP4:
         out["w_up_q"], out["w_up_sf"], out["w_up_gs"] = quantize_nvfp4(w_up)
@@ -175,6 +222,12 @@ def make_x(shape: MoEShape, T: int, device="cpu", stream_id: int = 0) -> torch.T
     """Hidden rows [T, d] ~ N(0,1) in the activation dtype."""
     if T == 0:
         return torch.empty((0, shape.d_model), dtype=_act_torch_dtype(shape.act_dtype), device=device)
+    if shape.relu_sparsity > 0:
+        # hidden rows with their component along u replaced by c
+        z = _normal((T, shape.d_model), 1.0, device, _seed(shape, TID_X, stream_id, extra=T), torch.float32)
+        u, c, _, _ = _sparse_frame(shape, device)
+        z = z - (z @ u)[:, None] * u[None, :] + c * u[None, :]
+        return z.to(_act_torch_dtype(shape.act_dtype))
     return _normal((T, shape.d_model), 1.0, device,
                    _seed(shape, TID_X, stream_id, extra=T), _act_torch_dtype(shape.act_dtype))
 

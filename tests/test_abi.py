@@ -37,7 +37,12 @@ def test_library_exports_every_declared_entry_point(lib):
 def test_struct_layout_matches_header(lib):
     from routed_relu_expert_gb300 import MoeConfig, MoeWeights
     assert ctypes.sizeof(MoeConfig) == 12 * 4
-    assert ctypes.sizeof(MoeWeights) == 12 * 8
+    # one pointer per member the header declares in moe_weights_t, in order
+    text = open(HEADER).read()
+    body = text[text.index("typedef struct moe_weights {"):text.index("} moe_weights_t;")]
+    members = re.findall(r"\*\s*(w_[a-z_]+|router_bias)\s*;", body)
+    assert [f[0] for f in MoeWeights._fields_] == members
+    assert ctypes.sizeof(MoeWeights) == len(members) * 8
 
 
 def _cfg(**kw):
