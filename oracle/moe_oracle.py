@@ -478,6 +478,155 @@ def block_forward(x: np.ndarray, gamma: np.ndarray, eps: float, weights: Dict[st
     return out
 
 
+# ----------------------------------------------------------------------------
+# backward (page "M6.1 Routed Capacity", section 0x06F: the forward relation is
+# frozen, the route tensors are the coordinates of the backward; combine
+# backward is a broadcast and a dot product, the gather's adjoint a
+# scatter-add, and the router and expert paths meet again at the input)
+# ----------------------------------------------------------------------------
+
+
+def gate_backward(scores_sel: np.ndarray, q: np.ndarray, norm_topk_prob: int, rsf: float) -> np.ndarray:
+    """dL/ds of the chosen experts' scores from q = dL/dw.  The weights are
+    w_k = rsf s_k / sum_j s_j (or rsf s_k without normalisation), so
+    dL/ds_j = rsf / S (q_j - sum_k q_k s_k / S), S = sum_j s_j.  This is the
+    page's selected-gate Jacobian contraction (section 0x06F.3) for this
+    layer's sigmoid-then-normalise gate instead of a selected softmax."""
+    s = np.asarray(scores_sel, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    if not norm_topk_prob:
+        return rsf * q
+    S = s.sum(axis=-1, keepdims=True)
+    return rsf / S * (q - (q * s).sum(axis=-1, keepdims=True) / S)
+
+
+def layer_backward(x: np.ndarray, weights: Dict[str, np.ndarray], ids: np.ndarray, scores: np.ndarray,
+                   dy: np.ndarray, n_experts: int, norm_topk_prob: int, rsf: float) -> Dict[str, object]:
+    """Gradients of L = <dy, y> for the layer with its routing frozen.
+
+    The chosen ids are fixed metadata (no gradient; the selection bias only
+    chooses); ``scores`` [T, E] are the forward's sigmoid scores.  Real
+    arithmetic in float64: no rounding point of the forward is modelled.
+    Per route r = (t, k) of expert e (page section 0x06F.2, 0x06F.6):
+      U_r = W_down,e relu(a_r)^2, a_r = W_up,e x_e,t;   q_r = <dy_r,t, U_r>;
+      dU_r = w_r dy_r,t;  dh_r = W_down,e^T dU_r;  da_r = dh_r * 2 relu(a_r);
+      dW_down,e += dU_r h_r^T;  dW_up,e += da_r x_e,t^T;  dx_e,t += W_up,e^T da_r
+    (dy_r = dy, or dy W_lu for latent layers, where dW_lu = dy^T y_r).
+    Gates (section 0x06F.3, 0x06F.4): ds from q (``gate_backward``),
+    dz = ds s (1 - s) at the chosen experts, zero elsewhere;
+    dW_r += dz x_t per chosen expert, dx_t += dz W_r,e.
+    Shared expert: the dense ReLU^2 MLP's backward on x.  Latent down:
+    dW_ld = dx_e^T x, dx += dx_e W_ld; otherwise dx += dx_e."""
+    x = np.asarray(x, dtype=np.float64)
+    D = np.asarray(dy, dtype=np.float64)
+    ids = np.asarray(ids)
+    T, K = ids.shape
+    s_all = np.asarray(scores, dtype=np.float64)
+    s_sel = np.take_along_axis(s_all, ids.astype(np.int64), axis=1)
+    w = rsf * (s_sel / s_sel.sum(axis=1, keepdims=True) if norm_topk_prob else s_sel)
+    latent = "w_lat_down" in weights
+    out: Dict[str, object] = {}
+    dx = np.zeros_like(x)
+    if latent:
+        W_ld = np.asarray(weights["w_lat_down"], dtype=np.float64)
+        x_e = x @ W_ld.T
+    else:
+        x_e = x
+    de = x_e.shape[1]
+    # routed experts, route by route
+    y_r = np.zeros((T, de))
+    U = np.zeros((T, K, de))
+    acts = {}
+    for t in range(T):
+        for k in range(K):
+            e = int(ids[t, k])
+            up, down = expert_matrices(weights, e)
+            a = up @ x_e[t]
+            h = np.maximum(a, 0.0) ** 2
+            U[t, k] = down @ h
+            acts[(t, k)] = (a, h)
+            y_r[t] += w[t, k] * U[t, k]
+    if latent:
+        W_lu = np.asarray(weights["w_lat_up"], dtype=np.float64)
+        dy_r = D @ W_lu
+        out["d_w_lat_up"] = D.T @ y_r
+    else:
+        dy_r = D
+    q = np.einsum("td,tkd->tk", dy_r, U)
+    d_up: Dict[int, np.ndarray] = {}
+    d_down: Dict[int, np.ndarray] = {}
+    dx_e = np.zeros_like(x_e)
+    for t in range(T):
+        for k in range(K):
+            e = int(ids[t, k])
+            up, down = expert_matrices(weights, e)
+            a, h = acts[(t, k)]
+            dU = w[t, k] * dy_r[t]
+            dh = down.T @ dU
+            da = dh * 2.0 * np.maximum(a, 0.0)
+            d_down[e] = d_down.get(e, 0.0) + np.outer(dU, h)
+            d_up[e] = d_up.get(e, 0.0) + np.outer(da, x_e[t])
+            dx_e[t] += up.T @ da
+    ds = gate_backward(s_sel, q, norm_topk_prob, rsf)
+    dz = ds * s_sel * (1.0 - s_sel)
+    W_r = np.asarray(weights["w_router"], dtype=np.float64)
+    d_router = np.zeros_like(W_r)
+    for t in range(T):
+        for k in range(K):
+            e = int(ids[t, k])
+            d_router[e] += dz[t, k] * x[t]
+            dx[t] += dz[t, k] * W_r[e]
+    if "w_sh_up" in weights:
+        W_su = np.asarray(weights["w_sh_up"], dtype=np.float64)
+        W_sd = np.asarray(weights["w_sh_down"], dtype=np.float64)
+        a_s = x @ W_su.T
+        h_s = np.maximum(a_s, 0.0) ** 2
+        out["d_w_sh_down"] = D.T @ h_s
+        da_s = (D @ W_sd) * 2.0 * np.maximum(a_s, 0.0)
+        out["d_w_sh_up"] = da_s.T @ x
+        dx += da_s @ W_su
+    if latent:
+        out["d_w_lat_down"] = dx_e.T @ x
+        dx += dx_e @ W_ld
+    else:
+        dx += dx_e
+    out.update({"dx": dx, "d_w_router": d_router, "d_w_up": d_up, "d_w_down": d_down, "q": q, "ds": ds,
+                "dz": dz, "w": w, "y_routed": y_r})
+    return out
+
+
+def rms_norm_backward(x: np.ndarray, gamma: np.ndarray, eps: float, dxn: np.ndarray):
+    """(dx, dgamma) of xn = gamma * x r, r = 1 / sqrt(mean(x^2) + eps):
+    dx_i = r gamma_i dxn_i - r^3 x_i / d * sum_j gamma_j dxn_j x_j;
+    dgamma = sum over rows of dxn * x r."""
+    x = np.asarray(x, dtype=np.float64)
+    g = np.asarray(gamma, dtype=np.float64)[None, :]
+    dxn = np.asarray(dxn, dtype=np.float64)
+    d = x.shape[1]
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + eps)
+    dot = np.sum(g * dxn * x, axis=1, keepdims=True)
+    dx = r * g * dxn - r ** 3 * x * dot / d
+    return dx, np.sum(dxn * x * r, axis=0)
+
+
+def block_backward(x: np.ndarray, gamma: np.ndarray, eps: float, weights: Dict[str, np.ndarray],
+                   ids: np.ndarray, scores: np.ndarray, dout: np.ndarray, n_experts: int,
+                   norm_topk_prob: int, rsf: float, xn: Optional[np.ndarray] = None) -> Dict[str, object]:
+    """Gradients of L = <dout, out> for out = x + layer(RMSNorm(x)) with the
+    routing frozen: the residual passes dout to x unchanged (page section
+    0x06F.6: the residual is the third path into the block input), the layer's
+    input gradient goes back through the RMSNorm.  ``xn``: the normalised rows
+    the layer read (as the device stored them), else the float64 RMSNorm."""
+    xn_v = rms_norm(x, gamma, eps) if xn is None else np.asarray(xn, dtype=np.float64)
+    out = layer_backward(xn_v, weights, ids, scores, dout, n_experts, norm_topk_prob, rsf)
+    dxn = out["dx"]
+    dx, dgamma = rms_norm_backward(x, gamma, eps, dxn)
+    out["dxn"] = dxn
+    out["dx"] = np.asarray(dout, dtype=np.float64) + dx
+    out["d_norm_w"] = dgamma
+    return out
+
+
 class _LazyExpert:
     """Expert e as a callable (matrices fetched, and dequantised, on first use)."""
 
