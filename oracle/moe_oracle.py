@@ -501,7 +501,8 @@ def gate_backward(scores_sel: np.ndarray, q: np.ndarray, norm_topk_prob: int, rs
 
 
 def layer_backward(x: np.ndarray, weights: Dict[str, np.ndarray], ids: np.ndarray, scores: np.ndarray,
-                   dy: np.ndarray, n_experts: int, norm_topk_prob: int, rsf: float) -> Dict[str, object]:
+                   dy: np.ndarray, n_experts: int, norm_topk_prob: int, rsf: float,
+                   bf16_points: bool = False) -> Dict[str, object]:
     """Gradients of L = <dy, y> for the layer with its routing frozen.
 
     The chosen ids are fixed metadata (no gradient; the selection bias only
@@ -512,6 +513,12 @@ def layer_backward(x: np.ndarray, weights: Dict[str, np.ndarray], ids: np.ndarra
       dU_r = w_r dy_r,t;  dh_r = W_down,e^T dU_r;  da_r = dh_r * 2 relu(a_r);
       dW_down,e += dU_r h_r^T;  dW_up,e += da_r x_e,t^T;  dx_e,t += W_up,e^T da_r
     (dy_r = dy, or dy W_lu for latent layers, where dW_lu = dy^T y_r).
+    ``bf16_points``: the forward's rounding points (latent rows, a, h, the
+    latent combine y_r; see ``relu2_mlp``) and a BF16 reading of the
+    backward's tensor-core operands: dy_r = bf16(dy W_lu), dU = bf16(w dy_r),
+    da = bf16(dh * 2 sqrt(h)) (relu(a) taken from the stored h), the latent
+    input gradient rounded before its two products, and the shared expert's
+    da_s = bf16((dy W_sd) * 2 sqrt(h_s)); everything else stays float64.
     Gates (section 0x06F.3, 0x06F.4): ds from q (``gate_backward``),
     dz = ds s (1 - s) at the chosen experts, zero elsewhere;
     dW_r += dz x_t per chosen expert, dx_t += dz W_r,e.
@@ -527,9 +534,10 @@ def layer_backward(x: np.ndarray, weights: Dict[str, np.ndarray], ids: np.ndarra
     latent = "w_lat_down" in weights
     out: Dict[str, object] = {}
     dx = np.zeros_like(x)
+    rnd = bf16_round if bf16_points else (lambda v: v)
     if latent:
         W_ld = np.asarray(weights["w_lat_down"], dtype=np.float64)
-        x_e = x @ W_ld.T
+        x_e = rnd(x @ W_ld.T)
     else:
         x_e = x
     de = x_e.shape[1]
@@ -541,15 +549,15 @@ def layer_backward(x: np.ndarray, weights: Dict[str, np.ndarray], ids: np.ndarra
         for k in range(K):
             e = int(ids[t, k])
             up, down = expert_matrices(weights, e)
-            a = up @ x_e[t]
-            h = np.maximum(a, 0.0) ** 2
+            a = rnd(up @ x_e[t])
+            h = rnd(np.maximum(a, 0.0) ** 2)
             U[t, k] = down @ h
             acts[(t, k)] = (a, h)
             y_r[t] += w[t, k] * U[t, k]
     if latent:
         W_lu = np.asarray(weights["w_lat_up"], dtype=np.float64)
-        dy_r = D @ W_lu
-        out["d_w_lat_up"] = D.T @ y_r
+        dy_r = rnd(D @ W_lu)
+        out["d_w_lat_up"] = D.T @ rnd(y_r)
     else:
         dy_r = D
     q = np.einsum("td,tkd->tk", dy_r, U)
@@ -561,9 +569,9 @@ def layer_backward(x: np.ndarray, weights: Dict[str, np.ndarray], ids: np.ndarra
             e = int(ids[t, k])
             up, down = expert_matrices(weights, e)
             a, h = acts[(t, k)]
-            dU = w[t, k] * dy_r[t]
+            dU = rnd(w[t, k] * dy_r[t])
             dh = down.T @ dU
-            da = dh * 2.0 * np.maximum(a, 0.0)
+            da = rnd(dh * 2.0 * np.sqrt(h)) if bf16_points else dh * 2.0 * np.maximum(a, 0.0)
             d_down[e] = d_down.get(e, 0.0) + np.outer(dU, h)
             d_up[e] = d_up.get(e, 0.0) + np.outer(da, x_e[t])
             dx_e[t] += up.T @ da
@@ -579,15 +587,19 @@ def layer_backward(x: np.ndarray, weights: Dict[str, np.ndarray], ids: np.ndarra
     if "w_sh_up" in weights:
         W_su = np.asarray(weights["w_sh_up"], dtype=np.float64)
         W_sd = np.asarray(weights["w_sh_down"], dtype=np.float64)
-        a_s = x @ W_su.T
-        h_s = np.maximum(a_s, 0.0) ** 2
+        a_s = rnd(x @ W_su.T)
+        h_s = rnd(np.maximum(a_s, 0.0) ** 2)
         out["d_w_sh_down"] = D.T @ h_s
-        da_s = (D @ W_sd) * 2.0 * np.maximum(a_s, 0.0)
+        if bf16_points:
+            da_s = rnd((D @ W_sd) * 2.0 * np.sqrt(h_s))
+        else:
+            da_s = (D @ W_sd) * 2.0 * np.maximum(a_s, 0.0)
         out["d_w_sh_up"] = da_s.T @ x
         dx += da_s @ W_su
     if latent:
-        out["d_w_lat_down"] = dx_e.T @ x
-        dx += dx_e @ W_ld
+        dx_l = rnd(dx_e)
+        out["d_w_lat_down"] = dx_l.T @ x
+        dx += dx_l @ W_ld
     else:
         dx += dx_e
     out.update({"dx": dx, "d_w_router": d_router, "d_w_up": d_up, "d_w_down": d_down, "q": q, "ds": ds,
@@ -611,14 +623,15 @@ def rms_norm_backward(x: np.ndarray, gamma: np.ndarray, eps: float, dxn: np.ndar
 
 def block_backward(x: np.ndarray, gamma: np.ndarray, eps: float, weights: Dict[str, np.ndarray],
                    ids: np.ndarray, scores: np.ndarray, dout: np.ndarray, n_experts: int,
-                   norm_topk_prob: int, rsf: float, xn: Optional[np.ndarray] = None) -> Dict[str, object]:
+                   norm_topk_prob: int, rsf: float, xn: Optional[np.ndarray] = None,
+                   bf16_points: bool = False) -> Dict[str, object]:
     """Gradients of L = <dout, out> for out = x + layer(RMSNorm(x)) with the
     routing frozen: the residual passes dout to x unchanged (page section
     0x06F.6: the residual is the third path into the block input), the layer's
     input gradient goes back through the RMSNorm.  ``xn``: the normalised rows
     the layer read (as the device stored them), else the float64 RMSNorm."""
     xn_v = rms_norm(x, gamma, eps) if xn is None else np.asarray(xn, dtype=np.float64)
-    out = layer_backward(xn_v, weights, ids, scores, dout, n_experts, norm_topk_prob, rsf)
+    out = layer_backward(xn_v, weights, ids, scores, dout, n_experts, norm_topk_prob, rsf, bf16_points)
     dxn = out["dx"]
     dx, dgamma = rms_norm_backward(x, gamma, eps, dxn)
     out["dxn"] = dxn

@@ -151,3 +151,41 @@ def test_block_backward_matches_central_differences():
     for j in range(D_MODEL):
         num = _fd(loss, gamma, j)
         assert abs(g["d_norm_w"][j] - num) <= 1e-7 + 1e-6 * abs(num), (j, g["d_norm_w"][j], num)
+
+
+def test_bf16_points_change_nothing_when_every_operand_is_representable():
+    # small integers and powers of two: a, h, dU, dh, da and all products are
+    # exact in BF16, so the rounding points must leave every gradient unchanged
+    rng = np.random.default_rng(11)
+    d, E_, I_ = 8, 4, 8
+    w = {"w_router": rng.integers(-2, 3, (E_, d)).astype(np.float64) / 8,
+         "w_up": rng.integers(-2, 3, (E_, I_, d)).astype(np.float64) / 4,
+         "w_down": rng.integers(-2, 3, (E_, d, I_)).astype(np.float64) / 4}
+    x = rng.integers(-2, 3, (3, d)).astype(np.float64)
+    D = rng.integers(-2, 3, (3, d)).astype(np.float64)
+    ids = np.array([[0, 2], [1, 3], [2, 0]])
+    scores = np.full((3, E_), 0.5)
+    a = O.layer_backward(x, w, ids, scores, D, E_, 0, 1.0, bf16_points=False)
+    b = O.layer_backward(x, w, ids, scores, D, E_, 0, 1.0, bf16_points=True)
+    for k in ("dx", "d_w_router"):
+        np.testing.assert_array_equal(a[k], b[k])
+    for e in a["d_w_up"]:
+        np.testing.assert_array_equal(a["d_w_up"][e], b["d_w_up"][e])
+        np.testing.assert_array_equal(a["d_w_down"][e], b["d_w_down"][e])
+
+
+def test_bf16_points_round_the_backward_operands():
+    # a gate of 1/3 makes dU = w dy inexact in BF16: the rounded run differs,
+    # by at most one BF16 step of dU, where dU enters
+    rng = np.random.default_rng(12)
+    d, E_, I_ = 8, 2, 8
+    w = {"w_router": rng.standard_normal((E_, d)), "w_up": np.ones((E_, I_, d)) / 8,
+         "w_down": np.ones((E_, d, I_)) / 8}
+    x = np.ones((1, d))
+    D = np.ones((1, d))
+    ids = np.array([[0]])
+    scores = np.array([[1.0 / 3.0, 0.5]])
+    a = O.layer_backward(x, w, ids, scores, D, E_, 0, 1.0, bf16_points=False)
+    b = O.layer_backward(x, w, ids, scores, D, E_, 0, 1.0, bf16_points=True)
+    rel = np.abs(b["d_w_down"][0] - a["d_w_down"][0]) / np.abs(a["d_w_down"][0])
+    assert 0 < rel.max() <= 2.0 ** -8
