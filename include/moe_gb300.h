@@ -108,10 +108,10 @@ typedef struct moe_weights {
   const void* w_sh_up;        /* [S, d] shared expert up   (S > 0)                                    */
   const void* w_sh_down;      /* [d, S] shared expert down (S > 0)                                    */
   /* optional: the expert down weights again, in the group-major layout of
-   * moe_sparse_down_layout (NULL = not given).  When given, decode steps (the
-   * streaming GEMV path: up to 64 tokens, and for NVFP4 experts the FP16
-   * path) compute the down projection by the ReLU^2-sparse kernel, which
-   * reads only the 16-neuron groups of W_down with a live neuron.           */
+   * moe_sparse_down_layout (NULL = not given).  When given, decode steps of
+   * up to 16 tokens (BF16 experts; NVFP4 experts on their FP16 path)
+   * compute the down projection by the ReLU^2-sparse kernel, which reads
+   * only the 16-neuron groups of W_down with a live neuron.                 */
   const void* w_down_g;       /* BF16 [E, de * I] / NVFP4 values [E, de * I / 2] u8                   */
   const uint8_t* w_down_g_sf; /* NVFP4: E4M3 scales [E, de * I / 16]                                  */
 } moe_weights_t;
@@ -286,6 +286,79 @@ moe_status_t moe_block_forward(const moe_config_t* cfg, int32_t T, const void* x
                                int32_t* topk_ids_out, float* topk_w_out,
                                float* logits_out, float* scores_out,
                                void* ws, size_t ws_bytes, void* stream);
+
+/* ---- backward (page "M6.1 Routed Capacity", section 0x06F "Single-Device
+ * Forward And Backward Integration Contract") ------------------------------
+ * Gradients of a scalar loss L with upstream gradient dy = dL/dy, for the
+ * forward relation the forward call froze: the chosen ids are metadata (no
+ * gradient; the selection bias only chooses), the gates w = rsf s_k / sum_j s_j
+ * (or rsf s_k) carry the router's gradient to the chosen experts' logits
+ * (dL/dz_k = dL/ds_k s_k (1 - s_k), zero for every other expert), the
+ * combine's backward is dU = w dy_r and dL/dw = <dy_r, U>, the gather's
+ * adjoint a scatter-add in ascending expert order, and the router, expert,
+ * shared and (block) residual paths add at the input.  BF16 layers only
+ * (MOE_ERR_UNSUPPORTED otherwise); BF16 operands, FP32 accumulation; the
+ * ReLU^2 derivative 2 relu(a) is taken as 2 sqrt(h) from the forward's stored
+ * h.  Weight gradients are ADDED to the given FP32 buffers (zero them once
+ * per step; a NULL buffer skips that gradient); experts without routes are
+ * left untouched (their gradient is zero).                                  */
+typedef struct moe_grads {
+  float* d_router;    /* [E, d]      */
+  float* d_lat_down;  /* [L, d]      latent shapes */
+  float* d_lat_up;    /* [d, L]      latent shapes */
+  float* d_up;        /* [E, I, de]  */
+  float* d_down;      /* [E, de, I]  */
+  float* d_sh_up;     /* [S, d]      shared expert */
+  float* d_sh_down;   /* [d, S]      shared expert */
+  float* d_norm_w;    /* [d]         moe_block_backward only */
+} moe_grads_t;
+
+/* Bytes of the backward scratch `bws` for T tokens (0 on an invalid config). */
+size_t moe_backward_workspace_bytes(const moe_config_t* cfg, int32_t T);
+
+/* Where the backward scratch keeps its BF16 operands and the gate gradient
+ * after a backward call (host arithmetic only), so a caller can inspect them:
+ *   MOE_BWS_DU         [T*K, de] bf16  dU = bf16(w dy_r), packed row order
+ *   MOE_BWS_DA         [T*K, I]  bf16  da = bf16((dU W_down) * 2 sqrt(h))
+ *   MOE_BWS_DZ         [T, K]    FP32  dL/dz of the chosen experts' logits
+ *   MOE_BWS_DX_LATENT  [T, L]    bf16  the latent input gradient (latent shapes)
+ *   MOE_BWS_DA_SHARED  [T, S]    bf16  the shared expert's da
+ *   MOE_BWS_DY_LATENT  [T, L]    bf16  dy_r = bf16(dy W_lu) (latent shapes)  */
+enum {
+  MOE_BWS_DU = 0, MOE_BWS_DA = 1, MOE_BWS_DZ = 2, MOE_BWS_DX_LATENT = 3, MOE_BWS_DA_SHARED = 4,
+  MOE_BWS_DY_LATENT = 5
+};
+moe_status_t moe_backward_workspace_region(const moe_config_t* cfg, int32_t T, int32_t region,
+                                           size_t* offset, size_t* bytes);
+
+/* Backward of moe_layer_forward.  `ws` must be the workspace of a
+ * moe_layer_forward call on the same x, weights and T, with no other call on
+ * it since (its route tables, h, u, latent rows and shared h are the saved
+ * forward state).  topk_ids / topk_w / scores: the forward's router outputs
+ * ([T, K] int32, [T, K] FP32, [T, E] FP32; its *_out buffers, or the
+ * workspace regions MOE_WS_TOPK_IDS / _TOPK_W / _SCORES when they were NULL).
+ *   x [T, d] the forward's input; dy [T, d] act_dtype upstream gradient;
+ *   dx [T, d] FP32 out: dL/dx through the router, the experts (and latent
+ *   pair) and the shared expert.                                           */
+moe_status_t moe_layer_backward(const moe_config_t* cfg, int32_t T, const void* x,
+                                const moe_weights_t* w, const void* dy,
+                                const int32_t* topk_ids, const float* topk_w, const float* scores,
+                                float* dx, const moe_grads_t* grads,
+                                const void* ws, size_t ws_bytes, void* bws, size_t bws_bytes,
+                                void* stream);
+
+/* Backward of moe_block_forward (out = x + layer(RMSNorm(x))): dout [T, d]
+ * act_dtype; dx [T, d] FP32 = dout (the residual) + the RMSNorm's backward of
+ * the layer's input gradient; grads->d_norm_w gets dL/dgamma added.  x_norm:
+ * the forward's x_norm_out buffer, or NULL when the forward kept the rows in
+ * the workspace.  Same state rules as moe_layer_backward.                   */
+moe_status_t moe_block_backward(const moe_config_t* cfg, int32_t T, const void* x,
+                                const float* norm_w, float norm_eps, const void* x_norm,
+                                const moe_weights_t* w, const void* dout,
+                                const int32_t* topk_ids, const float* topk_w, const float* scores,
+                                float* dx, const moe_grads_t* grads,
+                                const void* ws, size_t ws_bytes, void* bws, size_t bws_bytes,
+                                void* stream);
 
 /* Synchronises `stream`, copies the device error word of `ws` to *code (host
  * pointer) and returns MOE_ERR_DEVICE if any bit is set, else MOE_OK.         */

@@ -22,6 +22,7 @@ MOE_NOALLOC_MAX_SPLIT_ELEMS = 7340032
  MOE_WS_X_TERM_SCALES, MOE_WS_X_ROW_SCALES, MOE_WS_H_TERMS, MOE_WS_H_TERM_SCALES, MOE_WS_H_ROW_SCALES,
  MOE_WS_X_NORM) = range(19)
 ACT_TERMS_MAX = 4
+MOE_BWS_DU, MOE_BWS_DA, MOE_BWS_DZ, MOE_BWS_DX_LATENT, MOE_BWS_DA_SHARED, MOE_BWS_DY_LATENT = range(6)
 
 
 class MoeConfig(ctypes.Structure):
@@ -47,12 +48,18 @@ class MoeWeights(ctypes.Structure):
         "w_up_sf", "w_down_sf", "w_up_gs", "w_down_gs", "w_sh_up", "w_sh_down", "w_down_g", "w_down_g_sf")]
 
 
+class MoeGrads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "d_router", "d_lat_down", "d_lat_up", "d_up", "d_down", "d_sh_up", "d_sh_down", "d_norm_w")]
+
+
 EXPORTS = (
     "moe_version", "moe_status_string", "moe_check_config", "moe_workspace_bytes", "moe_router",
     "moe_dispatch", "moe_experts_up", "moe_experts_down", "moe_experts_down_combine", "moe_latent_down", "moe_shared",
     "moe_layer_forward", "moe_get_device_error", "moe_clear_device_error", "moe_layer_forward_host",
     "moe_launch_count", "moe_router_noalloc", "moe_workspace_region", "moe_set_nvfp4_act_terms",
     "moe_nvfp4_act_terms_for", "moe_block_forward", "moe_sparse_down_bytes", "moe_sparse_down_layout",
+    "moe_backward_workspace_bytes", "moe_layer_backward", "moe_block_backward", "moe_backward_workspace_region",
 )
 
 _lib = None
@@ -88,6 +95,11 @@ def load() -> ctypes.CDLL:
         "moe_block_forward": (I32, [CFG, I32, P, P, ctypes.c_float, W, P, P, P, P, P, P, P, S, P]),
         "moe_sparse_down_bytes": (I32, [CFG, ctypes.POINTER(S), ctypes.POINTER(S)]),
         "moe_sparse_down_layout": (I32, [CFG, W, P, P, P]),
+        "moe_backward_workspace_bytes": (S, [CFG, I32]),
+        "moe_backward_workspace_region": (I32, [CFG, I32, I32, ctypes.POINTER(S), ctypes.POINTER(S)]),
+        "moe_layer_backward": (I32, [CFG, I32, P, W, P, P, P, P, P, ctypes.POINTER(MoeGrads), P, S, P, S, P]),
+        "moe_block_backward": (I32, [CFG, I32, P, P, ctypes.c_float, P, W, P, P, P, P, P,
+                                     ctypes.POINTER(MoeGrads), P, S, P, S, P]),
         "moe_get_device_error": (I32, [P, P, ctypes.POINTER(I32)]),
         "moe_clear_device_error": (I32, [P, P]),
         "moe_layer_forward_host": (I32, [CFG, I32, P, P, W, P, P, P, S, P]),

@@ -280,10 +280,16 @@ moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x
   return MOE_OK;
 }
 
+// the decode down projection runs ReLU^2-sparse up to this many tokens: above
+// it too few 16-neuron groups are dead in every row of an expert (8 % at 64
+// tokens of a 92.5 %-sparse Nano layer, where the sparse product measured 10 %
+// slower than the dense GEMV; 16 % dead and 2 % faster at 16 tokens)
+constexpr int kSparseDownMaxT = 16;
+
 // the decode down projection can run ReLU^2-sparse: group-major weights given,
 // BF16 activations, BF16 experts or NVFP4 experts with FP16 h, shapes that fit
-bool sparse_down_ok(const moe_config_t* c, const moe_weights_t* w, bool f16) {
-  if (!w->w_down_g || c->act_dtype != MOE_DT_BF16) return false;
+bool sparse_down_ok(const moe_config_t* c, int T, const moe_weights_t* w, bool f16) {
+  if (!w->w_down_g || c->act_dtype != MOE_DT_BF16 || T > kSparseDownMaxT) return false;
   const bool fp4 = c->expert_dtype == MOE_DT_NVFP4;
   if (fp4 && (!f16 || !w->w_down_g_sf)) return false;
   if (!fp4 && c->expert_dtype != MOE_DT_BF16) return false;
@@ -311,7 +317,7 @@ moe_status_t run_down(const moe_config_t* c, int T, const void* h, const int32_t
                       tc_tile_rows(R / segs, segs, de), s));
     return MOE_OK;
   }
-  if (sparse_down_ok(c, w, f16)) {
+  if (sparse_down_ok(c, T, w, f16)) {
     // ReLU^2-sparse: only the 16-neuron groups of W_down with a live neuron
     a.W = w->w_down_g;
     a.W_sf = w->w_down_g_sf;
@@ -558,6 +564,182 @@ moe_status_t run_layer(const moe_config_t* cfg, int32_t T, const void* x, const 
   return MOE_OK;
 }
 
+// ---- backward ----------------------------------------------------------------
+// backward scratch [T tokens]: bf16 and f32 intermediates of moe_layer_backward
+struct BwLayout {
+  size_t tprefix, dyr, dU, q, dz, da, dxr, dxe, dxl, das, dxs, dxa, dxn, xr, total;
+};
+
+BwLayout make_bw_layout(const moe_config_t* c, int32_t T) {
+  BwLayout B{};
+  const size_t t = (size_t)T, R = t * c->top_k, de = de_of(c), d = c->d_model, I = c->d_expert;
+  const size_t S = c->d_shared, L = c->d_latent;
+  size_t off = 0;
+  B.tprefix = take(off, ((size_t)c->n_experts + 1) * 4);
+  B.dyr = take(off, L ? t * L * 2 : 0);
+  B.dU = take(off, R * de * 2);
+  B.q = take(off, R * 4);
+  B.dz = take(off, R * 4);
+  B.da = take(off, R * I * 2);
+  B.dxr = take(off, R * de * 4);
+  B.dxe = take(off, t * de * 4);
+  B.dxl = take(off, L ? t * L * 2 : 0);
+  B.das = take(off, t * S * 2);
+  B.dxs = take(off, S ? t * d * 4 : 0);
+  B.dxa = take(off, L ? t * d * 4 : 0);
+  B.dxn = take(off, t * d * 4);
+  B.xr = take(off, t * d * 4);
+  B.total = (off + 255) & ~(size_t)255;
+  return B;
+}
+
+moe_status_t check_backward(const moe_config_t* c, int32_t T, const void* ws, size_t ws_bytes, const void* bws,
+                            size_t bws_bytes) {
+  moe_status_t st = check_common(c, T, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  if (c->act_dtype != MOE_DT_BF16 || c->expert_dtype != MOE_DT_BF16) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!bws || !aligned16(bws)) return MOE_ERR_INVALID_ARG;
+  if (bws_bytes < make_bw_layout(c, T).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+// one backward GEMM's arguments
+GemmArgs gemm_args(int mode, int epi, const void* A, int64_t lda, bool a_t, const void* B, int64_t ldb, void* C,
+                   int64_t ldc, int M, int N, int K) {
+  GemmArgs g{};
+  g.mode = mode; g.epi = epi;
+  g.A = reinterpret_cast<const bf16*>(A); g.lda = lda; g.a_t = a_t;
+  g.B = reinterpret_cast<const bf16*>(B); g.ldb = ldb;
+  g.C = C; g.ldc = ldc;
+  g.M = M; g.N = N; g.K = K;
+  return g;
+}
+
+// Gradients of L = <dy, y> for the layer whose forward on x left its route
+// tables, h, u, the latent rows, y_rl and the shared h in P (no other layer
+// call on that workspace since).  dx (FP32) is written; weight gradients are
+// added to g's non-NULL buffers.
+moe_status_t run_backward(const moe_config_t* c, int T, const void* x, const moe_weights_t* w, const void* dy,
+                          const int32_t* ids, const float* topw, const float* scores, float* dx,
+                          const moe_grads_t* gr, const Ptrs& P, char* bws, cudaStream_t s) {
+  const BwLayout B = make_bw_layout(c, T);
+  auto at = [&](size_t o) { return bws + o; };
+  const int d = c->d_model, de = de_of(c), I = c->d_expert, S = c->d_shared, L = c->d_latent;
+  const int E = c->n_experts, K = c->top_k, R = T * K;
+  const bool latent = L > 0, shared = S > 0;
+  const int segs = (int)std::min<int64_t>(E, R);
+  const int32_t* offs = P.at<int32_t>(P.L.offsets);
+  const int32_t* active = P.at<int32_t>(P.L.active);
+  const int32_t* rt = P.at<int32_t>(P.L.route_token);
+  const int32_t* rs = P.at<int32_t>(P.L.route_slot);
+  const int32_t* tsr = P.at<int32_t>(P.L.tsr);
+  const WsHeader* hdr = P.hdr();
+  const void* x_e = latent ? P.at<void>(P.L.x_l) : x;
+  int32_t* tpre = reinterpret_cast<int32_t*>(at(B.tprefix));
+  auto grouped = [&](GemmArgs& g) {
+    g.offsets = offs; g.active = active; g.hdr = hdr; g.tprefix = tpre;
+  };
+  CU(launch_tile_scan(offs, active, hdr, tpre, s));
+  // upstream gradient of the routed sum: dy, or dy W_lu (latent)
+  const void* dyr = dy;
+  int64_t dyr_ld = d;
+  if (latent) {
+    GemmArgs g = gemm_args(GM_ROWS, GE_STORE_BF16, dy, d, false, w->w_lat_up, L, at(B.dyr), L, 0, L, d);
+    g.dense_rows = T;
+    CU(launch_gemm_bwd(g, 1, T, s));
+    if (gr->d_lat_up) {
+      // dW_lu += dy^T y_rl  (y_rl: the forward's rounded latent combine)
+      GemmArgs gw = gemm_args(GM_KSEG, GE_ACC_F32, dy, d, true, P.at<void>(P.L.y_rl), L, gr->d_lat_up, L, d, L, 0);
+      gw.dense_rows = T;
+      CU(launch_gemm_bwd(gw, 1, 0, s));
+    }
+    dyr = at(B.dyr);
+    dyr_ld = L;
+  }
+  // combine backward: dU = w dy_r (packed rows), q = <dy_r, U>
+  CU(launch_combine_bwd(dyr, dyr_ld, P.at<float>(P.L.u), rt, rs, topw, R, K, de, at(B.dU),
+                        reinterpret_cast<float*>(at(B.q)), s));
+  // gate backward and the router weight gradient
+  float* dz = reinterpret_cast<float*>(at(B.dz));
+  CU(launch_gate_bwd(scores, ids, reinterpret_cast<float*>(at(B.q)), T, E, K, c->norm_topk_prob,
+                     c->routed_scaling_factor, dz, s));
+  if (gr->d_router)
+    CU(launch_router_wgrad(x, false, d, dz, rt, rs, K, offs, active, hdr, segs, gr->d_router, s));
+  // experts: da = (dU W_down,e) * 2 relu(a);  dW_down,e += dU^T h;  dW_up,e += da^T x_e;  dx_e rows = da W_up,e
+  {
+    GemmArgs g = gemm_args(GM_ROWS, GE_RELU2_GRAD, at(B.dU), de, false, w->w_down, I, at(B.da), I, 0, I, de);
+    g.b_seg = (int64_t)de * I;
+    g.aux = P.at<bf16>(P.L.h);
+    g.aux_ld = I;
+    grouped(g);
+    CU(launch_gemm_bwd(g, segs, R, s));
+  }
+  if (gr->d_down) {
+    GemmArgs g = gemm_args(GM_KSEG, GE_ACC_F32, at(B.dU), de, true, P.at<void>(P.L.h), I, gr->d_down, I, de, I, 0);
+    g.c_seg = (int64_t)de * I;
+    grouped(g);
+    CU(launch_gemm_bwd(g, segs, 0, s));
+  }
+  if (gr->d_up) {
+    GemmArgs g = gemm_args(GM_KSEG, GE_ACC_F32, at(B.da), I, true, x_e, de, gr->d_up, de, I, de, 0);
+    g.c_seg = (int64_t)I * de;
+    g.b_gather = rt;
+    grouped(g);
+    CU(launch_gemm_bwd(g, segs, 0, s));
+  }
+  {
+    GemmArgs g = gemm_args(GM_ROWS, GE_STORE_F32, at(B.da), I, false, w->w_up, de, at(B.dxr), de, 0, de, I);
+    g.b_seg = (int64_t)I * de;
+    grouped(g);
+    CU(launch_gemm_bwd(g, segs, R, s));
+  }
+  // scatter-add of the routed rows' input gradients to their tokens, in
+  // ascending packed row (= expert) order (the combine's own order)
+  float* dxe = reinterpret_cast<float*>(at(B.dxe));
+  CU(launch_combine(reinterpret_cast<float*>(at(B.dxr)), tsr, T, K, de, dxe, latent ? at(B.dxl) : nullptr,
+                    MOE_DT_BF16, s));
+  const float* dx_expert = dxe;
+  if (latent) {
+    // dW_ld += dx_l^T x;  dx_latent = dx_l W_ld   (dx_l rounded to BF16 for the products)
+    if (gr->d_lat_down) {
+      GemmArgs gw = gemm_args(GM_KSEG, GE_ACC_F32, at(B.dxl), L, true, x, d, gr->d_lat_down, d, L, d, 0);
+      gw.dense_rows = T;
+      CU(launch_gemm_bwd(gw, 1, 0, s));
+    }
+    GemmArgs g = gemm_args(GM_ROWS, GE_STORE_F32, at(B.dxl), L, false, w->w_lat_down, d, at(B.dxa), d, 0, d, L);
+    g.dense_rows = T;
+    CU(launch_gemm_bwd(g, 1, T, s));
+    dx_expert = reinterpret_cast<float*>(at(B.dxa));
+  }
+  const float* dx_shared = nullptr;
+  if (shared) {
+    // da_s = (dy W_sd) * 2 relu(a_s);  dW_sd += dy^T h_s;  dW_su += da_s^T x;  dx_s = da_s W_su
+    GemmArgs g = gemm_args(GM_ROWS, GE_RELU2_GRAD, dy, d, false, w->w_sh_down, S, at(B.das), S, 0, S, d);
+    g.dense_rows = T;
+    g.aux = P.at<bf16>(P.L.hs);
+    g.aux_ld = S;
+    CU(launch_gemm_bwd(g, 1, T, s));
+    if (gr->d_sh_down) {
+      GemmArgs gw = gemm_args(GM_KSEG, GE_ACC_F32, dy, d, true, P.at<void>(P.L.hs), S, gr->d_sh_down, S, d, S, 0);
+      gw.dense_rows = T;
+      CU(launch_gemm_bwd(gw, 1, 0, s));
+    }
+    if (gr->d_sh_up) {
+      GemmArgs gw = gemm_args(GM_KSEG, GE_ACC_F32, at(B.das), S, true, x, d, gr->d_sh_up, d, S, d, 0);
+      gw.dense_rows = T;
+      CU(launch_gemm_bwd(gw, 1, 0, s));
+    }
+    GemmArgs g2 = gemm_args(GM_ROWS, GE_STORE_F32, at(B.das), S, false, w->w_sh_up, d, at(B.dxs), d, 0, d, S);
+    g2.dense_rows = T;
+    CU(launch_gemm_bwd(g2, 1, T, s));
+    dx_shared = reinterpret_cast<float*>(at(B.dxs));
+  }
+  // dx = router path + expert path + shared path
+  CU(launch_input_grad(dz, ids, T, K, w->w_router, d, dx_expert, dx_shared, dx, s));
+  return MOE_OK;
+}
+
 }  // namespace
 
 // ============================================================================
@@ -789,6 +971,73 @@ moe_status_t moe_block_forward(const moe_config_t* cfg, int32_t T, const void* x
   void* xn = x_norm_out ? x_norm_out : P.at<void>(P.L.xn);
   CU(launch_rmsnorm(x, norm_w, norm_eps, T, cfg->d_model, cfg->act_dtype, xn, P.hdr(), (int)sizeof(WsHeader), s));
   return run_layer(cfg, T, xn, x, w, out, topk_ids_out, topk_w_out, logits_out, scores_out, P, s);
+}
+
+size_t moe_backward_workspace_bytes(const moe_config_t* cfg, int32_t T) {
+  if (check_config(cfg) != MOE_OK || T < 0) return 0;
+  return make_bw_layout(cfg, T).total;
+}
+
+moe_status_t moe_backward_workspace_region(const moe_config_t* cfg, int32_t T, int32_t region, size_t* offset,
+                                           size_t* bytes) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (T < 0 || !offset || !bytes) return MOE_ERR_INVALID_ARG;
+  const BwLayout B = make_bw_layout(cfg, T);
+  const size_t t = (size_t)T, R = t * cfg->top_k, de = de_of(cfg), I = cfg->d_expert;
+  size_t o = 0, n = 0;
+  switch (region) {
+    case MOE_BWS_DU: o = B.dU; n = R * de * 2; break;
+    case MOE_BWS_DA: o = B.da; n = R * I * 2; break;
+    case MOE_BWS_DZ: o = B.dz; n = R * 4; break;
+    case MOE_BWS_DX_LATENT: o = B.dxl; n = cfg->d_latent ? t * cfg->d_latent * 2 : 0; break;
+    case MOE_BWS_DA_SHARED: o = B.das; n = t * (size_t)cfg->d_shared * 2; break;
+    case MOE_BWS_DY_LATENT: o = B.dyr; n = cfg->d_latent ? t * cfg->d_latent * 2 : 0; break;
+    default: return MOE_ERR_INVALID_ARG;
+  }
+  *offset = o;
+  *bytes = n;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_backward(const moe_config_t* cfg, int32_t T, const void* x, const moe_weights_t* w,
+                                const void* dy, const int32_t* topk_ids, const float* topk_w, const float* scores,
+                                float* dx, const moe_grads_t* grads, const void* ws, size_t ws_bytes, void* bws,
+                                size_t bws_bytes, void* stream) {
+  moe_status_t st = check_backward(cfg, T, ws, ws_bytes, bws, bws_bytes);
+  if (st != MOE_OK || T == 0) return st;
+  if ((st = check_weights(cfg, w, true, true, true)) != MOE_OK) return st;
+  if (!grads) return MOE_ERR_INVALID_ARG;
+  REQ(x); REQ(dy); REQ(topk_ids); REQ(topk_w); REQ(scores); REQ(dx);
+  OPT(grads->d_router); OPT(grads->d_lat_down); OPT(grads->d_lat_up); OPT(grads->d_up); OPT(grads->d_down);
+  OPT(grads->d_sh_up); OPT(grads->d_sh_down);
+  Ptrs P{(char*)const_cast<void*>(ws), make_layout(cfg, T)};
+  return run_backward(cfg, T, x, w, dy, topk_ids, topk_w, scores, dx, grads, P, (char*)bws, (cudaStream_t)stream);
+}
+
+moe_status_t moe_block_backward(const moe_config_t* cfg, int32_t T, const void* x, const float* norm_w,
+                                float norm_eps, const void* x_norm, const moe_weights_t* w, const void* dout,
+                                const int32_t* topk_ids,
+                                const float* topk_w, const float* scores, float* dx, const moe_grads_t* grads,
+                                const void* ws, size_t ws_bytes, void* bws, size_t bws_bytes, void* stream) {
+  moe_status_t st = check_backward(cfg, T, ws, ws_bytes, bws, bws_bytes);
+  if (st != MOE_OK || T == 0) return st;
+  if ((st = check_weights(cfg, w, true, true, true)) != MOE_OK) return st;
+  if (!grads) return MOE_ERR_INVALID_ARG;
+  REQ(x); REQ(norm_w); REQ(dout); REQ(topk_ids); REQ(topk_w); REQ(scores); REQ(dx); OPT(x_norm);
+  OPT(grads->d_norm_w);
+  if (!std::isfinite(norm_eps) || norm_eps < 0.f) return MOE_ERR_INVALID_ARG;
+  Ptrs P{(char*)const_cast<void*>(ws), make_layout(cfg, T)};
+  const BwLayout B = make_bw_layout(cfg, T);
+  char* b = (char*)bws;
+  cudaStream_t s = (cudaStream_t)stream;
+  float* dxn = reinterpret_cast<float*>(b + B.dxn);
+  // the layer read the normalised rows the block's forward wrote (x_norm_out, or the workspace)
+  const void* xn = x_norm ? x_norm : P.at<void>(P.L.xn);
+  if ((st = run_backward(cfg, T, xn, w, dout, topk_ids, topk_w, scores, dxn, grads, P, b, s)) != MOE_OK) return st;
+  CU(launch_rmsnorm_bwd(x, norm_w, norm_eps, T, cfg->d_model, dout, dxn, dx, reinterpret_cast<float*>(b + B.xr),
+                        grads->d_norm_w, s));
+  return MOE_OK;
 }
 
 moe_status_t moe_get_device_error(const void* ws, void* stream, int32_t* code) {

@@ -235,6 +235,63 @@ cudaError_t launch_sparse_down(const GemvArgs& a, bool nvfp4, int segs, cudaStre
 cudaError_t launch_sparse_down_layout(const void* w, const uint8_t* sf, int E, int de, int I, bool nvfp4, void* out,
                                       void* out_sf, cudaStream_t s);
 
+// ---- backward -------------------------------------------------------------
+// Grouped BF16 GEMM of the backward, C[m, n] = sum_k A[m, k] B[k, n], FP32
+// accumulation.  GM_ROWS: the rows of expert segment e (offsets / active /
+// hdr, or dense_rows rows when offsets is NULL) times B + e * b_seg (K = K);
+// GM_KSEG: C + e * c_seg [M, N] from K = the segment's rows.  A is [m][k]
+// (a_t = false; a_gather maps m to an A row) or [k][m] (a_t = true); B is
+// [k][n] (b_gather maps k to a B row).  Dimensions: N % 8 == 0; GM_ROWS:
+// K % 32 == 0; GM_KSEG: M % 8 == 0.
+enum { GM_ROWS = 0, GM_KSEG = 1 };
+enum {
+  GE_ACC_F32 = 0,      // C (f32) += acc
+  GE_STORE_F32 = 1,    // C (f32) = acc
+  GE_STORE_BF16 = 2,   // C (bf16) = bf16(acc)
+  GE_RELU2_GRAD = 3    // C (bf16) = bf16(acc * 2 sqrt(aux)), aux: BF16 h = relu(a)^2 at [m][n]
+};
+struct GemmArgs {
+  int mode, epi;
+  const bf16* A;
+  int64_t lda;
+  bool a_t;
+  const int32_t* a_gather;
+  const bf16* B;
+  int64_t ldb, b_seg;
+  const int32_t* b_gather;
+  void* C;
+  int64_t ldc, c_seg;
+  int M, N, K;
+  const int32_t* offsets;
+  const int32_t* active;
+  const WsHeader* hdr;
+  int dense_rows;
+  const bf16* aux;
+  int64_t aux_ld;
+  const int32_t* tprefix;   // GM_ROWS over segments: 64-row tile prefix (launch_tile_scan)
+};
+// segs: active segments launched (1 for a dense product); rows: all rows
+// (GM_ROWS: the sum over segments, or the dense rows)
+cudaError_t launch_gemm_bwd(const GemmArgs& g, int segs, int rows, cudaStream_t s);
+cudaError_t launch_tile_scan(const int32_t* offsets, const int32_t* active, const WsHeader* hdr, int32_t* tprefix,
+                             cudaStream_t s);
+// combine backward: packed row r = (t, k): dU[r] = bf16(w_tk dy[t]), q[t, k] = <dy[t], u[r]> / w_tk
+cudaError_t launch_combine_bwd(const void* dy, int64_t dy_ld, const float* u, const int32_t* rt, const int32_t* rs,
+                               const float* topw, int R, int K, int de, void* dU, float* q, cudaStream_t s);
+// gate backward: dz[t, k] from q and the chosen scores
+cudaError_t launch_gate_bwd(const float* scores, const int32_t* ids, const float* q, int T, int E, int K, int norm,
+                            float rsf, float* dz, cudaStream_t s);
+// dW_r[e] += sum over expert e's packed rows of dz x[token]
+cudaError_t launch_router_wgrad(const void* x, bool x_f32, int d, const float* dz, const int32_t* rt,
+                                const int32_t* rs, int K, const int32_t* offsets, const int32_t* active,
+                                const WsHeader* hdr, int segs, float* dW, cudaStream_t s);
+// dx[t] = sum_k dz_tk W_r[id_tk] + a[t] + b[t]
+cudaError_t launch_input_grad(const float* dz, const int32_t* ids, int T, int K, const float* w_router, int d,
+                              const float* a, const float* b, float* dx, cudaStream_t s);
+// RMSNorm backward of the block (BF16 x and dout): dx, and dgamma += (if not NULL)
+cudaError_t launch_rmsnorm_bwd(const void* x, const float* gamma, float eps, int T, int d, const void* dout,
+                               const float* dxn, float* dx, float* xr, float* dgamma, cudaStream_t s);
+
 // RMSNorm prologue of a block: xn[t] = act(gamma * (x[t] / sqrt(mean(x[t]^2) + eps)))
 // in FP32 (x, xn: act dtype [T, d]; gamma: f32 [d]); block 0 also clears the
 // workspace header `hdr` (bytes), so that it replaces the step's header memset

@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kSpThreads) sparse_down_bf16_kernel(const Gemv
 // the scales of its two rows in each tile.  E2M1 x E4M3 products are exact in
 // FP16; the MMA accumulates in FP32 and the per-tensor scale multiplies the
 // FP32 sum.
-__global__ void __launch_bounds__(kSpThreads) sparse_down_nvfp4_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(kSpThreads, 3) sparse_down_nvfp4_kernel(const GemvArgs a) {
   pdl_wait();
   __shared__ int list[kSpMaxGroups];
   __shared__ int wc[kSpWarps];

@@ -214,6 +214,55 @@ def moe_block_forward(cfg, x, norm_w, norm_eps: float, weights: Weights, out, ws
             "moe_block_forward")
 
 
+GRAD_FIELDS = ("d_router", "d_lat_down", "d_lat_up", "d_up", "d_down", "d_sh_up", "d_sh_down", "d_norm_w")
+
+
+def _grads(grads: Optional[Dict[str, torch.Tensor]]) -> N.MoeGrads:
+    grads = grads or {}
+    for k in grads:
+        if k not in GRAD_FIELDS:
+            raise KeyError(f"unknown gradient {k}")
+    return N.MoeGrads(**{f: _p(grads.get(f)) for f in GRAD_FIELDS})
+
+
+def backward_workspace_bytes(cfg, T: int) -> int:
+    return int(N.load().moe_backward_workspace_bytes(ctypes.byref(cfg), T))
+
+
+def backward_workspace_region(cfg, T: int, region: int):
+    """(byte offset, bytes) of a region of the backward scratch (MOE_BWS_*)."""
+    off, nb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    N.check(N.load().moe_backward_workspace_region(ctypes.byref(cfg), T, region, ctypes.byref(off),
+                                                   ctypes.byref(nb)), "moe_backward_workspace_region")
+    return int(off.value), int(nb.value)
+
+
+def new_backward_workspace(cfg, T: int, device="cuda") -> torch.Tensor:
+    return torch.empty(max(backward_workspace_bytes(cfg, T), 256), dtype=torch.uint8, device=device)
+
+
+def moe_layer_backward(cfg, x, weights: Weights, dy, ids, topw, scores, dx, grads, ws, bws, stream=None):
+    """dx (FP32) and weight gradients (added to the FP32 tensors in ``grads``,
+    keys from GRAD_FIELDS) of the forward whose state ``ws`` holds."""
+    w, n = _ws(ws)
+    b, nb = _ws(bws)
+    g = _grads(grads)
+    N.check(N.load().moe_layer_backward(ctypes.byref(cfg), x.shape[0], _p(x), weights.ref, _p(dy), _p(ids),
+                                        _p(topw), _p(scores), _p(dx), ctypes.byref(g), w, n, b, nb, _s(stream)),
+            "moe_layer_backward")
+
+
+def moe_block_backward(cfg, x, norm_w, norm_eps: float, weights: Weights, dout, ids, topw, scores, dx, grads, ws,
+                       bws, x_norm=None, stream=None):
+    w, n = _ws(ws)
+    b, nb = _ws(bws)
+    g = _grads(grads)
+    N.check(N.load().moe_block_backward(ctypes.byref(cfg), x.shape[0], _p(x), _p(norm_w), ctypes.c_float(norm_eps),
+                                        _p(x_norm), weights.ref, _p(dout), _p(ids), _p(topw), _p(scores), _p(dx),
+                                        ctypes.byref(g), w, n, b, nb, _s(stream)),
+            "moe_block_backward")
+
+
 def moe_layer_forward_host(cfg, x_host, x_dev, weights: Weights, y_dev, y_host, ws, stream=None):
     w, n = _ws(ws)
     N.check(N.load().moe_layer_forward_host(ctypes.byref(cfg), x_host.shape[0], _hp(x_host), _p(x_dev),

@@ -43,6 +43,10 @@ def test_struct_layout_matches_header(lib):
     members = re.findall(r"\*\s*(w_[a-z_]+|router_bias)\s*;", body)
     assert [f[0] for f in MoeWeights._fields_] == members
     assert ctypes.sizeof(MoeWeights) == len(members) * 8
+    from routed_relu_expert_gb300._native import MoeGrads
+    body = text[text.index("typedef struct moe_grads {"):text.index("} moe_grads_t;")]
+    members = re.findall(r"\*\s*(d_[a-z_]+)\s*;", body)
+    assert [f[0] for f in MoeGrads._fields_] == members
 
 
 def _cfg(**kw):
