@@ -60,6 +60,8 @@ def parse(argv=None):
     ap.add_argument("--points", default="all",
                     help="per_workload entries: all, none, or one workload name")
     ap.add_argument("--eager", action="store_true", help="time eager calls instead of CUDA-graph replays")
+    ap.add_argument("--no-backward", dest="backward", action="store_false",
+                    help="skip the backward timings")
     ap.add_argument("--no-blocks", dest="blocks", action="store_false",
                     help="skip the MoE-block chains (RMSNorm + layer + residual) at the verify shapes")
     ap.add_argument("--nvfp4-act-terms", type=int, default=-1,
@@ -535,6 +537,145 @@ def measure_point(run: Runner, shape, T, layers, warmup):
 VERIFY_ROWS = (1, 2, 4, 8, 16)   # verify-block shapes the block chain is timed at
 
 
+def dead_groups(run: Runner, shape, T, layer, x):
+    """(dead, total) (expert, 16-neuron group) pairs of one step of `layer` on
+    x: groups whose h values are zero in every row of the expert, the part of
+    W_down the ReLU^2-sparse down projection does not read."""
+    torch, M = run.torch, run.M
+    from routed_relu_expert_gb300 import _native as N
+    cfg = layer.cfg
+    layer.forward(x, torch.empty_like(x))
+    ws = layer.workspace(T, x.device)
+    R, I = T * shape.top_k, shape.d_expert
+
+    def region(r, dt):
+        off, nb = M.workspace_region(cfg, T, r)
+        return ws[off:off + nb].view(dt)
+    h = (region(N.MOE_WS_H, torch.int16).view(R, I).cpu().numpy() & 0x7FFF) != 0
+    offs = region(N.MOE_WS_OFFSETS, torch.int32).cpu().numpy()
+    dead = tot = 0
+    for e in range(shape.n_experts):
+        a, b = int(offs[e]), int(offs[e + 1])
+        if b > a:
+            live = h[a:b].reshape(b - a, I // 16, 16).any(axis=(0, 2))
+            dead += int((~live).sum())
+            tot += live.size
+    return dead, tot
+
+
+BACKWARD_POINTS = {"nano_decode": (64,), "nano_prefill": (2048, 8192), "super_latent": (256, 4096)}
+
+
+def backward_flops(shape, T: int) -> int:
+    """Algorithmic FLOPs of the backward: two products (input and weight
+    gradient) for each forward product of the experts, shared expert and
+    latent pair; the router's backward touches only the chosen logits
+    (2 T K d for dW_r and again for dx)."""
+    de, I, d, S, K = shape.d_e, shape.d_expert, shape.d_model, shape.d_shared, shape.top_k
+    fwd = K * 4 * de * I + 4 * d * S + 4 * d * shape.d_latent
+    return int(T * (2 * fwd + 4 * K * d))
+
+
+def measure_backward(run: Runner, shape, T, layers, pk):
+    """moe_layer_backward of one forward (its state in the workspace), timed as
+    CUDA-graph replays rotating the weight replicas; FLOPs / time against the
+    BF16 tensor peak."""
+    torch, M = run.torch, run.M
+    from synth import make_x
+    n = len(layers)
+    cfg = layers[0].cfg
+    x = make_x(shape, T, run.dev)
+    g = torch.Generator(device=run.dev)
+    g.manual_seed(77)
+    dy = torch.randn((T, shape.d_model), generator=g, device=run.dev).to(torch.bfloat16)
+    E, K = shape.n_experts, shape.top_k
+    states = []
+    for L in layers:
+        ws = M.new_workspace(cfg, T, run.dev)
+        L._ws = ws
+        st = {"ids": torch.empty((T, K), dtype=torch.int32, device=run.dev),
+              "topw": torch.empty((T, K), dtype=torch.float32, device=run.dev),
+              "scores": torch.empty((T, E), dtype=torch.float32, device=run.dev), "ws": ws}
+        L.forward(x, torch.empty_like(x), ids_out=st["ids"], topw_out=st["topw"], scores_out=st["scores"])
+        states.append(st)
+    z = lambda *sh: torch.zeros(sh, dtype=torch.float32, device=run.dev)
+    de, I, d, S, Ld = shape.d_e, shape.d_expert, shape.d_model, shape.d_shared, shape.d_latent
+    grads = {"d_router": z(E, d), "d_up": z(E, I, de), "d_down": z(E, de, I)}
+    if Ld:
+        grads["d_lat_down"], grads["d_lat_up"] = z(Ld, d), z(d, Ld)
+    if S:
+        grads["d_sh_up"], grads["d_sh_down"] = z(S, d), z(d, S)
+    dx = torch.empty((T, d), dtype=torch.float32, device=run.dev)
+    bws = M.new_backward_workspace(cfg, T, run.dev)
+
+    def call(i):
+        st = states[i % n]
+        M.moe_layer_backward(cfg, x, layers[i % n].weights, dy, st["ids"], st["topw"], st["scores"], dx, grads,
+                             st["ws"], bws)
+
+    for i in range(n):
+        call(i)
+    torch.cuda.synchronize()
+    graphs = []
+    c0 = M.load().moe_launch_count()
+    for i in range(n):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            call(i)
+        graphs.append(gr)
+    per = (M.load().moe_launch_count() - c0) // n
+
+    def fn(i):
+        graphs[i % n].replay()
+
+    for i in range(3):
+        fn(i)
+    K_ = run.steps_for(fn, target_ms=150.0, lo=10, hi=500)
+    ms = run.timed(fn, K_) / K_
+    fl = backward_flops(shape, T)
+    return {"ms_per_backward": round(ms, 5), "tokens_per_s": round(T / (ms / 1e3), 1), "timed_steps": K_,
+            "launches_per_backward": int(per), "algorithmic_flops": fl,
+            "tflops": round(fl / (ms / 1e3) / 1e12, 2),
+            "tensor_frac_bf16_burst": round(fl / (ms / 1e3) / 1e12 / pk["bf16_tflops"], 4),
+            "kernel": "gemm_bwd_kernel (mma.sync m16n8k16, 64x64x32 tiles)"}
+
+
+def measure_sparse_point(run: Runner, shape, T, layers, pk):
+    """The layer with the plain and with the group-major (ReLU^2-sparse) down
+    weights at one decode size: step times, the dead-group fraction, the bytes
+    the sparse step reads, and the down product alone (moe_experts_down)."""
+    torch, M = run.torch, run.M
+    from synth import make_x
+    dense = measure_point(run, shape, T, layers, 3)
+    saved = [L.weights for L in layers]
+    for L in layers:
+        L.enable_sparse_down()
+    try:
+        sparse = measure_point(run, shape, T, layers, 3)
+        x = make_x(shape, T, run.dev)
+        dead, tot = dead_groups(run, shape, T, layers[0], x)
+        prods = {}
+        if shape.expert_dtype != 2:
+            sp = measure_products(run, shape, T, layers, x, dense["n_active"], pk)["down"]
+            for L, w in zip(layers, saved):
+                L.weights = w
+            dp = measure_products(run, shape, T, layers, x, dense["n_active"], pk)["down"]
+            prods = {"down_dense_ms": round(dp["ms"], 5), "down_sparse_ms": round(sp["ms"], 5)}
+    finally:
+        for L, w in zip(layers, saved):
+            L.weights = w
+    elt = 0.5 + 1.0 / 16 if shape.expert_dtype == 2 else 2.0
+    skipped = dead * shape.d_e * 16 * elt
+    led = layer_bytes(shape, dense["n_active"], T)
+    read = led["total"] - skipped
+    return {"ms_dense": round(dense["ms"], 5), "ms_sparse": round(sparse["ms"], 5),
+            "speedup": round(dense["ms"] / sparse["ms"], 3), "dead_group_frac": round(dead / max(tot, 1), 4),
+            "experts_active": dense["n_active"], "bytes_dense": int(led["total"]), "bytes_read_sparse": int(read),
+            "hbm_frac_dense_bytes": round(led["total"] / (sparse["ms"] / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+            "hbm_frac_bytes_read": round(read / (sparse["ms"] / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+            "launches_per_step": sparse["launches_per_step"], "device_error_word": sparse["err"], **prods}
+
+
 def measure_block_chain(run: Runner, shape, T, layers, warmup):
     """The MoE block (RMSNorm, layer, residual) chained over the weight
     replicas: block r reads block r-1's output, all captured in one CUDA graph;
@@ -627,7 +768,8 @@ def run_ours(args, rank, world, dev):
     # every workload at every token count it is defined for
     per_workload, pw_clocks = {}, None
     if args.points != "none":
-        names = [n for n in ("tiny_fp32", "nano_decode", "nano_prefill", "super_latent", "super_nvfp4")
+        names = [n for n in ("tiny_fp32", "nano_decode", "nano_prefill", "super_latent", "super_nvfp4",
+                             "nano_decode_relu_sparse", "super_nvfp4_relu_sparse")
                  if args.points in ("all", n)]
         sampler = ClockSampler(torch.cuda.current_device() if not os.environ.get("CUDA_VISIBLE_DEVICES") else 0)
         sampler.start()
@@ -640,6 +782,12 @@ def run_ours(args, rank, world, dev):
                 lay = None
                 torch.cuda.empty_cache()
                 lay = run.layers(sh, need)[1]
+            if sh.relu_sparsity > 0:
+                # ReLU^2-sparse decode: the same layer with plain and with group-major down weights
+                for Ts in sh.tokens:
+                    per_workload[f"{name} T={Ts}"] = measure_sparse_point(run, sh, Ts, lay, pk)
+                del lay
+                continue
             for Ts in sh.tokens:
                 p = measure_point(run, sh, Ts, lay, 3)
                 entry = {"ms_per_step": round(p["ms"], 5), "tokens_per_s": round(Ts / (p["ms"] / 1e3), 1),
@@ -648,6 +796,9 @@ def run_ours(args, rank, world, dev):
                 entry.update(roofline_fractions(sh, Ts, p["n_active"], p["ms"], pk))
                 entry["routing"] = p["routing"]
                 per_workload[f"{name} T={Ts}"] = entry
+            if args.backward:
+                for Ts in BACKWARD_POINTS.get(name, ()):
+                    per_workload[f"{name} backward T={Ts}"] = measure_backward(run, sh, Ts, lay, pk)
             if name in ("nano_decode", "super_latent", "super_nvfp4") and args.blocks:
                 # the MoE block (RMSNorm + layer + residual) at the verify shapes,
                 # a chain of blocks with independent weights in one graph
