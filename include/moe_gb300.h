@@ -71,7 +71,12 @@ enum {
   MOE_DEVERR_EXPERT_ID = 1,      /* an expert id outside [0, n_experts) reached dispatch */
   MOE_DEVERR_NONFINITE = 2,      /* a router score was NaN (ranked last, never chosen before a finite one) */
   MOE_DEVERR_SCHEDULE = 4,       /* a tile schedule disagreed with the dispatch offsets */
-  MOE_DEVERR_TIMEOUT = 8         /* a kernel's bounded wait expired; that kernel stopped early */
+  MOE_DEVERR_TIMEOUT = 8,        /* a kernel's bounded wait expired; that kernel stopped early */
+  MOE_DEVERR_RANGE = 16          /* NVFP4 experts on the FP16 path (one token, or above 64): a value
+                                    beyond FP16's range (|v| > 65504) reached an FP16 operand (expert
+                                    input row or h); the affected outputs are not finite.  The FP4
+                                    tensor path (2..64 tokens) carries each row's magnitude in its
+                                    FP32 row scale and has no such limit */
 };
 
 typedef int32_t moe_dtype_t;

@@ -13,7 +13,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "libmoe_gb300.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(6)
-MOE_DEVERR_EXPERT_ID, MOE_DEVERR_NONFINITE, MOE_DEVERR_SCHEDULE, MOE_DEVERR_TIMEOUT = 1, 2, 4, 8
+MOE_DEVERR_EXPERT_ID, MOE_DEVERR_NONFINITE, MOE_DEVERR_SCHEDULE, MOE_DEVERR_TIMEOUT, MOE_DEVERR_RANGE = 1, 2, 4, 8, 16
 MOE_DT_F32, MOE_DT_BF16, MOE_DT_NVFP4 = 0, 1, 2
 MOE_NOALLOC_MAX_ROUTER_ELEMS = 131072
 MOE_NOALLOC_MAX_SPLIT_ELEMS = 7340032

@@ -267,7 +267,7 @@ moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x
       // the tensor-core kernel reads contiguous rows: gather them into the
       // workspace's packed-row region first
       void* xp = P.at<void>(P.L.x_packed);
-      CU(launch_pack_rows(x_e, rt, offsets, c->n_experts, (int)R, de, act_bytes(c), f16, xp, s));
+      CU(launch_pack_rows(x_e, rt, offsets, c->n_experts, (int)R, de, act_bytes(c), f16, xp, s, &P.hdr()->err));
       a.X = xp;
       a.gather = nullptr;
     }
@@ -512,7 +512,7 @@ moe_status_t run_layer(const moe_config_t* cfg, int32_t T, const void* x, const 
     CU(cudaEventRecord(aux->fork, s));
     CU(cudaStreamWaitEvent(aux->s, aux->fork, 0));
     if (latent && (st = run_latent_down(cfg, T, x, w, const_cast<void*>(x_e), aux->s)) != MOE_OK) return st;
-    if (conv) CU(launch_bf16_to_f16(x_e, (int64_t)T * de_of(cfg), x16, aux->s));
+    if (conv) CU(launch_bf16_to_f16(x_e, (int64_t)T * de_of(cfg), x16, aux->s, &P.hdr()->err));
     if (pre) CU(cudaEventRecord(aux->latent, aux->s));
     if (shared && (st = run_shared_to_f32(cfg, T, x, w, ys, P, aux->s)) != MOE_OK) return st;
     CU(cudaEventRecord(aux->join, aux->s));

@@ -52,6 +52,10 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
                : "l"(p));
   return r;
 }
+__device__ __forceinline__ float4 ldg_stream_f4(const float* p) {
+  const uint4 q = ldg_stream(p);
+  return make_float4(__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z), __uint_as_float(q.w));
+}
 
 // 16-byte load of reused data (activations): cached normally.
 __device__ __forceinline__ uint4 ldg_keep(const void* p) {

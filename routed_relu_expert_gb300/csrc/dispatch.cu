@@ -108,7 +108,7 @@ template <bool TO_F16>
 __global__ void __launch_bounds__(256) pack_rows_kernel(const uint4* __restrict__ x_e,
                                                         const int32_t* __restrict__ route_token,
                                                         const int32_t* __restrict__ offsets, int E, int row_vecs,
-                                                        uint4* __restrict__ x_packed) {
+                                                        uint4* __restrict__ x_packed, int32_t* __restrict__ err) {
   pdl_wait();
   const int R = offsets[E];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -124,9 +124,11 @@ __global__ void __launch_bounds__(256) pack_rows_kernel(const uint4* __restrict_
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (v0 + 32 * u >= row_vecs) continue;
-        if (TO_F16)
+        if (TO_F16) {
+          if (err && bf16x4_beyond_f16(q[u])) set_error(err, MOE_DEVERR_RANGE);
           q[u] = make_uint4(bf16x2_to_f16x2(q[u].x), bf16x2_to_f16x2(q[u].y), bf16x2_to_f16x2(q[u].z),
                             bf16x2_to_f16x2(q[u].w));
+        }
         dst[v0 + 32 * u] = q[u];
       }
     }
@@ -352,19 +354,19 @@ PerDeviceOnce g_attr_single, g_attr_multi;
 cudaError_t launch_pack(const DispatchArgs& a, cudaStream_t s) {
   if (!a.x_packed || !a.x_e) return cudaSuccess;
   return launch_pack_rows(a.x_e, a.route_token, a.offsets, a.E, a.T * a.K, a.de, a.elem_bytes, a.pack_f16,
-                          a.x_packed, s);
+                          a.x_packed, s, &a.hdr->err);
 }
 
 }  // namespace
 
 cudaError_t launch_pack_rows(const void* x_e, const int32_t* route_token, const int32_t* offsets, int E, int R,
-                             int de, int elem_bytes, bool to_f16, void* x_packed, cudaStream_t s) {
+                             int de, int elem_bytes, bool to_f16, void* x_packed, cudaStream_t s, int32_t* err) {
   if (R <= 0) return cudaSuccess;
   if ((to_f16 && elem_bytes != 2) || (de * elem_bytes) % 16) return cudaErrorNotSupported;
   const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(R, 8), 16384);
   launch_k(to_f16 ? pack_rows_kernel<true> : pack_rows_kernel<false>, grid, 256, 0, s,
            reinterpret_cast<const uint4*>(x_e), route_token, offsets, E, de * elem_bytes / 16,
-           reinterpret_cast<uint4*>(x_packed));
+           reinterpret_cast<uint4*>(x_packed), err);
   return cudaGetLastError();
 }
 

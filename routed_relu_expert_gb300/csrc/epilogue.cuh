@@ -80,8 +80,9 @@ __device__ __forceinline__ void epilogue_pre(const GemvArgs& a, int row, int f, 
 // inside FP16's range), for a consumer that multiplies in FP16.
 template <int EPI>
 __device__ __forceinline__ void epilogue_pre_f16(const GemvArgs& a, int row, int f, float v, float gs, float wr) {
-  const float r = epi_value<EPI, false>(a, row, f, v * gs, wr);
-  reinterpret_cast<__half*>(a.out)[(int64_t)row * a.out_ld + f] = __float2half_rn(round_bf16(r));
+  const float r = round_bf16(epi_value<EPI, false>(a, row, f, v * gs, wr));
+  if (!(fabsf(r) <= 65504.f) && a.err) set_error(a.err, MOE_DEVERR_RANGE);
+  reinterpret_cast<__half*>(a.out)[(int64_t)row * a.out_ld + f] = __float2half_rn(r);
 }
 
 // routing weight of packed row `row` (EPI_SCALE)

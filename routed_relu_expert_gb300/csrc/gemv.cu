@@ -563,12 +563,14 @@ cudaError_t bulk_attr() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmemMax);
 }
 
-// FP16 copy of BF16 activations, 8 values per thread
-__global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* x, int64_t n8, uint4* out) {
+// FP16 copy of BF16 activations, 8 values per thread; a value beyond FP16's
+// range sets MOE_DEVERR_RANGE
+__global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* x, int64_t n8, uint4* out, int32_t* err) {
   pdl_wait();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n8) return;
   const uint4 v = x[i];
+  if (err && bf16x4_beyond_f16(v)) set_error(err, MOE_DEVERR_RANGE);
   out[i] = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
 }
 
@@ -593,11 +595,11 @@ bool gemv_nvfp4_streams(const GemvArgs& a) {
          !(reinterpret_cast<uintptr_t>(a.W) & 15) && !(reinterpret_cast<uintptr_t>(a.W_sf) & 15);
 }
 
-cudaError_t launch_bf16_to_f16(const void* x, int64_t n, void* out, cudaStream_t s) {
+cudaError_t launch_bf16_to_f16(const void* x, int64_t n, void* out, cudaStream_t s, int32_t* err) {
   if (n <= 0) return cudaSuccess;
   const int64_t v = n / 8;
   launch_k(bf16_to_f16_kernel, dim3((unsigned)ceil_div(v, 256)), 256, 0, s, reinterpret_cast<const uint4*>(x), v,
-           reinterpret_cast<uint4*>(out));
+           reinterpret_cast<uint4*>(out), err);
   return cudaGetLastError();
 }
 

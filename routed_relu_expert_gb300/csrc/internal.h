@@ -113,7 +113,8 @@ cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int act, int epi, bool out_
 bool gemv_nvfp4_streams(const GemvArgs& a);
 
 // out[i] = FP16(x[i]) for n BF16 values (n a multiple of 8, 16-byte aligned)
-cudaError_t launch_bf16_to_f16(const void* x, int64_t n, void* out, cudaStream_t s);
+// (err: MOE_DEVERR_RANGE is set there when a value is beyond FP16's range)
+cudaError_t launch_bf16_to_f16(const void* x, int64_t n, void* out, cudaStream_t s, int32_t* err);
 
 // Tensor-core grouped GEMM (tcgen05): same arguments as launch_gemv; X rows must
 // be contiguous (no gather).  w_rows/x_rows: rows of the W and X matrices (TMA
@@ -193,7 +194,8 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
 // x_packed[j] = x_e[route_token[j]] for the offsets[E] <= R packed rows (rows
 // of de elements of elem_bytes; to_f16: BF16 rows stored as FP16 copies)
 cudaError_t launch_pack_rows(const void* x_e, const int32_t* route_token, const int32_t* offsets, int E, int R,
-                             int de, int elem_bytes, bool to_f16, void* x_packed, cudaStream_t s);
+                             int de, int elem_bytes, bool to_f16, void* x_packed, cudaStream_t s,
+                             int32_t* err = nullptr);
 
 // selection arguments (see launch_router_select)
 struct SelectArgs {

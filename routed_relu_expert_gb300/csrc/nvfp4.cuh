@@ -25,6 +25,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t s16) {
   return r;
 }
 
+// true if either BF16 value of the pair is beyond FP16's range (a BF16
+// magnitude of at least 65536, infinity or NaN: the BF16 values below it end
+// at 65280, inside FP16's 65504)
+__device__ __forceinline__ bool bf16x2_beyond_f16(uint32_t v) {
+  return (v & 0x7FFFu) >= 0x4780u || ((v >> 16) & 0x7FFFu) >= 0x4780u;
+}
+__device__ __forceinline__ bool bf16x4_beyond_f16(uint4 q) {
+  return bf16x2_beyond_f16(q.x) || bf16x2_beyond_f16(q.y) || bf16x2_beyond_f16(q.z) || bf16x2_beyond_f16(q.w);
+}
+
 // BF16 pair -> FP16 pair (exact inside FP16's range)
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));

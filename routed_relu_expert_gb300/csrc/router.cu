@@ -206,6 +206,92 @@ cudaError_t launch_small_t(const void* x, int act, int T, int d, const float* w,
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// logits, 5..64 tokens of a wide router (E >= 256): a CTA computes 16 experts x
+// TT tokens.  Each 256-wide K chunk of its TT token rows is staged in shared
+// memory (FP32) once for all 8 warps; a warp owns 2 experts, a lane 4 + 4
+// values of each chunk (k0 + 4l .. +3 and k0 + 128 + 4l .. +3, conflict-free
+// 16-byte reads), with 2 x TT FP32 partial sums in registers, added across
+// the lanes by a fixed shuffle tree at the end.  The token rows are read from
+// L2 once per 16 experts instead of once per 2.
+// ---------------------------------------------------------------------------
+template <int TT, bool XF32>
+__global__ void __launch_bounds__(256) router_logits_wide(const void* __restrict__ X, int T, int d,
+                                                          const float* __restrict__ Wr, int E,
+                                                          float* __restrict__ logits) {
+  pdl_wait();
+  constexpr int KC = 256, EW = 2;
+  __shared__ __align__(16) float xs[TT][KC];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int eb = blockIdx.x * 16 + warp * EW;
+  const int t0 = blockIdx.y * TT;
+  const int nt = min(TT, T - t0);
+  float acc[EW][TT];
+#pragma unroll
+  for (int i = 0; i < EW; ++i)
+#pragma unroll
+    for (int t = 0; t < TT; ++t) acc[i][t] = 0.f;
+  for (int k0 = 0; k0 < d; k0 += KC) {
+    __syncthreads();                        // the previous chunk has been read
+    for (int i = threadIdx.x; i < TT * KC / 4; i += 256) {
+      const int r = i / (KC / 4), c4 = (i % (KC / 4)) * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r < nt && k0 + c4 < d) {
+        if (XF32) {
+          v = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(X) + (int64_t)(t0 + r) * d + k0 + c4);
+        } else {
+          const uint2 q = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(X) + (int64_t)(t0 + r) * d + k0 + c4);
+          v = make_float4(bf16_lo(q.x), bf16_hi(q.x), bf16_lo(q.y), bf16_hi(q.y));
+        }
+      }
+      *reinterpret_cast<float4*>(&xs[r][c4]) = v;
+    }
+    __syncthreads();
+    float4 wa[EW], wb[EW];
+#pragma unroll
+    for (int i = 0; i < EW; ++i) {
+      const int e = eb + i;
+      wa[i] = wb[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < E) {
+        const float* w = Wr + (int64_t)e * d + k0;
+        if (k0 + 4 * lane < d) wa[i] = ldg_stream_f4(w + 4 * lane);
+        if (k0 + 128 + 4 * lane < d) wb[i] = ldg_stream_f4(w + 128 + 4 * lane);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      const float4 xa = *reinterpret_cast<const float4*>(&xs[t][4 * lane]);
+      const float4 xb = *reinterpret_cast<const float4*>(&xs[t][128 + 4 * lane]);
+#pragma unroll
+      for (int i = 0; i < EW; ++i) {
+        float a = acc[i][t];
+        a = fmaf(wa[i].x, xa.x, a); a = fmaf(wa[i].y, xa.y, a); a = fmaf(wa[i].z, xa.z, a); a = fmaf(wa[i].w, xa.w, a);
+        a = fmaf(wb[i].x, xb.x, a); a = fmaf(wb[i].y, xb.y, a); a = fmaf(wb[i].z, xb.z, a); a = fmaf(wb[i].w, xb.w, a);
+        acc[i][t] = a;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < EW; ++i)
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      float v = acc[i][t];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane == 0 && t < nt && eb + i < E) logits[(int64_t)(t0 + t) * E + eb + i] = v;
+    }
+}
+
+template <int TT>
+cudaError_t launch_wide(const void* x, int act, int T, int d, const float* w, int E, float* logits, cudaStream_t s) {
+  const dim3 grid((unsigned)ceil_div(E, 16), (unsigned)ceil_div(T, TT));
+  if (act == MOE_DT_F32)
+    launch_k(router_logits_wide<TT, true>, grid, 256, 0, s, x, T, d, w, E, logits);
+  else
+    launch_k(router_logits_wide<TT, false>, grid, 256, 0, s, x, T, d, w, E, logits);
+  return cudaGetLastError();
+}
+
 template <int TMAX>
 cudaError_t launch_small(const void* x, int act, int T, int d, const float* w, int E, float* logits,
                          cudaStream_t s) {
@@ -242,6 +328,13 @@ cudaError_t launch_router_logits(const void* x, int act, int T, int d, const flo
     return launch_gemm_tc(a, EPI_STORE, true, E, T, 0, bn, s, d, ks);
   }
   if (T <= 4) return launch_small<4>(x, act, T, d, w_router, E, logits, s);
+  if (T <= 64 && E >= 256 && d % 8 == 0) {
+    // wide routers: token rows staged once per 16 experts; about four CTAs of
+    // tokens per 16 experts at every size
+    if (T <= 16) return launch_wide<4>(x, act, T, d, w_router, E, logits, s);
+    if (T <= 32) return launch_wide<8>(x, act, T, d, w_router, E, logits, s);
+    return launch_wide<16>(x, act, T, d, w_router, E, logits, s);
+  }
   if (T <= 64) return launch_small<8>(x, act, T, d, w_router, E, logits, s);
   dim3 grid((unsigned)ceil_div(T, 64), (unsigned)ceil_div(E, 64));
   if (act == MOE_DT_F32)

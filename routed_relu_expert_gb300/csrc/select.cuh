@@ -61,6 +61,111 @@ __device__ __forceinline__ void top2_merge(Top2& t, int span) {
   }
 }
 
+// Top-K of a warp's candidates for K > 8 (K <= 32), by selection instead of K
+// rounds of maxima: the ordering keys, as unsigned numbers (non-candidates 0,
+// every candidate at least 1), give the K-th largest key thr by a bitwise
+// search from the highest bit where the candidates differ (a warp-wide count of
+// keys >= a trial value per bit); the chosen are the keys above thr and, of
+// the keys equal to it, the lowest ids (values ascend in id across lanes and
+// within a lane); a chosen value's slot is the number of chosen values ahead of
+// it in (key descending, id ascending) order.  Same ids, slots and weights as
+// the rounds (the weight sum still runs in slot order).
+template <int P>
+__device__ __forceinline__ void topk_radix(const int (&key)[P], uint32_t cand, const float (&s)[P], int e0, int E,
+                                           int K, int norm, float rsf, int t, int32_t* __restrict__ ids,
+                                           float* __restrict__ wout, int warp, int lane) {
+  __shared__ uint32_t sel_key[32][32];
+  __shared__ int sel_e[32][32];
+  __shared__ float sel_s[32][32];
+  __shared__ float slot_s[32][32];
+  constexpr unsigned FULL = 0xffffffffu;
+  uint32_t uk[P];
+  uint32_t lmax = 0u, lmin = 0xffffffffu;
+#pragma unroll
+  for (int j = 0; j < P; ++j) {
+    const bool ok = ((cand >> j) & 1u) && e0 + j < E;
+    uk[j] = ok ? ((uint32_t)key[j] ^ 0x80000000u) : 0u;
+    if (ok) {
+      lmax = max(lmax, uk[j]);
+      lmin = min(lmin, uk[j]);
+    }
+  }
+  const uint32_t hi = __reduce_max_sync(FULL, lmax), lo = __reduce_min_sync(FULL, lmin);
+  // the K-th largest key lies in [lo, hi]: it shares their common high bits
+  const int top = hi == lo ? -1 : 31 - __clz(hi ^ lo);
+  uint32_t thr = top < 0 ? hi : (top == 31 ? 0u : (hi & ~((2u << top) - 1u)));
+  for (int b = top; b >= 0; --b) {
+    const uint32_t trial = thr | (1u << b);
+    int cnt = 0;
+#pragma unroll
+    for (int j = 0; j < P; ++j) cnt += uk[j] >= trial ? 1 : 0;
+    if (__reduce_add_sync(FULL, cnt) >= K) thr = trial;
+  }
+  int ngt = 0, neq = 0;
+#pragma unroll
+  for (int j = 0; j < P; ++j) {
+    ngt += uk[j] > thr ? 1 : 0;
+    neq += uk[j] == thr ? 1 : 0;
+  }
+  const int need = K - __reduce_add_sync(FULL, ngt);      // >= 1 keys equal to thr are taken
+  int pre = neq;                                          // equal keys in lower lanes
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(FULL, pre, off);
+    if (lane >= off) pre += v;
+  }
+  pre -= neq;
+  uint32_t take = 0u;
+  int nsel = 0;
+#pragma unroll
+  for (int j = 0; j < P; ++j) {
+    const bool eq = uk[j] == thr;
+    if (uk[j] > thr || (eq && pre < need)) {
+      take |= 1u << j;
+      ++nsel;
+    }
+    if (eq) ++pre;
+  }
+  int base = nsel;                                        // chosen values in lower lanes
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(FULL, base, off);
+    if (lane >= off) base += v;
+  }
+  base -= nsel;
+#pragma unroll
+  for (int j = 0; j < P; ++j) {
+    if ((take >> j) & 1u) {
+      sel_key[warp][base] = uk[j];
+      sel_e[warp][base] = e0 + j;
+      sel_s[warp][base] = s[j];
+      ++base;
+    }
+  }
+  __syncwarp();
+  int rank = 0, ei = 0;
+  float si = 0.f;
+  if (lane < K) {
+    const uint32_t ki = sel_key[warp][lane];
+    ei = sel_e[warp][lane];
+    si = sel_s[warp][lane];
+    for (int j = 0; j < K; ++j) {
+      const uint32_t kj = sel_key[warp][j];
+      rank += (kj > ki || (kj == ki && sel_e[warp][j] < ei)) ? 1 : 0;
+    }
+    slot_s[warp][rank] = si;
+  }
+  __syncwarp();
+  float wsum = 0.f;
+  for (int k = 0; k < K; ++k) wsum += slot_s[warp][k];   // slot order, FP32
+  if (lane < K) {
+    const float wv = norm ? (si / wsum) * rsf : si * rsf;
+    ids[(int64_t)t * K + rank] = ei;
+    wout[(int64_t)t * K + rank] = wv;
+  }
+  __syncwarp();          // the shared rows are reused by this warp's next token
+}
+
 // One token's selection, by one warp (lane = its lane, warp = its warp index in
 // the CTA).  logits: slab 0 of nparts slabs part_stride floats apart.
 template <int P>
@@ -78,11 +183,22 @@ __device__ __forceinline__ void select_token(const float* __restrict__ logits, i
   // every load first (logits, their K parts, the bias), then the arithmetic,
   // then the stores: interleaved, each store would order the next load behind it
   float zv[P], bv[P];
+  if (P % 4 == 0 && E == 32 * P) {
+    // every lane full: 16-byte loads (rows of E floats, E a multiple of 4)
 #pragma unroll
-  for (int j = 0; j < P; ++j) {
-    const int e = e0 + j;
-    zv[j] = e < E ? zrow[e] : 0.f;
-    bv[j] = (bias && e < E) ? bias[e] : 0.f;
+    for (int j = 0; j < P; j += 4) {
+      const float4 z4 = *reinterpret_cast<const float4*>(zrow + e0 + j);
+      zv[j] = z4.x; zv[j + 1] = z4.y; zv[j + 2] = z4.z; zv[j + 3] = z4.w;
+      const float4 b4 = bias ? *reinterpret_cast<const float4*>(bias + e0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      bv[j] = b4.x; bv[j + 1] = b4.y; bv[j + 2] = b4.z; bv[j + 3] = b4.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+      const int e = e0 + j;
+      zv[j] = e < E ? zrow[e] : 0.f;
+      bv[j] = (bias && e < E) ? bias[e] : 0.f;
+    }
   }
   for (int p = 1; p < nparts; ++p) {
 #pragma unroll
@@ -172,6 +288,11 @@ __device__ __forceinline__ void select_token(const float* __restrict__ logits, i
       for (int j = 0; j < P; ++j)
         if (e0 + j < E && ((kept >> ((e0 + j) / gsz)) & 1u)) cand |= 1u << j;
     }
+  }
+
+  if (K > 8) {
+    topk_radix<P>(key, cand, s, e0, E, K, norm, rsf, t, ids, wout, warp, lane);
+    return;
   }
 
   // top-K: every lane keeps the best of its remaining candidates; each round

@@ -298,6 +298,13 @@ __device__ __forceinline__ void tile_epilogue(const GemvArgs& a, const CUtensorM
       v[c] = u * u;
     }
   }
+  if (OUT16) {
+    // FP16 copies of the BF16 values: a value beyond FP16's range is flagged
+    bool over = false;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) over |= c < nc && !(fabsf(round_bf16(v[c])) <= 65504.f);
+    if (over && a.err) set_error(a.err, MOE_DEVERR_RANGE);
+  }
   if (out_map && nc == 32) {
     if (lane == 0) bulk_wait_read_all();   // the previous chunk's store has left the staging buffer
     __syncwarp();

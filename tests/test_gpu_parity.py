@@ -371,3 +371,67 @@ def test_out_of_range_ids_are_flagged_and_skipped():
     assert int(counts.sum()) == T * K - 2
     t = tsr.cpu().numpy()
     assert t[4, 1] == -1 and t[6, 0] == -1
+
+
+@pytest.mark.parametrize("T", [1, 9, 200])
+def test_nvfp4_rows_beyond_fp16_range(T):
+    """Expert input rows scaled by 2^16 (exact in BF16, beyond FP16's 65504):
+    the FP16 path (one token; above 64 tokens) flags MOE_DEVERR_RANGE instead
+    of returning silent infinities; the FP4 path (2..64 tokens) carries the
+    magnitude in each row's FP32 scale and still matches the oracle."""
+    from routed_relu_expert_gb300 import _native as N
+    shape = SMALL_NVFP4
+    w = device_weights(shape)
+    x = (make_x(shape, T, "cuda").float() * 65536.0).to(torch.bfloat16)
+    g = run_gpu(shape, w, x)
+    ws = g.pop("ws")
+    if M.nvfp4_act_terms_for(T) == 0:
+        assert g["err"] & N.MOE_DEVERR_RANGE, f"FP16 path at T={T} did not flag the range"
+        return
+    assert g["err"] == 0
+    g = to_np(g)
+    assert np.all(np.isfinite(g["y"]))
+    ow = oracle_weights(w)
+    x_np = x.float().cpu().numpy().astype(np.float64)
+    ids_o, w_o = check_router(shape, x_np, ow, g)
+    check_output(shape, x_np, ow, ids_o, w_o, g["y"], tol_of(shape))
+
+
+@pytest.mark.parametrize("T,groups", [(3, 1), (3, 8), (40, 1), (40, 8), (100, 8)])
+def test_topk_above_eight_with_exact_ties(T, groups):
+    """K = 12 of E = 256 (the selection-by-threshold path for K > 8): router
+    rows duplicated in pairs and a zero bias give exactly equal scores, so
+    every choice crosses ties; ids must match the oracle's selection (lower id
+    first) on the GPU's own scores, through the fused tiny kernel (T = 3) and
+    the per-token selection kernel."""
+    from synth import make_weights as mw
+    shape = scaled(NANO_DECODE, name=f"ties_{groups}", d_model=256, n_experts=256, top_k=12, n_group=groups,
+                   topk_group=4 if groups > 1 else 1, d_expert=128, d_shared=0, weight_seed=67, tokens=())
+    w = mw(shape, "cuda")
+    w["w_router"] = w["w_router"][0::2].repeat_interleave(2, dim=0).contiguous()
+    w["bias"] = torch.zeros_like(w["bias"])
+    x = make_x(shape, T, "cuda")
+    g = run_gpu(shape, w, x)
+    assert g["err"] == 0
+    g.pop("ws")
+    g = to_np(g)
+    ow = oracle_weights(w)
+    s = g["scores"]
+    assert np.array_equal(s[:, 0::2], s[:, 1::2])          # every score tied with its pair
+    check_router(shape, x.float().cpu().numpy().astype(np.float64), ow, g)
+
+
+@pytest.mark.parametrize("T", [5, 16, 17, 32, 33, 64])
+def test_wide_router_logits_every_tile_height(T):
+    """Routers with E >= 256 at 5..64 tokens compute their logits with token
+    rows staged per 16 experts (tiles of 4, 8 or 16 tokens): logits within
+    1e-5 of sum |x W|, ids and weights against the oracle on the GPU scores."""
+    shape = scaled(SUPER_LATENT, name="wide_router", d_model=1024, d_latent=256, n_experts=256, top_k=12,
+                   n_group=8, topk_group=4, d_expert=128, d_shared=0, weight_seed=71, tokens=())
+    w = device_weights(shape)
+    x = make_x(shape, T, "cuda")
+    g = run_gpu(shape, w, x)
+    assert g["err"] == 0
+    g.pop("ws")
+    g = to_np(g)
+    check_router(shape, x.float().cpu().numpy().astype(np.float64), oracle_weights(w), g)
