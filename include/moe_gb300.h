@@ -29,10 +29,15 @@
  *    synchronises (except moe_get_device_error and the _host convenience
  *    call).  Every call only enqueues work on `stream` (a cudaStream_t passed
  *    as void*; NULL = the legacy default stream) and returns.
- *    moe_layer_forward runs the shared expert on a library-owned auxiliary
- *    stream (one per device, created with two events on the first call),
- *    forked from and joined back to `stream` by events, so the layer is
- *    still ordered as one operation on `stream` (and capturable).
+ *    moe_layer_forward (and moe_block_forward) runs the latent down
+ *    projection and the shared expert on a library-owned auxiliary stream
+ *    (one per device, created with its events on the first call), forked
+ *    from and joined back to `stream` by events, so the layer is still
+ *    ordered as one operation on `stream`.  Calls from several host threads
+ *    take turns enqueuing (a per-device lock is held while a call enqueues),
+ *    and their auxiliary work runs one call after another on that one
+ *    stream: correct, but two layers on different caller streams overlap
+ *    only in their routed parts.
  *  - Row-major storage.  Weight matrices are stored [out, in] (the
  *    nn.Linear orientation, page "M6.1 ...", section 0x04A).
  *  - Every device pointer must be 16-byte aligned; every inner width

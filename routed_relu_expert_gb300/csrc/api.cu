@@ -517,7 +517,9 @@ moe_status_t run_layer(const moe_config_t* cfg, int32_t T, const void* x, const 
     if (shared && (st = run_shared_to_f32(cfg, T, x, w, ys, P, aux->s)) != MOE_OK) return st;
     CU(cudaEventRecord(aux->join, aux->s));
   }
-  aux_lock.unlock();
+  // the lock stays held until this call's waits on the fork/latent/join events
+  // are enqueued on the caller's stream (at return): another thread cannot
+  // re-record the events in between
   float* logits = logits_out ? logits_out : P.at<float>(P.L.logits);
   float* scores = scores_out ? scores_out : P.at<float>(P.L.scores);
   int32_t* ids = topk_ids_out ? topk_ids_out : P.at<int32_t>(P.L.ids);

@@ -300,10 +300,11 @@ __device__ __forceinline__ void tile_epilogue(const GemvArgs& a, const CUtensorM
   }
   if (OUT16) {
     // FP16 copies of the BF16 values: a value beyond FP16's range is flagged
-    bool over = false;
+    // (rounding is monotonic, so the rounded maximum decides)
+    float m = 0.f;
 #pragma unroll
-    for (int c = 0; c < 32; ++c) over |= c < nc && !(fabsf(round_bf16(v[c])) <= 65504.f);
-    if (over && a.err) set_error(a.err, MOE_DEVERR_RANGE);
+    for (int c = 0; c < 32; ++c) m = fmaxf(m, c < nc ? fabsf(v[c]) : 0.f);
+    if (round_bf16(m) > 65504.f && a.err) set_error(a.err, MOE_DEVERR_RANGE);
   }
   if (out_map && nc == 32) {
     if (lane == 0) bulk_wait_read_all();   // the previous chunk's store has left the staging buffer

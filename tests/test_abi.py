@@ -159,3 +159,52 @@ def test_workspace_regions_lie_inside_the_workspace(lib):
         off = ctypes.c_size_t(0)
         assert lib.moe_workspace_region(ctypes.byref(cfg), T, 99, ctypes.byref(off), ctypes.byref(off)) == \
             N.MOE_ERR_INVALID_ARG
+
+
+def test_block_sparse_and_backward_arguments_are_checked_before_any_work(lib):
+    """The block, sparse-down and backward entry points refuse bad arguments
+    and unsupported configurations on the host, before any CUDA call (these
+    addresses are never dereferenced)."""
+    from routed_relu_expert_gb300 import _native as N
+    c = _cfg()
+    n = lib.moe_workspace_bytes(ctypes.byref(c), 4)
+    nb = lib.moe_backward_workspace_bytes(ctypes.byref(c), 4)
+    assert n > 0 and nb > 0
+    ws, good = ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 21)
+    P = [ctypes.c_void_p((1 << 22) + 256 * i) for i in range(16)]
+    w = N.MoeWeights(w_router=P[0], w_up=P[1], w_down=P[2], w_sh_up=P[3], w_sh_down=P[4])
+    # block: a negative or non-finite epsilon, a missing norm weight, an output overlapping x
+    blk = lambda x, g, eps, out, xn=None: lib.moe_block_forward(ctypes.byref(c), 4, x, g, ctypes.c_float(eps),
+                                                               ctypes.byref(w), out, xn, None, None, None, None,
+                                                               ws, n, None)
+    assert blk(good, P[5], -1.0, P[6]) == N.MOE_ERR_INVALID_ARG
+    assert blk(good, P[5], float("nan"), P[6]) == N.MOE_ERR_INVALID_ARG
+    assert blk(good, None, 1e-5, P[6]) == N.MOE_ERR_INVALID_ARG
+    assert blk(good, P[5], 1e-5, ctypes.c_void_p((1 << 21) + 256)) == N.MOE_ERR_INVALID_ARG   # partial overlap
+    assert blk(good, P[5], 1e-5, P[6], good) == N.MOE_ERR_INVALID_ARG                          # xn is x
+    # sparse down: FP32 layers and unfit shapes are refused
+    v, s = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    f32 = _cfg(act_dtype=N.MOE_DT_F32, expert_dtype=N.MOE_DT_F32)
+    assert lib.moe_sparse_down_bytes(ctypes.byref(f32), ctypes.byref(v), ctypes.byref(s)) == N.MOE_ERR_UNSUPPORTED
+    assert lib.moe_sparse_down_bytes(ctypes.byref(c), ctypes.byref(v), ctypes.byref(s)) == N.MOE_OK
+    assert v.value == 8 * 256 * 128 * 2 and s.value == 0
+    fp4 = _cfg(expert_dtype=N.MOE_DT_NVFP4)
+    assert lib.moe_sparse_down_bytes(ctypes.byref(fp4), ctypes.byref(v), ctypes.byref(s)) == N.MOE_OK
+    assert v.value == 8 * 256 * 128 // 2 and s.value == 8 * 256 * 128 // 16
+    # backward: BF16 layers only, a big enough scratch, every saved tensor given
+    g = N.MoeGrads()
+    bwd = lambda cfg, ids, nbw: lib.moe_layer_backward(ctypes.byref(cfg), 4, good, ctypes.byref(w), P[7], ids, P[8],
+                                                       P[9], P[10], ctypes.byref(g), ws,
+                                                       lib.moe_workspace_bytes(ctypes.byref(cfg), 4), P[11], nbw,
+                                                       None)
+    assert bwd(fp4, P[12], 1 << 30) == N.MOE_ERR_UNSUPPORTED
+    assert bwd(c, P[12], nb - 1) == N.MOE_ERR_WORKSPACE
+    assert bwd(c, None, nb) == N.MOE_ERR_INVALID_ARG
+    # regions of the backward scratch lie inside it
+    for region in range(6):
+        off, nbytes = ctypes.c_size_t(0), ctypes.c_size_t(0)
+        assert lib.moe_backward_workspace_region(ctypes.byref(c), 4, region, ctypes.byref(off),
+                                                 ctypes.byref(nbytes)) == N.MOE_OK
+        assert off.value % 256 == 0 and off.value + nbytes.value <= nb
+    assert lib.moe_backward_workspace_region(ctypes.byref(c), 4, 6, ctypes.byref(off), ctypes.byref(nbytes)) == \
+        N.MOE_ERR_INVALID_ARG
