@@ -77,10 +77,10 @@ enum {
   MOE_DEVERR_NONFINITE = 2,      /* a router score was NaN (ranked last, never chosen before a finite one) */
   MOE_DEVERR_SCHEDULE = 4,       /* a tile schedule disagreed with the dispatch offsets */
   MOE_DEVERR_TIMEOUT = 8,        /* a kernel's bounded wait expired; that kernel stopped early */
-  MOE_DEVERR_RANGE = 16          /* NVFP4 experts on the FP16 path (one token, or above 64): a value
+  MOE_DEVERR_RANGE = 16          /* NVFP4 experts on the FP16 path (under 8 tokens, or above 64): a value
                                     beyond FP16's range (|v| > 65504) reached an FP16 operand (expert
                                     input row or h); the affected outputs are not finite.  The FP4
-                                    tensor path (2..64 tokens) carries each row's magnitude in its
+                                    tensor path (8..64 tokens) carries each row's magnitude in its
                                     FP32 row scale and has no such limit */
 };
 
@@ -379,7 +379,7 @@ moe_status_t moe_clear_device_error(void* ws, void* stream);
 
 /* How the activations of NVFP4 experts enter their products (process-wide;
  * applies to the calls made after it):
- *   n = -1    the default: three terms on the FP4 tensor path for 2 to 64
+ *   n = -1    the default: three terms on the FP4 tensor path for 8 to 64
  *             tokens, the FP16 path otherwise (the faster one at each size
  *             as measured on GB300)
  *   n = 1..4  the FP4 tensor path: every expert input row and every row of h

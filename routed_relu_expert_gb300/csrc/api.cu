@@ -28,13 +28,15 @@ inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // NVFP4 expert products: activation terms on the FP4 tensor path (1..4), 0
 // for the FP16 path (weights decoded to FP16 inside the kernels), or -1 for
-// the measured choice: kActTerms terms on the FP4 path from 2 to 64 tokens
+// the measured choice: kActTerms terms on the FP4 path from 8 to 64 tokens
 // (a grouped decode product there streams the weights at 70-85 % of HBM
-// against 45 % for the FP16 GEMV), the FP16 path for one token (where the
-// GEMV's shorter launch chain wins) and above 64 tokens (where quantising
-// every routed row and h into terms costs more than the FP4 products save)
+// against 45 % for the FP16 GEMV), the FP16 path below 8 tokens (where the
+// GEMV's shorter launch chain wins: Super NVFP4 layer 0.081 vs 0.090 ms at 1
+// token, 0.109 vs 0.115 ms at 4, equal at 8, 0.181 vs 0.207 ms at 16) and
+// above 64 tokens (where quantising every routed row and h into terms costs
+// more than the FP4 products save)
 std::atomic<int> g_act_terms{-1};
-constexpr int kFp4MinT = 2, kFp4MaxT = 64;
+constexpr int kFp4MinT = 8, kFp4MaxT = 64;
 
 // activation terms a layer of T tokens uses on the FP4 path (0: FP16 path)
 inline int act_terms_for(int T) {

@@ -78,7 +78,7 @@ SUPER_NVFP4 = replace(SUPER_LATENT, name="super_nvfp4", expert_dtype=NVFP4,
 NANO_DECODE_SPARSE = replace(NANO_DECODE, name="nano_decode_relu_sparse", relu_sparsity=0.925,
                              tokens=(1, 2, 4, 16, 64))
 SUPER_NVFP4_SPARSE = replace(SUPER_NVFP4, name="super_nvfp4_relu_sparse", relu_sparsity=0.925, zipf_s=0.0,
-                             tokens=(1, 2))
+                             tokens=(1, 2, 4))
 ROUTER_ONLY_GROUPED = MoEShape("router_only_grouped", 2688, 0, 128, 6, 8, 3, 1856, 3712, 2.5,
                                weight_seed=5, tokens=(64,))
 

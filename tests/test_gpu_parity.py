@@ -376,8 +376,8 @@ def test_out_of_range_ids_are_flagged_and_skipped():
 @pytest.mark.parametrize("T", [1, 9, 200])
 def test_nvfp4_rows_beyond_fp16_range(T):
     """Expert input rows scaled by 2^16 (exact in BF16, beyond FP16's 65504):
-    the FP16 path (one token; above 64 tokens) flags MOE_DEVERR_RANGE instead
-    of returning silent infinities; the FP4 path (2..64 tokens) carries the
+    the FP16 path (under 8 tokens; above 64 tokens) flags MOE_DEVERR_RANGE instead
+    of returning silent infinities; the FP4 path (8..64 tokens) carries the
     magnitude in each row's FP32 scale and still matches the oracle."""
     from routed_relu_expert_gb300 import _native as N
     shape = SMALL_NVFP4

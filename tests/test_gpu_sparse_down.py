@@ -117,10 +117,10 @@ def test_nano_sparse_decode(T):
     _sparse_parity(NANO_DECODE_SPARSE, T, min_dead=0.2 if T == 1 else None)
 
 
-@pytest.mark.parametrize("T", [1, 2])
+@pytest.mark.parametrize("T", [1, 2, 9])
 def test_super_nvfp4_sparse_decode(T):
-    # T = 1 runs the FP16 decode path (sparse down); T = 2 the FP4 tensor path
-    # (the group-major weights are present but that path does not use them)
+    # below 8 tokens the FP16 decode path runs the sparse down product; at 9
+    # the FP4 tensor path (the group-major weights are present but unused)
     _sparse_parity(SUPER_NVFP4_SPARSE, T, min_dead=0.2 if T == 1 else None)
 
 
