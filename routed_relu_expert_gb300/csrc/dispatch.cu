@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kTinyThreads) select_dispatch_tiny(const Selec
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp < a.T)
     select_token<P>(sa.logits, sa.nparts, sa.part_stride, sa.logits_out, warp, sa.E, sa.bias, sa.G, sa.TG, sa.K,
-                    sa.norm, sa.rsf, sa.scores, sa.ids, sa.w, sa.err, warp, lane);
+                    sa.norm, sa.rsf, sa.scores, sa.ids, sa.w, sa.err, warp, lane, a.T > 8);
   __syncthreads();                        // this CTA's id writes are visible to it
   const int R = a.T * a.K;
   const int r = threadIdx.x;

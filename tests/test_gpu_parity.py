@@ -423,9 +423,10 @@ def test_topk_above_eight_with_exact_ties(T, groups):
 
 @pytest.mark.parametrize("T", [5, 16, 17, 32, 33, 64])
 def test_wide_router_logits_every_tile_height(T):
-    """Routers with E >= 256 at 5..64 tokens compute their logits with token
-    rows staged per 16 experts (tiles of 4, 8 or 16 tokens): logits within
-    1e-5 of sum |x W|, ids and weights against the oracle on the GPU scores."""
+    """Routers with E >= 256 at 5..64 tokens: above 32 tokens the logits come
+    from token rows staged per 16 experts, below from the per-2-experts
+    kernel; logits within 1e-5 of sum |x W|, ids and weights against the
+    oracle on the GPU scores, on both sides of the switch."""
     shape = scaled(SUPER_LATENT, name="wide_router", d_model=1024, d_latent=256, n_experts=256, top_k=12,
                    n_group=8, topk_group=4, d_expert=128, d_shared=0, weight_seed=71, tokens=())
     w = device_weights(shape)
