@@ -150,9 +150,25 @@ inline bool use_tc(const moe_config_t* c, int T) {
   return c->act_dtype == MOE_DT_BF16 && c->expert_dtype != MOE_DT_F32 && T > kDecodeMaxT;
 }
 
+inline bool fp4_path(const moe_config_t* c, int T);
+
+// Dense products (shared expert, latent pair) run on the tensor cores above
+// 64 tokens, and from 32 tokens when the expert products themselves run on
+// the persistent FP4 kernels: at 32-64 rows the GEMV's 16-row passes are
+// issue-bound (a 44 MB Super shared product took 46 us), and with the expert
+// products on persistent kernels nothing overlaps them anyway (Super NVFP4
+// layer at 64 tokens 0.329 -> 0.293 ms).  Next to streaming expert GEMVs the
+// GEMV shared expert overlaps them and stays (Super BF16 at 64 tokens:
+// 0.877 ms with GEMVs, 1.034 ms with tensor-core dense products).
+constexpr int kDenseTcMinT = 32;
+inline bool dense_tc(const moe_config_t* c, int T) {
+  if (c->act_dtype != MOE_DT_BF16 || c->expert_dtype == MOE_DT_F32) return false;
+  return T > kDecodeMaxT || (T >= kDenseTcMinT && fp4_path(c, T));
+}
+
 // dense product out[T, N] = X[T, K] W[N, K]^T through the GEMV or the tensor cores
 cudaError_t run_dense(const moe_config_t* c, const GemvArgs& a, int epi, bool out_f32, int T, cudaStream_t s) {
-  if (use_tc(c, T))
+  if (dense_tc(c, T))
     return launch_gemm_tc(a, epi, out_f32, a.N, T, 0, tc_tile_rows(T, 1, a.N), s);
   return launch_gemv(a, dense_fmt(c), c->act_dtype, epi, out_f32, T, 1, s);
 }
@@ -247,7 +263,6 @@ moe_status_t run_up_fp4(const moe_config_t* c, int T, const void* x_e, const voi
 moe_status_t run_down_fp4(const moe_config_t* c, int T, const void* h, const int32_t* offsets, const int32_t* rt,
                           const int32_t* rs, const float* topw, const moe_weights_t* w, float* u, const Ptrs& P,
                           cudaStream_t s);
-inline bool fp4_path(const moe_config_t* c, int T);
 
 moe_status_t run_up(const moe_config_t* c, int T, const void* x_e, const void* x_packed, const int32_t* rt,
                     const int32_t* offsets, const moe_weights_t* w, void* h, const Ptrs& P, cudaStream_t s,
