@@ -207,7 +207,7 @@ cudaError_t launch_small_t(const void* x, int act, int T, int d, const float* w,
 }
 
 // ---------------------------------------------------------------------------
-// logits, 5..64 tokens of a wide router (E >= 256): a CTA computes 16 experts x
+// logits, 33..64 tokens of a wide router (E >= 256): a CTA computes 16 experts x
 // TT tokens.  Each 256-wide K chunk of its TT token rows is staged in shared
 // memory (FP32) once for all 8 warps; a warp owns 2 experts, a lane 4 + 4
 // values of each chunk (k0 + 4l .. +3 and k0 + 128 + 4l .. +3, conflict-free
