@@ -462,8 +462,9 @@ int64_t moe_launch_count(void);
  *     tokens need the split router matrix and 3 * n_experts * d_model >
  *     MOE_NOALLOC_MAX_SPLIT_ELEMS.
  *   - The first call on a device looks the array up (cudaGetSymbolAddress,
- *     once per device, with that device current): make it before any stream
- *     capture.
+ *     once per device, with that device current) and keeps the address for
+ *     the life of the process: it assumes the device's primary context is
+ *     never reset (cudaDeviceReset) while the library is loaded.
  *   - All calls share the array: calls whose work overlaps on the GPU race.
  *     Each call clears the error word first; device error bits are not
  *     reported by this entry point.

@@ -15,9 +15,8 @@
 //    matrix (E * 3d BF16 values) and the logits split over up to four K parts
 //    (four logit-sized slabs), both held in the array.
 //  - The first call on a device looks up the array's device address with
-//    cudaGetSymbolAddress (once per device, with that device current); make
-//    that first call before any stream capture.  The address is kept for the
-//    life of the process: it assumes the device's primary context is never
+//    cudaGetSymbolAddress (once per device, with that device current).  The
+//    address is kept for the life of the process: it assumes the device's primary context is never
 //    reset (after cudaDeviceReset the array would have to be looked up again).
 //  - Every call shares the one array: two calls whose work overlaps on the GPU
 //    (different streams, no ordering between them) race on it.  The error
