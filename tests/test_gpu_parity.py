@@ -161,7 +161,10 @@ def test_super_latent_4096_full():
     _parity(SUPER_LATENT, 4096, chunk=2048)
 
 
-@pytest.mark.parametrize("T", [1, 9, 64, 65, 200])
+# 1 and 4 tokens: the FP16 path; 9: the FP4 path; 40 and 64: the FP4 path
+# with the dense products on the tensor cores (40: a ragged token tile);
+# 65 and 200: the FP16 tensor-core path
+@pytest.mark.parametrize("T", [1, 4, 9, 40, 64, 65, 200])
 def test_scaled_nvfp4_layer(T):
     _parity(SMALL_NVFP4, T)
 
