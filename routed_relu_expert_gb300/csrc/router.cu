@@ -208,60 +208,102 @@ cudaError_t launch_small_t(const void* x, int act, int T, int d, const float* w,
 
 // ---------------------------------------------------------------------------
 // logits, 33..64 tokens of a wide router (E >= 256): a CTA computes 16 experts x
-// TT tokens.  Each 256-wide K chunk of its TT token rows is staged in shared
-// memory (FP32) once for all 8 warps; a warp owns 2 experts, a lane 4 + 4
-// values of each chunk (k0 + 4l .. +3 and k0 + 128 + 4l .. +3, conflict-free
-// 16-byte reads), with 2 x TT FP32 partial sums in registers, added across
-// the lanes by a fixed shuffle tree at the end.  The token rows are read from
-// L2 once per 16 experts instead of once per 2.
+// TT tokens over 256-wide K chunks.  Each chunk's 16 weight rows (FP32) and TT
+// token rows (as stored) are copied into shared memory with cp.async, four
+// chunks in flight, so the copies of the next three chunks overlap the
+// products of the current one.  A warp owns 2 experts, a lane 4 + 4 values of
+// each chunk (k0 + 4l .. +3 and k0 + 128 + 4l .. +3: conflict-free reads),
+// with 2 x TT FP32 partial sums in registers, added across the lanes by a
+// fixed shuffle tree at the end.  The token rows are read from L2 once per 16
+// experts.
 // ---------------------------------------------------------------------------
+constexpr int kWideKC = 256, kWideEPC = 16, kWideStages = 4;
+
 template <int TT, bool XF32>
-__global__ void __launch_bounds__(256) router_logits_wide(const void* __restrict__ X, int T, int d,
-                                                          const float* __restrict__ Wr, int E,
-                                                          float* __restrict__ logits) {
+constexpr int wide_stage_bytes() { return kWideEPC * kWideKC * 4 + TT * kWideKC * (XF32 ? 4 : 2); }
+
+__device__ __forceinline__ void wide_cp16(uint32_t dst, const void* src, bool valid) {
+  const int n = valid ? 16 : 0;     // 0: the 16 bytes are zero-filled, nothing is read
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+
+template <int TT, bool XF32>
+__global__ void __launch_bounds__(256, 1) router_logits_wide(const void* __restrict__ X, int T, int d,
+                                                             const float* __restrict__ Wr, int E,
+                                                             float* __restrict__ logits) {
   pdl_wait();
-  constexpr int KC = 256, EW = 2;
-  __shared__ __align__(16) float xs[TT][KC];
+  constexpr int KC = kWideKC, EPC = kWideEPC, S = kWideStages, EW = EPC / 8;
+  constexpr int XB = XF32 ? 4 : 2;                          // bytes of one token value
+  constexpr int W_BYTES = EPC * KC * 4, STAGE = wide_stage_bytes<TT, XF32>();
+  constexpr int W_PIECES = W_BYTES / 16 / 256;              // 16-byte copies a thread issues per chunk
+  constexpr int X_PIECES = (STAGE - W_BYTES) / 16 / 256;
+  constexpr int XPR = KC * XB / 16;                         // 16-byte pieces in a chunk of a token row
+  static_assert(W_BYTES % (16 * 256) == 0 && (STAGE - W_BYTES) % (16 * 256) == 0, "whole copies per thread");
+  extern __shared__ __align__(16) unsigned char wide_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int eb = blockIdx.x * 16 + warp * EW;
+  const int e_blk = blockIdx.x * EPC;
   const int t0 = blockIdx.y * TT;
   const int nt = min(TT, T - t0);
+  const int nchunks = (d + KC - 1) / KC;
+  const unsigned char* xbytes = reinterpret_cast<const unsigned char*>(X);
+  const uint32_t sbase = smem_u32(wide_smem);
+  // chunk c into stage c % S: weight rows [e_blk, e_blk + 16) then token rows
+  // [t0, t0 + TT), zero past E, the tile's rows or d (d is a multiple of 8)
+  auto issue = [&](int c) {
+    const uint32_t st = sbase + (uint32_t)((c % S) * STAGE);
+    const int k0 = c * KC;
+#pragma unroll
+    for (int j = 0; j < W_PIECES; ++j) {
+      const int i = threadIdx.x + j * 256;
+      const int r = i / (KC / 4), k = k0 + (i % (KC / 4)) * 4;
+      const bool ok = e_blk + r < E && k < d;
+      wide_cp16(st + 16u * i, ok ? (const void*)(Wr + (int64_t)(e_blk + r) * d + k) : (const void*)Wr, ok);
+    }
+#pragma unroll
+    for (int j = 0; j < X_PIECES; ++j) {
+      const int i = threadIdx.x + j * 256;
+      const int r = i / XPR, k = k0 + (i % XPR) * (16 / XB);
+      const bool ok = r < nt && k < d;
+      wide_cp16(st + W_BYTES + 16u * i, ok ? (const void*)(xbytes + ((int64_t)(t0 + r) * d + k) * XB) : X, ok);
+    }
+  };
   float acc[EW][TT];
 #pragma unroll
   for (int i = 0; i < EW; ++i)
 #pragma unroll
     for (int t = 0; t < TT; ++t) acc[i][t] = 0.f;
-  for (int k0 = 0; k0 < d; k0 += KC) {
-    __syncthreads();                        // the previous chunk has been read
-    for (int i = threadIdx.x; i < TT * KC / 4; i += 256) {
-      const int r = i / (KC / 4), c4 = (i % (KC / 4)) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (r < nt && k0 + c4 < d) {
-        if (XF32) {
-          v = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(X) + (int64_t)(t0 + r) * d + k0 + c4);
-        } else {
-          const uint2 q = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(X) + (int64_t)(t0 + r) * d + k0 + c4);
-          v = make_float4(bf16_lo(q.x), bf16_hi(q.x), bf16_lo(q.y), bf16_hi(q.y));
-        }
-      }
-      *reinterpret_cast<float4*>(&xs[r][c4]) = v;
-    }
-    __syncthreads();
+#pragma unroll
+  for (int c = 0; c < S - 1; ++c) {
+    if (c < nchunks) issue(c);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  for (int c = 0; c < nchunks; ++c) {
+    if (c + S - 1 < nchunks) issue(c + S - 1);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group %0;" ::"n"(S - 1) : "memory");   // this thread's copies of chunk c
+    __syncthreads();                                                  // everyone's
+    const unsigned char* st = wide_smem + (c % S) * STAGE;
+    const float* ws = reinterpret_cast<const float*>(st);
     float4 wa[EW], wb[EW];
 #pragma unroll
     for (int i = 0; i < EW; ++i) {
-      const int e = eb + i;
-      wa[i] = wb[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e < E) {
-        const float* w = Wr + (int64_t)e * d + k0;
-        if (k0 + 4 * lane < d) wa[i] = ldg_stream_f4(w + 4 * lane);
-        if (k0 + 128 + 4 * lane < d) wb[i] = ldg_stream_f4(w + 128 + 4 * lane);
-      }
+      wa[i] = *reinterpret_cast<const float4*>(ws + (warp * EW + i) * KC + 4 * lane);
+      wb[i] = *reinterpret_cast<const float4*>(ws + (warp * EW + i) * KC + 128 + 4 * lane);
     }
 #pragma unroll
     for (int t = 0; t < TT; ++t) {
-      const float4 xa = *reinterpret_cast<const float4*>(&xs[t][4 * lane]);
-      const float4 xb = *reinterpret_cast<const float4*>(&xs[t][128 + 4 * lane]);
+      float4 xa, xb;
+      if (XF32) {
+        const float* xs = reinterpret_cast<const float*>(st + W_BYTES) + t * KC;
+        xa = *reinterpret_cast<const float4*>(xs + 4 * lane);
+        xb = *reinterpret_cast<const float4*>(xs + 128 + 4 * lane);
+      } else {
+        const bf16* xs = reinterpret_cast<const bf16*>(st + W_BYTES) + t * KC;
+        const uint2 qa = *reinterpret_cast<const uint2*>(xs + 4 * lane);
+        const uint2 qb = *reinterpret_cast<const uint2*>(xs + 128 + 4 * lane);
+        xa = make_float4(bf16_lo(qa.x), bf16_hi(qa.x), bf16_lo(qa.y), bf16_hi(qa.y));
+        xb = make_float4(bf16_lo(qb.x), bf16_hi(qb.x), bf16_lo(qb.y), bf16_hi(qb.y));
+      }
 #pragma unroll
       for (int i = 0; i < EW; ++i) {
         float a = acc[i][t];
@@ -270,7 +312,10 @@ __global__ void __launch_bounds__(256) router_logits_wide(const void* __restrict
         acc[i][t] = a;
       }
     }
+    __syncthreads();                      // stage c % S is refilled by the next iteration's copies
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  const int eb = e_blk + warp * EW;
 #pragma unroll
   for (int i = 0; i < EW; ++i)
 #pragma unroll
@@ -282,14 +327,24 @@ __global__ void __launch_bounds__(256) router_logits_wide(const void* __restrict
     }
 }
 
+template <int TT, bool XF32>
+cudaError_t launch_wide_t(const void* x, int T, int d, const float* w, int E, float* logits, cudaStream_t s) {
+  auto kernel = router_logits_wide<TT, XF32>;
+  constexpr int smem = kWideStages * wide_stage_bytes<TT, XF32>();
+  static PerDeviceOnce attr;
+  const cudaError_t e = attr.run([&](int&) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)ceil_div(E, kWideEPC), (unsigned)ceil_div(T, TT));
+  launch_k(kernel, grid, 256, smem, s, x, T, d, w, E, logits);
+  return cudaGetLastError();
+}
+
 template <int TT>
 cudaError_t launch_wide(const void* x, int act, int T, int d, const float* w, int E, float* logits, cudaStream_t s) {
-  const dim3 grid((unsigned)ceil_div(E, 16), (unsigned)ceil_div(T, TT));
-  if (act == MOE_DT_F32)
-    launch_k(router_logits_wide<TT, true>, grid, 256, 0, s, x, T, d, w, E, logits);
-  else
-    launch_k(router_logits_wide<TT, false>, grid, 256, 0, s, x, T, d, w, E, logits);
-  return cudaGetLastError();
+  if (act == MOE_DT_F32) return launch_wide_t<TT, true>(x, T, d, w, E, logits, s);
+  return launch_wide_t<TT, false>(x, T, d, w, E, logits, s);
 }
 
 template <int TMAX>
@@ -329,9 +384,10 @@ cudaError_t launch_router_logits(const void* x, int act, int T, int d, const flo
   }
   if (T <= 4) return launch_small<4>(x, act, T, d, w_router, E, logits, s);
   if (T > 32 && T <= 64 && E >= 256 && d % 8 == 0) {
-    // wide routers above 32 tokens: token rows staged once per 16 experts
-    // (Super NVFP4 layer at 64 tokens 0.338 -> 0.330 ms; at 8 and 16 tokens
-    // the per-2-experts kernel below measured 5-8 us faster)
+    // wide routers above 32 tokens: weight and token rows copied into shared
+    // memory four K chunks ahead (Super NVFP4 layer at 64 tokens 0.293 ->
+    // 0.280 ms, at 33 tokens 0.248 -> 0.241; from 5 or 17 tokens on, no
+    // faster at 16 tokens and slower at 8 than the per-2-experts kernel below)
     return launch_wide<16>(x, act, T, d, w_router, E, logits, s);
   }
   if (T <= 64) return launch_small<8>(x, act, T, d, w_router, E, logits, s);

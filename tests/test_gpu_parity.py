@@ -424,13 +424,15 @@ def test_topk_above_eight_with_exact_ties(T, groups):
     check_router(shape, x.float().cpu().numpy().astype(np.float64), ow, g)
 
 
-@pytest.mark.parametrize("T", [5, 16, 17, 32, 33, 64])
-def test_wide_router_logits_every_tile_height(T):
+@pytest.mark.parametrize("T,d_model", [(5, 1024), (16, 1024), (17, 1024), (32, 1024), (33, 1024), (64, 1024),
+                                       (40, 1088)])
+def test_wide_router_logits_every_tile_height(T, d_model):
     """Routers with E >= 256 at 5..64 tokens: above 32 tokens the logits come
     from token rows staged per 16 experts, below from the per-2-experts
     kernel; logits within 1e-5 of sum |x W|, ids and weights against the
-    oracle on the GPU scores, on both sides of the switch."""
-    shape = scaled(SUPER_LATENT, name="wide_router", d_model=1024, d_latent=256, n_experts=256, top_k=12,
+    oracle on the GPU scores, on both sides of the switch.  A hidden width of
+    1088 leaves a last K chunk of 64 values."""
+    shape = scaled(SUPER_LATENT, name="wide_router", d_model=d_model, d_latent=256, n_experts=256, top_k=12,
                    n_group=8, topk_group=4, d_expert=128, d_shared=0, weight_seed=71, tokens=())
     w = device_weights(shape)
     x = make_x(shape, T, "cuda")
