@@ -386,8 +386,9 @@ cudaError_t launch_router_logits(const void* x, int act, int T, int d, const flo
   if (T > 32 && T <= 64 && E >= 256 && d % 8 == 0) {
     // wide routers above 32 tokens: weight and token rows copied into shared
     // memory four K chunks ahead (Super NVFP4 layer at 64 tokens 0.293 ->
-    // 0.280 ms, at 33 tokens 0.248 -> 0.241; from 5 or 17 tokens on, no
-    // faster at 16 tokens and slower at 8 than the per-2-experts kernel below)
+    // 0.280 ms, at 33 tokens 0.248 -> 0.241; used from 5 tokens on it measured
+    // equal at 8 tokens and 1-2 % slower at 16 than the per-2-experts kernel
+    // below)
     return launch_wide<16>(x, act, T, d, w_router, E, logits, s);
   }
   if (T <= 64) return launch_small<8>(x, act, T, d, w_router, E, logits, s);
