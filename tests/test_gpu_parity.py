@@ -441,3 +441,14 @@ def test_wide_router_logits_every_tile_height(T, d_model):
     g.pop("ws")
     g = to_np(g)
     check_router(shape, x.float().cpu().numpy().astype(np.float64), oracle_weights(w), g)
+
+
+@pytest.mark.parametrize("T", [20, 40])
+def test_wide_router_fp32_layer(T):
+    """An FP32 layer with a 256-expert router: at 40 tokens the router reads
+    FP32 token rows through the staged wide kernel, at 20 through the
+    per-2-experts kernel; routing and the whole layer against the oracle."""
+    from synth import TINY_FP32
+    shape = scaled(TINY_FP32, name="wide_router_fp32", d_model=512, n_experts=256, top_k=8, n_group=8,
+                   topk_group=4, d_expert=128, d_shared=256, weight_seed=73, tokens=())
+    _parity(shape, T)
