@@ -73,3 +73,30 @@ def test_roofline_numerators_match_the_worked_ledgers():
     assert fp4["total"] == 181_389_488
     assert bench.layer_flops(SUPER_LATENT, 1) == 351_272_960
     assert bench.layer_flops(TINY_FP32, 16) == 16 * 528_384
+
+
+def test_recorded_traffic_is_reported_only_for_unchanged_sources(tmp_path, monkeypatch):
+    """The roofline `traffic` comes from the committed ncu table only while the
+    kernel family's sources hash to the value recorded beside it."""
+    want = bench.sources_sha16("gemv")
+    assert len(want) == 16 and int(want, 16) >= 0
+    table = tmp_path / "traffic.md"
+    table.write_text("| kernel | workload | dram bytes per launch | sources sha16 |\n|---|---|---|---|\n"
+                     f"| `k<0>` | w T=1 | 1,234,000 | {want} |\n"
+                     "| `k<1>` | w T=1 | 5,678,000 | 0000000000000000 |\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(table))
+    assert bench.recorded_traffic("k<0>", "w T=1", "gemv") == (1234000, want)
+    assert bench.recorded_traffic("k<1>", "w T=1", "gemv") == (None, "0000000000000000")
+    assert bench.recorded_traffic("k<2>", "w T=1", "gemv") == (None, None)
+
+
+def test_committed_traffic_rows_parse():
+    """Every row of the committed table names a kernel, a workload, a byte
+    count and a 16-digit source hash (whether or not it is current)."""
+    rows = 0
+    for line in open(bench.TRAFFIC_FILE):
+        cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
+        if len(cells) == 4 and cells[3] and all(ch in "0123456789abcdef" for ch in cells[3]) and len(cells[3]) == 16:
+            assert int(cells[2].replace(",", "")) > 0
+            rows += 1
+    assert rows >= 1
