@@ -207,34 +207,35 @@ cudaError_t launch_small_t(const void* x, int act, int T, int d, const float* w,
 }
 
 // ---------------------------------------------------------------------------
-// logits, 33..64 tokens of a wide router (E >= 256): a CTA computes 16 experts x
-// TT tokens over 256-wide K chunks.  Each chunk's 16 weight rows (FP32) and TT
-// token rows (as stored) are copied into shared memory with cp.async, four
+// logits, 5..8 and 33..64 tokens of a wide router (E >= 256): a CTA computes
+// 8 * EW experts x TT tokens over 256-wide K chunks.  Each chunk's weight rows
+// (FP32) and TT token rows (as stored) are copied into shared memory with cp.async, four
 // chunks in flight, so the copies of the next three chunks overlap the
-// products of the current one.  A warp owns 2 experts, a lane 4 + 4 values of
+// products of the current one.  A warp owns EW experts, a lane 4 + 4 values of
 // each chunk (k0 + 4l .. +3 and k0 + 128 + 4l .. +3: conflict-free reads),
-// with 2 x TT FP32 partial sums in registers, added across the lanes by a
-// fixed shuffle tree at the end.  The token rows are read from L2 once per 16
-// experts.
+// with EW x TT FP32 partial sums in registers, added across the lanes by a
+// fixed shuffle tree at the end.  The token rows are read from L2 once per
+// 8 * EW experts.
 // ---------------------------------------------------------------------------
-constexpr int kWideKC = 256, kWideEPC = 16, kWideStages = 4;
+constexpr int kWideKC = 256, kWideStages = 4;
 
-template <int TT, bool XF32>
-constexpr int wide_stage_bytes() { return kWideEPC * kWideKC * 4 + TT * kWideKC * (XF32 ? 4 : 2); }
+// one stage: 8 * EW weight rows and TT token rows of one K chunk
+template <int TT, int EW, bool XF32>
+constexpr int wide_stage_bytes() { return 8 * EW * kWideKC * 4 + TT * kWideKC * (XF32 ? 4 : 2); }
 
 __device__ __forceinline__ void wide_cp16(uint32_t dst, const void* src, bool valid) {
   const int n = valid ? 16 : 0;     // 0: the 16 bytes are zero-filled, nothing is read
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
 }
 
-template <int TT, bool XF32>
+template <int TT, int EW, bool XF32>
 __global__ void __launch_bounds__(256, 1) router_logits_wide(const void* __restrict__ X, int T, int d,
                                                              const float* __restrict__ Wr, int E,
                                                              float* __restrict__ logits) {
   pdl_wait();
-  constexpr int KC = kWideKC, EPC = kWideEPC, S = kWideStages, EW = EPC / 8;
+  constexpr int KC = kWideKC, EPC = 8 * EW, S = kWideStages;
   constexpr int XB = XF32 ? 4 : 2;                          // bytes of one token value
-  constexpr int W_BYTES = EPC * KC * 4, STAGE = wide_stage_bytes<TT, XF32>();
+  constexpr int W_BYTES = EPC * KC * 4, STAGE = wide_stage_bytes<TT, EW, XF32>();
   constexpr int W_PIECES = W_BYTES / 16 / 256;              // 16-byte copies a thread issues per chunk
   constexpr int X_PIECES = (STAGE - W_BYTES) / 16 / 256;
   constexpr int XPR = KC * XB / 16;                         // 16-byte pieces in a chunk of a token row
@@ -327,24 +328,24 @@ __global__ void __launch_bounds__(256, 1) router_logits_wide(const void* __restr
     }
 }
 
-template <int TT, bool XF32>
+template <int TT, int EW, bool XF32>
 cudaError_t launch_wide_t(const void* x, int T, int d, const float* w, int E, float* logits, cudaStream_t s) {
-  auto kernel = router_logits_wide<TT, XF32>;
-  constexpr int smem = kWideStages * wide_stage_bytes<TT, XF32>();
+  auto kernel = router_logits_wide<TT, EW, XF32>;
+  constexpr int smem = kWideStages * wide_stage_bytes<TT, EW, XF32>();
   static PerDeviceOnce attr;
   const cudaError_t e = attr.run([&](int&) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)ceil_div(E, kWideEPC), (unsigned)ceil_div(T, TT));
+  const dim3 grid((unsigned)ceil_div(E, 8 * EW), (unsigned)ceil_div(T, TT));
   launch_k(kernel, grid, 256, smem, s, x, T, d, w, E, logits);
   return cudaGetLastError();
 }
 
-template <int TT>
+template <int TT, int EW>
 cudaError_t launch_wide(const void* x, int act, int T, int d, const float* w, int E, float* logits, cudaStream_t s) {
-  if (act == MOE_DT_F32) return launch_wide_t<TT, true>(x, T, d, w, E, logits, s);
-  return launch_wide_t<TT, false>(x, T, d, w, E, logits, s);
+  if (act == MOE_DT_F32) return launch_wide_t<TT, EW, true>(x, T, d, w, E, logits, s);
+  return launch_wide_t<TT, EW, false>(x, T, d, w, E, logits, s);
 }
 
 template <int TMAX>
@@ -389,7 +390,14 @@ cudaError_t launch_router_logits(const void* x, int act, int T, int d, const flo
     // 0.280 ms, at 33 tokens 0.248 -> 0.241; used from 5 tokens on it measured
     // equal at 8 tokens and 1-2 % slower at 16 than the per-2-experts kernel
     // below)
-    return launch_wide<16>(x, act, T, d, w_router, E, logits, s);
+    return launch_wide<16, 2>(x, act, T, d, w_router, E, logits, s);
+  }
+  if (T > 4 && T <= 8 && E >= 256 && d % 8 == 0) {
+    // the same pipeline at 8 experts x 8 tokens a CTA (Super NVFP4 layer at 8
+    // tokens 0.146 -> 0.1435 ms).  Measured no faster, or slower, at 9-32
+    // tokens of a wide router and at 5-64 tokens of the 128-expert router
+    // (Nano at 16 tokens 0.217 -> 0.231 ms: 32 CTAs)
+    return launch_wide<8, 1>(x, act, T, d, w_router, E, logits, s);
   }
   if (T <= 64) return launch_small<8>(x, act, T, d, w_router, E, logits, s);
   dim3 grid((unsigned)ceil_div(T, 64), (unsigned)ceil_div(E, 64));

@@ -424,14 +424,14 @@ def test_topk_above_eight_with_exact_ties(T, groups):
     check_router(shape, x.float().cpu().numpy().astype(np.float64), ow, g)
 
 
-@pytest.mark.parametrize("T,d_model", [(5, 1024), (16, 1024), (17, 1024), (32, 1024), (33, 1024), (64, 1024),
-                                       (40, 1088)])
+@pytest.mark.parametrize("T,d_model", [(4, 1024), (5, 1024), (8, 1024), (9, 1024), (16, 1024), (17, 1024),
+                                       (32, 1024), (33, 1024), (64, 1024), (6, 1088), (40, 1088)])
 def test_wide_router_logits_every_tile_height(T, d_model):
-    """Routers with E >= 256 at 5..64 tokens: above 32 tokens the logits come
-    from token rows staged per 16 experts, below from the per-2-experts
-    kernel; logits within 1e-5 of sum |x W|, ids and weights against the
-    oracle on the GPU scores, on both sides of the switch.  A hidden width of
-    1088 leaves a last K chunk of 64 values."""
+    """Routers with E >= 256 at 4..64 tokens: at 5-8 tokens the logits come
+    from rows staged per 8 experts x 8 tokens, above 32 tokens per 16 x 16,
+    otherwise from the per-2-experts kernel; logits within 1e-5 of sum |x W|,
+    ids and weights against the oracle on the GPU scores, on both sides of
+    every switch.  A hidden width of 1088 leaves a last K chunk of 64 values."""
     shape = scaled(SUPER_LATENT, name="wide_router", d_model=d_model, d_latent=256, n_experts=256, top_k=12,
                    n_group=8, topk_group=4, d_expert=128, d_shared=0, weight_seed=71, tokens=())
     w = device_weights(shape)
@@ -443,10 +443,10 @@ def test_wide_router_logits_every_tile_height(T, d_model):
     check_router(shape, x.float().cpu().numpy().astype(np.float64), oracle_weights(w), g)
 
 
-@pytest.mark.parametrize("T", [20, 40])
+@pytest.mark.parametrize("T", [7, 20, 40])
 def test_wide_router_fp32_layer(T):
-    """An FP32 layer with a 256-expert router: at 40 tokens the router reads
-    FP32 token rows through the staged wide kernel, at 20 through the
+    """An FP32 layer with a 256-expert router: at 7 and 40 tokens the router
+    reads FP32 token rows through the staged kernels, at 20 through the
     per-2-experts kernel; routing and the whole layer against the oracle."""
     from synth import TINY_FP32
     shape = scaled(TINY_FP32, name="wide_router_fp32", d_model=512, n_experts=256, top_k=8, n_group=8,
