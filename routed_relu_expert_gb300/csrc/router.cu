@@ -394,7 +394,7 @@ cudaError_t launch_router_logits(const void* x, int act, int T, int d, const flo
   }
   if (T > 4 && T <= 8 && E >= 256 && d % 8 == 0) {
     // the same pipeline at 8 experts x 8 tokens a CTA (Super NVFP4 layer at 8
-    // tokens 0.146 -> 0.1435 ms).  Measured no faster, or slower, at 9-32
+    // tokens 0.146 -> 0.1435 ms, one run).  Measured no faster, or slower, at 9-32
     // tokens of a wide router and at 5-64 tokens of the 128-expert router
     // (Nano at 16 tokens 0.217 -> 0.231 ms: 32 CTAs)
     return launch_wide<8, 1>(x, act, T, d, w_router, E, logits, s);
