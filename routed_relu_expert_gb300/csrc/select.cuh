@@ -345,4 +345,133 @@ __device__ __forceinline__ void select_token(const float* __restrict__ logits, i
 }
 
 
+
+// ---------------------------------------------------------------------------
+// One token's selection by a whole CTA of NT threads (E <= NT, K <= 32; with a
+// group limit, groups of a multiple of 32 experts, at most 32 groups): thread
+// i holds expert i, so the loads, sigmoids and stores take one step instead
+// of P per lane.  Every value that decides or is stored comes from the same
+// expressions in the same order as select_token: the group score is the sum
+// of the group's two best biased scores, the K-th largest ordering key is
+// found bit by bit (a CTA-wide count per bit), keys above it are chosen and,
+// of the keys equal to it, the lowest ids; slots are (key descending, id
+// ascending) and the weight sum runs in slot order.  Every thread of the CTA
+// calls it (it holds CTA barriers).
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ bool cta_select_fits(int NT, int E, int G, int TG, int K) {
+  return E <= NT && K <= 32 && (G <= 1 || TG >= G || (G <= 32 && E % G == 0 && (E / G) % 32 == 0));
+}
+
+template <int NT>
+__device__ __forceinline__ void select_token_cta(const float* __restrict__ logits, int nparts, int64_t part_stride,
+                                                 float* __restrict__ logits_out, int t, int E,
+                                                 const float* __restrict__ bias, int G, int TG, int K, int norm,
+                                                 float rsf, float* __restrict__ scores, int32_t* __restrict__ ids,
+                                                 float* __restrict__ wout, int32_t* err) {
+  constexpr int NW = NT / 32;
+  constexpr unsigned FULL = 0xffffffffu;
+  __shared__ int c_k1[NW], c_e1[NW], c_k2[NW], c_e2[NW];
+  __shared__ float c_v1[NW], c_v2[NW];
+  __shared__ int c_gkey[32];
+  __shared__ int c_cnt[NW];
+  __shared__ uint32_t c_sel_key[32];
+  __shared__ int c_sel_e[32];
+  __shared__ float c_sel_s[32], c_slot_s[32];
+  const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
+  const bool live = i < E;
+  float sv = 0.f, cv = 0.f;
+  int key = INT_MIN;
+  if (live) {
+    const float* zrow = logits + (int64_t)t * E;
+    float z = zrow[i];
+    for (int p = 1; p < nparts; ++p) z += zrow[p * part_stride + i];   // K parts added in part order
+    sv = 1.0f / (1.0f + expf(-z));
+    cv = bias ? sv + bias[i] : sv;
+    key = order_key(cv);
+    scores[(int64_t)t * E + i] = sv;
+    if (logits_out) logits_out[(int64_t)t * E + i] = z;
+  }
+  if (__syncthreads_or(live && isnan(cv)) && i == 0) set_error(err, MOE_DEVERR_NONFINITE);
+
+  // group limit: each warp's best two, merged per group, ranked
+  bool cand = live;
+  if (G > 1 && TG < G) {
+    const int gsz = E / G, wpg = gsz / 32;
+    Top2 tp{INT_MIN, INT_MAX, INT_MIN, INT_MAX, 0.f, 0.f};
+    if (live) top2_add(tp, key, i, cv);
+    top2_merge(tp, 32);
+    if (lane == 0) {
+      c_k1[warp] = tp.k1; c_e1[warp] = tp.e1; c_v1[warp] = tp.v1;
+      c_k2[warp] = tp.k2; c_e2[warp] = tp.e2; c_v2[warp] = tp.v2;
+    }
+    __syncthreads();
+    if (i < G) {
+      Top2 g2{INT_MIN, INT_MAX, INT_MIN, INT_MAX, 0.f, 0.f};
+      for (int w = i * wpg; w < (i + 1) * wpg; ++w) {
+        top2_add(g2, c_k1[w], c_e1[w], c_v1[w]);
+        top2_add(g2, c_k2[w], c_e2[w], c_v2[w]);
+      }
+      c_gkey[i] = order_key(g2.v1 + g2.v2);
+    }
+    __syncthreads();
+    if (live) {
+      const int g = i / gsz, gk = c_gkey[g];
+      int rank = 0;
+      for (int g2 = 0; g2 < G; ++g2) rank += better(c_gkey[g2], g2, gk, g) ? 1 : 0;
+      cand = rank < TG;
+    }
+  }
+
+  // the K-th largest key among the candidates (as unsigned numbers, every
+  // candidate at least 1): the largest value with at least K keys at or above it
+  const uint32_t uk = cand ? ((uint32_t)key ^ 0x80000000u) : 0u;
+  uint32_t thr = 0u;
+  for (int b = 31; b >= 0; --b) {
+    const uint32_t trial = thr | (1u << b);
+    if (__syncthreads_count(cand && uk >= trial) >= K) thr = trial;
+  }
+  const int need = K - __syncthreads_count(cand && uk > thr);   // >= 1 keys equal to thr are taken
+  const bool eq = cand && uk == thr;
+  const uint32_t eqm = __ballot_sync(FULL, eq);
+  if (lane == 0) c_cnt[warp] = __popc(eqm);
+  __syncthreads();
+  int pre = __popc(eqm & ((1u << lane) - 1u));                   // equal keys at lower ids
+  for (int w = 0; w < warp; ++w) pre += c_cnt[w];
+  const bool take = cand && (uk > thr || (eq && pre < need));
+  const uint32_t tm = __ballot_sync(FULL, take);
+  __syncthreads();                                              // every thread has read c_cnt
+  if (lane == 0) c_cnt[warp] = __popc(tm);
+  __syncthreads();
+  if (take) {
+    int pos = __popc(tm & ((1u << lane) - 1u));                 // K chosen in id order
+    for (int w = 0; w < warp; ++w) pos += c_cnt[w];
+    c_sel_key[pos] = uk;
+    c_sel_e[pos] = i;
+    c_sel_s[pos] = sv;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int rank = 0, ei = 0;
+    float si = 0.f;
+    if (lane < K) {
+      const uint32_t ki = c_sel_key[lane];
+      ei = c_sel_e[lane];
+      si = c_sel_s[lane];
+      for (int j = 0; j < K; ++j) {
+        const uint32_t kj = c_sel_key[j];
+        rank += (kj > ki || (kj == ki && c_sel_e[j] < ei)) ? 1 : 0;
+      }
+      c_slot_s[rank] = si;
+    }
+    __syncwarp();
+    float wsum = 0.f;
+    for (int k = 0; k < K; ++k) wsum += c_slot_s[k];            // slot order, FP32
+    if (lane < K) {
+      const float wv = norm ? (si / wsum) * rsf : si * rsf;
+      ids[(int64_t)t * K + rank] = ei;
+      wout[(int64_t)t * K + rank] = wv;
+    }
+  }
+}
+
 }  // namespace moe

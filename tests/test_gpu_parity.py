@@ -400,13 +400,14 @@ def test_nvfp4_rows_beyond_fp16_range(T):
     check_output(shape, x_np, ow, ids_o, w_o, g["y"], tol_of(shape))
 
 
-@pytest.mark.parametrize("T,groups", [(3, 1), (3, 8), (40, 1), (40, 8), (100, 8)])
+@pytest.mark.parametrize("T,groups", [(1, 1), (1, 8), (3, 1), (3, 8), (40, 1), (40, 8), (100, 8)])
 def test_topk_above_eight_with_exact_ties(T, groups):
     """K = 12 of E = 256 (the selection-by-threshold path for K > 8): router
     rows duplicated in pairs and a zero bias give exactly equal scores, so
     every choice crosses ties; ids must match the oracle's selection (lower id
-    first) on the GPU's own scores, through the fused tiny kernel (T = 3) and
-    the per-token selection kernel."""
+    first) on the GPU's own scores, through the fused tiny kernel (T = 1: the
+    whole CTA selects the token of this 256-expert router; T = 3: a warp a
+    token) and the per-token selection kernel."""
     from synth import make_weights as mw
     shape = scaled(NANO_DECODE, name=f"ties_{groups}", d_model=256, n_experts=256, top_k=12, n_group=groups,
                    topk_group=4 if groups > 1 else 1, d_expert=128, d_shared=0, weight_seed=67, tokens=())
